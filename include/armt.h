@@ -1,0 +1,214 @@
+/*
+ * armt.h -- C ABI of the diagonal-batched ARMT forward pass (GB300, sm_103a).
+ *
+ * Source of the method: the summary page of "Diagonal Batching Unlocks
+ * Parallelism in Recurrent Memory Transformers for Long Contexts" (Sivtsov,
+ * Rodkin, Kuzmin, Kuratov, Oseledets; arXiv:2506.05229).
+ *   - Section 二: in a parallel recurrent memory transformer (PRMT) such as
+ *     ARMT every layer l owns an associative memory A_l, updated from that
+ *     layer's output on the previous segment, so cell (layer l, segment s)
+ *     depends only on (l-1, s) and (l, s-1); all cells with l + s = i can run
+ *     together in iteration i ("one diagonal").
+ *   - Section 三: all layers become one grouped layer -- stacked weights,
+ *     grouped matrix multiplication with the outputs preallocated as one
+ *     tensor and viewed per group, stacked norm gains, everything else run
+ *     as a larger batch (attention batched over the layers of a diagonal).
+ *   - Sections 一 and 五: the reordering keeps the exact recurrence.
+ * The associative read/write equations are not printed on the page; the
+ * reading implemented here is the delta rule with DPFP features:
+ *   read  (every row x of a cell, before the attention sub-layer):
+ *         x <- x + A_l phi(Wq_a x) / (z_l^T phi(Wq_a x) + assoc_eps)
+ *   write (memory-token rows h_i of the cell's output, i = 0..M-1, batched
+ *         against the state before the write):
+ *         k_i = Wk_a h_i, v_i = Wv_a h_i, beta_i = sigmoid(wbeta_a^T h_i),
+ *         p_i = phi(k_i), vbar_i = A_l p_i / (z_l^T p_i + assoc_eps),
+ *         gamma_i = 1 - z_l^T p_i / (p_i^T p_i + assoc_eps),
+ *         A_l += sum_i beta_i (v_i - vbar_i) p_i^T,  z_l += sum_i gamma_i p_i
+ *   phi = DPFP of order nu: r = [relu(k), relu(-k)], blocks r * roll(r, j),
+ *         j = 1..nu, roll(r, j)_i = r_{(i-j) mod 2k};  P = 2 * key_dim * nu.
+ * Each cell runs a LLaMA decoder layer (RMSNorm, rotate-half RoPE at cell
+ * positions 0..S+M-1, causal grouped-query attention, SwiGLU, no biases) on
+ * its S segment rows followed by the M memory-token rows.
+ *
+ * Conventions for every entry point
+ *   - Sizes are element counts.  Matrices are row-major; a linear map is
+ *     stored (out, in) like torch.nn.Linear.weight.
+ *   - Device pointers must come from the current CUDA device; `stream` is a
+ *     cudaStream_t (NULL = legacy default stream).  Work is enqueued
+ *     asynchronously on `stream`; nothing synchronises the host unless the
+ *     entry point says so.
+ *   - Errors are returned as armt_status and never abort the process.
+ *     Argument and shape checks happen before any work is enqueued; on an
+ *     argument error nothing is written.  A device-side bounded wait that
+ *     gives up records ARMT_ERR_TIMEOUT, reported by armt_sync_status().
+ *   - Not thread-safe per model: one host thread at a time per armt_model,
+ *     and calls on one model must not overlap on the device (they share the
+ *     model's activation workspace).  Different models are independent.
+ */
+#ifndef ARMT_H
+#define ARMT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum armt_status {
+  ARMT_OK = 0,
+  ARMT_ERR_ARG = 1,          /* NULL pointer, non-positive count, bad enum value */
+  ARMT_ERR_SHAPE = 2,        /* sizes inconsistent with the config or the kernels' tiling */
+  ARMT_ERR_UNSUPPORTED = 3,  /* a config the kernels do not cover (e.g. head_dim 96) */
+  ARMT_ERR_OOM = 4,          /* device allocation failed or exceeded the allocation cap */
+  ARMT_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
+  ARMT_ERR_TIMEOUT = 6,      /* a bounded device-side wait gave up (kernel returned early) */
+  ARMT_ERR_NO_DEVICE = 7     /* no CUDA device, or not a compute capability 10.3 device */
+} armt_status;
+
+typedef enum armt_dtype {
+  ARMT_F32 = 0,   /* weights fp32, all matrix products in fp32 on CUDA cores */
+  ARMT_BF16 = 1   /* weights bf16, matrix products on tcgen05 tensor cores, fp32 accumulation */
+} armt_dtype;
+
+typedef enum armt_schedule {
+  ARMT_SCHEDULE_DIAGONAL = 0,   /* one grouped launch per anti-diagonal l + s = i */
+  ARMT_SCHEDULE_SEQUENTIAL = 1  /* segment by segment, layer by layer, one cell per launch */
+} armt_schedule;
+
+/* Model shape.  LLaMA decoder layer + per-layer associative memory. */
+typedef struct armt_config {
+  int32_t n_layers;    /* L */
+  int32_t d_model;     /* d */
+  int32_t n_q_heads;   /* Hq */
+  int32_t n_kv_heads;  /* Hkv, divides Hq */
+  int32_t head_dim;    /* hd (even; 64 or 128 for ARMT_BF16) */
+  int32_t ffn_dim;     /* F, SwiGLU hidden size */
+  int32_t vocab;       /* V, rows of the token embedding */
+  int32_t seg_len;     /* S, segment tokens per cell */
+  int32_t n_mem;       /* M, memory tokens appended after the segment rows */
+  int32_t key_dim;     /* k, associative key dim */
+  int32_t dpfp_nu;     /* nu, DPFP order; P = 2 * k * nu */
+  float norm_eps;      /* RMSNorm epsilon */
+  float assoc_eps;     /* epsilon in the associative denominators */
+  double rope_base;    /* RoPE base (theta) */
+  int32_t dtype;       /* armt_dtype */
+} armt_config;
+
+/* Weights, stacked over layers (section 三: one grouped layer holds every
+ * layer's parameters).  Element type: float for ARMT_F32, bf16 (raw 16-bit
+ * patterns) for ARMT_BF16.  Either all host pointers (on_device = 0) or all
+ * device pointers (on_device = 1).  armt_create copies them into its own
+ * layout; the caller may free them once armt_create returns. */
+typedef struct armt_weights {
+  const void* embed;    /* [V, d] token embedding */
+  const void* mem;      /* [M, d] memory-token embeddings (same for every segment) */
+  const void* wq;       /* [L, Hq*hd, d] */
+  const void* wk;       /* [L, Hkv*hd, d] */
+  const void* wv;       /* [L, Hkv*hd, d] */
+  const void* wo;       /* [L, d, Hq*hd] */
+  const void* w_gate;   /* [L, F, d] */
+  const void* w_up;     /* [L, F, d] */
+  const void* w_down;   /* [L, d, F] */
+  const void* a_wq;     /* [L, k, d] associative query projection */
+  const void* a_wk;     /* [L, k, d] associative key projection */
+  const void* a_wv;     /* [L, d, d] associative value projection */
+  const void* a_wbeta;  /* [L, d]    write-strength projection (sigmoid) */
+  const void* norm1;    /* [L, d] RMSNorm gain before attention */
+  const void* norm2;    /* [L, d] RMSNorm gain before the MLP */
+  const void* norm_f;   /* [d]    final RMSNorm gain */
+  int32_t on_device;    /* 1: device pointers, 0: host pointers */
+} armt_weights;
+
+typedef struct armt_model armt_model;  /* opaque */
+
+/* Builds a model on the current device: validates `cfg` (uniform layers are
+ * implied by the stacked layout; unsupported shapes -> ARMT_ERR_UNSUPPORTED),
+ * copies the weights into the library's stacked device layout (fused Q|K|V
+ * rows, gate/up rows interleaved in blocks of 128, TMA descriptors per
+ * projection) and allocates the activation workspace for every layer.  The
+ * copies are enqueued on `stream` and finished before return (synchronous).
+ * On success *out owns all of it until armt_destroy. */
+armt_status armt_create(const armt_config* cfg, const armt_weights* w, void* stream,
+                        armt_model** out);
+
+/* Releases everything armt_create allocated (synchronises the device first).
+ * NULL is accepted. */
+armt_status armt_destroy(armt_model* m);
+
+/* ARMT forward over n_segments * S tokens with the diagonal schedule
+ * (section 二): for i = 0 .. L + n_segments - 2 one grouped step runs every
+ * cell (l, s = i - l) with 0 <= s < n_segments, each with layer l's weights
+ * and layer l's memory.
+ *   tokens      device int32 [n_segments * S], each in [0, V) (out-of-range
+ *               ids are clamped to V-1 on the device; they are not checked)
+ *   hidden_out  device fp32 [n_segments * S, d]: last layer's segment rows
+ *               after the final RMSNorm (memory-token rows are not returned)
+ *   mem_A       device fp32 [L, d, P], mem_z device fp32 [L, P]: the memory
+ *               state, updated in place.  mem_in_valid = 0: the state starts
+ *               at zero (the buffers are overwritten); 1: the buffers hold
+ *               the state to resume from (e.g. a previous call's result).
+ * Caller owns all buffers; they must not alias each other.  Results are
+ * bit-identical to armt_forward_sequential on the same inputs. */
+armt_status armt_forward(armt_model* m, const int32_t* tokens, int64_t n_segments,
+                         float* hidden_out, float* mem_A, float* mem_z, int32_t mem_in_valid,
+                         void* stream);
+
+/* Same arguments and results; cells run one per step, segment by segment and
+ * layer by layer (the schedule the diagonal one reorders), through the same
+ * kernels.  For checking and as the speed-up denominator. */
+armt_status armt_forward_sequential(armt_model* m, const int32_t* tokens, int64_t n_segments,
+                                    float* hidden_out, float* mem_A, float* mem_z,
+                                    int32_t mem_in_valid, void* stream);
+
+/* End-to-end variant with HOST buffers (pinned or pageable): copies tokens
+ * (and the state when mem_in_valid) to the device, runs `schedule`, copies
+ * hidden states and state back, and synchronises `stream` before returning.
+ * Device staging buffers are owned by the model and grow on demand. */
+armt_status armt_forward_host(armt_model* m, const int32_t* h_tokens, int64_t n_segments,
+                              float* h_hidden_out, float* h_mem_A, float* h_mem_z,
+                              int32_t mem_in_valid, int32_t schedule, void* stream);
+
+/* Grouped matrix multiplication, the building block of the grouped layer
+ * (section 三: weights stacked per group, outputs preallocated as one tensor
+ * and viewed per group):  C[g] = A[g] * B[g]^T for g = 0..G-1, with
+ *   A device bf16 [G, M, K] row-major, B device bf16 [G, N, K] (out, in),
+ *   C device fp32 [G, M, N].  fp32 accumulation on tcgen05 tensor cores.
+ * Requires K % 64 == 0, N % 256 == 0, 16-byte aligned base pointers, any
+ * M >= 1.  A fixed reduction order per element independent of G. */
+armt_status armt_grouped_gemm_bf16(const void* A, const void* B, float* C, int32_t G, int32_t M,
+                                   int32_t N, int32_t K, void* stream);
+
+/* Sizes of the memory state buffers for this model (elements). */
+armt_status armt_state_sizes(const armt_model* m, int64_t* a_elems, int64_t* z_elems);
+
+/* Number of kernel launches one forward of n_segments makes with `schedule`. */
+armt_status armt_launch_count(const armt_model* m, int64_t n_segments, int32_t schedule,
+                              int64_t* launches);
+
+/* Per-kernel timing with CUDA events recorded on the launch stream around
+ * every launch of each kernel class (off by default).  armt_kernel_times
+ * synchronises, then returns for class c (see armt_kernel_class) the number
+ * of launches and total milliseconds since the last reset, and resets. */
+typedef enum armt_kernel_class {
+  ARMT_KC_GEMM_QKV = 0, ARMT_KC_GEMM_O = 1, ARMT_KC_GEMM_GATEUP = 2, ARMT_KC_GEMM_DOWN = 3,
+  ARMT_KC_ATTENTION = 4, ARMT_KC_ASSOC_READ = 5, ARMT_KC_ASSOC_WRITE = 6, ARMT_KC_NORM = 7,
+  ARMT_KC_OTHER = 8, ARMT_KC_COUNT = 9
+} armt_kernel_class;
+armt_status armt_set_profiling(armt_model* m, int32_t enable);
+armt_status armt_kernel_times(armt_model* m, int64_t* launches, double* ms, int32_t n_classes);
+
+/* Waits for `stream` and reports a device-side error recorded since the last
+ * call (ARMT_ERR_TIMEOUT when a bounded wait gave up), then clears it. */
+armt_status armt_sync_status(armt_model* m, void* stream);
+
+/* Static description of a status code; never NULL. */
+const char* armt_status_string(armt_status s);
+
+/* Thread-local detail of the last error returned on this thread ("" if none). */
+const char* armt_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ARMT_H */

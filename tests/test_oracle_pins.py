@@ -1,0 +1,296 @@
+"""Pins for the fp64 oracle against facts fixed by the pages and by mathematics.
+
+Every check here compares the oracle with something other than itself: a
+closed form, a brute-force loop written differently, a special case that
+reduces to an independently written plain transformer, or an invariant the
+method must satisfy (the diagonal order reaching the sequential result
+exactly: summary page of "Diagonal Batching Unlocks Parallelism in Recurrent
+Memory Transformers for Long Contexts", sections 二 and 五).
+"""
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+
+from oracle import armt_oracle as O
+from recurrent_memory_transformer_gb300 import inputs as I
+from tests.plain_llama import plain_layer, plain_stack
+
+pytestmark = pytest.mark.oracle
+
+
+# ---------------------------------------------------------------- DPFP ----
+
+def _dpfp_loops(x, nu):
+    k = len(x)
+    r = [max(v, 0.0) for v in x] + [max(-v, 0.0) for v in x]
+    n = 2 * k
+    out = []
+    for j in range(1, nu + 1):
+        for i in range(n):
+            out.append(r[i] * r[(i - j) % n])
+    return np.array(out)
+
+
+def test_dpfp_shape_and_sign():
+    rng = np.random.default_rng(0)
+    for k, nu in ((16, 3), (64, 3), (5, 2)):
+        x = rng.standard_normal((7, k))
+        phi = O.dpfp(x, nu)
+        assert phi.shape == (7, 2 * k * nu)
+        assert (phi >= 0).all()
+    assert O.dpfp(np.zeros(16), 3).shape == (96,)
+    assert O.dpfp(np.zeros(64), 3).shape == (384,)
+
+
+def test_dpfp_brute_force():
+    rng = np.random.default_rng(1)
+    for _ in range(5):
+        x = rng.standard_normal(6)
+        np.testing.assert_array_equal(O.dpfp(x, 3), _dpfp_loops(list(x), 3))
+
+
+def test_dpfp_closed_form_adjacent_pair():
+    # x = [a, b, 0, ...]: r has a at 0 and b at 1, so only block j=1 at index 1
+    # holds r_1 * r_0 = a*b; this fixes the roll direction.
+    a, b, k = 1.5, 0.25, 8
+    x = np.zeros(k); x[0], x[1] = a, b
+    phi = O.dpfp(x, 3)
+    expect = np.zeros(2 * k * 3); expect[1] = a * b
+    np.testing.assert_array_equal(phi, expect)
+
+
+def test_dpfp_closed_form_wraparound():
+    # x_{k-1} = a > 0 puts a at r_{k-1}; x_0 = -b puts b at r_k: adjacent in r,
+    # so block 1 holds a*b at index k.  x = [c] * ... at both ends of r wraps:
+    # r_{2k-1} = relu(-x_{k-1}) and r_0 = relu(x_0) meet at index 0 of block 1.
+    k, a, b = 4, 2.0, 3.0
+    x = np.zeros(k); x[k - 1], x[0] = a, -b
+    phi = O.dpfp(x, 2)
+    expect = np.zeros(2 * k * 2); expect[k] = a * b
+    np.testing.assert_array_equal(phi, expect)
+    x = np.zeros(k); x[k - 1], x[0] = -a, b
+    phi = O.dpfp(x, 2)
+    expect = np.zeros(2 * k * 2); expect[0] = a * b
+    np.testing.assert_array_equal(phi, expect)
+
+
+# ---------------------------------------------------------- row blocks ----
+
+def test_rmsnorm_closed_form():
+    c, eps, d = 0.3, 1e-5, 10
+    g = np.arange(1, d + 1, dtype=float)
+    out = O.rmsnorm(np.full(d, c), g, eps)
+    np.testing.assert_allclose(out, c / math.sqrt(c * c + eps) * g, rtol=1e-15)
+
+
+def test_silu_sigmoid_closed_forms():
+    from scipy.special import expit
+    x = np.linspace(-8, 8, 101)
+    np.testing.assert_allclose(O.sigmoid(x), expit(x), rtol=1e-14)
+    np.testing.assert_allclose(O.silu(x), x * expit(x), rtol=1e-13, atol=1e-300)
+
+
+def test_rope_identity_norm_relative():
+    rng = np.random.default_rng(2)
+    T, H, hd = 9, 3, 8
+    x = rng.standard_normal((T, H, hd))
+    y = O.rope_rotate_half(x, 10000.0)
+    np.testing.assert_array_equal(y[0], x[0])                       # position 0
+    half = hd // 2
+    pn = lambda a: a[..., :half] ** 2 + a[..., half:] ** 2
+    np.testing.assert_allclose(pn(y), pn(x), rtol=1e-12)            # pairwise norms
+    # <R_t q, R_u k> depends only on t - u
+    q = rng.standard_normal(hd); kk = rng.standard_normal(hd)
+    Q = O.rope_rotate_half(np.tile(q, (T, 1, 1)), 10000.0)[:, 0]
+    K = O.rope_rotate_half(np.tile(kk, (T, 1, 1)), 10000.0)[:, 0]
+    for t, u in ((5, 3), (7, 5), (2, 0)):
+        np.testing.assert_allclose(Q[t] @ K[u], Q[8] @ K[6], rtol=1e-10)
+    # explicit angle for pair 1 at position 3
+    th = 3 * 10000.0 ** (-2.0 / hd)
+    np.testing.assert_allclose(y[3, 0, 1], x[3, 0, 1] * math.cos(th) - x[3, 0, 1 + half] * math.sin(th))
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(3)
+    T, Hq, Hkv, hd = 6, 4, 2, 4
+    q = rng.standard_normal((T, Hq, hd)); k = rng.standard_normal((T, Hkv, hd))
+    v = rng.standard_normal((T, Hkv, hd))
+    out = O.causal_gqa_attention(q, k, v).reshape(T, Hq, hd)
+    for h in range(Hq):
+        np.testing.assert_allclose(out[0, h], v[0, h // 2], rtol=1e-14)   # row 0 sees only 0
+    out0 = O.causal_gqa_attention(q, np.zeros_like(k), v).reshape(T, Hq, hd)
+    for t in range(T):                                                    # equal scores: mean
+        np.testing.assert_allclose(out0[t, 3], v[:t + 1, 1].mean(axis=0), rtol=1e-12)
+
+
+# -------------------------------------------------------- delta rule ----
+
+def test_single_write_then_read_returns_value():
+    rng = np.random.default_rng(4)
+    k, d, nu, eps = 16, 12, 3, 1e-6
+    P = 2 * k * nu
+    key = rng.standard_normal(k); val = rng.standard_normal(d)
+    for beta in (1.0, 0.37):
+        A, z = O.delta_rule_update(np.zeros((d, P)), np.zeros(P), key[None], val[None],
+                                   np.array([beta]), nu, eps)
+        phi = _dpfp_loops(list(key), nu)
+        ff = phi @ phi
+        np.testing.assert_allclose(z, phi, rtol=1e-15)                    # gamma = 1 at z = 0
+        got = O.assoc_lookup(A, z, phi[None], eps)[0]
+        np.testing.assert_allclose(got, beta * val * ff / (ff + eps), rtol=1e-12)
+        assert np.max(np.abs(got - beta * val)) <= abs(beta) * np.max(np.abs(val)) * eps / ff * 1.01
+
+
+def test_disjoint_keys_recall_exactly():
+    # Keys whose DPFP features have disjoint supports do not interfere.
+    k, d, nu, eps = 8, 5, 1, 1e-6
+    k1 = np.zeros(k); k1[0], k1[1] = 1.0, 2.0
+    k2 = np.zeros(k); k2[4], k2[5] = 0.5, 1.5
+    rng = np.random.default_rng(5)
+    vals = rng.standard_normal((2, d))
+    A, z = O.delta_rule_update(np.zeros((d, 2 * k * nu)), np.zeros(2 * k * nu), np.stack([k1, k2]),
+                               vals, np.ones(2), nu, eps)
+    for key, v in ((k1, vals[0]), (k2, vals[1])):
+        phi = _dpfp_loops(list(key), nu)
+        ff = phi @ phi
+        np.testing.assert_allclose(O.assoc_lookup(A, z, phi[None], eps)[0], v * ff / (ff + eps), rtol=1e-12)
+
+
+def test_rewrite_same_pair_is_nearly_idempotent():
+    rng = np.random.default_rng(6)
+    k, d, nu, eps = 16, 9, 3, 1e-6
+    P = 2 * k * nu
+    key = rng.standard_normal(k); val = rng.standard_normal(d)
+    A1, z1 = O.delta_rule_update(np.zeros((d, P)), np.zeros(P), key[None], val[None], np.ones(1), nu, eps)
+    A2, z2 = O.delta_rule_update(A1, z1, key[None], val[None], np.ones(1), nu, eps)
+    phi = _dpfp_loops(list(key), nu)
+    ff = phi @ phi
+    # second write only adds the eps-sized residue (v - vbar) ~ v * eps / ff
+    assert np.max(np.abs(A2 - A1)) <= np.max(np.abs(val)) * eps / ff * np.max(phi) * 2
+    assert np.max(np.abs(z2 - z1)) <= eps / ff * np.max(phi) * 2
+
+
+def test_assoc_read_empty_memory_is_exact_zero():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((5, 6)); wq = rng.standard_normal((4, 6))
+    np.testing.assert_array_equal(O.assoc_read(x, wq, np.zeros((6, 24)), np.zeros(24), 3, 1e-6), x)
+
+
+# -------------------------------------------------------- whole model ----
+
+def _tiny(**over):
+    return dataclasses.replace(I.TINY, **over)
+
+
+@pytest.mark.parametrize("over,n_seg", [({}, 4), ({"n_q_heads": 4, "n_kv_heads": 2, "head_dim": 16}, 3),
+                                         ({"n_layers": 3}, 5), ({"n_layers": 4}, 2)])
+def test_diag_order_equals_seq_order_bitwise(over, n_seg):
+    cfg = _tiny(**over)
+    W = I.make_weights(cfg, seed=11, norm_jitter=0.1)
+    tok = I.make_tokens(cfg, n_seg, seed=11)
+    a = O.forward(cfg, W, tok, n_seg, order="seq")
+    b = O.forward(cfg, W, tok, n_seg, order="diag")
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_schedule_covers_grid_in_dependency_order():
+    for L, n in ((1, 1), (2, 4), (16, 8), (5, 3)):
+        steps = O.schedule(L, n, "diag")
+        assert len(steps) == L + n - 1
+        seen = {}
+        for i, step in enumerate(steps):
+            assert 1 <= len(step) <= min(L, n)
+            for (l, s) in step:
+                assert (l, s) not in seen
+                seen[(l, s)] = i
+        assert len(seen) == L * n
+        for (l, s), i in seen.items():
+            if l > 0:
+                assert seen[(l - 1, s)] < i
+            if s > 0:
+                assert seen[(l, s - 1)] < i
+
+
+@pytest.mark.parametrize("over", [{}, {"n_q_heads": 4, "n_kv_heads": 2, "head_dim": 16}])
+def test_one_segment_empty_memory_equals_plain_transformer(over):
+    cfg = _tiny(**over)
+    W = I.make_weights(cfg, seed=12, norm_jitter=0.1)
+    tok = I.make_tokens(cfg, 1, seed=12)
+    out, _, _ = O.forward(cfg, W, tok, 1)
+    S = cfg.seg_len
+    X = np.concatenate([W["embed"][tok], W["mem"]]).astype(np.float64)
+    ref = plain_stack(X, W, cfg)
+    np.testing.assert_allclose(out, ref[:S], rtol=1e-10, atol=1e-12)
+    # causality: memory rows come after the segment, so the segment rows are
+    # also the plain transformer over the S segment tokens alone
+    ref_s = plain_stack(X[:S], W, cfg)
+    np.testing.assert_allclose(out, ref_s, rtol=1e-10, atol=1e-12)
+
+
+def test_two_segments_one_layer_hand_expansion():
+    cfg = _tiny(n_layers=1)
+    W = I.make_weights(cfg, seed=13, norm_jitter=0.1)
+    tok = I.make_tokens(cfg, 2, seed=13)
+    out, A, z = O.forward(cfg, W, tok, 2)
+    S, k, nu, eps = cfg.seg_len, cfg.key_dim, cfg.dpfp_nu, cfg.assoc_eps
+    W64 = {kk: np.asarray(v, np.float64) for kk, v in W.items()}
+    gf = W64["norm_f"]
+
+    def write(Hm, A, z):
+        # loops over memory rows and entries, written out
+        P = A.shape[1]
+        dA = np.zeros_like(A); dz = np.zeros(P)
+        for i in range(Hm.shape[0]):
+            key = W64["a_wk"][0] @ Hm[i]; val = W64["a_wv"][0] @ Hm[i]
+            beta = 1.0 / (1.0 + math.exp(-(W64["a_wbeta"][0] @ Hm[i])))
+            phi = _dpfp_loops(list(key), nu)
+            zp = float(z @ phi)
+            vbar = (A @ phi) / (zp + eps)
+            gamma = 1.0 - zp / (float(phi @ phi) + eps)
+            dA += beta * np.outer(val - vbar, phi)
+            dz += gamma * phi
+        return A + dA, z + dz
+
+    P = cfg.phi_dim
+    X0 = np.concatenate([W64["embed"][tok[:S]], W64["mem"]])
+    H0 = plain_layer(X0, W64, 0, cfg)
+    A1, z1 = write(H0[S:], np.zeros((cfg.d_model, P)), np.zeros(P))
+    X1 = np.concatenate([W64["embed"][tok[S:]], W64["mem"]])
+    for t in range(X1.shape[0]):
+        phi = _dpfp_loops(list(W64["a_wq"][0] @ X1[t]), nu)
+        X1[t] = X1[t] + (A1 @ phi) / (float(z1 @ phi) + eps)
+    H1 = plain_layer(X1, W64, 0, cfg)
+    A2, z2 = write(H1[S:], A1, z1)
+    ms = lambda r: r / math.sqrt(float(np.mean(r * r)) + cfg.norm_eps) * gf
+    ref = np.stack([ms(r) for r in np.concatenate([H0[:S], H1[:S]])])
+    np.testing.assert_allclose(out, ref, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(A[0], A2, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(z[0], z2, rtol=1e-9, atol=1e-11)
+
+
+def test_resume_from_carried_state():
+    cfg = I.TINY
+    W = I.make_weights(cfg, seed=14)
+    tok = I.make_tokens(cfg, 4, seed=14)
+    full = O.forward(cfg, W, tok, 4)
+    S = cfg.seg_len
+    h1, A1, z1 = O.forward(cfg, W, tok[:2 * S], 2)
+    h2, A2, z2 = O.forward(cfg, W, tok[2 * S:], 2, A0=A1, z0=z1)
+    np.testing.assert_array_equal(np.concatenate([h1, h2]), full[0])
+    np.testing.assert_array_equal(A2, full[1])
+    np.testing.assert_array_equal(z2, full[2])
+
+
+def test_tiny_workload_is_well_conditioned():
+    cfg, n, W, tok = I.make_workload("tiny")
+    out, A, z = O.forward(cfg, W, tok, n)
+    assert np.isfinite(out).all() and np.isfinite(A).all() and np.isfinite(z).all()
+    # the memory was actually written and read: later segments differ from a
+    # run whose memory is reset at every segment
+    S = cfg.seg_len
+    alone = np.concatenate([O.forward(cfg, W, tok[s * S:(s + 1) * S], 1)[0] for s in range(n)])
+    np.testing.assert_array_equal(out[:S], alone[:S])
+    assert np.max(np.abs(out[S:] - alone[S:])) > 1e-3
