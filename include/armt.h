@@ -51,6 +51,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define ARMT_API __attribute__((visibility("default")))
+#else
+#define ARMT_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -129,12 +135,12 @@ typedef struct armt_model armt_model;  /* opaque */
  * projection) and allocates the activation workspace for every layer.  The
  * copies are enqueued on `stream` and finished before return (synchronous).
  * On success *out owns all of it until armt_destroy. */
-armt_status armt_create(const armt_config* cfg, const armt_weights* w, void* stream,
+ARMT_API armt_status armt_create(const armt_config* cfg, const armt_weights* w, void* stream,
                         armt_model** out);
 
 /* Releases everything armt_create allocated (synchronises the device first).
  * NULL is accepted. */
-armt_status armt_destroy(armt_model* m);
+ARMT_API armt_status armt_destroy(armt_model* m);
 
 /* ARMT forward over n_segments * S tokens with the diagonal schedule
  * (section 二): for i = 0 .. L + n_segments - 2 one grouped step runs every
@@ -150,14 +156,14 @@ armt_status armt_destroy(armt_model* m);
  *               the state to resume from (e.g. a previous call's result).
  * Caller owns all buffers; they must not alias each other.  Results are
  * bit-identical to armt_forward_sequential on the same inputs. */
-armt_status armt_forward(armt_model* m, const int32_t* tokens, int64_t n_segments,
+ARMT_API armt_status armt_forward(armt_model* m, const int32_t* tokens, int64_t n_segments,
                          float* hidden_out, float* mem_A, float* mem_z, int32_t mem_in_valid,
                          void* stream);
 
 /* Same arguments and results; cells run one per step, segment by segment and
  * layer by layer (the schedule the diagonal one reorders), through the same
  * kernels.  For checking and as the speed-up denominator. */
-armt_status armt_forward_sequential(armt_model* m, const int32_t* tokens, int64_t n_segments,
+ARMT_API armt_status armt_forward_sequential(armt_model* m, const int32_t* tokens, int64_t n_segments,
                                     float* hidden_out, float* mem_A, float* mem_z,
                                     int32_t mem_in_valid, void* stream);
 
@@ -165,7 +171,7 @@ armt_status armt_forward_sequential(armt_model* m, const int32_t* tokens, int64_
  * (and the state when mem_in_valid) to the device, runs `schedule`, copies
  * hidden states and state back, and synchronises `stream` before returning.
  * Device staging buffers are owned by the model and grow on demand. */
-armt_status armt_forward_host(armt_model* m, const int32_t* h_tokens, int64_t n_segments,
+ARMT_API armt_status armt_forward_host(armt_model* m, const int32_t* h_tokens, int64_t n_segments,
                               float* h_hidden_out, float* h_mem_A, float* h_mem_z,
                               int32_t mem_in_valid, int32_t schedule, void* stream);
 
@@ -176,14 +182,14 @@ armt_status armt_forward_host(armt_model* m, const int32_t* h_tokens, int64_t n_
  *   C device fp32 [G, M, N].  fp32 accumulation on tcgen05 tensor cores.
  * Requires K % 64 == 0, N % 256 == 0, 16-byte aligned base pointers, any
  * M >= 1.  A fixed reduction order per element independent of G. */
-armt_status armt_grouped_gemm_bf16(const void* A, const void* B, float* C, int32_t G, int32_t M,
+ARMT_API armt_status armt_grouped_gemm_bf16(const void* A, const void* B, float* C, int32_t G, int32_t M,
                                    int32_t N, int32_t K, void* stream);
 
 /* Sizes of the memory state buffers for this model (elements). */
-armt_status armt_state_sizes(const armt_model* m, int64_t* a_elems, int64_t* z_elems);
+ARMT_API armt_status armt_state_sizes(const armt_model* m, int64_t* a_elems, int64_t* z_elems);
 
 /* Number of kernel launches one forward of n_segments makes with `schedule`. */
-armt_status armt_launch_count(const armt_model* m, int64_t n_segments, int32_t schedule,
+ARMT_API armt_status armt_launch_count(const armt_model* m, int64_t n_segments, int32_t schedule,
                               int64_t* launches);
 
 /* Per-kernel timing with CUDA events recorded on the launch stream around
@@ -195,18 +201,18 @@ typedef enum armt_kernel_class {
   ARMT_KC_ATTENTION = 4, ARMT_KC_ASSOC_READ = 5, ARMT_KC_ASSOC_WRITE = 6, ARMT_KC_NORM = 7,
   ARMT_KC_OTHER = 8, ARMT_KC_COUNT = 9
 } armt_kernel_class;
-armt_status armt_set_profiling(armt_model* m, int32_t enable);
-armt_status armt_kernel_times(armt_model* m, int64_t* launches, double* ms, int32_t n_classes);
+ARMT_API armt_status armt_set_profiling(armt_model* m, int32_t enable);
+ARMT_API armt_status armt_kernel_times(armt_model* m, int64_t* launches, double* ms, int32_t n_classes);
 
 /* Waits for `stream` and reports a device-side error recorded since the last
  * call (ARMT_ERR_TIMEOUT when a bounded wait gave up), then clears it. */
-armt_status armt_sync_status(armt_model* m, void* stream);
+ARMT_API armt_status armt_sync_status(armt_model* m, void* stream);
 
 /* Static description of a status code; never NULL. */
-const char* armt_status_string(armt_status s);
+ARMT_API const char* armt_status_string(armt_status s);
 
 /* Thread-local detail of the last error returned on this thread ("" if none). */
-const char* armt_last_error(void);
+ARMT_API const char* armt_last_error(void);
 
 #ifdef __cplusplus
 }

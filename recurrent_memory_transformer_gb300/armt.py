@@ -1,0 +1,240 @@
+"""ctypes binding of libarmt.so (include/armt.h), same entry-point names.
+
+Argument marshalling only: every step of the forward pass runs in the
+library's CUDA kernels.  PyTorch is used for device memory and streams.  If
+the library has not been built, importing the binding raises; there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+import numpy as np
+
+from . import inputs as _inputs
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libarmt.so")
+
+ARMT_OK = 0
+STATUS_NAMES = {0: "ARMT_OK", 1: "ARMT_ERR_ARG", 2: "ARMT_ERR_SHAPE", 3: "ARMT_ERR_UNSUPPORTED",
+                4: "ARMT_ERR_OOM", 5: "ARMT_ERR_CUDA", 6: "ARMT_ERR_TIMEOUT", 7: "ARMT_ERR_NO_DEVICE"}
+ARMT_F32, ARMT_BF16 = 0, 1
+SCHEDULE_DIAGONAL, SCHEDULE_SEQUENTIAL = 0, 1
+KERNEL_CLASSES = ("gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down", "attention", "assoc_read",
+                  "assoc_write", "norm", "other")
+
+EXPORTED = ("armt_create", "armt_destroy", "armt_forward", "armt_forward_sequential",
+            "armt_forward_host", "armt_grouped_gemm_bf16", "armt_state_sizes", "armt_launch_count",
+            "armt_set_profiling", "armt_kernel_times", "armt_sync_status", "armt_status_string",
+            "armt_last_error")
+
+
+class ArmtError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {detail}")
+
+
+class armt_config(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("d_model", ctypes.c_int32),
+                ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("ffn_dim", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("seg_len", ctypes.c_int32),
+                ("n_mem", ctypes.c_int32), ("key_dim", ctypes.c_int32),
+                ("dpfp_nu", ctypes.c_int32), ("norm_eps", ctypes.c_float),
+                ("assoc_eps", ctypes.c_float), ("rope_base", ctypes.c_double),
+                ("dtype", ctypes.c_int32)]
+
+
+_WKEYS = ("embed", "mem", "wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "a_wq", "a_wk",
+          "a_wv", "a_wbeta", "norm1", "norm2", "norm_f")
+
+
+class armt_weights(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_void_p) for k in _WKEYS] + [("on_device", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libarmt.so; raises FileNotFoundError when it was not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise FileNotFoundError(f"{path} not built: run python -m recurrent_memory_transformer_gb300.build")
+    lib = ctypes.CDLL(path)
+    P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    S = ctypes.c_int
+    lib.armt_create.argtypes = [ctypes.POINTER(armt_config), ctypes.POINTER(armt_weights), P,
+                                ctypes.POINTER(P)]
+    lib.armt_destroy.argtypes = [P]
+    for fn in (lib.armt_forward, lib.armt_forward_sequential):
+        fn.argtypes = [P, P, I64, P, P, P, I32, P]
+    lib.armt_forward_host.argtypes = [P, P, I64, P, P, P, I32, I32, P]
+    lib.armt_grouped_gemm_bf16.argtypes = [P, P, P, I32, I32, I32, I32, P]
+    lib.armt_state_sizes.argtypes = [P, ctypes.POINTER(I64), ctypes.POINTER(I64)]
+    lib.armt_launch_count.argtypes = [P, I64, I32, ctypes.POINTER(I64)]
+    lib.armt_set_profiling.argtypes = [P, I32]
+    lib.armt_kernel_times.argtypes = [P, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double), I32]
+    lib.armt_sync_status.argtypes = [P, P]
+    for name in EXPORTED:
+        getattr(lib, name).restype = S
+    lib.armt_status_string.restype = ctypes.c_char_p
+    lib.armt_status_string.argtypes = [S]
+    lib.armt_last_error.restype = ctypes.c_char_p
+    lib.armt_last_error.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != ARMT_OK:
+        detail = _lib.armt_last_error().decode(errors="replace")
+        raise ArmtError(status, where, detail)
+
+
+def make_config(cfg: "_inputs.ArmtConfig") -> armt_config:
+    return armt_config(cfg.n_layers, cfg.d_model, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim,
+                       cfg.ffn_dim, cfg.vocab, cfg.seg_len, cfg.n_mem, cfg.key_dim, cfg.dpfp_nu,
+                       cfg.norm_eps, cfg.assoc_eps, cfg.rope_base,
+                       ARMT_BF16 if cfg.dtype == "bf16" else ARMT_F32)
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _ptr(t) -> int:
+    return t.data_ptr()
+
+
+def host_weight_arrays(cfg, weights: Dict[str, np.ndarray]) -> Dict[str, np.ndarray]:
+    """Contiguous host arrays in the model's element type (fp32, or bf16 bits as uint16)."""
+    out = {}
+    for k in _WKEYS:
+        a = np.ascontiguousarray(weights[k], dtype=np.float32)
+        out[k] = _inputs.bf16_bits(a) if cfg.dtype == "bf16" else a
+    return out
+
+
+def device_weight_tensors(cfg, weights: Dict[str, np.ndarray], device="cuda"):
+    """Device tensors in the model's element type (exact: inputs are bf16-representable)."""
+    import torch
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    return {k: torch.from_numpy(np.ascontiguousarray(weights[k], dtype=np.float32)).to(device).to(dt)
+            for k in _WKEYS}
+
+
+class Model:
+    """Owns one armt_model; wraps the forward entry points."""
+
+    def __init__(self, cfg, weights, stream=None):
+        """`weights`: dict of numpy arrays (host path) or torch tensors on the device."""
+        lib = load_library()
+        self.cfg = cfg
+        self._c = make_config(cfg)
+        w = armt_weights()
+        keep = []
+        first = weights["embed"]
+        on_device = hasattr(first, "is_cuda") and first.is_cuda
+        if on_device:
+            for k in _WKEYS:
+                t = weights[k].contiguous()
+                keep.append(t)
+                setattr(w, k, t.data_ptr())
+        else:
+            arrs = host_weight_arrays(cfg, weights)
+            for k in _WKEYS:
+                keep.append(arrs[k])
+                setattr(w, k, arrs[k].ctypes.data)
+        w.on_device = 1 if on_device else 0
+        h = ctypes.c_void_p()
+        _check(lib.armt_create(ctypes.byref(self._c), ctypes.byref(w), _stream_ptr(stream),
+                               ctypes.byref(h)), "armt_create")
+        self._h = h
+        a, z = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib.armt_state_sizes(h, ctypes.byref(a), ctypes.byref(z)), "armt_state_sizes")
+        self.a_elems, self.z_elems = a.value, z.value
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _check(_lib.armt_destroy(self._h), "armt_destroy")
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def armt_forward(self, tokens, n_segments, hidden_out, mem_A, mem_z, mem_in_valid=0,
+                     stream=None, schedule=SCHEDULE_DIAGONAL):
+        fn = _lib.armt_forward if schedule == SCHEDULE_DIAGONAL else _lib.armt_forward_sequential
+        _check(fn(self._h, _ptr(tokens), int(n_segments), _ptr(hidden_out), _ptr(mem_A),
+                  _ptr(mem_z), int(mem_in_valid), _stream_ptr(stream)),
+               "armt_forward" if schedule == SCHEDULE_DIAGONAL else "armt_forward_sequential")
+
+    def armt_forward_sequential(self, tokens, n_segments, hidden_out, mem_A, mem_z, mem_in_valid=0,
+                                stream=None):
+        self.armt_forward(tokens, n_segments, hidden_out, mem_A, mem_z, mem_in_valid, stream,
+                          SCHEDULE_SEQUENTIAL)
+
+    def armt_forward_host(self, tokens: np.ndarray, n_segments, hidden_out: np.ndarray,
+                          mem_A: np.ndarray, mem_z: np.ndarray, mem_in_valid=0,
+                          schedule=SCHEDULE_DIAGONAL, stream=None):
+        """Host-buffer forward (numpy arrays or pinned CPU tensors); synchronous."""
+        def hp(x):
+            return x.data_ptr() if hasattr(x, "data_ptr") else x.ctypes.data
+        _check(_lib.armt_forward_host(self._h, hp(tokens), int(n_segments), hp(hidden_out),
+                                      hp(mem_A), hp(mem_z), int(mem_in_valid), int(schedule),
+                                      _stream_ptr(stream)), "armt_forward_host")
+
+    def forward(self, tokens, n_segments, schedule=SCHEDULE_DIAGONAL, mem_A=None, mem_z=None,
+                stream=None):
+        """Allocates outputs with torch and runs one forward; returns (hidden, A, z)."""
+        import torch
+        dev = tokens.device
+        hidden = torch.empty((n_segments * self.cfg.seg_len, self.cfg.d_model), dtype=torch.float32,
+                             device=dev)
+        valid = mem_A is not None
+        A = mem_A.clone() if valid else torch.empty(self.a_elems, dtype=torch.float32, device=dev)
+        z = mem_z.clone() if valid else torch.empty(self.z_elems, dtype=torch.float32, device=dev)
+        self.armt_forward(tokens, n_segments, hidden, A, z, 1 if valid else 0, stream, schedule)
+        L, d, P = self.cfg.n_layers, self.cfg.d_model, self.cfg.phi_dim
+        return hidden, A.view(L, d, P), z.view(L, P)
+
+    def armt_launch_count(self, n_segments, schedule=SCHEDULE_DIAGONAL) -> int:
+        n = ctypes.c_int64()
+        _check(_lib.armt_launch_count(self._h, int(n_segments), int(schedule), ctypes.byref(n)),
+               "armt_launch_count")
+        return n.value
+
+    def armt_set_profiling(self, enable: bool):
+        _check(_lib.armt_set_profiling(self._h, 1 if enable else 0), "armt_set_profiling")
+
+    def armt_kernel_times(self):
+        n = len(KERNEL_CLASSES)
+        launches = (ctypes.c_int64 * n)()
+        ms = (ctypes.c_double * n)()
+        _check(_lib.armt_kernel_times(self._h, launches, ms, n), "armt_kernel_times")
+        return {KERNEL_CLASSES[i]: (launches[i], ms[i]) for i in range(n)}
+
+    def armt_sync_status(self, stream=None):
+        _check(_lib.armt_sync_status(self._h, _stream_ptr(stream)), "armt_sync_status")
+
+
+def armt_grouped_gemm_bf16(A, B, C, stream=None):
+    """C[g] = A[g] @ B[g]^T: A bf16 [G,M,K], B bf16 [G,N,K], C fp32 [G,M,N] (torch, cuda)."""
+    lib = load_library()
+    G, M, K = A.shape
+    N = B.shape[1]
+    _check(lib.armt_grouped_gemm_bf16(_ptr(A), _ptr(B), _ptr(C), G, M, N, K, _stream_ptr(stream)),
+           "armt_grouped_gemm_bf16")

@@ -1,0 +1,781 @@
+// C ABI, model state and the two cell schedules of the ARMT forward pass.
+//
+// Summary page of "Diagonal Batching Unlocks Parallelism in Recurrent Memory
+// Transformers for Long Contexts":
+//   section 二  cell (l, s) depends on (l-1, s) and (l, s-1) only, so every
+//             cell with l + s = i runs in grouped step i (n_layers +
+//             n_segments - 1 steps in all);
+//   section 三  all layers become one grouped layer: stacked weights,
+//             grouped matrix products with one preallocated output tensor
+//             addressed per group, stacked norm gains, the rest batched.
+// The cells of step i are the contiguous layer range
+//   [max(0, i - n + 1), min(L - 1, i)],
+// so every kernel of a step takes (first layer, layer count) and indexes all
+// per-layer tensors -- weights, activations, memory -- by layer.  Buffers are
+// per layer: layer l's input slot X[l] is written by cell (l-1, s+1) in the
+// same step in which cell (l, s) reads it, but every read of X[l] in a step
+// (associative query and read) is enqueued before the down projection that
+// overwrites it, so one slot per layer suffices.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/armt.h"
+#include "common.cuh"
+#include "epilogues.cuh"
+#include "gemm_tc.cuh"
+#include "kernels.cuh"
+
+using namespace armt;
+
+// ----------------------------------------------------------- errors --
+
+static thread_local std::string g_last_error;
+
+static armt_status fail(armt_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+#define CK(call)                                                                          \
+  do {                                                                                    \
+    cudaError_t e_ = (call);                                                              \
+    if (e_ != cudaSuccess) {                                                              \
+      return fail(e_ == cudaErrorMemoryAllocation ? ARMT_ERR_OOM : ARMT_ERR_CUDA,         \
+                  std::string(#call) + ": " + cudaGetErrorString(e_));                    \
+    }                                                                                     \
+  } while (0)
+
+#define CKS(expr)                   \
+  do {                              \
+    armt_status s_ = (expr);        \
+    if (s_ != ARMT_OK) return s_;   \
+  } while (0)
+
+// --------------------------------------------------------- TMA maps --
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+namespace armt {
+bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int K, int rows, int layers,
+                         int box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (K * 2) % 16 != 0) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)layers};
+  cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)K * 2 * (cuuint64_t)rows};
+  cuuint32_t box[3] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+}  // namespace armt
+
+// ------------------------------------------------------- allocation --
+
+static long long alloc_cap_bytes() {
+  const char* s = getenv("ARMT_ALLOC_CAP_BYTES");  // test hook: simulated device memory limit
+  return s ? atoll(s) : -1;
+}
+
+struct DevAllocs {
+  std::vector<void*> ptrs;
+  long long total = 0;
+  armt_status alloc(void** p, size_t bytes) {
+    const long long cap = alloc_cap_bytes();
+    if (cap >= 0 && total + (long long)bytes > cap)
+      return fail(ARMT_ERR_OOM, "allocation cap exceeded (" + std::to_string(total + bytes) +
+                                    " > " + std::to_string(cap) + " bytes)");
+    cudaError_t e = cudaMalloc(p, bytes < 256 ? 256 : bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(ARMT_ERR_OOM, std::string("cudaMalloc: ") + cudaGetErrorString(e));
+    }
+    ptrs.push_back(*p);
+    total += (long long)bytes;
+    return ARMT_OK;
+  }
+  template <typename T>
+  armt_status alloc_n(T** p, size_t n) {
+    return alloc(reinterpret_cast<void**>(p), n * sizeof(T));
+  }
+  void free_all() {
+    for (void* p : ptrs) cudaFree(p);
+    ptrs.clear();
+    total = 0;
+  }
+};
+
+template <typename T>
+__global__ void to_f32_kernel(const T* __restrict__ src, float* __restrict__ dst, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    dst[i] = ld_as_f32(src + i);
+}
+
+// ------------------------------------------------------------ model --
+
+struct ModelBase {
+  armt_config cfg{};
+  int device = 0, num_sms = 148;
+  DevAllocs mem;
+  int* d_err = nullptr;
+  // profiling
+  bool profiling = false;
+  std::vector<cudaEvent_t> ev_start, ev_stop;
+  std::vector<int> ev_class;
+  size_t ev_used = 0;
+  // host-buffer staging (armt_forward_host)
+  int32_t* st_tokens = nullptr;
+  float *st_hidden = nullptr, *st_A = nullptr, *st_z = nullptr;
+  size_t st_tokens_n = 0, st_hidden_n = 0;
+
+  virtual ~ModelBase() {
+    for (cudaEvent_t e : ev_start) cudaEventDestroy(e);
+    for (cudaEvent_t e : ev_stop) cudaEventDestroy(e);
+    if (st_tokens) cudaFree(st_tokens);
+    if (st_hidden) cudaFree(st_hidden);
+    if (st_A) cudaFree(st_A);
+    if (st_z) cudaFree(st_z);
+    mem.free_all();
+  }
+  virtual armt_status create(const armt_weights* w, cudaStream_t st) = 0;
+  virtual armt_status forward(const int32_t* tokens, int64_t n, float* hidden, float* A, float* z,
+                              int mem_in_valid, int schedule, cudaStream_t st) = 0;
+
+  int rows() const { return cfg.seg_len + cfg.n_mem; }
+  int phi_dim() const { return 2 * cfg.key_dim * cfg.dpfp_nu; }
+  int n_qkv() const { return (cfg.n_q_heads + 2 * cfg.n_kv_heads) * cfg.head_dim; }
+
+  // Kernel launches of one step covering layers [lo, hi].
+  int64_t step_launches(int lo, int hi) const {
+    const int per_gemm = cfg.dtype == ARMT_BF16 ? 1 : 2;
+    int64_t n = 0;
+    if (lo == 0) n += 1;                    // layer-0 input gather
+    n += per_gemm + 1 + per_gemm;           // associative query GEMM, phi, read GEMM
+    n += 1 + per_gemm + 1 + per_gemm;       // norm1, QKV GEMM, attention, O GEMM
+    n += 1 + per_gemm + per_gemm;           // norm2, gate-up GEMM, down GEMM
+    n += 3;                                 // delta-rule write
+    if (hi == cfg.n_layers - 1) n += 1;     // final norm
+    return n;
+  }
+  int64_t launches(int64_t n_seg, int schedule, int mem_in_valid) const {
+    const int L = cfg.n_layers;
+    int64_t total = (mem_in_valid && cfg.dtype == ARMT_BF16) ? 1 : 0;  // state copy
+    if (schedule == ARMT_SCHEDULE_DIAGONAL) {
+      for (int64_t i = 0; i < L + n_seg - 1; ++i) {
+        const int lo = (int)(i - n_seg + 1 > 0 ? i - n_seg + 1 : 0);
+        const int hi = (int)(i < L - 1 ? i : L - 1);
+        total += step_launches(lo, hi);
+      }
+    } else {
+      for (int64_t s = 0; s < n_seg; ++s)
+        for (int l = 0; l < L; ++l) total += step_launches(l, l);
+    }
+    return total;
+  }
+
+  // Event pair around one launch when profiling.
+  armt_status prof_begin(int cls, cudaStream_t st) {
+    if (!profiling) return ARMT_OK;
+    if (ev_used == ev_start.size()) {
+      cudaEvent_t a, b;
+      CK(cudaEventCreate(&a));
+      CK(cudaEventCreate(&b));
+      ev_start.push_back(a);
+      ev_stop.push_back(b);
+      ev_class.push_back(cls);
+    }
+    ev_class[ev_used] = cls;
+    CK(cudaEventRecord(ev_start[ev_used], st));
+    return ARMT_OK;
+  }
+  armt_status prof_end(cudaStream_t st) {
+    if (!profiling) return ARMT_OK;
+    CK(cudaEventRecord(ev_stop[ev_used], st));
+    ++ev_used;
+    return ARMT_OK;
+  }
+};
+
+struct armt_model {
+  ModelBase* impl;
+};
+
+template <typename WT>
+struct Model : ModelBase {
+  static constexpr bool kTC = sizeof(WT) == 2;  // bf16: tensor-core GEMMs
+  typedef WT AT;                               // activation dtype of GEMM operands
+
+  // weights (library layout)
+  WT *embed = nullptr, *memtok = nullptr, *Wqkv = nullptr, *Wo = nullptr, *Wgu = nullptr,
+     *Wd = nullptr, *aWq = nullptr, *aWk = nullptr, *aWv = nullptr, *aWb = nullptr;
+  float *g1 = nullptr, *g2 = nullptr, *gf = nullptr, *cosT = nullptr, *sinT = nullptr;
+  // activations, all [layer or slot][rows][width]
+  float *X = nullptr, *Res = nullptr, *Qa = nullptr, *Den = nullptr, *KB = nullptr,
+        *PhiM = nullptr, *Coef = nullptr, *Cscr = nullptr;
+  AT *Xa = nullptr, *Nrm = nullptr, *QKV = nullptr, *Att = nullptr, *U = nullptr, *Phi = nullptr,
+     *Aa = nullptr;
+  int nmax = 0;  // widest GEMM output (fp32 scratch row stride)
+  // tensor maps (bf16 path)
+  CUtensorMap tmXa, tmAWq, tmPhi, tmAa, tmNrm, tmWqkv, tmAtt, tmWo, tmWgu, tmU, tmWd;
+  size_t upd_smem = 0, feat_smem = 0, attn_smem = 0;
+  int upd_rows_per_block = 64;
+
+  armt_status copy_in(void* dst, const void* src, size_t bytes, cudaStream_t st) {
+    CK(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, st));
+    return ARMT_OK;
+  }
+
+  armt_status gain_to_f32(float** dst, const void* src, size_t n, cudaStream_t st) {
+    CKS(mem.alloc_n(dst, n));
+    WT* tmp = nullptr;
+    CK(cudaMalloc(&tmp, n * sizeof(WT)));
+    cudaError_t e = cudaMemcpyAsync(tmp, src, n * sizeof(WT), cudaMemcpyDefault, st);
+    if (e == cudaSuccess) {
+      to_f32_kernel<WT><<<64, 256, 0, st>>>(tmp, *dst, (long long)n);
+      e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    cudaFree(tmp);
+    if (e != cudaSuccess) return fail(ARMT_ERR_CUDA, std::string("gain copy: ") + cudaGetErrorString(e));
+    return ARMT_OK;
+  }
+
+  armt_status create(const armt_weights* w, cudaStream_t st) override {
+    const armt_config& c = cfg;
+    const size_t L = c.n_layers, d = c.d_model, hd = c.head_dim, F = c.ffn_dim, T = rows();
+    const size_t Hq = c.n_q_heads, Hkv = c.n_kv_heads, k = c.key_dim, P = phi_dim();
+    const size_t Nq = n_qkv(), es = sizeof(WT);
+    // weights
+    CKS(mem.alloc_n(&embed, (size_t)c.vocab * d));
+    CKS(copy_in(embed, w->embed, (size_t)c.vocab * d * es, st));
+    CKS(mem.alloc_n(&memtok, (size_t)c.n_mem * d));
+    CKS(copy_in(memtok, w->mem, (size_t)c.n_mem * d * es, st));
+    CKS(mem.alloc_n(&Wqkv, L * Nq * d));
+    // fused rows: per layer [wq; wk; wv]
+    CK(cudaMemcpy2DAsync(Wqkv, Nq * d * es, w->wq, Hq * hd * d * es, Hq * hd * d * es, L,
+                         cudaMemcpyDefault, st));
+    CK(cudaMemcpy2DAsync(Wqkv + Hq * hd * d, Nq * d * es, w->wk, Hkv * hd * d * es,
+                         Hkv * hd * d * es, L, cudaMemcpyDefault, st));
+    CK(cudaMemcpy2DAsync(Wqkv + (Hq + Hkv) * hd * d, Nq * d * es, w->wv, Hkv * hd * d * es,
+                         Hkv * hd * d * es, L, cudaMemcpyDefault, st));
+    CKS(mem.alloc_n(&Wo, L * d * Hq * hd));
+    CKS(copy_in(Wo, w->wo, L * d * Hq * hd * es, st));
+    // gate/up interleaved in blocks of GU_BLK rows
+    CKS(mem.alloc_n(&Wgu, L * 2 * F * d));
+    const size_t blk = (size_t)GU_BLK * d * es, nblk = L * F / GU_BLK;
+    CK(cudaMemcpy2DAsync(Wgu, 2 * blk, w->w_gate, blk, blk, nblk, cudaMemcpyDefault, st));
+    CK(cudaMemcpy2DAsync(reinterpret_cast<char*>(Wgu) + blk, 2 * blk, w->w_up, blk, blk, nblk,
+                         cudaMemcpyDefault, st));
+    CKS(mem.alloc_n(&Wd, L * d * F));
+    CKS(copy_in(Wd, w->w_down, L * d * F * es, st));
+    CKS(mem.alloc_n(&aWq, L * k * d));
+    CKS(copy_in(aWq, w->a_wq, L * k * d * es, st));
+    CKS(mem.alloc_n(&aWk, L * k * d));
+    CKS(copy_in(aWk, w->a_wk, L * k * d * es, st));
+    CKS(mem.alloc_n(&aWv, L * d * d));
+    CKS(copy_in(aWv, w->a_wv, L * d * d * es, st));
+    CKS(mem.alloc_n(&aWb, L * d));
+    CKS(copy_in(aWb, w->a_wbeta, L * d * es, st));
+    CKS(gain_to_f32(&g1, w->norm1, L * d, st));
+    CKS(gain_to_f32(&g2, w->norm2, L * d, st));
+    CKS(gain_to_f32(&gf, w->norm_f, d, st));
+    // RoPE tables (double precision on the host, stored fp32)
+    {
+      std::vector<float> hc(T * (hd / 2)), hs(T * (hd / 2));
+      for (size_t t = 0; t < T; ++t)
+        for (size_t i = 0; i < hd / 2; ++i) {
+          const double ang = (double)t * std::pow(c.rope_base, -2.0 * (double)i / (double)hd);
+          hc[t * (hd / 2) + i] = (float)std::cos(ang);
+          hs[t * (hd / 2) + i] = (float)std::sin(ang);
+        }
+      CKS(mem.alloc_n(&cosT, hc.size()));
+      CKS(mem.alloc_n(&sinT, hs.size()));
+      CK(cudaMemcpy(cosT, hc.data(), hc.size() * 4, cudaMemcpyHostToDevice));
+      CK(cudaMemcpy(sinT, hs.data(), hs.size() * 4, cudaMemcpyHostToDevice));
+    }
+    // activations
+    CKS(mem.alloc_n(&X, (L + 1) * T * d));
+    if (kTC) {
+      CKS(mem.alloc_n(&Xa, (L + 1) * T * d));
+    } else {
+      Xa = reinterpret_cast<AT*>(X);
+    }
+    CKS(mem.alloc_n(&Res, L * T * d));
+    CKS(mem.alloc_n(&Nrm, L * T * d));
+    CKS(mem.alloc_n(&QKV, L * T * Nq));
+    CKS(mem.alloc_n(&Att, L * T * Hq * hd));
+    CKS(mem.alloc_n(&U, L * T * F));
+    CKS(mem.alloc_n(&Qa, L * T * k));
+    CKS(mem.alloc_n(&Phi, L * T * P));
+    CKS(mem.alloc_n(&Den, L * T));
+    CKS(mem.alloc_n(&KB, L * c.n_mem * (k + 1)));
+    CKS(mem.alloc_n(&PhiM, L * c.n_mem * P));
+    CKS(mem.alloc_n(&Coef, L * c.n_mem * 2));
+    if (kTC) CKS(mem.alloc_n(&Aa, L * d * P));
+    nmax = (int)std::max(std::max(Nq, d), std::max(2 * F, k));
+    if (!kTC) CKS(mem.alloc_n(&Cscr, L * T * (size_t)nmax));
+    CKS(mem.alloc_n(&d_err, 1));
+    CK(cudaMemsetAsync(d_err, 0, sizeof(int), st));
+    // kernel configuration
+    upd_smem = ((size_t)c.n_mem * d + (size_t)c.n_mem * P + 2 * c.n_mem) * sizeof(float);
+    feat_smem = ((size_t)c.n_mem * 2 * k + 2 * c.n_mem) * sizeof(float);
+    attn_smem = 2 * 64 * hd * sizeof(float);
+    if (upd_smem > 200 * 1024)
+      return fail(ARMT_ERR_UNSUPPORTED, "n_mem * (d_model + P) too large for the write kernel");
+    CK(cudaFuncSetAttribute(assoc_write_update_kernel<WT, AT>,
+                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem));
+    if (hd == 64)
+      CK(cudaFuncSetAttribute(attn_simt_kernel<AT, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)attn_smem));
+    else if (hd == 128)
+      CK(cudaFuncSetAttribute(attn_simt_kernel<AT, 128>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem));
+    if (kTC) {
+      bool ok = true;
+      ok &= encode_tmap_bf16_3d(&tmXa, Xa, (int)d, (int)T, (int)L + 1, TC_BM);
+      ok &= encode_tmap_bf16_3d(&tmAWq, aWq, (int)d, (int)k, (int)L, 64);
+      ok &= encode_tmap_bf16_3d(&tmPhi, Phi, (int)P, (int)T, (int)L, TC_BM);
+      ok &= encode_tmap_bf16_3d(&tmAa, Aa, (int)P, (int)d, (int)L, 256);
+      ok &= encode_tmap_bf16_3d(&tmNrm, Nrm, (int)d, (int)T, (int)L, TC_BM);
+      ok &= encode_tmap_bf16_3d(&tmWqkv, Wqkv, (int)d, (int)Nq, (int)L, 256);
+      ok &= encode_tmap_bf16_3d(&tmAtt, Att, (int)(Hq * hd), (int)T, (int)L, TC_BM);
+      ok &= encode_tmap_bf16_3d(&tmWo, Wo, (int)(Hq * hd), (int)d, (int)L, 256);
+      ok &= encode_tmap_bf16_3d(&tmWgu, Wgu, (int)d, (int)(2 * F), (int)L, 256);
+      ok &= encode_tmap_bf16_3d(&tmU, U, (int)F, (int)T, (int)L, TC_BM);
+      ok &= encode_tmap_bf16_3d(&tmWd, Wd, (int)F, (int)d, (int)L, 256);
+      if (!ok) return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    }
+    CK(cudaStreamSynchronize(st));
+    return ARMT_OK;
+  }
+
+  // One grouped GEMM over layers [lo, lo+g): tensor cores for bf16, SIMT +
+  // row epilogue for fp32.
+  template <int BN, class Epi>
+  armt_status gemm(int cls, const CUtensorMap& ta, const CUtensorMap& tb, const AT* a, long long a_gs,
+                   const WT* b, int N, int K, const Epi& epi, int lo, int g, cudaStream_t st) {
+    const int T = rows();
+    CKS(prof_begin(cls, st));
+    if constexpr (kTC) {
+      CK((launch_gemm_tc<Epi, BN>(ta, tb, T, N, K, lo, g, d_err, epi, num_sms, st)));
+    } else {
+      dim3 grid((N + 63) / 64, (T + 63) / 64, g);
+      gemm_simt_f32_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float*>(a), a_gs, K,
+                                                 reinterpret_cast<const float*>(b), (long long)N * K,
+                                                 Cscr, (long long)T * nmax, nmax, T, N, K, lo);
+      CK(cudaGetLastError());
+      epi_rows_kernel<Epi><<<dim3(T, g), 128, 0, st>>>(Cscr, (long long)T * nmax, nmax, N, lo, epi);
+      CK(cudaGetLastError());
+    }
+    CKS(prof_end(st));
+    return ARMT_OK;
+  }
+
+  // All kernels of one grouped step over layers [lo, hi].  seg0: segment of
+  // the layer-0 cell (when lo == 0); segL: segment of the last-layer cell
+  // (when hi == L-1).
+  armt_status step(int lo, int hi, int64_t seg0, int64_t segL, const int32_t* tokens, float* hidden,
+                   float* A, float* z, cudaStream_t st) {
+    const armt_config& c = cfg;
+    const int L = c.n_layers, d = c.d_model, hd = c.head_dim, F = c.ffn_dim, T = rows();
+    const int Hq = c.n_q_heads, Hkv = c.n_kv_heads, k = c.key_dim, P = phi_dim(), M = c.n_mem;
+    const int S = c.seg_len, Nq = n_qkv();
+    const int g = hi - lo + 1;
+    const long long Td = (long long)T * d;
+    if (lo == 0) {
+      CKS(prof_begin(ARMT_KC_OTHER, st));
+      embed_gather_kernel<WT><<<T, 256, 0, st>>>(tokens + seg0 * S, embed, memtok, X, Xa, S, d,
+                                                 c.vocab);
+      CK(cudaGetLastError());
+      CKS(prof_end(st));
+    }
+    // associative read: q = Wq_a x, phi, den, then x' = x + A phi / den
+    CKS((gemm<64>(ARMT_KC_ASSOC_READ, tmXa, tmAWq, Xa, Td, aWq, k, d,
+                  EpiStore{Qa, (long long)k, (long long)T * k}, lo, g, st)));
+    CKS(prof_begin(ARMT_KC_ASSOC_READ, st));
+    assoc_phi_kernel<AT><<<dim3(T, g), 128, 2 * k * sizeof(float), st>>>(Qa, z, Phi, Den, T, k,
+                                                                        c.dpfp_nu, c.assoc_eps, lo);
+    CK(cudaGetLastError());
+    CKS(prof_end(st));
+    const AT* Asrc = kTC ? Aa : reinterpret_cast<const AT*>(A);
+    CKS((gemm<256>(ARMT_KC_ASSOC_READ, tmPhi, tmAa, Phi, (long long)T * P,
+                   reinterpret_cast<const WT*>(Asrc), d, P, EpiAssocRead{X, Den, Res, T, d}, lo, g,
+                   st)));
+    // attention sub-layer
+    CKS(prof_begin(ARMT_KC_NORM, st));
+    rmsnorm_kernel<AT><<<dim3(T, g), 256, 0, st>>>(Res, Td, g1, d, Nrm, Td, d, c.norm_eps, lo);
+    CK(cudaGetLastError());
+    CKS(prof_end(st));
+    CKS((gemm<256>(ARMT_KC_GEMM_QKV, tmNrm, tmWqkv, Nrm, Td, Wqkv, Nq, d,
+                   EpiQkvRope<AT>{QKV, cosT, sinT, T, hd, (Hq + Hkv) * hd, Nq}, lo, g, st)));
+    CKS(prof_begin(ARMT_KC_ATTENTION, st));
+    {
+      dim3 grid((T + 63) / 64, Hq, g);
+      const float scale = 1.0f / sqrtf((float)hd);
+      if (hd == 64)
+        attn_simt_kernel<AT, 64><<<grid, 256, attn_smem, st>>>(QKV, Att, T, Hq, Hkv, scale, lo);
+      else if (hd == 128)
+        attn_simt_kernel<AT, 128><<<grid, 256, attn_smem, st>>>(QKV, Att, T, Hq, Hkv, scale, lo);
+      else
+        attn_simt_kernel<AT, 32><<<grid, 256, attn_smem, st>>>(QKV, Att, T, Hq, Hkv, scale, lo);
+      CK(cudaGetLastError());
+    }
+    CKS(prof_end(st));
+    CKS((gemm<256>(ARMT_KC_GEMM_O, tmAtt, tmWo, Att, (long long)T * Hq * hd, Wo, d, Hq * hd,
+                   EpiResidual<AT>{Res, Res, nullptr, T, d, 0}, lo, g, st)));
+    // MLP sub-layer
+    CKS(prof_begin(ARMT_KC_NORM, st));
+    rmsnorm_kernel<AT><<<dim3(T, g), 256, 0, st>>>(Res, Td, g2, d, Nrm, Td, d, c.norm_eps, lo);
+    CK(cudaGetLastError());
+    CKS(prof_end(st));
+    CKS((gemm<256>(ARMT_KC_GEMM_GATEUP, tmNrm, tmWgu, Nrm, Td, Wgu, 2 * F, d,
+                   EpiSwiGLU<AT>{U, T, F}, lo, g, st)));
+    CKS((gemm<256>(ARMT_KC_GEMM_DOWN, tmU, tmWd, U, (long long)T * F, Wd, d, F,
+                   EpiResidual<AT>{Res, X, kTC ? Xa : nullptr, T, d, 1}, lo, g, st)));
+    // delta-rule write from the memory-token rows of this layer's output
+    CKS(prof_begin(ARMT_KC_ASSOC_WRITE, st));
+    const float* Hout = X + Td;  // slot l+1 is layer l's output
+    assoc_write_proj_kernel<WT><<<dim3(k + 1, g), 256, 0, st>>>(Hout, Td, aWk, aWb, KB, S, M, d, k, lo);
+    CK(cudaGetLastError());
+    assoc_write_feat_kernel<<<g, 256, feat_smem, st>>>(KB, z, PhiM, Coef, M, k, c.dpfp_nu,
+                                                       c.assoc_eps, lo);
+    CK(cudaGetLastError());
+    {
+      dim3 grid((d + upd_rows_per_block - 1) / upd_rows_per_block, g);
+      AT* Adst = kTC ? Aa : reinterpret_cast<AT*>(A);
+      assoc_write_update_kernel<WT, AT><<<grid, 512, upd_smem, st>>>(
+          Hout, Td, aWv, PhiM, Coef, A, Adst, S, M, d, P, upd_rows_per_block, lo);
+      CK(cudaGetLastError());
+    }
+    CKS(prof_end(st));
+    if (hi == L - 1) {
+      CKS(prof_begin(ARMT_KC_NORM, st));
+      rmsnorm_kernel<float><<<dim3(S, 1), 256, 0, st>>>(X + (long long)L * Td, 0, gf, 0,
+                                                        hidden + segL * S * (long long)d, 0, d,
+                                                        c.norm_eps, 0);
+      CK(cudaGetLastError());
+      CKS(prof_end(st));
+    }
+    return ARMT_OK;
+  }
+
+  armt_status forward(const int32_t* tokens, int64_t n, float* hidden, float* A, float* z,
+                      int mem_in_valid, int schedule, cudaStream_t st) override {
+    const int L = cfg.n_layers, d = cfg.d_model, P = phi_dim();
+    const size_t a_n = (size_t)L * d * P, z_n = (size_t)L * P;
+    if (!mem_in_valid) {
+      CK(cudaMemsetAsync(A, 0, a_n * sizeof(float), st));
+      CK(cudaMemsetAsync(z, 0, z_n * sizeof(float), st));
+      if (kTC) CK(cudaMemsetAsync(Aa, 0, a_n * sizeof(AT), st));
+    } else if (kTC) {
+      CKS(prof_begin(ARMT_KC_OTHER, st));
+      convert_state_kernel<AT><<<4 * num_sms, 256, 0, st>>>(A, Aa, (long long)a_n);
+      CK(cudaGetLastError());
+      CKS(prof_end(st));
+    }
+    if (schedule == ARMT_SCHEDULE_DIAGONAL) {
+      for (int64_t i = 0; i < L + n - 1; ++i) {
+        const int lo = (int)(i - n + 1 > 0 ? i - n + 1 : 0);
+        const int hi = (int)(i < L - 1 ? i : L - 1);
+        CKS(step(lo, hi, i, i - (L - 1), tokens, hidden, A, z, st));
+      }
+    } else {
+      for (int64_t s = 0; s < n; ++s)
+        for (int l = 0; l < L; ++l) CKS(step(l, l, s, s, tokens, hidden, A, z, st));
+    }
+    return ARMT_OK;
+  }
+};
+
+// --------------------------------------------------------- checking --
+
+static armt_status validate(const armt_config* c) {
+  if (c->n_layers <= 0 || c->d_model <= 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0 ||
+      c->head_dim <= 0 || c->ffn_dim <= 0 || c->vocab <= 0 || c->seg_len <= 0 || c->n_mem <= 0 ||
+      c->key_dim <= 0 || c->dpfp_nu <= 0)
+    return fail(ARMT_ERR_ARG, "config sizes must be positive");
+  if (!(c->norm_eps > 0.f) || !(c->assoc_eps > 0.f) || !(c->rope_base > 1.0))
+    return fail(ARMT_ERR_ARG, "norm_eps, assoc_eps must be > 0 and rope_base > 1");
+  if (c->dtype != ARMT_F32 && c->dtype != ARMT_BF16) return fail(ARMT_ERR_ARG, "unknown dtype");
+  if (c->n_q_heads % c->n_kv_heads != 0)
+    return fail(ARMT_ERR_SHAPE, "n_q_heads must be a multiple of n_kv_heads");
+  if (c->n_mem > 32) return fail(ARMT_ERR_UNSUPPORTED, "n_mem > 32");
+  if (c->dpfp_nu >= 2 * c->key_dim) return fail(ARMT_ERR_SHAPE, "dpfp_nu must be < 2 * key_dim");
+  const int hd = c->head_dim, d = c->d_model, F = c->ffn_dim;
+  const int Nq = (c->n_q_heads + 2 * c->n_kv_heads) * hd;
+  const int P = 2 * c->key_dim * c->dpfp_nu;
+  const int T = c->seg_len + c->n_mem;
+  if (hd != 32 && hd != 64 && hd != 128) return fail(ARMT_ERR_UNSUPPORTED, "head_dim must be 32, 64 or 128");
+  if (F % GU_BLK != 0) return fail(ARMT_ERR_SHAPE, "ffn_dim must be a multiple of 128");
+  if (d % 32 != 0 || Nq % 64 != 0) return fail(ARMT_ERR_SHAPE, "d_model % 32, qkv width % 64");
+  if (c->dtype == ARMT_BF16) {
+    if (hd == 32) return fail(ARMT_ERR_UNSUPPORTED, "bf16 models need head_dim 64 or 128");
+    if (d % 256 != 0 || Nq % 256 != 0)
+      return fail(ARMT_ERR_SHAPE, "bf16: d_model and (Hq+2Hkv)*head_dim must be multiples of 256");
+    if (c->key_dim != 64) return fail(ARMT_ERR_UNSUPPORTED, "bf16: key_dim must be 64");
+    if (P % 64 != 0 || (c->n_q_heads * hd) % 64 != 0 || F % 64 != 0)
+      return fail(ARMT_ERR_SHAPE, "bf16: P, Hq*head_dim, ffn_dim must be multiples of 64");
+  }
+  if (T > 65535) return fail(ARMT_ERR_SHAPE, "seg_len + n_mem too large");
+  return ARMT_OK;
+}
+
+static int g_num_sms(int dev) {
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+// ------------------------------------------------------------- C ABI --
+
+extern "C" {
+
+const char* armt_status_string(armt_status s) {
+  switch (s) {
+    case ARMT_OK: return "ok";
+    case ARMT_ERR_ARG: return "invalid argument";
+    case ARMT_ERR_SHAPE: return "inconsistent shape";
+    case ARMT_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ARMT_ERR_OOM: return "out of device memory";
+    case ARMT_ERR_CUDA: return "CUDA error";
+    case ARMT_ERR_TIMEOUT: return "device-side wait timed out";
+    case ARMT_ERR_NO_DEVICE: return "no compute capability 10.3 device";
+  }
+  return "unknown status";
+}
+
+const char* armt_last_error(void) { return g_last_error.c_str(); }
+
+static armt_status check_device(int* dev) {
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || n == 0) {
+    cudaGetLastError();
+    return fail(ARMT_ERR_NO_DEVICE, "no CUDA device");
+  }
+  CK(cudaGetDevice(dev));
+  int major = 0, minor = 0;
+  CK(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev));
+  CK(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev));
+  if (major != 10 || minor != 3)
+    return fail(ARMT_ERR_NO_DEVICE, "device is sm_" + std::to_string(major * 10 + minor) +
+                                        ", this library is built for sm_103a");
+  return ARMT_OK;
+}
+
+armt_status armt_create(const armt_config* cfg, const armt_weights* w, void* stream,
+                        armt_model** out) {
+  if (cfg == nullptr || w == nullptr || out == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
+  *out = nullptr;
+  const void* ptrs[] = {w->embed, w->mem, w->wq, w->wk, w->wv, w->wo, w->w_gate, w->w_up,
+                        w->w_down, w->a_wq, w->a_wk, w->a_wv, w->a_wbeta, w->norm1, w->norm2,
+                        w->norm_f};
+  for (const void* p : ptrs)
+    if (p == nullptr) return fail(ARMT_ERR_ARG, "NULL weight pointer");
+  CKS(validate(cfg));
+  int dev = 0;
+  CKS(check_device(&dev));
+  ModelBase* m = cfg->dtype == ARMT_BF16 ? static_cast<ModelBase*>(new Model<bf16>())
+                                         : static_cast<ModelBase*>(new Model<float>());
+  m->cfg = *cfg;
+  m->device = dev;
+  m->num_sms = g_num_sms(dev);
+  armt_status s = m->create(w, reinterpret_cast<cudaStream_t>(stream));
+  if (s != ARMT_OK) {
+    cudaDeviceSynchronize();
+    delete m;
+    return s;
+  }
+  *out = new armt_model{m};
+  return ARMT_OK;
+}
+
+armt_status armt_destroy(armt_model* m) {
+  if (m == nullptr) return ARMT_OK;
+  cudaDeviceSynchronize();
+  delete m->impl;
+  delete m;
+  return ARMT_OK;
+}
+
+static armt_status forward_common(armt_model* m, const int32_t* tokens, int64_t n, float* hidden,
+                                  float* A, float* z, int32_t mem_in_valid, int schedule,
+                                  void* stream) {
+  if (m == nullptr || tokens == nullptr || hidden == nullptr || A == nullptr || z == nullptr)
+    return fail(ARMT_ERR_ARG, "NULL argument");
+  if (n <= 0) return fail(ARMT_ERR_ARG, "n_segments must be positive");
+  if (mem_in_valid != 0 && mem_in_valid != 1) return fail(ARMT_ERR_ARG, "mem_in_valid must be 0 or 1");
+  if (n > ((int64_t)1 << 24)) return fail(ARMT_ERR_SHAPE, "n_segments too large");
+  return m->impl->forward(tokens, n, hidden, A, z, mem_in_valid, schedule,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+armt_status armt_forward(armt_model* m, const int32_t* tokens, int64_t n_segments, float* hidden_out,
+                         float* mem_A, float* mem_z, int32_t mem_in_valid, void* stream) {
+  return forward_common(m, tokens, n_segments, hidden_out, mem_A, mem_z, mem_in_valid,
+                        ARMT_SCHEDULE_DIAGONAL, stream);
+}
+
+armt_status armt_forward_sequential(armt_model* m, const int32_t* tokens, int64_t n_segments,
+                                    float* hidden_out, float* mem_A, float* mem_z,
+                                    int32_t mem_in_valid, void* stream) {
+  return forward_common(m, tokens, n_segments, hidden_out, mem_A, mem_z, mem_in_valid,
+                        ARMT_SCHEDULE_SEQUENTIAL, stream);
+}
+
+armt_status armt_forward_host(armt_model* m, const int32_t* h_tokens, int64_t n, float* h_hidden,
+                              float* h_A, float* h_z, int32_t mem_in_valid, int32_t schedule,
+                              void* stream) {
+  if (m == nullptr || h_tokens == nullptr || h_hidden == nullptr || h_A == nullptr || h_z == nullptr)
+    return fail(ARMT_ERR_ARG, "NULL argument");
+  if (n <= 0) return fail(ARMT_ERR_ARG, "n_segments must be positive");
+  if (schedule != ARMT_SCHEDULE_DIAGONAL && schedule != ARMT_SCHEDULE_SEQUENTIAL)
+    return fail(ARMT_ERR_ARG, "unknown schedule");
+  ModelBase* b = m->impl;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const armt_config& c = b->cfg;
+  const size_t ntok = (size_t)n * c.seg_len, nh = ntok * c.d_model;
+  const size_t na = (size_t)c.n_layers * c.d_model * b->phi_dim(), nz = (size_t)c.n_layers * b->phi_dim();
+  if (b->st_tokens_n < ntok) {
+    if (b->st_tokens) cudaFree(b->st_tokens);
+    b->st_tokens = nullptr;
+    b->st_tokens_n = 0;
+    CK(cudaMalloc(&b->st_tokens, ntok * sizeof(int32_t)));
+    b->st_tokens_n = ntok;
+  }
+  if (b->st_hidden_n < nh) {
+    if (b->st_hidden) cudaFree(b->st_hidden);
+    b->st_hidden = nullptr;
+    b->st_hidden_n = 0;
+    CK(cudaMalloc(&b->st_hidden, nh * sizeof(float)));
+    b->st_hidden_n = nh;
+  }
+  if (b->st_A == nullptr) {
+    CK(cudaMalloc(&b->st_A, na * sizeof(float)));
+    CK(cudaMalloc(&b->st_z, nz * sizeof(float)));
+  }
+  CK(cudaMemcpyAsync(b->st_tokens, h_tokens, ntok * sizeof(int32_t), cudaMemcpyHostToDevice, st));
+  if (mem_in_valid) {
+    CK(cudaMemcpyAsync(b->st_A, h_A, na * sizeof(float), cudaMemcpyHostToDevice, st));
+    CK(cudaMemcpyAsync(b->st_z, h_z, nz * sizeof(float), cudaMemcpyHostToDevice, st));
+  }
+  CKS(forward_common(m, b->st_tokens, n, b->st_hidden, b->st_A, b->st_z, mem_in_valid, schedule,
+                     stream));
+  CK(cudaMemcpyAsync(h_hidden, b->st_hidden, nh * sizeof(float), cudaMemcpyDeviceToHost, st));
+  CK(cudaMemcpyAsync(h_A, b->st_A, na * sizeof(float), cudaMemcpyDeviceToHost, st));
+  CK(cudaMemcpyAsync(h_z, b->st_z, nz * sizeof(float), cudaMemcpyDeviceToHost, st));
+  CK(cudaStreamSynchronize(st));
+  return ARMT_OK;
+}
+
+armt_status armt_grouped_gemm_bf16(const void* A, const void* B, float* C, int32_t G, int32_t M,
+                                   int32_t N, int32_t K, void* stream) {
+  if (A == nullptr || B == nullptr || C == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
+  if (G <= 0 || M <= 0 || N <= 0 || K <= 0) return fail(ARMT_ERR_ARG, "sizes must be positive");
+  if (K % TC_BK != 0 || N % 256 != 0) return fail(ARMT_ERR_SHAPE, "need K % 64 == 0 and N % 256 == 0");
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+       reinterpret_cast<uintptr_t>(C)) & 15)
+    return fail(ARMT_ERR_ARG, "pointers must be 16-byte aligned");
+  if ((long long)M > (1ll << 30) || (long long)G * N > (1ll << 30))
+    return fail(ARMT_ERR_SHAPE, "sizes too large");
+  int dev = 0;
+  CKS(check_device(&dev));
+  static int* err = nullptr;
+  if (err == nullptr) {
+    CK(cudaMalloc(&err, sizeof(int)));
+    CK(cudaMemset(err, 0, sizeof(int)));
+  }
+  CUtensorMap ta, tb;
+  if (!encode_tmap_bf16_3d(&ta, A, K, M, G, TC_BM) || !encode_tmap_bf16_3d(&tb, B, K, N, G, 256))
+    return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  EpiStore epi{C, (long long)N, (long long)M * N};
+  CK((launch_gemm_tc<EpiStore, 256>(ta, tb, M, N, K, 0, G, err, epi, g_num_sms(dev),
+                                    reinterpret_cast<cudaStream_t>(stream))));
+  return ARMT_OK;
+}
+
+armt_status armt_state_sizes(const armt_model* m, int64_t* a_elems, int64_t* z_elems) {
+  if (m == nullptr || a_elems == nullptr || z_elems == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
+  const armt_config& c = m->impl->cfg;
+  *a_elems = (int64_t)c.n_layers * c.d_model * m->impl->phi_dim();
+  *z_elems = (int64_t)c.n_layers * m->impl->phi_dim();
+  return ARMT_OK;
+}
+
+armt_status armt_launch_count(const armt_model* m, int64_t n, int32_t schedule, int64_t* launches) {
+  if (m == nullptr || launches == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
+  if (n <= 0) return fail(ARMT_ERR_ARG, "n_segments must be positive");
+  if (schedule != ARMT_SCHEDULE_DIAGONAL && schedule != ARMT_SCHEDULE_SEQUENTIAL)
+    return fail(ARMT_ERR_ARG, "unknown schedule");
+  *launches = m->impl->launches(n, schedule, 0);
+  return ARMT_OK;
+}
+
+armt_status armt_set_profiling(armt_model* m, int32_t enable) {
+  if (m == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
+  m->impl->profiling = enable != 0;
+  m->impl->ev_used = 0;
+  return ARMT_OK;
+}
+
+armt_status armt_kernel_times(armt_model* m, int64_t* launches, double* ms, int32_t n_classes) {
+  if (m == nullptr || launches == nullptr || ms == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
+  if (n_classes <= 0 || n_classes > ARMT_KC_COUNT) return fail(ARMT_ERR_ARG, "bad n_classes");
+  ModelBase* b = m->impl;
+  for (int i = 0; i < n_classes; ++i) {
+    launches[i] = 0;
+    ms[i] = 0.0;
+  }
+  for (size_t i = 0; i < b->ev_used; ++i) {
+    CK(cudaEventSynchronize(b->ev_stop[i]));
+    float t = 0.f;
+    CK(cudaEventElapsedTime(&t, b->ev_start[i], b->ev_stop[i]));
+    const int c = b->ev_class[i];
+    if (c < n_classes) {
+      launches[c] += 1;
+      ms[c] += t;
+    }
+  }
+  b->ev_used = 0;
+  return ARMT_OK;
+}
+
+armt_status armt_sync_status(armt_model* m, void* stream) {
+  if (m == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
+  CK(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+  int h = 0;
+  CK(cudaMemcpy(&h, m->impl->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (h != 0) {
+    CK(cudaMemset(m->impl->d_err, 0, sizeof(int)));
+    return fail(ARMT_ERR_TIMEOUT, "device wait timed out (code " + std::to_string(h) + ")");
+  }
+  return ARMT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,237 @@
+// GEMM epilogues of the grouped layer.
+//
+// Each functor turns accumulator values of one output row segment into the
+// next activation, so the projections of a cell write what the following
+// step consumes with no extra pass over HBM:
+//   EpiStore     C = acc (fp32)                        plain grouped GEMM
+//   EpiAssocRead x' = x + acc / den[row]               associative read + residual
+//   EpiQkvRope   q|k|v = acc with rotate-half RoPE on q and k, act dtype
+//   EpiResidual  out = res + acc (fp32), optional act-dtype copy
+//   EpiSwiGLU    u = silu(gate) * up, gate/up interleaved in blocks of 128
+// A functor is called once per (row, group of GROUP columns) with a source
+// that yields accumulator columns `c .. c+n-1` relative to the group start.
+// `valid` is false for padding rows past the end of the cell; the functor
+// must still read its source (TMEM loads are warp-collective) but stores
+// nothing.
+#pragma once
+
+#include "common.cuh"
+
+namespace armt {
+
+constexpr int GU_BLK = 128;  // gate/up interleave block (rows of W_gate then W_up)
+
+// ---------------------------------------------------------------- stores --
+
+__device__ __forceinline__ void store_row(float* dst, const float* v, int n) {
+  if (n == 32 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4)
+      *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+  } else {
+    for (int i = 0; i < n; ++i) dst[i] = v[i];
+  }
+}
+
+__device__ __forceinline__ void store_row(bf16* dst, const float* v, int n) {
+  if (n == 32 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+      uint4 p;
+      p.x = pack_bf16x2(v[i], v[i + 1]);
+      p.y = pack_bf16x2(v[i + 2], v[i + 3]);
+      p.z = pack_bf16x2(v[i + 4], v[i + 5]);
+      p.w = pack_bf16x2(v[i + 6], v[i + 7]);
+      *reinterpret_cast<uint4*>(dst + i) = p;
+    }
+  } else {
+    for (int i = 0; i < n; ++i) dst[i] = f2bf(v[i]);
+  }
+}
+
+__device__ __forceinline__ void load_row(const float* src, float* v, int n) {
+  if (n == 32 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      float4 t = *reinterpret_cast<const float4*>(src + i);
+      v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+    }
+  } else {
+    for (int i = 0; i < n; ++i) v[i] = src[i];
+  }
+}
+
+// ------------------------------------------------------------- functors --
+
+struct EpiStore {
+  static constexpr int GROUP = 32;
+  float* C;
+  long long ld;        // row stride (elements)
+  long long g_stride;  // stride between layers/groups (elements)
+  template <class Src>
+  __device__ __forceinline__ void operator()(int g, int row, bool valid, int col0, int ncols,
+                                             Src& src) const {
+    for (int c = 0; c < ncols; c += 32) {
+      float v[32];
+      src.template load<32>(c, v);
+      if (valid) store_row(C + g * g_stride + (long long)row * ld + col0 + c, v, 32);
+    }
+  }
+};
+
+// x' = x + acc / den[row]: the associative read (numerator from the grouped
+// GEMM of phi rows with the state) added to the residual stream.
+struct EpiAssocRead {
+  static constexpr int GROUP = 32;
+  const float* x;      // [slots][rows][d] layer input (slot = layer)
+  const float* den;    // [L][rows]  z^T phi + eps
+  float* out;          // [L][rows][d]
+  int rows, d;
+  template <class Src>
+  __device__ __forceinline__ void operator()(int l, int row, bool valid, int col0, int ncols,
+                                             Src& src) const {
+    const long long off = ((long long)l * rows + row) * d + col0;
+    const float dn = valid ? den[(long long)l * rows + row] : 1.f;
+    for (int c = 0; c < ncols; c += 32) {
+      float a[32], xv[32];
+      src.template load<32>(c, a);
+      if (valid) {
+        load_row(x + off + c, xv, 32);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a[i] = xv[i] + a[i] / dn;
+        store_row(out + off + c, a, 32);
+      }
+    }
+  }
+};
+
+// Fused Q|K|V projection output with rotate-half RoPE on the q and k heads.
+// Columns [0, Hq*hd) are q, then Hkv*hd of k, then Hkv*hd of v.  cos/sin
+// tables are [rows][hd/2] (position = row within the cell).
+template <typename OutT>
+struct EpiQkvRope {
+  static constexpr int GROUP = 64;  // callers pass whole heads (ncols a multiple of hd)
+  OutT* out;                        // [L][rows][(Hq+2Hkv)*hd]
+  const float* cosT;
+  const float* sinT;
+  int rows, hd, n_rope_cols, ncols_total;  // n_rope_cols = (Hq+Hkv)*hd
+  template <int CH, class Src>
+  __device__ __forceinline__ void rope_chunk(int row, bool valid, bool rope, int hcol, int h0,
+                                             int i0, long long rbase, Src& src) const {
+    const int half = hd >> 1;
+    float x1[CH], x2[CH];
+    src.template load<CH>(h0 + i0, x1);
+    src.template load<CH>(h0 + half + i0, x2);
+    if (!valid) return;
+    if (rope) {
+      const float* cr = cosT + (long long)row * half + i0;
+      const float* sr = sinT + (long long)row * half + i0;
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        const float c = cr[i], s = sr[i];
+        const float a = x1[i], b = x2[i];
+        x1[i] = a * c - b * s;
+        x2[i] = b * c + a * s;
+      }
+    }
+    store_row(out + rbase + hcol + i0, x1, CH);
+    store_row(out + rbase + hcol + half + i0, x2, CH);
+  }
+
+  template <class Src>
+  __device__ __forceinline__ void operator()(int l, int row, bool valid, int col0, int ncols,
+                                             Src& src) const {
+    const long long rbase = ((long long)l * rows + row) * ncols_total;
+    const int half = hd >> 1;
+    for (int h0 = 0; h0 < ncols; h0 += hd) {
+      const int hcol = col0 + h0;
+      const bool rope = hcol < n_rope_cols;
+      if (half >= 32) {
+        for (int i0 = 0; i0 < half; i0 += 32) rope_chunk<32>(row, valid, rope, hcol, h0, i0, rbase, src);
+      } else {
+        rope_chunk<16>(row, valid, rope, hcol, h0, 0, rbase, src);
+      }
+    }
+  }
+};
+
+// out = res + acc (fp32 residual stream), plus an optional copy in the
+// activation dtype (the next layer's associative-query GEMM operand).
+template <typename CopyT>
+struct EpiResidual {
+  static constexpr int GROUP = 32;
+  const float* res;    // [L][rows][n]
+  float* out;          // [slots][rows][n] at slot l + out_slot_offset
+  CopyT* copy;         // same indexing as out, or nullptr
+  int rows, n, out_slot_offset;
+  template <class Src>
+  __device__ __forceinline__ void operator()(int l, int row, bool valid, int col0, int ncols,
+                                             Src& src) const {
+    const long long ri = ((long long)l * rows + row) * n + col0;
+    const long long oi = ((long long)(l + out_slot_offset) * rows + row) * n + col0;
+    for (int c = 0; c < ncols; c += 32) {
+      float a[32], r[32];
+      src.template load<32>(c, a);
+      if (valid) {
+        load_row(res + ri + c, r, 32);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a[i] += r[i];
+        store_row(out + oi + c, a, 32);
+        if (copy != nullptr) store_row(copy + oi + c, a, 32);
+      }
+    }
+  }
+};
+
+// SwiGLU over interleaved gate/up columns: block b of 2*GU_BLK accumulator
+// columns holds gate rows [b*GU_BLK, (b+1)*GU_BLK) then the same up rows.
+template <typename OutT>
+struct EpiSwiGLU {
+  static constexpr int GROUP = 2 * GU_BLK;
+  OutT* out;           // [L][rows][F]
+  int rows, F;
+  template <class Src>
+  __device__ __forceinline__ void operator()(int l, int row, bool valid, int col0, int ncols,
+                                             Src& src) const {
+    for (int b0 = 0; b0 < ncols; b0 += 2 * GU_BLK) {
+      const int f0 = (col0 + b0) / 2;
+      OutT* dst = out + ((long long)l * rows + row) * F + f0;
+      for (int c = 0; c < GU_BLK; c += 32) {
+        float g[32], u[32];
+        src.template load<32>(b0 + c, g);
+        src.template load<32>(b0 + GU_BLK + c, u);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
+          store_row(dst + c, g, 32);
+        }
+      }
+    }
+  }
+};
+
+// Accumulator sources.
+struct TmemSrc {
+  uint32_t taddr;  // lane base of this warp | column of the tile start
+  template <int N>
+  __device__ __forceinline__ void load(int c, float* v) const;
+};
+template <>
+__device__ __forceinline__ void TmemSrc::load<32>(int c, float* v) const {
+  tmem_ld32(taddr + (uint32_t)c, v);
+}
+template <>
+__device__ __forceinline__ void TmemSrc::load<16>(int c, float* v) const {
+  tmem_ld16(taddr + (uint32_t)c, v);
+}
+
+struct PtrSrc {
+  const float* p;  // row pointer at the group start
+  template <int N>
+  __device__ __forceinline__ void load(int c, float* v) const {
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = p[c + i];
+  }
+};
+
+}  // namespace armt

@@ -1,0 +1,221 @@
+// Grouped bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// The grouped layer of the summary page of "Diagonal Batching Unlocks
+// Parallelism in Recurrent Memory Transformers for Long Contexts" (section 三):
+// every linear layer of the cells of one diagonal runs as one grouped matrix
+// product over stacked per-layer weights, the outputs preallocated as one
+// tensor and addressed per group.  Here a group is a layer l in
+// [g_first, g_first + g_count); for each of them
+//     out[l] = epilogue( A[l] (rows x K, bf16)  *  B[l]^T (B: N x K, bf16) )
+// with fp32 accumulation.  A and B are read through 3-D TMA tensor maps
+// {K, rows, layer} so that row tiles past the end of a cell are zero-filled.
+//
+// One persistent CTA per SM walks the tiles (layer-major, then N tile, then
+// M tile, so CTAs running at the same time share the weight tile in L2):
+//   warp 0      TMA producer: A tile 128 x 64 and B tile BN x 64 per stage,
+//   warp 1      MMA issuer (one thread): 4 x tcgen05.mma (K = 16 each) per
+//               stage into a 128 x BN fp32 accumulator in TMEM,
+//   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows),
+//               fused epilogue, direct stores.
+// Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile
+// i+1.  Every output element is reduced in the same fixed K order no matter
+// how many groups a launch holds (no split-K, no atomics), so a cell gives
+// bit-identical results in a one-cell launch and in a full diagonal.
+#pragma once
+
+#include "common.cuh"
+#include "epilogues.cuh"
+
+namespace armt {
+
+constexpr int TC_BM = 128;
+constexpr int TC_BK = 64;  // one 128-byte swizzle row of bf16
+
+struct GemmTcShape {
+  int rows;       // valid rows per group (M)
+  int N, K;
+  int g_first, g_count;
+  int m_tiles, n_tiles, k_blocks;
+  int* err;       // device error word
+};
+
+template <int BN>
+struct TcCfg {
+  static constexpr int STAGES = BN >= 256 ? 4 : 8;
+  static constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
+  static constexpr uint32_t B_BYTES = BN * TC_BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
+  static constexpr size_t SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+};
+
+template <class Epi, int BN>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmTcShape sh, const Epi epi) {
+  using C = TcCfg<BN>;
+  static_assert(BN % Epi::GROUP == 0, "tile width must hold whole epilogue groups");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + C::STAGES * C::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);  // one arrival per epilogue warp
+    }
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int tiles_per_g = sh.m_tiles * sh.n_tiles;
+  const int num_tiles = sh.g_count * tiles_per_g;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        const int g = t / tiles_per_g, r = t - g * tiles_per_g;
+        const int nt = r / sh.m_tiles, mt = r - nt * sh.m_tiles;
+        const int layer = sh.g_first + g;
+        for (int kb = 0; kb < sh.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, sh.err, DEV_TIMEOUT_EMPTY)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          tma_load_3d(sA + stage * C::A_BYTES, &tmA, kb * TC_BK, mt * TC_BM, layer, &full[stage]);
+          tma_load_3d(sB + stage * C::B_BYTES, &tmB, kb * TC_BK, nt * BN, layer, &full[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(TC_BM, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, sh.err, DEV_TIMEOUT_ACC_EMPTY)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < sh.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, sh.err, DEV_TIMEOUT_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES));
+          const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + stage * C::B_BYTES));
+#pragma unroll
+          for (int k = 0; k < TC_BK / 16; ++k) {
+            // advance 16 bf16 = 32 bytes along K inside the swizzled row
+            tc_mma_bf16(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
+                        (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);  // stage reusable once these MMAs finish
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[acc]);  // accumulator ready for the epilogue
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+    }
+  } else {
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      const int g = t / tiles_per_g, r = t - g * tiles_per_g;
+      const int nt = r / sh.m_tiles, mt = r - nt * sh.m_tiles;
+      const bool got = mbar_wait_bounded(&acc_full[acc], acc_phase, sh.err, DEV_TIMEOUT_ACC_FULL);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const int row = mt * TC_BM + quarter * 32 + lane;
+      TmemSrc src{tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16)};
+      epi(sh.g_first + g, row, row < sh.rows, nt * BN, BN, src);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// Host side --------------------------------------------------------------
+
+// Encodes a 3-D bf16 tensor map over [layers][rows][K] (K contiguous) with a
+// box of {64, box_rows, 1} and 128-byte swizzling.  Returns false on error.
+bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int K, int rows, int layers,
+                         int box_rows);
+
+template <class Epi, int BN>
+cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int rows, int N, int K,
+                           int g_first, int g_count, int* err, const Epi& epi, int num_sms,
+                           cudaStream_t stream) {
+  using C = TcCfg<BN>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<Epi, BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  GemmTcShape sh;
+  sh.rows = rows;
+  sh.N = N;
+  sh.K = K;
+  sh.g_first = g_first;
+  sh.g_count = g_count;
+  sh.m_tiles = (rows + TC_BM - 1) / TC_BM;
+  sh.n_tiles = N / BN;
+  sh.k_blocks = K / TC_BK;
+  sh.err = err;
+  const int tiles = g_count * sh.m_tiles * sh.n_tiles;
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  if (grid <= 0) return cudaSuccess;
+  gemm_tc_kernel<Epi, BN><<<grid, 192, C::SMEM, stream>>>(tmA, tmB, sh, epi);
+  return cudaGetLastError();
+}
+
+}  // namespace armt

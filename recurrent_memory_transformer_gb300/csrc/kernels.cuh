@@ -1,0 +1,407 @@
+// Row-wise, associative-memory, attention and fp32 GEMM kernels of one
+// diagonal step.  Every kernel takes a contiguous layer range
+// [g_first, g_first + gridDim.{y|z}) -- the cells of one anti-diagonal, or a
+// single cell in the sequential schedule -- and computes each cell with the
+// same per-element operation order either way.
+//
+// Method: summary page of "Diagonal Batching Unlocks Parallelism in Recurrent
+// Memory Transformers for Long Contexts".  Section 二: each layer owns an
+// associative memory (A_l, z_l) read by every token and updated by the delta
+// rule from that layer's memory-token outputs; section 三: the norms use
+// stacked per-layer gains and every other operation runs batched over the
+// cells of a diagonal.
+#pragma once
+
+#include "common.cuh"
+#include "epilogues.cuh"
+
+namespace armt {
+
+// ------------------------------------------------------- layer-0 input --
+
+// X[0] = [E[tokens of the segment]; memory embeddings] (fp32 residual stream)
+// plus the activation-dtype copy Xa[0] (used as a GEMM operand).
+template <typename WT>
+__global__ void embed_gather_kernel(const int32_t* __restrict__ tokens, const WT* __restrict__ embed,
+                                    const WT* __restrict__ mem, float* __restrict__ X,
+                                    WT* __restrict__ Xa, int S, int d, int vocab) {
+  const int t = blockIdx.x;
+  const WT* src;
+  if (t < S) {
+    int id = tokens[t];
+    id = id < 0 ? 0 : (id >= vocab ? vocab - 1 : id);
+    src = embed + (long long)id * d;
+  } else {
+    src = mem + (long long)(t - S) * d;
+  }
+  float* xo = X + (long long)t * d;
+  WT* xa = Xa + (long long)t * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const float v = ld_as_f32(src + i);
+    xo[i] = v;
+    if ((void*)Xa != (void*)X) xa[i] = src[i];
+  }
+}
+
+// ------------------------------------------------------------- RMSNorm --
+
+// out[l][row] = x[l][row] / sqrt(mean(x^2) + eps) * gain[l]  for the rows
+// [0, rows) of layers g_first + blockIdx.y.  One block per row.
+template <typename OutT>
+__global__ void rmsnorm_kernel(const float* __restrict__ x, long long x_gs, const float* __restrict__ gain,
+                               long long gain_gs, OutT* __restrict__ out, long long out_gs, int d,
+                               float eps, int g_first) {
+  __shared__ float red[32];
+  const int l = g_first + blockIdx.y;
+  const float* xr = x + l * x_gs + (long long)blockIdx.x * d;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) ss += xr[i] * xr[i];
+  ss = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+  const float* g = gain + l * gain_gs;
+  OutT* o = out + l * out_gs + (long long)blockIdx.x * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) st_from_f32(o + i, xr[i] * inv * g[i]);
+}
+
+// ----------------------------------------------- associative read side --
+
+// From q = Wq_a x (fp32 [rows][k] per layer): phi = DPFP_nu(q) (act dtype,
+// [rows][P]) and den = z^T phi + eps.  One block per (row, layer).
+template <typename PhiT>
+__global__ void assoc_phi_kernel(const float* __restrict__ q, const float* __restrict__ z,
+                                 PhiT* __restrict__ phi, float* __restrict__ den, int rows, int k,
+                                 int nu, float eps, int g_first) {
+  extern __shared__ float r[];  // 2k
+  __shared__ float red[32];
+  const int l = g_first + blockIdx.y, row = blockIdx.x;
+  const int k2 = 2 * k, P = k2 * nu;
+  const float* qr = q + ((long long)l * rows + row) * k;
+  for (int i = threadIdx.x; i < k; i += blockDim.x) {
+    const float v = qr[i];
+    r[i] = v > 0.f ? v : 0.f;
+    r[i + k] = v < 0.f ? -v : 0.f;
+  }
+  __syncthreads();
+  const float* zl = z + (long long)l * P;
+  PhiT* pr = phi + ((long long)l * rows + row) * P;
+  float acc = 0.f;
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int j = p / k2 + 1, i = p - (j - 1) * k2;
+    int src = i - j;
+    src = src < 0 ? src + k2 : src;
+    const float f = r[i] * r[src];
+    st_from_f32(pr + p, f);
+    acc += zl[p] * f;
+  }
+  acc = block_sum(acc, red);
+  if (threadIdx.x == 0) den[(long long)l * rows + row] = acc + eps;
+}
+
+// ---------------------------------------------- associative write side --
+
+// Projections of the memory-token rows h_i (rows S..S+M-1 of the layer's
+// output): kb[l][i][0..k) = Wk_a h_i, kb[l][i][k] = wbeta^T h_i (logit).
+// Grid (k + 1 outputs, layers).  M <= 32.
+template <typename WT>
+__global__ void assoc_write_proj_kernel(const float* __restrict__ H, long long h_gs,
+                                        const WT* __restrict__ wk, const WT* __restrict__ wbeta,
+                                        float* __restrict__ kb, int S, int M, int d, int k,
+                                        int g_first) {
+  __shared__ float part[32][33];
+  const int l = g_first + blockIdx.y, o = blockIdx.x;
+  const WT* w = (o < k) ? wk + ((long long)l * k + o) * d : wbeta + (long long)l * d;
+  const float* hb = H + l * h_gs + (long long)S * d;
+  float acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+  for (int e = threadIdx.x; e < d; e += blockDim.x) {
+    const float we = ld_as_f32(w + e);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < M) acc[i] += we * hb[(long long)i * d + e];
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float s = warp_sum(acc[i]);
+    if (lane == 0) part[warp][i] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < M) {
+    float s = 0.f;
+    for (int w2 = 0; w2 < nw; ++w2) s += part[w2][threadIdx.x];
+    kb[((long long)l * M + threadIdx.x) * (k + 1) + o] = s;
+  }
+}
+
+// Per layer (one block): phi_i = DPFP(k_i), zphi_i = z^T phi_i,
+// gamma_i = 1 - zphi_i / (phi_i^T phi_i + eps), beta_i = sigmoid(logit_i);
+// stores phiM[l][i][:], coef[l][i] = {beta_i, zphi_i + eps}; then
+// z += sum_i gamma_i phi_i (after every zphi_i has been taken).
+__global__ void assoc_write_feat_kernel(const float* __restrict__ kb, float* __restrict__ z,
+                                        float* __restrict__ phiM, float* __restrict__ coef, int M,
+                                        int k, int nu, float eps, int g_first) {
+  extern __shared__ float sm[];  // M * 2k (r rows) + 2 * M
+  __shared__ float red[32];
+  const int l = g_first + blockIdx.x;
+  const int k2 = 2 * k, P = k2 * nu;
+  float* r = sm;
+  float* gam = sm + M * k2;
+  for (int t = threadIdx.x; t < M * k; t += blockDim.x) {
+    const int i = t / k, c = t - i * k;
+    const float v = kb[((long long)l * M + i) * (k + 1) + c];
+    r[i * k2 + c] = v > 0.f ? v : 0.f;
+    r[i * k2 + c + k] = v < 0.f ? -v : 0.f;
+  }
+  __syncthreads();
+  float* zl = z + (long long)l * P;
+  for (int i = 0; i < M; ++i) {
+    float zp = 0.f, ff = 0.f;
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+      const int j = p / k2 + 1, c = p - (j - 1) * k2;
+      int src = c - j;
+      src = src < 0 ? src + k2 : src;
+      const float f = r[i * k2 + c] * r[i * k2 + src];
+      phiM[((long long)l * M + i) * P + p] = f;
+      zp += zl[p] * f;
+      ff += f * f;
+    }
+    zp = block_sum(zp, red);
+    ff = block_sum(ff, red);
+    if (threadIdx.x == 0) {
+      const float logit = kb[((long long)l * M + i) * (k + 1) + k];
+      coef[((long long)l * M + i) * 2 + 0] = sigmoid_f(logit);
+      coef[((long long)l * M + i) * 2 + 1] = zp + eps;
+      gam[i] = 1.0f - zp / (ff + eps);
+    }
+  }
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    float dz = 0.f;
+    for (int i = 0; i < M; ++i) dz += gam[i] * phiM[((long long)l * M + i) * P + p];
+    zl[p] += dz;
+  }
+}
+
+// Delta-rule update of the rows of A_l.  Row j of A only needs row j of the
+// values and of vbar, so one pass reads each row of A once:
+//   v_i[j]    = Wv_a[j] . h_i
+//   vbar_i[j] = A[j] . phi_i / (zphi_i + eps)
+//   A[j]     += sum_i beta_i (v_i[j] - vbar_i[j]) phi_i
+// One warp per row j (several rows per warp); h_i and phi_i in shared memory.
+// Also refreshes the activation-dtype copy Aa of the state (GEMM operand of
+// the next read), when Aa != A.
+template <typename WT, typename AT>
+__global__ void assoc_write_update_kernel(const float* __restrict__ H, long long h_gs,
+                                          const WT* __restrict__ wv, const float* __restrict__ phiM,
+                                          const float* __restrict__ coef, float* __restrict__ A,
+                                          AT* __restrict__ Aa, int S, int M, int d, int P,
+                                          int rows_per_block, int g_first) {
+  extern __shared__ float sm[];
+  float* hs = sm;                 // [M][d]
+  float* ps = sm + M * d;         // [M][P]
+  float* cs = ps + M * P;         // [M][2]
+  const int l = g_first + blockIdx.y;
+  const float* hb = H + l * h_gs + (long long)S * d;
+  for (int t = threadIdx.x; t < M * d; t += blockDim.x) hs[t] = hb[t];
+  for (int t = threadIdx.x; t < M * P; t += blockDim.x) ps[t] = phiM[(long long)l * M * P + t];
+  for (int t = threadIdx.x; t < 2 * M; t += blockDim.x) cs[t] = coef[(long long)l * M * 2 + t];
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int j0 = blockIdx.x * rows_per_block;
+  float* Al = A + (long long)l * d * P;
+  AT* Aal = Aa + (long long)l * d * P;
+  for (int j = j0 + warp; j < j0 + rows_per_block && j < d; j += nw) {
+    const WT* wr = wv + ((long long)l * d + j) * d;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+    for (int e = lane; e < d; e += 32) {
+      const float we = ld_as_f32(wr + e);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < M) v[i] += we * hs[i * d + e];
+    }
+    float vb[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) vb[i] = 0.f;
+    float* arow = Al + (long long)j * P;
+    for (int p = lane; p < P; p += 32) {
+      const float a = arow[p];
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < M) vb[i] += a * ps[i * P + p];
+    }
+    float c[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i < M) {
+        const float vi = warp_sum(v[i]);
+        const float vbi = warp_sum(vb[i]) / cs[2 * i + 1];
+        c[i] = cs[2 * i] * (vi - vbi);
+      } else {
+        c[i] = 0.f;
+      }
+    }
+    for (int p = lane; p < P; p += 32) {
+      float dlt = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < M) dlt += c[i] * ps[i * P + p];
+      const float a = arow[p] + dlt;
+      arow[p] = a;
+      if ((void*)Aal != (void*)Al) st_from_f32(Aal + (long long)j * P + p, a);
+    }
+  }
+}
+
+// State copy in the activation dtype: Aa = A (all layers).
+template <typename AT>
+__global__ void convert_state_kernel(const float* __restrict__ A, AT* __restrict__ Aa, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    st_from_f32(Aa + i, A[i]);
+}
+
+// ------------------------------------------------------ SIMT attention --
+
+// Causal grouped-query attention inside one cell, fp32 arithmetic.
+// qkv [L][rows][(Hq+2Hkv)*hd] (q and k already rotated), out [L][rows][Hq*hd].
+// Block: 64 queries of one head of one layer; 4 threads per query, each
+// owning hd/4 dimensions; keys processed in tiles of 64 with an online
+// softmax.  Grid (ceil(rows/64), Hq, layers).
+template <typename T, int HD>
+__global__ void __launch_bounds__(256) attn_simt_kernel(const T* __restrict__ qkv, T* __restrict__ out,
+                                                        int rows, int Hq, int Hkv, float scale,
+                                                        int g_first) {
+  constexpr int DPT = HD / 4;  // dims per thread
+  extern __shared__ float kv[];  // K tile [64][HD], V tile [64][HD]
+  float* Ks = kv;
+  float* Vs = kv + 64 * HD;
+  const int l = g_first + blockIdx.z, h = blockIdx.y, kvh = (h * Hkv) / Hq;
+  const int qi = blockIdx.x * 64 + (threadIdx.x >> 2), part = threadIdx.x & 3;
+  const int ncols = (Hq + 2 * Hkv) * HD;
+  const T* base = qkv + (long long)l * rows * ncols;
+  float q[DPT], o[DPT];
+  const bool qvalid = qi < rows;
+#pragma unroll
+  for (int e = 0; e < DPT; ++e) {
+    q[e] = qvalid ? ld_as_f32(base + (long long)qi * ncols + h * HD + part * DPT + e) * scale : 0.f;
+    o[e] = 0.f;
+  }
+  float m = -INFINITY, lsum = 0.f;
+  const int q_last = min(blockIdx.x * 64 + 63, rows - 1);
+  for (int k0 = 0; k0 <= q_last; k0 += 64) {
+    __syncthreads();
+    for (int t = threadIdx.x; t < 64 * HD; t += blockDim.x) {
+      const int kr = k0 + t / HD, c = t % HD;
+      float kvv = 0.f, vvv = 0.f;
+      if (kr < rows) {
+        kvv = ld_as_f32(base + (long long)kr * ncols + (Hq + kvh) * HD + c);
+        vvv = ld_as_f32(base + (long long)kr * ncols + (Hq + Hkv + kvh) * HD + c);
+      }
+      Ks[t] = kvv;
+      Vs[t] = vvv;
+    }
+    __syncthreads();
+    float s[64];
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+      float a = 0.f;
+#pragma unroll
+      for (int e = 0; e < DPT; ++e) a += q[e] * Ks[j * HD + part * DPT + e];
+      a += __shfl_xor_sync(0xffffffffu, a, 1);
+      a += __shfl_xor_sync(0xffffffffu, a, 2);
+      const bool ok = (k0 + j) <= qi && (k0 + j) < rows;
+      s[j] = ok ? a : -INFINITY;
+      tmax = fmaxf(tmax, s[j]);
+    }
+    const float mnew = fmaxf(m, tmax);
+    if (mnew == -INFINITY) continue;  // nothing visible yet (padding query rows)
+    const float corr = expf(m - mnew);
+    lsum *= corr;
+#pragma unroll
+    for (int e = 0; e < DPT; ++e) o[e] *= corr;
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+      const float p = expf(s[j] - mnew);
+      lsum += p;
+#pragma unroll
+      for (int e = 0; e < DPT; ++e) o[e] += p * Vs[j * HD + part * DPT + e];
+    }
+    m = mnew;
+  }
+  if (qvalid) {
+    T* orow = out + ((long long)l * rows + qi) * (Hq * HD) + h * HD + part * DPT;
+    const float inv = 1.0f / lsum;
+#pragma unroll
+    for (int e = 0; e < DPT; ++e) st_from_f32(orow + e, o[e] * inv);
+  }
+}
+
+// --------------------------------------------------- fp32 SIMT GEMM ----
+
+// C[l] = A[l] * B[l]^T, fp32, for l = g_first + blockIdx.z.  A [rows][K]
+// (row stride lda), B [N][K], C [rows][N] (row stride ldc).  64 x 64 tiles,
+// 16-wide K steps, 4 x 4 outputs per thread, fixed K order.
+__global__ void __launch_bounds__(256) gemm_simt_f32_kernel(const float* __restrict__ A, long long a_gs,
+                                                            int lda, const float* __restrict__ B,
+                                                            long long b_gs, float* __restrict__ C,
+                                                            long long c_gs, int ldc, int rows, int N,
+                                                            int K, int g_first) {
+  __shared__ float As[16][64 + 4];
+  __shared__ float Bs[16][64 + 4];
+  const int l = g_first + blockIdx.z;
+  const float* Al = A + l * a_gs;
+  const float* Bl = B + l * b_gs;
+  float* Cl = C + l * c_gs;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int t = threadIdx.x; t < 64 * 16; t += 256) {
+      const int r = t / 16, c = t % 16;
+      const int gm = m0 + r, gn = n0 + r, gk = k0 + c;
+      As[c][r] = (gm < rows && gk < K) ? Al[(long long)gm * lda + gk] : 0.f;
+      Bs[c][r] = (gn < N && gk < K) ? Bl[(long long)gn * K + gk] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[i] = As[kk][ty * 4 + i];
+        b[i] = Bs[kk][tx * 4 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] += a[i] * b[j];
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int gm = m0 + ty * 4 + i, gn = n0 + tx * 4 + j;
+      if (gm < rows && gn < N) Cl[(long long)gm * ldc + gn] = acc[i][j];
+    }
+}
+
+// Applies an epilogue functor to raw fp32 GEMM output rows (the fp32 path's
+// counterpart of the tensor-core epilogue warps).  Grid (rows, layers).
+template <class Epi>
+__global__ void epi_rows_kernel(const float* __restrict__ C, long long c_gs, int ldc, int N,
+                                int g_first, Epi epi) {
+  const int l = g_first + blockIdx.y, row = blockIdx.x;
+  const float* cr = C + l * c_gs + (long long)row * ldc;
+  for (int grp = threadIdx.x; grp < N / Epi::GROUP; grp += blockDim.x) {
+    PtrSrc src{cr + grp * Epi::GROUP};
+    epi(l, row, true, grp * Epi::GROUP, Epi::GROUP, src);
+  }
+}
+
+}  // namespace armt

@@ -1,0 +1,211 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Tolerances (written here, derived in the design notes):
+  fp32 model (tiny):   max |gpu - oracle| <= 1e-4 on hidden states, A and z.
+  bf16 models:         hidden states: max-abs <= 2e-2 and cosine >= 0.999;
+                       memory state A, z: cosine >= 0.999 and max-abs <= 2e-2
+                       relative to the state's largest magnitude (the state
+                       is not unit-scale, so an absolute bound has no fixed
+                       meaning for it).
+  diagonal vs sequential schedule on the GPU: bitwise equal, always.
+"""
+import dataclasses
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import armt_oracle as O
+from recurrent_memory_transformer_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from recurrent_memory_transformer_gb300 import armt as B  # noqa: E402
+from recurrent_memory_transformer_gb300 import build as build_mod  # noqa: E402
+
+STATS_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                          "gpurun_out", "parity_stats.json")
+
+
+def record(name, **kv):
+    os.makedirs(os.path.dirname(STATS_PATH), exist_ok=True)
+    data = {}
+    if os.path.exists(STATS_PATH):
+        try:
+            data = json.load(open(STATS_PATH))
+        except Exception:
+            data = {}
+    data[name] = kv
+    json.dump(data, open(STATS_PATH, "w"), indent=1)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build_mod.build()
+    B.load_library()
+
+
+def cosine(a, b):
+    a = np.asarray(a, np.float64).ravel(); b = np.asarray(b, np.float64).ravel()
+    return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b) + 1e-300))
+
+
+def stats(gpu, ref):
+    gpu = np.asarray(gpu, np.float64); ref = np.asarray(ref, np.float64)
+    err = np.abs(gpu - ref)
+    return dict(max_abs=float(err.max()), mean_abs=float(err.mean()), ref_absmax=float(np.abs(ref).max()),
+                cos=cosine(gpu, ref), finite=bool(np.isfinite(gpu).all()))
+
+
+def run_gpu(cfg, W, tok, n_seg, schedule):
+    m = B.Model(cfg, W)
+    tok_d = torch.from_numpy(tok).cuda()
+    h, A, z = m.forward(tok_d, n_seg, schedule=schedule)
+    torch.cuda.synchronize()
+    m.armt_sync_status()
+    out = h.cpu().numpy(), A.cpu().numpy(), z.cpu().numpy()
+    m.close()
+    return out
+
+
+# ------------------------------------------------------------ GEMM unit --
+
+@pytest.mark.parametrize("G,M,N,K", [(1, 128, 256, 64), (3, 1040, 512, 2048), (2, 17, 256, 384),
+                                     (1, 300, 768, 8192)])
+def test_grouped_gemm_bf16_matches_fp64_matmul(G, M, N, K):
+    g = torch.Generator(device="cpu").manual_seed(G * 1000 + M)
+    A = torch.randn(G, M, K, generator=g).to(torch.bfloat16)
+    Bm = torch.randn(G, N, K, generator=g).to(torch.bfloat16)
+    C = torch.full((G, M, N), float("nan"), device="cuda")
+    B.armt_grouped_gemm_bf16(A.cuda(), Bm.cuda(), C)
+    torch.cuda.synchronize()
+    ref = np.einsum("gmk,gnk->gmn", A.double().numpy(), Bm.double().numpy())
+    got = C.cpu().double().numpy()
+    err = np.abs(got - ref).max()
+    record(f"gemm_{G}_{M}_{N}_{K}", max_abs=float(err), ref_absmax=float(np.abs(ref).max()))
+    # fp32 accumulation of K products of N(0,1) values: error ~ K * 2^-24 * sqrt(K)
+    assert np.isfinite(got).all()
+    assert err <= 1e-5 * K * 4, err
+
+
+def test_grouped_gemm_each_group_independent():
+    # a group's result does not depend on how many groups share the launch
+    g = torch.Generator(device="cpu").manual_seed(7)
+    A = torch.randn(4, 200, 256, generator=g).to(torch.bfloat16).cuda()
+    Bm = torch.randn(4, 512, 256, generator=g).to(torch.bfloat16).cuda()
+    C4 = torch.empty(4, 200, 512, device="cuda")
+    B.armt_grouped_gemm_bf16(A, Bm, C4)
+    C1 = torch.empty(1, 200, 512, device="cuda")
+    B.armt_grouped_gemm_bf16(A[2:3].contiguous(), Bm[2:3].contiguous(), C1)
+    torch.cuda.synchronize()
+    assert torch.equal(C4[2], C1[0])
+
+
+# ----------------------------------------------------------- tiny fp32 --
+
+TINY_CASES = [
+    ("tiny", {}, 4, 0.0),
+    ("tiny_jitter", {}, 4, 0.1),
+    ("tiny_gqa", {"n_q_heads": 4, "n_kv_heads": 2, "head_dim": 32, "d_model": 128}, 3, 0.1),
+    ("tiny_L3_n5", {"n_layers": 3}, 5, 0.1),
+    ("tiny_one_segment", {}, 1, 0.1),
+    ("tiny_hd64", {"n_q_heads": 2, "n_kv_heads": 1, "head_dim": 64, "d_model": 128}, 3, 0.1),
+]
+
+
+@pytest.mark.parametrize("name,over,n_seg,jit", TINY_CASES)
+def test_tiny_fp32_matches_oracle(name, over, n_seg, jit):
+    cfg = dataclasses.replace(I.TINY, **over)
+    W = I.make_weights(cfg, seed=21, norm_jitter=jit)
+    tok = I.make_tokens(cfg, n_seg, seed=21)
+    hd, Ad, zd = run_gpu(cfg, W, tok, n_seg, B.SCHEDULE_DIAGONAL)
+    hs, As, zs = run_gpu(cfg, W, tok, n_seg, B.SCHEDULE_SEQUENTIAL)
+    ho, Ao, zo = O.forward(cfg, W, tok, n_seg)
+    sh, sa, sz = stats(hd, ho), stats(Ad, Ao), stats(zd, zo)
+    record(name, hidden=sh, A=sa, z=sz)
+    assert np.array_equal(hd, hs) and np.array_equal(Ad, As) and np.array_equal(zd, zs)
+    assert sh["max_abs"] <= 1e-4, sh
+    assert sa["max_abs"] <= 1e-4, sa
+    assert sz["max_abs"] <= 1e-4, sz
+
+
+def test_tiny_resume_and_determinism():
+    cfg = I.TINY
+    W = I.make_weights(cfg, seed=22, norm_jitter=0.1)
+    tok = I.make_tokens(cfg, 4, seed=22)
+    m = B.Model(cfg, W)
+    t = torch.from_numpy(tok).cuda()
+    h, A, z = m.forward(t, 4)
+    h2, A2, z2 = m.forward(t, 4)
+    S = cfg.seg_len
+    ha, Aa, za = m.forward(t[:2 * S].contiguous(), 2)
+    hb, Ab, zb = m.forward(t[2 * S:].contiguous(), 2, mem_A=Aa.reshape(-1), mem_z=za.reshape(-1))
+    torch.cuda.synchronize()
+    assert torch.equal(h, h2) and torch.equal(A, A2) and torch.equal(z, z2)
+    assert torch.equal(torch.cat([ha, hb]), h) and torch.equal(Ab, A) and torch.equal(zb, z)
+    m.close()
+
+
+def test_tiny_host_entry_point_matches_device():
+    cfg = I.TINY
+    W = I.make_weights(cfg, seed=23)
+    tok = I.make_tokens(cfg, 4, seed=23)
+    m = B.Model(cfg, W)
+    h, A, z = m.forward(torch.from_numpy(tok).cuda(), 4)
+    hh = np.empty((4 * cfg.seg_len, cfg.d_model), np.float32)
+    Ah = np.empty(m.a_elems, np.float32); zh = np.empty(m.z_elems, np.float32)
+    m.armt_forward_host(tok, 4, hh, Ah, zh)
+    assert np.array_equal(hh, h.cpu().numpy())
+    assert np.array_equal(Ah, A.cpu().numpy().ravel()) and np.array_equal(zh, z.cpu().numpy().ravel())
+    m.close()
+
+
+def test_out_of_range_tokens_are_clamped_not_faulting():
+    cfg = I.TINY
+    W = I.make_weights(cfg, seed=24)
+    tok = I.make_tokens(cfg, 2, seed=24)
+    bad = tok.copy(); bad[3] = -5; bad[7] = cfg.vocab + 100
+    fixed = bad.copy(); fixed[3] = 0; fixed[7] = cfg.vocab - 1
+    m = B.Model(cfg, W)
+    h1, _, _ = m.forward(torch.from_numpy(bad).cuda(), 2)
+    h2, _, _ = m.forward(torch.from_numpy(fixed).cuda(), 2)
+    torch.cuda.synchronize()
+    assert torch.equal(h1, h2)
+    m.close()
+
+
+# ------------------------------------------------------------- ARMT-1B --
+
+@pytest.fixture(scope="module")
+def armt1b():
+    cfg, n, W, tok = I.make_workload("armt-1b-8k")
+    return cfg, n, W, tok
+
+
+def test_armt1b_8k_matches_oracle_and_schedules_agree(armt1b):
+    cfg, n, W, tok = armt1b
+    m = B.Model(cfg, B.device_weight_tensors(cfg, W))
+    t = torch.from_numpy(tok).cuda()
+    hd, Ad, zd = m.forward(t, n, schedule=B.SCHEDULE_DIAGONAL)
+    hs, As, zs = m.forward(t, n, schedule=B.SCHEDULE_SEQUENTIAL)
+    torch.cuda.synchronize()
+    m.armt_sync_status()
+    bitwise = bool(torch.equal(hd, hs) and torch.equal(Ad, As) and torch.equal(zd, zs))
+    hd, Ad, zd = hd.cpu().numpy(), Ad.cpu().numpy(), zd.cpu().numpy()
+    m.close()
+    ho, Ao, zo = O.forward(cfg, W, tok, n)
+    sh, sa, sz = stats(hd, ho), stats(Ad, Ao), stats(zd, zo)
+    per_seg = [stats(hd[s * cfg.seg_len:(s + 1) * cfg.seg_len], ho[s * cfg.seg_len:(s + 1) * cfg.seg_len])
+               for s in range(n)]
+    record("armt1b_8k", hidden=sh, A=sa, z=sz, bitwise_diag_seq=bitwise,
+           per_segment_max_abs=[p["max_abs"] for p in per_seg],
+           per_segment_cos=[p["cos"] for p in per_seg])
+    assert bitwise
+    assert sh["finite"] and sh["max_abs"] <= 2e-2 and sh["cos"] >= 0.999, sh
+    assert sa["cos"] >= 0.999 and sa["max_abs"] <= 2e-2 * sa["ref_absmax"], sa
+    assert sz["cos"] >= 0.999 and sz["max_abs"] <= 2e-2 * sz["ref_absmax"], sz
