@@ -27,11 +27,13 @@ Oseledets, arXiv:2506.05229):
   equations not printed on the page).  Reading used here, the standard ARMT
   delta rule with DPFP features:
     read:  x <- x + A phi(W_Q x) / (z^T phi(W_Q x) + eps)       (every row)
-    write: for memory rows h_i: k = W_K h, v = W_V h, beta = sigmoid(w_b^T h),
-           phi_i = phi(k), vbar = A phi_i / (z^T phi_i + eps),
-           gamma = 1 - z^T phi_i / (phi_i^T phi_i + eps),
-           A += sum_i beta_i (v_i - vbar_i) phi_i^T,  z += sum_i gamma_i phi_i
-           (all terms against the state before this segment's write).
+    write: for the memory rows h_i, i = 0..M-1 in order, one at a time:
+           k = W_K h_i, v = W_V h_i, beta = sigmoid(w_b^T h_i), p = phi(k),
+           vbar = A p / (z^T p + eps), gamma = 1 - z^T p / (p^T p + eps),
+           A <- A + beta (v - vbar) p^T,  z <- z + gamma p
+           (a delta rule: each write corrects against the state the previous
+           write left; applying all M writes against the pre-segment state
+           instead makes the state diverge on random-init models).
   DPFP_nu(x): r = [relu(x), relu(-x)], phi = concat_{j=1..nu} r * roll(r, j),
   roll(r, j)_i = r_{(i - j) mod 2k}.
 * The LLaMA block run inside each cell (section 三: Llama-3-family models,
@@ -145,9 +147,9 @@ def assoc_read(x, wq_a, A, z, nu, eps):
 
 
 def delta_rule_update(A, z, keys, values, beta, nu, eps) -> Tuple[np.ndarray, np.ndarray]:
-    """One batched delta-rule write of (keys [R,k], values [R,d], beta [R]).
+    """Delta-rule write of (keys [R,k], values [R,d], beta [R]) into (A, z).
 
-    Every term uses the state (A, z) from before the write.
+    All R terms use the state from before the call (R = 1 for one write).
     """
     phi = dpfp(keys, nu)                                   # [R, P]
     zphi = phi @ z                                         # [R]
@@ -159,11 +161,17 @@ def delta_rule_update(A, z, keys, values, beta, nu, eps) -> Tuple[np.ndarray, np
 
 
 def assoc_write(h_mem, wk_a, wv_a, wb_a, A, z, nu, eps):
-    """Write from the memory-token rows h_mem [M, d] of one layer's output."""
+    """Write from the memory-token rows h_mem [M, d] of one layer's output.
+
+    The rows are written one after another in row order; write i sees the
+    state that write i-1 produced.
+    """
     keys = h_mem @ wk_a.T
     values = h_mem @ wv_a.T
     beta = sigmoid(h_mem @ wb_a)
-    return delta_rule_update(A, z, keys, values, beta, nu, eps)
+    for i in range(h_mem.shape[0]):
+        A, z = delta_rule_update(A, z, keys[i:i + 1], values[i:i + 1], beta[i:i + 1], nu, eps)
+    return A, z
 
 
 # --------------------------------------------------------------------------

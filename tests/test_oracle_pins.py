@@ -240,19 +240,20 @@ def test_two_segments_one_layer_hand_expansion():
     gf = W64["norm_f"]
 
     def write(Hm, A, z):
-        # loops over memory rows and entries, written out
-        P = A.shape[1]
-        dA = np.zeros_like(A); dz = np.zeros(P)
+        # memory rows written one after another, each against the state the
+        # previous one left, with the entries written out
+        A = A.copy(); z = z.copy()
         for i in range(Hm.shape[0]):
             key = W64["a_wk"][0] @ Hm[i]; val = W64["a_wv"][0] @ Hm[i]
             beta = 1.0 / (1.0 + math.exp(-(W64["a_wbeta"][0] @ Hm[i])))
             phi = _dpfp_loops(list(key), nu)
             zp = float(z @ phi)
-            vbar = (A @ phi) / (zp + eps)
-            gamma = 1.0 - zp / (float(phi @ phi) + eps)
-            dA += beta * np.outer(val - vbar, phi)
-            dz += gamma * phi
-        return A + dA, z + dz
+            ff = float(phi @ phi)
+            for r in range(A.shape[0]):
+                vbar_r = float(A[r] @ phi) / (zp + eps)
+                A[r] = A[r] + beta * (val[r] - vbar_r) * phi
+            z = z + (1.0 - zp / (ff + eps)) * phi
+        return A, z
 
     P = cfg.phi_dim
     X0 = np.concatenate([W64["embed"][tok[:S]], W64["mem"]])
@@ -282,6 +283,40 @@ def test_resume_from_carried_state():
     np.testing.assert_array_equal(np.concatenate([h1, h2]), full[0])
     np.testing.assert_array_equal(A2, full[1])
     np.testing.assert_array_equal(z2, full[2])
+
+
+def test_memory_tokens_written_in_order():
+    # a state written from rows (h0, h1) differs from one written from (h1, h0)
+    # once the keys interact: the writes are sequential, not a sum
+    rng = np.random.default_rng(8)
+    d, k, nu, eps = 6, 4, 2, 1e-6
+    H = rng.standard_normal((2, d)); wk = rng.standard_normal((k, d)); wv = rng.standard_normal((d, d))
+    H[1] = H[0] + 0.3 * H[1]                     # nearby keys: overlapping features
+    wb = rng.standard_normal(d)
+    P = 2 * k * nu
+    assert _dpfp_loops(list(wk @ H[0]), nu) @ _dpfp_loops(list(wk @ H[1]), nu) > 0.1
+    A1, z1 = O.assoc_write(H, wk, wv, wb, np.zeros((d, P)), np.zeros(P), nu, eps)
+    A2, z2 = O.assoc_write(H[::-1], wk, wv, wb, np.zeros((d, P)), np.zeros(P), nu, eps)
+    assert np.max(np.abs(A1 - A2)) > 1e-6
+    # and the first write into an empty memory is exact recall, whatever follows
+    A0, z0 = O.assoc_write(H[:1], wk, wv, wb, np.zeros((d, P)), np.zeros(P), nu, eps)
+    phi = _dpfp_loops(list(wk @ H[0]), nu)
+    beta = 1.0 / (1.0 + math.exp(-(wb @ H[0])))
+    ff = phi @ phi
+    np.testing.assert_allclose(O.assoc_lookup(A0, z0, phi[None], eps)[0], beta * (wv @ H[0]) * ff / (ff + eps),
+                               rtol=1e-12)
+
+
+def test_state_stays_bounded_on_a_mid_size_model():
+    # 12 segments of a 2-layer d=256 model with the benchmark's weight scale:
+    # the memory state and residual stream stay O(1)
+    cfg = dataclasses.replace(I.ARMT_1B, n_layers=2, d_model=256, n_q_heads=4, n_kv_heads=2,
+                              head_dim=64, ffn_dim=512, vocab=500, seg_len=64, dtype="f32")
+    W = I.make_weights(cfg, seed=3)
+    tok = I.make_tokens(cfg, 12, seed=3)
+    out, A, z = O.forward(cfg, W, tok, 12)
+    assert np.isfinite(out).all()
+    assert np.abs(A).max() < 1.0 and np.abs(z).max() < 10.0
 
 
 def test_tiny_workload_is_well_conditioned():
