@@ -18,12 +18,12 @@
  * reading implemented here is the delta rule with DPFP features:
  *   read  (every row x of a cell, before the attention sub-layer):
  *         x <- x + A_l phi(Wq_a x) / (z_l^T phi(Wq_a x) + assoc_eps)
- *   write (memory-token rows h_i of the cell's output, i = 0..M-1, batched
- *         against the state before the write):
- *         k_i = Wk_a h_i, v_i = Wv_a h_i, beta_i = sigmoid(wbeta_a^T h_i),
- *         p_i = phi(k_i), vbar_i = A_l p_i / (z_l^T p_i + assoc_eps),
- *         gamma_i = 1 - z_l^T p_i / (p_i^T p_i + assoc_eps),
- *         A_l += sum_i beta_i (v_i - vbar_i) p_i^T,  z_l += sum_i gamma_i p_i
+ *   write (memory-token rows h_i of the cell's output, i = 0..M-1 in order,
+ *         each against the state the previous write left -- a delta rule):
+ *         k = Wk_a h_i, v = Wv_a h_i, beta = sigmoid(wbeta_a^T h_i), p = phi(k),
+ *         vbar = A_l p / (z_l^T p + assoc_eps),
+ *         gamma = 1 - z_l^T p / (p^T p + assoc_eps),
+ *         A_l <- A_l + beta (v - vbar) p^T,  z_l <- z_l + gamma p
  *   phi = DPFP of order nu: r = [relu(k), relu(-k)], blocks r * roll(r, j),
  *         j = 1..nu, roll(r, j)_i = r_{(i-j) mod 2k};  P = 2 * key_dim * nu.
  * Each cell runs a LLaMA decoder layer (RMSNorm, rotate-half RoPE at cell
@@ -184,6 +184,20 @@ ARMT_API armt_status armt_forward_host(armt_model* m, const int32_t* h_tokens, i
  * M >= 1.  A fixed reduction order per element independent of G. */
 ARMT_API armt_status armt_grouped_gemm_bf16(const void* A, const void* B, float* C, int32_t G, int32_t M,
                                    int32_t N, int32_t K, void* stream);
+
+/* Segment-local causal grouped-query attention, batched over G cells
+ * (section 三: attention is left as it is and batched over the cells of a
+ * diagonal).  For g = 0..G-1, query head h = 0..Hq-1 reads kv head
+ * h / (Hq/Hkv); row t attends to rows 0..t of the same cell:
+ *   out[g][t][h*hd : (h+1)*hd] = softmax_u(q_t . k_u / sqrt(hd)) v_u
+ *   qk  device bf16 [G][T][(Hq+Hkv)*hd]: q heads then k heads (already rotated)
+ *   vt  device bf16 [G][Hkv][hd][T]: v transposed (token index innermost)
+ *   out device bf16 [G][T][Hq*hd]
+ * tcgen05 tensor cores, fp32 softmax and accumulation.  hd in {64, 128},
+ * T % 8 == 0, 16-byte aligned pointers. */
+ARMT_API armt_status armt_segment_attention_bf16(const void* qk, const void* vt, void* out, int32_t G,
+                                                 int32_t T, int32_t Hq, int32_t Hkv, int32_t hd,
+                                                 void* stream);
 
 /* Sizes of the memory state buffers for this model (elements). */
 ARMT_API armt_status armt_state_sizes(const armt_model* m, int64_t* a_elems, int64_t* z_elems);

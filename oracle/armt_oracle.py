@@ -48,6 +48,15 @@ Everything is float64 with no intermediate rounding; bf16 models arrive as
 float32 arrays holding bf16 values and are widened exactly.  numpy matmul is
 used as a library primitive; nothing is blocked, fused or reordered beyond
 the definitions above.
+
+Optional precision model (``operands="bf16"``): the same arithmetic in fp64,
+except that every tensor-core operand of a bf16 kernel path is rounded to the
+nearest bf16 value first -- the layer input for the associative query, the
+features and the state copy of the associative read, both RMSNorm outputs,
+q/k after RoPE and v, the attention probabilities (before normalisation by
+the row sum) and the attention output, the SwiGLU output, and the memory
+rows fed to the write projections.  This is a model of a design choice, not
+of the method; the default (``operands=None``) is the method itself.
 """
 from __future__ import annotations
 
@@ -60,6 +69,25 @@ F64 = np.float64
 
 def _f64(a):
     return np.asarray(a, dtype=F64)
+
+
+def _identity(a):
+    return a
+
+
+def round_bf16(a):
+    """Nearest bf16 value (ties to even), via float32, returned as float64.
+
+    Values are first rounded to float32; the fp32 -> bf16 step keeps the top
+    16 bits after adding 0x7FFF plus the lowest kept bit (round half to even).
+    """
+    b = np.ascontiguousarray(np.asarray(a, dtype=np.float32)).view(np.uint32)
+    lsb = (b >> np.uint32(16)) & np.uint32(1)
+    r = (b + np.uint32(0x7FFF) + lsb) & np.uint32(0xFFFF0000)
+    return r.view(np.float32).astype(F64)
+
+
+ROUNDING = {None: _identity, "bf16": round_bf16}
 
 
 # --------------------------------------------------------------------------
@@ -108,11 +136,12 @@ def rope_rotate_half(x, base):
     return np.concatenate([x1 * cos - x2 * sin, x2 * cos + x1 * sin], axis=-1)
 
 
-def causal_gqa_attention(q, k, v):
+def causal_gqa_attention(q, k, v, rnd=_identity):
     """softmax(q k^T / sqrt(hd) + causal mask) v per query head.
 
     q [T, Hq, hd], k/v [T, Hkv, hd]; query head h reads kv head h*Hkv//Hq.
-    Returns [T, Hq*hd].
+    Returns [T, Hq*hd].  ``rnd`` (precision model only) is applied to the
+    unnormalised probabilities before they multiply v.
     """
     T, Hq, hd = q.shape
     Hkv = k.shape[1]
@@ -124,8 +153,7 @@ def causal_gqa_attention(q, k, v):
         s = np.where(mask, -np.inf, s)
         s = s - s.max(axis=-1, keepdims=True)
         p = np.exp(s)
-        p = p / p.sum(axis=-1, keepdims=True)
-        out[:, h, :] = p @ v[:, g, :]
+        out[:, h, :] = (rnd(p) @ v[:, g, :]) / p.sum(axis=-1, keepdims=True)
     return out.reshape(T, Hq * hd)
 
 
@@ -133,17 +161,17 @@ def causal_gqa_attention(q, k, v):
 # Associative memory (delta rule)
 # --------------------------------------------------------------------------
 
-def assoc_lookup(A, z, phi, eps):
+def assoc_lookup(A, z, phi, eps, rnd=_identity):
     """A phi / (z^T phi + eps) for each row of phi [R, P]; A [d, P], z [P]."""
-    num = phi @ A.T
+    num = rnd(phi) @ rnd(A).T
     den = phi @ z + eps
     return num / den[:, None]
 
 
-def assoc_read(x, wq_a, A, z, nu, eps):
+def assoc_read(x, wq_a, A, z, nu, eps, rnd=_identity):
     """Memory read added to the residual stream: x + lookup(phi(W_Q x))."""
-    phi = dpfp(x @ wq_a.T, nu)
-    return x + assoc_lookup(A, z, phi, eps)
+    phi = dpfp(rnd(x) @ wq_a.T, nu)
+    return x + assoc_lookup(A, z, phi, eps, rnd)
 
 
 def delta_rule_update(A, z, keys, values, beta, nu, eps) -> Tuple[np.ndarray, np.ndarray]:
@@ -160,12 +188,13 @@ def delta_rule_update(A, z, keys, values, beta, nu, eps) -> Tuple[np.ndarray, np
     return A + dA, z + dz
 
 
-def assoc_write(h_mem, wk_a, wv_a, wb_a, A, z, nu, eps):
+def assoc_write(h_mem, wk_a, wv_a, wb_a, A, z, nu, eps, rnd=_identity):
     """Write from the memory-token rows h_mem [M, d] of one layer's output.
 
     The rows are written one after another in row order; write i sees the
     state that write i-1 produced.
     """
+    h_mem = rnd(h_mem)
     keys = h_mem @ wk_a.T
     values = h_mem @ wv_a.T
     beta = sigmoid(h_mem @ wb_a)
@@ -178,29 +207,29 @@ def assoc_write(h_mem, wk_a, wv_a, wb_a, A, z, nu, eps):
 # One cell and the whole grid
 # --------------------------------------------------------------------------
 
-def llama_block(x, cfg, W, l):
+def llama_block(x, cfg, W, l, rnd=_identity):
     """Pre-norm LLaMA decoder layer on the rows of one cell (x [T_c, d])."""
     T = x.shape[0]
     Hq, Hkv, hd = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
-    n = rmsnorm(x, W["norm1"][l], cfg.norm_eps)
+    n = rnd(rmsnorm(x, W["norm1"][l], cfg.norm_eps))
     q = (n @ W["wq"][l].T).reshape(T, Hq, hd)
     k = (n @ W["wk"][l].T).reshape(T, Hkv, hd)
-    v = (n @ W["wv"][l].T).reshape(T, Hkv, hd)
-    q = rope_rotate_half(q, cfg.rope_base)
-    k = rope_rotate_half(k, cfg.rope_base)
-    y = x + causal_gqa_attention(q, k, v) @ W["wo"][l].T
-    n2 = rmsnorm(y, W["norm2"][l], cfg.norm_eps)
-    u = silu(n2 @ W["w_gate"][l].T) * (n2 @ W["w_up"][l].T)
+    v = rnd((n @ W["wv"][l].T).reshape(T, Hkv, hd))
+    q = rnd(rope_rotate_half(q, cfg.rope_base))
+    k = rnd(rope_rotate_half(k, cfg.rope_base))
+    y = x + rnd(causal_gqa_attention(q, k, v, rnd)) @ W["wo"][l].T
+    n2 = rnd(rmsnorm(y, W["norm2"][l], cfg.norm_eps))
+    u = rnd(silu(n2 @ W["w_gate"][l].T) * (n2 @ W["w_up"][l].T))
     return y + u @ W["w_down"][l].T
 
 
-def cell_forward(x, cfg, W, l, A, z):
+def cell_forward(x, cfg, W, l, A, z, rnd=_identity):
     """Cell (l, s): read, LLaMA block, write.  Returns (h, A', z')."""
     nu, eps = cfg.dpfp_nu, cfg.assoc_eps
-    x = assoc_read(x, W["a_wq"][l], A, z, nu, eps)
-    h = llama_block(x, cfg, W, l)
+    x = assoc_read(x, W["a_wq"][l], A, z, nu, eps, rnd)
+    h = llama_block(x, cfg, W, l, rnd)
     S = cfg.seg_len
-    A2, z2 = assoc_write(h[S:], W["a_wk"][l], W["a_wv"][l], W["a_wbeta"][l], A, z, nu, eps)
+    A2, z2 = assoc_write(h[S:], W["a_wk"][l], W["a_wv"][l], W["a_wbeta"][l], A, z, nu, eps, rnd)
     return h, A2, z2
 
 
@@ -226,12 +255,14 @@ def schedule(n_layers: int, n_segments: int, order: str):
     raise ValueError(order)
 
 
-def forward(cfg, W, tokens, n_segments, order="seq", A0=None, z0=None, W64=None):
+def forward(cfg, W, tokens, n_segments, order="seq", A0=None, z0=None, W64=None, operands=None):
     """ARMT forward over n_segments segments.
 
     Returns (hidden [n*S, d], A [L, d, P], z [L, P]) in float64.  ``A0``/``z0``
-    give an initial memory state (zeros when None).
+    give an initial memory state (zeros when None).  ``operands="bf16"``
+    selects the bf16 operand-rounding precision model (module docstring).
     """
+    rnd = ROUNDING[operands]
     L, d, P, S = cfg.n_layers, cfg.d_model, cfg.phi_dim, cfg.seg_len
     W = W64 if W64 is not None else widen_weights(W)
     tokens = np.asarray(tokens)
@@ -245,7 +276,7 @@ def forward(cfg, W, tokens, n_segments, order="seq", A0=None, z0=None, W64=None)
     for step in schedule(L, n_segments, order):
         for (l, s) in step:
             x = layer0_input(cfg, W, tokens, s) if l == 0 else acts.pop((l - 1, s))
-            h, A[l], z[l] = cell_forward(x, cfg, W, l, A[l], z[l])
+            h, A[l], z[l] = cell_forward(x, cfg, W, l, A[l], z[l], rnd)
             if l == L - 1:
                 out[s * S:(s + 1) * S] = rmsnorm(h[:S], W["norm_f"], cfg.norm_eps)
             else:

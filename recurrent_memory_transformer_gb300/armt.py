@@ -27,7 +27,8 @@ KERNEL_CLASSES = ("gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down", "attention",
                   "assoc_write", "norm", "other")
 
 EXPORTED = ("armt_create", "armt_destroy", "armt_forward", "armt_forward_sequential",
-            "armt_forward_host", "armt_grouped_gemm_bf16", "armt_state_sizes", "armt_launch_count",
+            "armt_forward_host", "armt_grouped_gemm_bf16", "armt_segment_attention_bf16",
+            "armt_state_sizes", "armt_launch_count",
             "armt_set_profiling", "armt_kernel_times", "armt_sync_status", "armt_status_string",
             "armt_last_error")
 
@@ -77,6 +78,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         fn.argtypes = [P, P, I64, P, P, P, I32, P]
     lib.armt_forward_host.argtypes = [P, P, I64, P, P, P, I32, I32, P]
     lib.armt_grouped_gemm_bf16.argtypes = [P, P, P, I32, I32, I32, I32, P]
+    lib.armt_segment_attention_bf16.argtypes = [P, P, P, I32, I32, I32, I32, I32, P]
     lib.armt_state_sizes.argtypes = [P, ctypes.POINTER(I64), ctypes.POINTER(I64)]
     lib.armt_launch_count.argtypes = [P, I64, I32, ctypes.POINTER(I64)]
     lib.armt_set_profiling.argtypes = [P, I32]
@@ -238,3 +240,12 @@ def armt_grouped_gemm_bf16(A, B, C, stream=None):
     N = B.shape[1]
     _check(lib.armt_grouped_gemm_bf16(_ptr(A), _ptr(B), _ptr(C), G, M, N, K, _stream_ptr(stream)),
            "armt_grouped_gemm_bf16")
+
+
+def armt_segment_attention_bf16(qk, vt, out, Hq, Hkv, stream=None):
+    """Causal GQA per cell: qk bf16 [G,T,(Hq+Hkv)*hd], vt bf16 [G,Hkv,hd,T], out bf16 [G,T,Hq*hd]."""
+    lib = load_library()
+    G, T, _ = qk.shape
+    hd = vt.shape[2]
+    _check(lib.armt_segment_attention_bf16(_ptr(qk), _ptr(vt), _ptr(out), G, T, Hq, Hkv, hd,
+                                           _stream_ptr(stream)), "armt_segment_attention_bf16")

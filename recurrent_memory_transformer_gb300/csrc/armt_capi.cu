@@ -30,6 +30,7 @@
 #include "../../include/armt.h"
 #include "common.cuh"
 #include "epilogues.cuh"
+#include "attn_tc.cuh"
 #include "gemm_tc.cuh"
 #include "kernels.cuh"
 
@@ -180,7 +181,7 @@ struct ModelBase {
     n += per_gemm + 1 + per_gemm;           // associative query GEMM, phi, read GEMM
     n += 1 + per_gemm + 1 + per_gemm;       // norm1, QKV GEMM, attention, O GEMM
     n += 1 + per_gemm + per_gemm;           // norm2, gate-up GEMM, down GEMM
-    n += 3;                                 // delta-rule write
+    n += per_gemm + 2;                      // delta-rule write: projection GEMM, z, A rows
     if (hi == cfg.n_layers - 1) n += 1;     // final norm
     return n;
   }
@@ -234,16 +235,19 @@ struct Model : ModelBase {
 
   // weights (library layout)
   WT *embed = nullptr, *memtok = nullptr, *Wqkv = nullptr, *Wo = nullptr, *Wgu = nullptr,
-     *Wd = nullptr, *aWq = nullptr, *aWk = nullptr, *aWv = nullptr, *aWb = nullptr;
+     *Wd = nullptr, *aWq = nullptr, *Ww = nullptr;  // Ww: per layer [Wv_a; Wk_a; wbeta_a; 0]
   float *g1 = nullptr, *g2 = nullptr, *gf = nullptr, *cosT = nullptr, *sinT = nullptr;
   // activations, all [layer or slot][rows][width]
-  float *X = nullptr, *Res = nullptr, *Qa = nullptr, *Den = nullptr, *KB = nullptr,
+  float *X = nullptr, *Res = nullptr, *Qa = nullptr, *Den = nullptr, *VKB = nullptr,
         *PhiM = nullptr, *Coef = nullptr, *Cscr = nullptr;
+  int nw = 0;  // rows of Ww per layer (d + k + 1 rounded up to the tile width)
   AT *Xa = nullptr, *Nrm = nullptr, *QKV = nullptr, *Att = nullptr, *U = nullptr, *Phi = nullptr,
-     *Aa = nullptr;
+     *Aa = nullptr, *Vt = nullptr;
+  int qkv_ld = 0, t_pad = 0;  // row stride of QKV; padded row count of Vt
   int nmax = 0;  // widest GEMM output (fp32 scratch row stride)
   // tensor maps (bf16 path)
-  CUtensorMap tmXa, tmAWq, tmPhi, tmAa, tmNrm, tmWqkv, tmAtt, tmWo, tmWgu, tmU, tmWd;
+  CUtensorMap tmXa, tmAWq, tmPhi, tmAa, tmNrm, tmWqkv, tmAtt, tmWo, tmWgu, tmU, tmWd, tmQK, tmVt,
+      tmWw;
   size_t upd_smem = 0, feat_smem = 0, attn_smem = 0;
   int upd_rows_per_block = 64;
 
@@ -297,12 +301,16 @@ struct Model : ModelBase {
     CKS(copy_in(Wd, w->w_down, L * d * F * es, st));
     CKS(mem.alloc_n(&aWq, L * k * d));
     CKS(copy_in(aWq, w->a_wq, L * k * d * es, st));
-    CKS(mem.alloc_n(&aWk, L * k * d));
-    CKS(copy_in(aWk, w->a_wk, L * k * d * es, st));
-    CKS(mem.alloc_n(&aWv, L * d * d));
-    CKS(copy_in(aWv, w->a_wv, L * d * d * es, st));
-    CKS(mem.alloc_n(&aWb, L * d));
-    CKS(copy_in(aWb, w->a_wbeta, L * d * es, st));
+    // write projections stacked per layer: rows [0,d) Wv_a, [d,d+k) Wk_a, d+k wbeta_a
+    nw = (int)((d + k + 1 + (kTC ? 255 : 15)) / (kTC ? 256 : 16) * (kTC ? 256 : 16));
+    CKS(mem.alloc_n(&Ww, L * (size_t)nw * d));
+    CK(cudaMemsetAsync(Ww, 0, L * (size_t)nw * d * es, st));
+    CK(cudaMemcpy2DAsync(Ww, (size_t)nw * d * es, w->a_wv, d * d * es, d * d * es, L,
+                         cudaMemcpyDefault, st));
+    CK(cudaMemcpy2DAsync(Ww + d * d, (size_t)nw * d * es, w->a_wk, k * d * es, k * d * es, L,
+                         cudaMemcpyDefault, st));
+    CK(cudaMemcpy2DAsync(Ww + (d + k) * d, (size_t)nw * d * es, w->a_wbeta, d * es, d * es, L,
+                         cudaMemcpyDefault, st));
     CKS(gain_to_f32(&g1, w->norm1, L * d, st));
     CKS(gain_to_f32(&g2, w->norm2, L * d, st));
     CKS(gain_to_f32(&gf, w->norm_f, d, st));
@@ -329,27 +337,29 @@ struct Model : ModelBase {
     }
     CKS(mem.alloc_n(&Res, L * T * d));
     CKS(mem.alloc_n(&Nrm, L * T * d));
-    CKS(mem.alloc_n(&QKV, L * T * Nq));
+    // bf16: q|k rows in QKV, v transposed into Vt; fp32: q|k|v rows in QKV
+    qkv_ld = kTC ? (int)((Hq + Hkv) * hd) : (int)Nq;
+    t_pad = (int)((T + 7) / 8 * 8);
+    CKS(mem.alloc_n(&QKV, L * T * (size_t)qkv_ld));
+    if (kTC) CKS(mem.alloc_n(&Vt, L * Hkv * hd * (size_t)t_pad));
     CKS(mem.alloc_n(&Att, L * T * Hq * hd));
     CKS(mem.alloc_n(&U, L * T * F));
     CKS(mem.alloc_n(&Qa, L * T * k));
     CKS(mem.alloc_n(&Phi, L * T * P));
     CKS(mem.alloc_n(&Den, L * T));
-    CKS(mem.alloc_n(&KB, L * c.n_mem * (k + 1)));
+    CKS(mem.alloc_n(&VKB, L * c.n_mem * (size_t)nw));
     CKS(mem.alloc_n(&PhiM, L * c.n_mem * P));
     CKS(mem.alloc_n(&Coef, L * c.n_mem * 2));
     if (kTC) CKS(mem.alloc_n(&Aa, L * d * P));
-    nmax = (int)std::max(std::max(Nq, d), std::max(2 * F, k));
+    nmax = (int)std::max(std::max(Nq, d), std::max(2 * F, std::max(k, (size_t)nw)));
     if (!kTC) CKS(mem.alloc_n(&Cscr, L * T * (size_t)nmax));
     CKS(mem.alloc_n(&d_err, 1));
     CK(cudaMemsetAsync(d_err, 0, sizeof(int), st));
     // kernel configuration
-    upd_smem = ((size_t)c.n_mem * d + (size_t)c.n_mem * P + 2 * c.n_mem) * sizeof(float);
-    feat_smem = ((size_t)c.n_mem * 2 * k + 2 * c.n_mem) * sizeof(float);
+    upd_smem = ((size_t)c.n_mem * P + 2 * c.n_mem) * sizeof(float);
+    feat_smem = (size_t)c.n_mem * 2 * k * sizeof(float);
     attn_smem = 2 * 64 * hd * sizeof(float);
-    if (upd_smem > 200 * 1024)
-      return fail(ARMT_ERR_UNSUPPORTED, "n_mem * (d_model + P) too large for the write kernel");
-    CK(cudaFuncSetAttribute(assoc_write_update_kernel<WT, AT>,
+    CK(cudaFuncSetAttribute(assoc_write_update_kernel<AT>,
                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem));
     if (hd == 64)
       CK(cudaFuncSetAttribute(attn_simt_kernel<AT, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -370,6 +380,9 @@ struct Model : ModelBase {
       ok &= encode_tmap_bf16_3d(&tmWgu, Wgu, (int)d, (int)(2 * F), (int)L, 256);
       ok &= encode_tmap_bf16_3d(&tmU, U, (int)F, (int)T, (int)L, TC_BM);
       ok &= encode_tmap_bf16_3d(&tmWd, Wd, (int)F, (int)d, (int)L, 256);
+      ok &= encode_tmap_bf16_3d(&tmQK, QKV, qkv_ld, (int)T, (int)L, 128);
+      ok &= encode_tmap_bf16_3d(&tmVt, Vt, t_pad, (int)hd, (int)(L * Hkv), (int)hd);
+      ok &= encode_tmap_bf16_3d(&tmWw, Ww, (int)d, nw, (int)L, 256);
       if (!ok) return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     }
     CK(cudaStreamSynchronize(st));
@@ -377,21 +390,26 @@ struct Model : ModelBase {
   }
 
   // One grouped GEMM over layers [lo, lo+g): tensor cores for bf16, SIMT +
-  // row epilogue for fp32.
+  // row epilogue for fp32.  Output rows 0..rows-1 read A rows row0.. of layer
+  // slot (layer + a_slot_off).
   template <int BN, class Epi>
   armt_status gemm(int cls, const CUtensorMap& ta, const CUtensorMap& tb, const AT* a, long long a_gs,
-                   const WT* b, int N, int K, const Epi& epi, int lo, int g, cudaStream_t st) {
-    const int T = rows();
+                   const WT* b, int N, int K, const Epi& epi, int lo, int g, cudaStream_t st,
+                   int rows = -1, int row0 = 0, int a_slot_off = 0) {
+    if (rows < 0) rows = this->rows();
     CKS(prof_begin(cls, st));
     if constexpr (kTC) {
-      CK((launch_gemm_tc<Epi, BN>(ta, tb, T, N, K, lo, g, d_err, epi, num_sms, st)));
+      CK((launch_gemm_tc<Epi, BN>(ta, tb, rows, N, K, lo, g, d_err, epi, num_sms, st, row0,
+                                  a_slot_off)));
     } else {
-      dim3 grid((N + 63) / 64, (T + 63) / 64, g);
-      gemm_simt_f32_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float*>(a), a_gs, K,
-                                                 reinterpret_cast<const float*>(b), (long long)N * K,
-                                                 Cscr, (long long)T * nmax, nmax, T, N, K, lo);
+      const float* a0 = reinterpret_cast<const float*>(a) + a_slot_off * a_gs + (long long)row0 * K;
+      dim3 grid((N + 63) / 64, (rows + 63) / 64, g);
+      gemm_simt_f32_kernel<<<grid, 256, 0, st>>>(a0, a_gs, K, reinterpret_cast<const float*>(b),
+                                                 (long long)N * K, Cscr,
+                                                 (long long)this->rows() * nmax, nmax, rows, N, K, lo);
       CK(cudaGetLastError());
-      epi_rows_kernel<Epi><<<dim3(T, g), 128, 0, st>>>(Cscr, (long long)T * nmax, nmax, N, lo, epi);
+      epi_rows_kernel<Epi><<<dim3(rows, g), 128, 0, st>>>(Cscr, (long long)this->rows() * nmax, nmax,
+                                                          N, lo, epi);
       CK(cudaGetLastError());
     }
     CKS(prof_end(st));
@@ -434,9 +452,24 @@ struct Model : ModelBase {
     CK(cudaGetLastError());
     CKS(prof_end(st));
     CKS((gemm<256>(ARMT_KC_GEMM_QKV, tmNrm, tmWqkv, Nrm, Td, Wqkv, Nq, d,
-                   EpiQkvRope<AT>{QKV, cosT, sinT, T, hd, (Hq + Hkv) * hd, Nq}, lo, g, st)));
+                   EpiQkvRope<AT>{QKV, cosT, sinT, T, hd, (Hq + Hkv) * hd, qkv_ld, Vt, Hkv, t_pad},
+                   lo, g, st)));
     CKS(prof_begin(ARMT_KC_ATTENTION, st));
-    {
+    if constexpr (kTC) {
+      AttnArgs aa;
+      aa.out = Att;
+      aa.T = T;
+      aa.Hq = Hq;
+      aa.Hkv = Hkv;
+      aa.g_first = lo;
+      aa.n_qtiles = (T + 127) / 128;
+      aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
+      aa.err = d_err;
+      if (hd == 64)
+        CK(launch_attn_tc<64>(tmQK, tmVt, aa, g, st));
+      else
+        CK(launch_attn_tc<128>(tmQK, tmVt, aa, g, st));
+    } else {
       dim3 grid((T + 63) / 64, Hq, g);
       const float scale = 1.0f / sqrtf((float)hd);
       if (hd == 64)
@@ -459,19 +492,23 @@ struct Model : ModelBase {
                    EpiSwiGLU<AT>{U, T, F}, lo, g, st)));
     CKS((gemm<256>(ARMT_KC_GEMM_DOWN, tmU, tmWd, U, (long long)T * F, Wd, d, F,
                    EpiResidual<AT>{Res, X, kTC ? Xa : nullptr, T, d, 1}, lo, g, st)));
-    // delta-rule write from the memory-token rows of this layer's output
+    // delta-rule write from the memory-token rows of this layer's output:
+    // [v | k | beta] = h_mem [Wv_a; Wk_a; wbeta_a]^T on the tensor cores (A =
+    // rows S..S+M-1 of layer slot l+1), then the normaliser recurrence and
+    // the row-wise update of A.
+    CKS((gemm<256>(ARMT_KC_ASSOC_WRITE, tmXa, tmWw, Xa, Td, Ww, nw, d,
+                   EpiStore{VKB, (long long)nw, (long long)M * nw}, lo, g, st, M, S, 1)));
     CKS(prof_begin(ARMT_KC_ASSOC_WRITE, st));
-    const float* Hout = X + Td;  // slot l+1 is layer l's output
-    assoc_write_proj_kernel<WT><<<dim3(k + 1, g), 256, 0, st>>>(Hout, Td, aWk, aWb, KB, S, M, d, k, lo);
+    assoc_write_feat_kernel<<<g, 256, feat_smem, st>>>(VKB, z, PhiM, Coef, M, k, c.dpfp_nu,
+                                                       c.assoc_eps, d, nw, lo);
     CK(cudaGetLastError());
-    assoc_write_feat_kernel<<<g, 256, feat_smem, st>>>(KB, z, PhiM, Coef, M, k, c.dpfp_nu,
-                                                       c.assoc_eps, lo);
-    CK(cudaGetLastError());
+    CKS(prof_end(st));
+    CKS(prof_begin(ARMT_KC_ASSOC_WRITE, st));
     {
       dim3 grid((d + upd_rows_per_block - 1) / upd_rows_per_block, g);
       AT* Adst = kTC ? Aa : reinterpret_cast<AT*>(A);
-      assoc_write_update_kernel<WT, AT><<<grid, 512, upd_smem, st>>>(
-          Hout, Td, aWv, PhiM, Coef, A, Adst, S, M, d, P, upd_rows_per_block, lo);
+      assoc_write_update_kernel<AT><<<grid, 256, upd_smem, st>>>(VKB, nw, PhiM, Coef, A, Adst, M, d,
+                                                                 P, upd_rows_per_block, lo);
       CK(cudaGetLastError());
     }
     CKS(prof_end(st));
@@ -528,6 +565,8 @@ static armt_status validate(const armt_config* c) {
     return fail(ARMT_ERR_SHAPE, "n_q_heads must be a multiple of n_kv_heads");
   if (c->n_mem > 32) return fail(ARMT_ERR_UNSUPPORTED, "n_mem > 32");
   if (c->dpfp_nu >= 2 * c->key_dim) return fail(ARMT_ERR_SHAPE, "dpfp_nu must be < 2 * key_dim");
+  if ((2 * c->key_dim * c->dpfp_nu) % 32 != 0 || 2 * c->key_dim * c->dpfp_nu > 512)
+    return fail(ARMT_ERR_SHAPE, "2 * key_dim * dpfp_nu must be a multiple of 32 and <= 512");
   const int hd = c->head_dim, d = c->d_model, F = c->ffn_dim;
   const int Nq = (c->n_q_heads + 2 * c->n_kv_heads) * hd;
   const int P = 2 * c->key_dim * c->dpfp_nu;
@@ -535,6 +574,7 @@ static armt_status validate(const armt_config* c) {
   if (hd != 32 && hd != 64 && hd != 128) return fail(ARMT_ERR_UNSUPPORTED, "head_dim must be 32, 64 or 128");
   if (F % GU_BLK != 0) return fail(ARMT_ERR_SHAPE, "ffn_dim must be a multiple of 128");
   if (d % 32 != 0 || Nq % 64 != 0) return fail(ARMT_ERR_SHAPE, "d_model % 32, qkv width % 64");
+  if (c->key_dim % 16 != 0) return fail(ARMT_ERR_SHAPE, "key_dim must be a multiple of 16");
   if (c->dtype == ARMT_BF16) {
     if (hd == 32) return fail(ARMT_ERR_UNSUPPORTED, "bf16 models need head_dim 64 or 128");
     if (d % 256 != 0 || Nq % 256 != 0)
@@ -717,6 +757,45 @@ armt_status armt_grouped_gemm_bf16(const void* A, const void* B, float* C, int32
   EpiStore epi{C, (long long)N, (long long)M * N};
   CK((launch_gemm_tc<EpiStore, 256>(ta, tb, M, N, K, 0, G, err, epi, g_num_sms(dev),
                                     reinterpret_cast<cudaStream_t>(stream))));
+  return ARMT_OK;
+}
+
+armt_status armt_segment_attention_bf16(const void* qk, const void* vt, void* out, int32_t G,
+                                        int32_t T, int32_t Hq, int32_t Hkv, int32_t hd,
+                                        void* stream) {
+  if (qk == nullptr || vt == nullptr || out == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
+  if (G <= 0 || T <= 0 || Hq <= 0 || Hkv <= 0) return fail(ARMT_ERR_ARG, "sizes must be positive");
+  if (Hq % Hkv != 0) return fail(ARMT_ERR_SHAPE, "Hq must be a multiple of Hkv");
+  if (hd != 64 && hd != 128) return fail(ARMT_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (T % 8 != 0) return fail(ARMT_ERR_SHAPE, "T must be a multiple of 8");
+  if ((reinterpret_cast<uintptr_t>(qk) | reinterpret_cast<uintptr_t>(vt) |
+       reinterpret_cast<uintptr_t>(out)) & 15)
+    return fail(ARMT_ERR_ARG, "pointers must be 16-byte aligned");
+  int dev = 0;
+  CKS(check_device(&dev));
+  static int* err = nullptr;
+  if (err == nullptr) {
+    CK(cudaMalloc(&err, sizeof(int)));
+    CK(cudaMemset(err, 0, sizeof(int)));
+  }
+  CUtensorMap tq, tv;
+  if (!encode_tmap_bf16_3d(&tq, qk, (Hq + Hkv) * hd, T, G, 128) ||
+      !encode_tmap_bf16_3d(&tv, vt, T, hd, G * Hkv, hd))
+    return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  AttnArgs aa;
+  aa.out = reinterpret_cast<bf16*>(out);
+  aa.T = T;
+  aa.Hq = Hq;
+  aa.Hkv = Hkv;
+  aa.g_first = 0;
+  aa.n_qtiles = (T + 127) / 128;
+  aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
+  aa.err = err;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (hd == 64)
+    CK(launch_attn_tc<64>(tq, tv, aa, G, st));
+  else
+    CK(launch_attn_tc<128>(tq, tv, aa, G, st));
   return ARMT_OK;
 }
 

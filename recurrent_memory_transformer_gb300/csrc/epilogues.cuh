@@ -64,17 +64,25 @@ __device__ __forceinline__ void load_row(const float* src, float* v, int n) {
 // ------------------------------------------------------------- functors --
 
 struct EpiStore {
-  static constexpr int GROUP = 32;
+  static constexpr int GROUP = 16;  // narrow outputs (e.g. a 16-wide key projection) too
   float* C;
   long long ld;        // row stride (elements)
   long long g_stride;  // stride between layers/groups (elements)
   template <class Src>
   __device__ __forceinline__ void operator()(int g, int row, bool valid, int col0, int ncols,
                                              Src& src) const {
-    for (int c = 0; c < ncols; c += 32) {
+    float* dst = C + g * g_stride + (long long)row * ld + col0;
+    int c = 0;
+    for (; c + 32 <= ncols; c += 32) {
       float v[32];
       src.template load<32>(c, v);
-      if (valid) store_row(C + g * g_stride + (long long)row * ld + col0 + c, v, 32);
+      if (valid) store_row(dst + c, v, 32);
+    }
+    for (; c < ncols; c += 16) {
+      float v[16];
+      src.template load<16>(c, v);
+      if (valid)
+        for (int i = 0; i < 16; ++i) dst[c + i] = v[i];
     }
   }
 };
@@ -106,23 +114,30 @@ struct EpiAssocRead {
 };
 
 // Fused Q|K|V projection output with rotate-half RoPE on the q and k heads.
-// Columns [0, Hq*hd) are q, then Hkv*hd of k, then Hkv*hd of v.  cos/sin
-// tables are [rows][hd/2] (position = row within the cell).
+// Accumulator columns [0, Hq*hd) are q, then Hkv*hd of k, then Hkv*hd of v.
+// q and k go to `out` (row stride `ld`); v goes to `out` too when vt is null
+// (fp32 path), else transposed into vt[l][g][c][t] (row stride t_pad) so the
+// tensor-core attention reads it K-major.  cos/sin tables are [rows][hd/2]
+// (position = row within the cell).
 template <typename OutT>
 struct EpiQkvRope {
   static constexpr int GROUP = 64;  // callers pass whole heads (ncols a multiple of hd)
-  OutT* out;                        // [L][rows][(Hq+2Hkv)*hd]
+  OutT* out;
   const float* cosT;
   const float* sinT;
-  int rows, hd, n_rope_cols, ncols_total;  // n_rope_cols = (Hq+Hkv)*hd
+  int rows, hd, n_rope_cols, ld;    // n_rope_cols = (Hq+Hkv)*hd
+  OutT* vt;                         // nullptr: v stays in `out`
+  int n_kv, t_pad;
+
   template <int CH, class Src>
-  __device__ __forceinline__ void rope_chunk(int row, bool valid, bool rope, int hcol, int h0,
-                                             int i0, long long rbase, Src& src) const {
+  __device__ __forceinline__ void rope_chunk(int l, int row, bool valid, int hcol, int h0, int i0,
+                                             long long rbase, Src& src) const {
     const int half = hd >> 1;
     float x1[CH], x2[CH];
     src.template load<CH>(h0 + i0, x1);
     src.template load<CH>(h0 + half + i0, x2);
     if (!valid) return;
+    const bool rope = hcol < n_rope_cols;
     if (rope) {
       const float* cr = cosT + (long long)row * half + i0;
       const float* sr = sinT + (long long)row * half + i0;
@@ -133,6 +148,15 @@ struct EpiQkvRope {
         x1[i] = a * c - b * s;
         x2[i] = b * c + a * s;
       }
+    } else if (vt != nullptr) {
+      const int g = (hcol - n_rope_cols) / hd;
+      OutT* col0 = vt + ((long long)(l * n_kv + g) * hd) * t_pad + row;
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        st_from_f32(col0 + (long long)(i0 + i) * t_pad, x1[i]);
+        st_from_f32(col0 + (long long)(half + i0 + i) * t_pad, x2[i]);
+      }
+      return;
     }
     store_row(out + rbase + hcol + i0, x1, CH);
     store_row(out + rbase + hcol + half + i0, x2, CH);
@@ -141,15 +165,14 @@ struct EpiQkvRope {
   template <class Src>
   __device__ __forceinline__ void operator()(int l, int row, bool valid, int col0, int ncols,
                                              Src& src) const {
-    const long long rbase = ((long long)l * rows + row) * ncols_total;
+    const long long rbase = ((long long)l * rows + row) * ld;
     const int half = hd >> 1;
     for (int h0 = 0; h0 < ncols; h0 += hd) {
       const int hcol = col0 + h0;
-      const bool rope = hcol < n_rope_cols;
       if (half >= 32) {
-        for (int i0 = 0; i0 < half; i0 += 32) rope_chunk<32>(row, valid, rope, hcol, h0, i0, rbase, src);
+        for (int i0 = 0; i0 < half; i0 += 32) rope_chunk<32>(l, row, valid, hcol, h0, i0, rbase, src);
       } else {
-        rope_chunk<16>(row, valid, rope, hcol, h0, 0, rbase, src);
+        rope_chunk<16>(l, row, valid, hcol, h0, 0, rbase, src);
       }
     }
   }

@@ -32,7 +32,9 @@ constexpr int TC_BM = 128;
 constexpr int TC_BK = 64;  // one 128-byte swizzle row of bf16
 
 struct GemmTcShape {
-  int rows;       // valid rows per group (M)
+  int rows;       // valid rows per group (M), counted from row0
+  int row0;       // first A row read (TMA row coordinate of output row 0)
+  int a_slot_off; // A is read from layer slot (layer + a_slot_off)
   int N, K;
   int g_first, g_count;
   int m_tiles, n_tiles, k_blocks;
@@ -105,7 +107,8 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_3d(sA + stage * C::A_BYTES, &tmA, kb * TC_BK, mt * TC_BM, layer, &full[stage]);
+          tma_load_3d(sA + stage * C::A_BYTES, &tmA, kb * TC_BK, sh.row0 + mt * TC_BM,
+                      layer + sh.a_slot_off, &full[stage]);
           tma_load_3d(sB + stage * C::B_BYTES, &tmB, kb * TC_BK, nt * BN, layer, &full[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
@@ -192,7 +195,7 @@ bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int K, int rows, in
 template <class Epi, int BN>
 cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int rows, int N, int K,
                            int g_first, int g_count, int* err, const Epi& epi, int num_sms,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, int row0 = 0, int a_slot_off = 0) {
   using C = TcCfg<BN>;
   static bool configured = false;
   if (!configured) {
@@ -203,6 +206,8 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int r
   }
   GemmTcShape sh;
   sh.rows = rows;
+  sh.row0 = row0;
+  sh.a_slot_off = a_slot_off;
   sh.N = N;
   sh.K = K;
   sh.g_first = g_first;

@@ -99,57 +99,26 @@ __global__ void assoc_phi_kernel(const float* __restrict__ q, const float* __res
 
 // ---------------------------------------------- associative write side --
 
-// Projections of the memory-token rows h_i (rows S..S+M-1 of the layer's
-// output): kb[l][i][0..k) = Wk_a h_i, kb[l][i][k] = wbeta^T h_i (logit).
-// Grid (k + 1 outputs, layers).  M <= 32.
-template <typename WT>
-__global__ void assoc_write_proj_kernel(const float* __restrict__ H, long long h_gs,
-                                        const WT* __restrict__ wk, const WT* __restrict__ wbeta,
-                                        float* __restrict__ kb, int S, int M, int d, int k,
-                                        int g_first) {
-  __shared__ float part[32][33];
-  const int l = g_first + blockIdx.y, o = blockIdx.x;
-  const WT* w = (o < k) ? wk + ((long long)l * k + o) * d : wbeta + (long long)l * d;
-  const float* hb = H + l * h_gs + (long long)S * d;
-  float acc[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-  for (int e = threadIdx.x; e < d; e += blockDim.x) {
-    const float we = ld_as_f32(w + e);
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < M) acc[i] += we * hb[(long long)i * d + e];
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float s = warp_sum(acc[i]);
-    if (lane == 0) part[warp][i] = s;
-  }
-  __syncthreads();
-  if (threadIdx.x < M) {
-    float s = 0.f;
-    for (int w2 = 0; w2 < nw; ++w2) s += part[w2][threadIdx.x];
-    kb[((long long)l * M + threadIdx.x) * (k + 1) + o] = s;
-  }
-}
-
-// Per layer (one block): phi_i = DPFP(k_i), zphi_i = z^T phi_i,
-// gamma_i = 1 - zphi_i / (phi_i^T phi_i + eps), beta_i = sigmoid(logit_i);
-// stores phiM[l][i][:], coef[l][i] = {beta_i, zphi_i + eps}; then
-// z += sum_i gamma_i phi_i (after every zphi_i has been taken).
-__global__ void assoc_write_feat_kernel(const float* __restrict__ kb, float* __restrict__ z,
+// Per layer (one block), memory tokens i = 0..M-1 in order:
+//   phi_i = DPFP(k_i),  zphi_i = z_{i-1}^T phi_i,
+//   gamma_i = 1 - zphi_i / (phi_i^T phi_i + eps),  z_i = z_{i-1} + gamma_i phi_i.
+// The normaliser's recurrence does not involve A, so it runs here on its own;
+// stores phiM[l][i][:] and coef[l][i] = {beta_i, zphi_i + eps} for the row
+// update of A.  Thread t owns entries p = t, t + blockDim, ... of z (no
+// cross-thread dependence between consecutive tokens).
+// vkb[l][i] = [v_i (d) | k_i (k) | beta logit | pad] (row stride nw), the
+// output of the memory-row projection GEMM.
+__global__ void assoc_write_feat_kernel(const float* __restrict__ vkb, float* __restrict__ z,
                                         float* __restrict__ phiM, float* __restrict__ coef, int M,
-                                        int k, int nu, float eps, int g_first) {
-  extern __shared__ float sm[];  // M * 2k (r rows) + 2 * M
+                                        int k, int nu, float eps, int d, int nw, int g_first) {
+  extern __shared__ float sm[];  // M * 2k (r rows)
   __shared__ float red[32];
   const int l = g_first + blockIdx.x;
   const int k2 = 2 * k, P = k2 * nu;
   float* r = sm;
-  float* gam = sm + M * k2;
   for (int t = threadIdx.x; t < M * k; t += blockDim.x) {
     const int i = t / k, c = t - i * k;
-    const float v = kb[((long long)l * M + i) * (k + 1) + c];
+    const float v = vkb[((long long)l * M + i) * nw + d + c];
     r[i * k2 + c] = v > 0.f ? v : 0.f;
     r[i * k2 + c + k] = v < 0.f ? -v : 0.f;
   }
@@ -157,100 +126,81 @@ __global__ void assoc_write_feat_kernel(const float* __restrict__ kb, float* __r
   float* zl = z + (long long)l * P;
   for (int i = 0; i < M; ++i) {
     float zp = 0.f, ff = 0.f;
+    float* pm = phiM + ((long long)l * M + i) * P;
     for (int p = threadIdx.x; p < P; p += blockDim.x) {
       const int j = p / k2 + 1, c = p - (j - 1) * k2;
       int src = c - j;
       src = src < 0 ? src + k2 : src;
       const float f = r[i * k2 + c] * r[i * k2 + src];
-      phiM[((long long)l * M + i) * P + p] = f;
+      pm[p] = f;
       zp += zl[p] * f;
       ff += f * f;
     }
     zp = block_sum(zp, red);
     ff = block_sum(ff, red);
+    const float gamma = 1.0f - zp / (ff + eps);
+    for (int p = threadIdx.x; p < P; p += blockDim.x) zl[p] += gamma * pm[p];
     if (threadIdx.x == 0) {
-      const float logit = kb[((long long)l * M + i) * (k + 1) + k];
+      const float logit = vkb[((long long)l * M + i) * nw + d + k];
       coef[((long long)l * M + i) * 2 + 0] = sigmoid_f(logit);
       coef[((long long)l * M + i) * 2 + 1] = zp + eps;
-      gam[i] = 1.0f - zp / (ff + eps);
     }
-  }
-  __syncthreads();
-  for (int p = threadIdx.x; p < P; p += blockDim.x) {
-    float dz = 0.f;
-    for (int i = 0; i < M; ++i) dz += gam[i] * phiM[((long long)l * M + i) * P + p];
-    zl[p] += dz;
   }
 }
 
-// Delta-rule update of the rows of A_l.  Row j of A only needs row j of the
-// values and of vbar, so one pass reads each row of A once:
-//   v_i[j]    = Wv_a[j] . h_i
-//   vbar_i[j] = A[j] . phi_i / (zphi_i + eps)
-//   A[j]     += sum_i beta_i (v_i[j] - vbar_i[j]) phi_i
-// One warp per row j (several rows per warp); h_i and phi_i in shared memory.
-// Also refreshes the activation-dtype copy Aa of the state (GEMM operand of
-// the next read), when Aa != A.
-template <typename WT, typename AT>
-__global__ void assoc_write_update_kernel(const float* __restrict__ H, long long h_gs,
-                                          const WT* __restrict__ wv, const float* __restrict__ phiM,
-                                          const float* __restrict__ coef, float* __restrict__ A,
-                                          AT* __restrict__ Aa, int S, int M, int d, int P,
-                                          int rows_per_block, int g_first) {
+// Delta-rule update of the rows of A_l, memory tokens applied in order.
+// Row j of A only ever needs row j of the values, so each warp keeps its row
+// of A in registers (lane owns entries lane + 32 t) and runs, for i = 0..M-1,
+//   vbar = A[j] . phi_i / (zphi_i + eps)
+//   A[j] += beta_i (v_i[j] - vbar) phi_i,
+// reading and writing each row of A once.  v_i[j] comes from the memory-row
+// projection GEMM (vkb), phi_i and the coefficients from the feature kernel.
+// Also refreshes the activation-dtype copy Aa of the state (the next read's
+// GEMM operand) when Aa != A.  Needs P % 32 == 0, P <= 32 * MAXT, M <= 32.
+template <typename AT>
+__global__ void __launch_bounds__(256) assoc_write_update_kernel(
+    const float* __restrict__ vkb, int nw, const float* __restrict__ phiM,
+    const float* __restrict__ coef, float* __restrict__ A, AT* __restrict__ Aa, int M, int d, int P,
+    int rows_per_block, int g_first) {
+  constexpr int MAXT = 16;
   extern __shared__ float sm[];
-  float* hs = sm;                 // [M][d]
-  float* ps = sm + M * d;         // [M][P]
+  float* ps = sm;                 // [M][P]
   float* cs = ps + M * P;         // [M][2]
   const int l = g_first + blockIdx.y;
-  const float* hb = H + l * h_gs + (long long)S * d;
-  for (int t = threadIdx.x; t < M * d; t += blockDim.x) hs[t] = hb[t];
   for (int t = threadIdx.x; t < M * P; t += blockDim.x) ps[t] = phiM[(long long)l * M * P + t];
   for (int t = threadIdx.x; t < 2 * M; t += blockDim.x) cs[t] = coef[(long long)l * M * 2 + t];
   __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw_ = blockDim.x >> 5;
+  const int nt = P >> 5;
   const int j0 = blockIdx.x * rows_per_block;
   float* Al = A + (long long)l * d * P;
   AT* Aal = Aa + (long long)l * d * P;
-  for (int j = j0 + warp; j < j0 + rows_per_block && j < d; j += nw) {
-    const WT* wr = wv + ((long long)l * d + j) * d;
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = 0.f;
-    for (int e = lane; e < d; e += 32) {
-      const float we = ld_as_f32(wr + e);
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < M) v[i] += we * hs[i * d + e];
-    }
-    float vb[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) vb[i] = 0.f;
+  const float* vl = vkb + (long long)l * M * nw;
+  for (int j = j0 + warp; j < j0 + rows_per_block && j < d; j += nw_) {
+    const float vj = lane < M ? vl[(long long)lane * nw + j] : 0.f;  // lane i holds v_i[j]
     float* arow = Al + (long long)j * P;
-    for (int p = lane; p < P; p += 32) {
-      const float a = arow[p];
+    float a[MAXT];
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < M) vb[i] += a * ps[i * P + p];
+    for (int t = 0; t < MAXT; ++t) a[t] = t < nt ? arow[lane + 32 * t] : 0.f;
+    for (int i = 0; i < M; ++i) {
+      const float* pi = ps + i * P + lane;
+      float dot = 0.f;
+#pragma unroll
+      for (int t = 0; t < MAXT; ++t)
+        if (t < nt) dot += a[t] * pi[32 * t];
+      dot = warp_sum(dot);
+      const float vi = __shfl_sync(0xffffffffu, vj, i);
+      const float c = cs[2 * i] * (vi - dot / cs[2 * i + 1]);
+#pragma unroll
+      for (int t = 0; t < MAXT; ++t)
+        if (t < nt) a[t] += c * pi[32 * t];
     }
-    float c[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (i < M) {
-        const float vi = warp_sum(v[i]);
-        const float vbi = warp_sum(vb[i]) / cs[2 * i + 1];
-        c[i] = cs[2 * i] * (vi - vbi);
-      } else {
-        c[i] = 0.f;
+    for (int t = 0; t < MAXT; ++t) {
+      if (t < nt) {
+        arow[lane + 32 * t] = a[t];
+        if ((void*)Aal != (void*)Al) st_from_f32(Aal + (long long)j * P + lane + 32 * t, a[t]);
       }
-    }
-    for (int p = lane; p < P; p += 32) {
-      float dlt = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < M) dlt += c[i] * ps[i * P + p];
-      const float a = arow[p] + dlt;
-      arow[p] = a;
-      if ((void*)Aal != (void*)Al) st_from_f32(Aal + (long long)j * P + p, a);
     }
   }
 }
@@ -398,6 +348,7 @@ __global__ void epi_rows_kernel(const float* __restrict__ C, long long c_gs, int
                                 int g_first, Epi epi) {
   const int l = g_first + blockIdx.y, row = blockIdx.x;
   const float* cr = C + l * c_gs + (long long)row * ldc;
+  // N must be a multiple of Epi::GROUP (checked when the model is created)
   for (int grp = threadIdx.x; grp < N / Epi::GROUP; grp += blockDim.x) {
     PtrSrc src{cr + grp * Epi::GROUP};
     epi(l, row, true, grp * Epi::GROUP, Epi::GROUP, src);

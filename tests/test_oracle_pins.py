@@ -329,3 +329,31 @@ def test_tiny_workload_is_well_conditioned():
     alone = np.concatenate([O.forward(cfg, W, tok[s * S:(s + 1) * S], 1)[0] for s in range(n)])
     np.testing.assert_array_equal(out[:S], alone[:S])
     assert np.max(np.abs(out[S:] - alone[S:])) > 1e-3
+
+
+# ------------------------------------------------- bf16 precision model ----
+
+def test_round_bf16_matches_torch_and_ties_to_even():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(9)
+    x = np.concatenate([rng.standard_normal(10000) * 10.0 ** rng.integers(-6, 6, 10000),
+                        [0.0, -0.0, 1.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8)]])
+    want = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(O.round_bf16(x), want)
+    # exact ties: 1 + 2^-8 is halfway between 1 and 1 + 2^-7 -> even (1.0)
+    assert O.round_bf16(np.array([1.0 + 2.0 ** -8]))[0] == 1.0
+    assert O.round_bf16(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 1.0 + 2.0 ** -6
+
+
+def test_bf16_precision_model_is_close_to_fp64_and_rounds():
+    cfg = dataclasses.replace(I.TINY, dtype="bf16")
+    W = I.make_weights(cfg, seed=15)
+    tok = I.make_tokens(cfg, 3, seed=15)
+    exact = O.forward(cfg, W, tok, 3)
+    model = O.forward(cfg, W, tok, 3, operands="bf16")
+    diff = np.abs(model[0] - exact[0]).max()
+    assert 1e-5 < diff < 0.2        # rounding is applied, and only perturbs
+    # diagonal order still equals sequential order under the precision model
+    model_d = O.forward(cfg, W, tok, 3, order="diag", operands="bf16")
+    for a, b in zip(model, model_d):
+        np.testing.assert_array_equal(a, b)
