@@ -199,6 +199,32 @@ ARMT_API armt_status armt_segment_attention_bf16(const void* qk, const void* vt,
                                                  int32_t T, int32_t Hq, int32_t Hkv, int32_t hd,
                                                  void* stream);
 
+/* Fixed device scratch of armt_segment_attention_bf16_noalloc (bytes). */
+#define ARMT_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* armt_segment_attention_bf16 for callers that cannot allocate device
+ * memory -- for example a serving process whose device memory is owned by
+ * its own arena or capped, or a latency-critical path that must not hit
+ * cudaMalloc's implicit device-wide synchronisation.  The paper has no
+ * counterpart to this entry point; it is a deployment convenience.
+ *   qkv device bf16 [G][T][(Hq+2Hkv)*hd]: q heads, k heads (already
+ *       rotated), then v heads -- the plain fused row layout
+ *   out device bf16 [G][T][Hq*hd]; same result as armt_segment_attention_bf16.
+ * It calls no cudaMalloc, cudaFree or allocating library routine.  Its
+ * scratch (the transposed values, G * Hkv * hd * round_up(T, 8) * 2 bytes,
+ * plus a 256-byte error word) lives in one file-scope device array of
+ * ARMT_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
+ * the process exits; larger problems are rejected with ARMT_ERR_SHAPE before
+ * anything is enqueued.  The first call on a device (with that device
+ * current) looks up the array's device address; make that first call before
+ * any stream capture.  Every call on a device shares the one array, which
+ * keeps the last call's contents, so calls that overlap on the GPU (e.g. on
+ * two streams without ordering) race -- order them.  hd in {64, 128},
+ * 16-byte aligned pointers. */
+ARMT_API armt_status armt_segment_attention_bf16_noalloc(const void* qkv, void* out, int32_t G,
+                                                         int32_t T, int32_t Hq, int32_t Hkv,
+                                                         int32_t hd, void* stream);
+
 /* Sizes of the memory state buffers for this model (elements). */
 ARMT_API armt_status armt_state_sizes(const armt_model* m, int64_t* a_elems, int64_t* z_elems);
 

@@ -28,7 +28,7 @@ KERNEL_CLASSES = ("gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down", "attention",
 
 EXPORTED = ("armt_create", "armt_destroy", "armt_forward", "armt_forward_sequential",
             "armt_forward_host", "armt_grouped_gemm_bf16", "armt_segment_attention_bf16",
-            "armt_state_sizes", "armt_launch_count",
+            "armt_segment_attention_bf16_noalloc", "armt_state_sizes", "armt_launch_count",
             "armt_set_profiling", "armt_kernel_times", "armt_sync_status", "armt_status_string",
             "armt_last_error")
 
@@ -79,6 +79,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.armt_forward_host.argtypes = [P, P, I64, P, P, P, I32, I32, P]
     lib.armt_grouped_gemm_bf16.argtypes = [P, P, P, I32, I32, I32, I32, P]
     lib.armt_segment_attention_bf16.argtypes = [P, P, P, I32, I32, I32, I32, I32, P]
+    lib.armt_segment_attention_bf16_noalloc.argtypes = [P, P, I32, I32, I32, I32, I32, P]
     lib.armt_state_sizes.argtypes = [P, ctypes.POINTER(I64), ctypes.POINTER(I64)]
     lib.armt_launch_count.argtypes = [P, I64, I32, ctypes.POINTER(I64)]
     lib.armt_set_profiling.argtypes = [P, I32]
@@ -249,3 +250,12 @@ def armt_segment_attention_bf16(qk, vt, out, Hq, Hkv, stream=None):
     hd = vt.shape[2]
     _check(lib.armt_segment_attention_bf16(_ptr(qk), _ptr(vt), _ptr(out), G, T, Hq, Hkv, hd,
                                            _stream_ptr(stream)), "armt_segment_attention_bf16")
+
+
+def armt_segment_attention_bf16_noalloc(qkv, out, Hq, Hkv, hd, stream=None):
+    """Same attention from the fused row layout qkv bf16 [G,T,(Hq+2Hkv)*hd]; allocates nothing."""
+    lib = load_library()
+    G, T, _ = qkv.shape
+    _check(lib.armt_segment_attention_bf16_noalloc(_ptr(qkv), _ptr(out), G, T, Hq, Hkv, hd,
+                                                   _stream_ptr(stream)),
+           "armt_segment_attention_bf16_noalloc")

@@ -45,6 +45,10 @@ static armt_status fail(armt_status s, const std::string& msg) {
   return s;
 }
 
+namespace armt {
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace armt
+
 #define CK(call)                                                                          \
   do {                                                                                    \
     cudaError_t e_ = (call);                                                              \
