@@ -25,6 +25,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <string>
+#include <type_traits>
 #include <vector>
 
 #include "../../include/armt.h"
@@ -183,8 +184,8 @@ struct ModelBase {
     int64_t n = 0;
     if (lo == 0) n += 1;                    // layer-0 input gather
     n += per_gemm + 1 + per_gemm;           // associative query GEMM, phi, read GEMM
-    n += 1 + per_gemm + 1 + per_gemm;       // norm1, QKV GEMM, attention, O GEMM
-    n += 1 + per_gemm + per_gemm;           // norm2, gate-up GEMM, down GEMM
+    n += per_gemm + 1 + per_gemm;           // QKV GEMM, attention, O GEMM (norms fused)
+    n += per_gemm + per_gemm;               // gate-up GEMM, down GEMM
     n += per_gemm + 2;                      // delta-rule write: projection GEMM, z, A rows
     if (hi == cfg.n_layers - 1) n += 1;     // final norm
     return n;
@@ -236,6 +237,13 @@ template <typename WT>
 struct Model : ModelBase {
   static constexpr bool kTC = sizeof(WT) == 2;  // bf16: tensor-core GEMMs
   typedef WT AT;                               // activation dtype of GEMM operands
+  // epilogue functors: staged (lanes across columns) on the tensor-core
+  // path, thread-per-row on the fp32 path
+  using FStore = std::conditional_t<kTC, SEpiStore, EpiStore>;
+  using FRead = std::conditional_t<kTC, SEpiAssocRead<AT>, EpiAssocRead<AT>>;
+  using FQkv = std::conditional_t<kTC, SEpiQkvRope<AT>, EpiQkvRope<AT>>;
+  using FRes = std::conditional_t<kTC, SEpiResidual<AT>, EpiResidual<AT>>;
+  using FSwi = std::conditional_t<kTC, SEpiSwiGLU<AT>, EpiSwiGLU<AT>>;
 
   // weights (library layout)
   WT *embed = nullptr, *memtok = nullptr, *Wqkv = nullptr, *Wo = nullptr, *Wgu = nullptr,
@@ -243,7 +251,8 @@ struct Model : ModelBase {
   float *g1 = nullptr, *g2 = nullptr, *gf = nullptr, *cosT = nullptr, *sinT = nullptr;
   // activations, all [layer or slot][rows][width]
   float *X = nullptr, *Res = nullptr, *Qa = nullptr, *Den = nullptr, *VKB = nullptr,
-        *PhiM = nullptr, *Coef = nullptr, *Cscr = nullptr;
+        *PhiM = nullptr, *Coef = nullptr, *Cscr = nullptr, *Ssq = nullptr;
+  int npart = 0;  // partial sums of squares per row (one per epilogue column tile)
   int nw = 0;  // rows of Ww per layer (d + k + 1 rounded up to the tile width)
   AT *Xa = nullptr, *Nrm = nullptr, *QKV = nullptr, *Att = nullptr, *U = nullptr, *Phi = nullptr,
      *Aa = nullptr, *Vt = nullptr;
@@ -351,6 +360,8 @@ struct Model : ModelBase {
     CKS(mem.alloc_n(&Qa, L * T * k));
     CKS(mem.alloc_n(&Phi, L * T * P));
     CKS(mem.alloc_n(&Den, L * T));
+    npart = (int)(kTC ? d / 256 : d / 32);
+    CKS(mem.alloc_n(&Ssq, L * T * (size_t)npart));
     CKS(mem.alloc_n(&VKB, L * c.n_mem * (size_t)nw));
     CKS(mem.alloc_n(&PhiM, L * c.n_mem * P));
     CKS(mem.alloc_n(&Coef, L * c.n_mem * 2));
@@ -371,6 +382,8 @@ struct Model : ModelBase {
     else if (hd == 128)
       CK(cudaFuncSetAttribute(attn_simt_kernel<AT, 128>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem));
+    if (kTC && ((Hq + Hkv) * hd) % 256 != 0)
+      return fail(ARMT_ERR_UNSUPPORTED, "(Hq + Hkv) * head_dim must be a multiple of 256");
     if (kTC) {
       bool ok = true;
       ok &= encode_tmap_bf16_3d(&tmXa, Xa, (int)d, (int)T, (int)L + 1, TC_BM);
@@ -440,23 +453,21 @@ struct Model : ModelBase {
     }
     // associative read: q = Wq_a x, phi, den, then x' = x + A phi / den
     CKS((gemm<64>(ARMT_KC_ASSOC_READ, tmXa, tmAWq, Xa, Td, aWq, k, d,
-                  EpiStore{Qa, (long long)k, (long long)T * k}, lo, g, st)));
+                  FStore{Qa, (long long)k, (long long)T * k}, lo, g, st)));
     CKS(prof_begin(ARMT_KC_ASSOC_READ, st));
     assoc_phi_kernel<AT><<<dim3(T, g), 128, 2 * k * sizeof(float), st>>>(Qa, z, Phi, Den, T, k,
                                                                         c.dpfp_nu, c.assoc_eps, lo);
     CK(cudaGetLastError());
     CKS(prof_end(st));
     const AT* Asrc = kTC ? Aa : reinterpret_cast<const AT*>(A);
+    const RowNormIn norm_in{Ssq, npart, 1.0f / (float)d, c.norm_eps};
     CKS((gemm<256>(ARMT_KC_ASSOC_READ, tmPhi, tmAa, Phi, (long long)T * P,
-                   reinterpret_cast<const WT*>(Asrc), d, P, EpiAssocRead{X, Den, Res, T, d}, lo, g,
-                   st)));
-    // attention sub-layer
-    CKS(prof_begin(ARMT_KC_NORM, st));
-    rmsnorm_kernel<AT><<<dim3(T, g), 256, 0, st>>>(Res, Td, g1, d, Nrm, Td, d, c.norm_eps, lo);
-    CK(cudaGetLastError());
-    CKS(prof_end(st));
+                   reinterpret_cast<const WT*>(Asrc), d, P,
+                   FRead{X, Den, Res, T, d, RowNormOut<AT>{g1, Nrm, Ssq}}, lo, g, st)));
+    // attention sub-layer (RMSNorm 1 completes in the QKV epilogue)
     CKS((gemm<256>(ARMT_KC_GEMM_QKV, tmNrm, tmWqkv, Nrm, Td, Wqkv, Nq, d,
-                   EpiQkvRope<AT>{QKV, cosT, sinT, T, hd, (Hq + Hkv) * hd, qkv_ld, Vt, Hkv, t_pad},
+                   FQkv{QKV, cosT, sinT, T, hd, (Hq + Hkv) * hd, qkv_ld, Vt, Hkv, t_pad,
+                                  norm_in},
                    lo, g, st)));
     CKS(prof_begin(ARMT_KC_ATTENTION, st));
     if constexpr (kTC) {
@@ -486,22 +497,21 @@ struct Model : ModelBase {
     }
     CKS(prof_end(st));
     CKS((gemm<256>(ARMT_KC_GEMM_O, tmAtt, tmWo, Att, (long long)T * Hq * hd, Wo, d, Hq * hd,
-                   EpiResidual<AT>{Res, Res, nullptr, T, d, 0}, lo, g, st)));
-    // MLP sub-layer
-    CKS(prof_begin(ARMT_KC_NORM, st));
-    rmsnorm_kernel<AT><<<dim3(T, g), 256, 0, st>>>(Res, Td, g2, d, Nrm, Td, d, c.norm_eps, lo);
-    CK(cudaGetLastError());
-    CKS(prof_end(st));
+                   FRes{Res, Res, nullptr, T, d, 0, RowNormOut<AT>{g2, Nrm, Ssq}}, lo, g,
+                   st)));
+    // MLP sub-layer (RMSNorm 2 completes in the gate-up epilogue)
     CKS((gemm<256>(ARMT_KC_GEMM_GATEUP, tmNrm, tmWgu, Nrm, Td, Wgu, 2 * F, d,
-                   EpiSwiGLU<AT>{U, T, F}, lo, g, st)));
+                   FSwi{U, T, F, norm_in}, lo, g, st)));
     CKS((gemm<256>(ARMT_KC_GEMM_DOWN, tmU, tmWd, U, (long long)T * F, Wd, d, F,
-                   EpiResidual<AT>{Res, X, kTC ? Xa : nullptr, T, d, 1}, lo, g, st)));
+                   FRes{Res, X, kTC ? Xa : nullptr, T, d, 1,
+                                   RowNormOut<AT>{nullptr, nullptr, nullptr}},
+                   lo, g, st)));
     // delta-rule write from the memory-token rows of this layer's output:
     // [v | k | beta] = h_mem [Wv_a; Wk_a; wbeta_a]^T on the tensor cores (A =
     // rows S..S+M-1 of layer slot l+1), then the normaliser recurrence and
     // the row-wise update of A.
     CKS((gemm<256>(ARMT_KC_ASSOC_WRITE, tmXa, tmWw, Xa, Td, Ww, nw, d,
-                   EpiStore{VKB, (long long)nw, (long long)M * nw}, lo, g, st, M, S, 1)));
+                   FStore{VKB, (long long)nw, (long long)M * nw}, lo, g, st, M, S, 1)));
     CKS(prof_begin(ARMT_KC_ASSOC_WRITE, st));
     assoc_write_feat_kernel<<<g, 256, feat_smem, st>>>(VKB, z, PhiM, Coef, M, k, c.dpfp_nu,
                                                        c.assoc_eps, d, nw, lo);
@@ -758,8 +768,8 @@ armt_status armt_grouped_gemm_bf16(const void* A, const void* B, float* C, int32
   CUtensorMap ta, tb;
   if (!encode_tmap_bf16_3d(&ta, A, K, M, G, TC_BM) || !encode_tmap_bf16_3d(&tb, B, K, N, G, 256))
     return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-  EpiStore epi{C, (long long)N, (long long)M * N};
-  CK((launch_gemm_tc<EpiStore, 256>(ta, tb, M, N, K, 0, G, err, epi, g_num_sms(dev),
+  SEpiStore epi{C, (long long)N, (long long)M * N};
+  CK((launch_gemm_tc<SEpiStore, 256>(ta, tb, M, N, K, 0, G, err, epi, g_num_sms(dev),
                                     reinterpret_cast<cudaStream_t>(stream))));
   return ARMT_OK;
 }

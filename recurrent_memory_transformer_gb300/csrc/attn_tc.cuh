@@ -167,36 +167,44 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
       const bool got = mbar_wait_bounded(&bar[B_SF], j & 1, a.err, DEV_TIMEOUT_ACC_FULL);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
+      // Only the diagonal tile j == m is masked (key index > query index);
+      // keys of earlier tiles are all visible.  lim = last visible key
+      // column of this row within the tile.
       const bool diag = (j == m);
-      // pass 1: row max of the scaled scores
+      const int lim = qi - j * 128;
+      // pass 1: row max of the raw scores (the scale is positive)
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float s[32];
         tmem_ld32(tS + lane_off + 32 * c, s);
+        if (diag) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = j * 128 + 32 * c + i;
-          const float t = (diag && key > qi) ? -INFINITY : s[i] * a.scale_log2;
-          mx = fmaxf(mx, t);
+          for (int i = 0; i < 32; ++i) mx = (32 * c + i <= lim) ? fmaxf(mx, s[i]) : mx;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, s[i]);
         }
       }
-      const float m_new = fmaxf(m_run, mx);
-      const float corr = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+      const float m_new = fmaxf(m_run, mx * a.scale_log2);
+      const float corr = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      // pass 2: probabilities, row sum, bf16 P into shared memory (swizzled)
+      // pass 2: p = 2^(s * scale - m), row sum, bf16 P into shared memory
       float rs = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float s[32];
         tmem_ld32(tS + lane_off + 32 * c, s);
+        if (diag) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = j * 128 + 32 * c + i;
-          const float p = (diag && key > qi) ? 0.f : exp2f(s[i] * a.scale_log2 - m_use);
-          s[i] = p;
-          rs += p;
+          for (int i = 0; i < 32; ++i)
+            s[i] = (32 * c + i <= lim) ? fast_exp2(fmaf(s[i], a.scale_log2, -m_use)) : 0.f;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[i] = fast_exp2(fmaf(s[i], a.scale_log2, -m_use));
         }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) rs += s[i];
         uint8_t* atom = prow + (c >> 1) * 16384;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {

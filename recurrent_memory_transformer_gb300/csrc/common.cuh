@@ -75,6 +75,14 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return red[0];
 }
 
+// 2^x with the SFU's approximate base-2 exponential instruction (denormal
+// results flush to zero; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 

@@ -5,9 +5,11 @@
 // step consumes with no extra pass over HBM:
 //   EpiStore     C = acc (fp32)                        plain grouped GEMM
 //   EpiAssocRead x' = x + acc / den[row]               associative read + residual
-//   EpiQkvRope   q|k|v = acc with rotate-half RoPE on q and k, act dtype
+//                (+ gain-weighted row and partial sums for RMSNorm 1)
+//   EpiQkvRope   q|k|v = acc / rms with rotate-half RoPE on q and k
 //   EpiResidual  out = res + acc (fp32), optional act-dtype copy
-//   EpiSwiGLU    u = silu(gate) * up, gate/up interleaved in blocks of 128
+//                (+ gain-weighted row and partial sums for RMSNorm 2)
+//   EpiSwiGLU    u = silu(gate / rms) * (up / rms), gate/up interleaved in blocks of 128
 // A functor is called once per (row, group of GROUP columns) with a source
 // that yields accumulator columns `c .. c+n-1` relative to the group start.
 // `valid` is false for padding rows past the end of the cell; the functor
@@ -61,6 +63,59 @@ __device__ __forceinline__ void load_row(const float* src, float* v, int n) {
   }
 }
 
+// RMSNorm folded across two GEMMs: the producing epilogue writes the
+// gain-weighted row (x * gain, activation dtype) and one partial sum of x^2
+// per (row, column tile); the consuming GEMM scales its accumulator row by
+// 1 / sqrt(sum / d + eps) -- the norm is linear in that factor, so
+//   RMSNorm(x) W^T = (x * gain) W^T / rms(x).
+// Partials are summed in a fixed order (deterministic).
+struct RowNormIn {
+  const float* ssq;  // [L][rows][npart] partial sums of squares, or nullptr
+  int npart;
+  float inv_d, eps;
+  __device__ __forceinline__ float scale(int l, int rows, int row) const {
+    if (ssq == nullptr) return 1.f;
+    const float* p = ssq + ((long long)l * rows + row) * npart;
+    float s = 0.f;
+    if ((npart & 3) == 0 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+      for (int i = 0; i < npart; i += 4) {  // fixed order: ((p0 + p1) + p2) + p3 ...
+        const float4 q = *reinterpret_cast<const float4*>(p + i);
+        s += q.x;
+        s += q.y;
+        s += q.z;
+        s += q.w;
+      }
+    } else {
+      for (int i = 0; i < npart; ++i) s += p[i];
+    }
+    return 1.0f / sqrtf(s * inv_d + eps);
+  }
+};
+
+template <typename AT>
+struct RowNormOut {
+  const float* gain;  // [L][d] stacked gains, or nullptr (no norm output)
+  AT* out;            // [L][rows][d] gain-weighted row
+  float* ssq;         // [L][rows][npart]
+  // v: 32 fp32 values of row `row` at columns col..col+31 (col0 = start of
+  // this call's columns; the call's partial index is col0 / ncols).
+  __device__ __forceinline__ void put(int l, int rows, int d, int row, int col, const float* v,
+                                      float& acc) const {
+    float w[32];
+    const float* g = gain + (long long)l * d + col;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      w[i] = v[i] * g[i];
+      acc += v[i] * v[i];
+    }
+    store_row(out + ((long long)l * rows + row) * d + col, w, 32);
+  }
+  __device__ __forceinline__ void finish(int l, int rows, int row, int col0, int ncols, int d,
+                                         float acc) const {
+    ssq[((long long)l * rows + row) * (d / ncols) + col0 / ncols] = acc;
+  }
+};
+
 // ------------------------------------------------------------- functors --
 
 struct EpiStore {
@@ -88,18 +143,22 @@ struct EpiStore {
 };
 
 // x' = x + acc / den[row]: the associative read (numerator from the grouped
-// GEMM of phi rows with the state) added to the residual stream.
+// GEMM of phi rows with the state) added to the residual stream; also the
+// first half of RMSNorm 1 (gain-weighted row + partial sums of squares).
+template <typename AT>
 struct EpiAssocRead {
   static constexpr int GROUP = 32;
   const float* x;      // [slots][rows][d] layer input (slot = layer)
   const float* den;    // [L][rows]  z^T phi + eps
   float* out;          // [L][rows][d]
   int rows, d;
+  RowNormOut<AT> norm;
   template <class Src>
   __device__ __forceinline__ void operator()(int l, int row, bool valid, int col0, int ncols,
                                              Src& src) const {
     const long long off = ((long long)l * rows + row) * d + col0;
     const float dn = valid ? den[(long long)l * rows + row] : 1.f;
+    float ss = 0.f;
     for (int c = 0; c < ncols; c += 32) {
       float a[32], xv[32];
       src.template load<32>(c, a);
@@ -108,8 +167,10 @@ struct EpiAssocRead {
 #pragma unroll
         for (int i = 0; i < 32; ++i) a[i] = xv[i] + a[i] / dn;
         store_row(out + off + c, a, 32);
+        norm.put(l, rows, d, row, col0 + c, a, ss);
       }
     }
+    if (valid) norm.finish(l, rows, row, col0, ncols, d, ss);
   }
 };
 
@@ -128,15 +189,21 @@ struct EpiQkvRope {
   int rows, hd, n_rope_cols, ld;    // n_rope_cols = (Hq+Hkv)*hd
   OutT* vt;                         // nullptr: v stays in `out`
   int n_kv, t_pad;
+  RowNormIn norm;                   // RMSNorm 1 row scale
 
   template <int CH, class Src>
   __device__ __forceinline__ void rope_chunk(int l, int row, bool valid, int hcol, int h0, int i0,
-                                             long long rbase, Src& src) const {
+                                             long long rbase, float rs, Src& src) const {
     const int half = hd >> 1;
     float x1[CH], x2[CH];
     src.template load<CH>(h0 + i0, x1);
     src.template load<CH>(h0 + half + i0, x2);
     if (!valid) return;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      x1[i] *= rs;
+      x2[i] *= rs;
+    }
     const bool rope = hcol < n_rope_cols;
     if (rope) {
       const float* cr = cosT + (long long)row * half + i0;
@@ -167,19 +234,22 @@ struct EpiQkvRope {
                                              Src& src) const {
     const long long rbase = ((long long)l * rows + row) * ld;
     const int half = hd >> 1;
+    const float rs = valid ? norm.scale(l, rows, row) : 1.f;
     for (int h0 = 0; h0 < ncols; h0 += hd) {
       const int hcol = col0 + h0;
       if (half >= 32) {
-        for (int i0 = 0; i0 < half; i0 += 32) rope_chunk<32>(l, row, valid, hcol, h0, i0, rbase, src);
+        for (int i0 = 0; i0 < half; i0 += 32)
+          rope_chunk<32>(l, row, valid, hcol, h0, i0, rbase, rs, src);
       } else {
-        rope_chunk<16>(l, row, valid, hcol, h0, 0, rbase, src);
+        rope_chunk<16>(l, row, valid, hcol, h0, 0, rbase, rs, src);
       }
     }
   }
 };
 
 // out = res + acc (fp32 residual stream), plus an optional copy in the
-// activation dtype (the next layer's associative-query GEMM operand).
+// activation dtype (the next layer's associative-query GEMM operand) and an
+// optional first half of RMSNorm 2 (norm.gain != nullptr).
 template <typename CopyT>
 struct EpiResidual {
   static constexpr int GROUP = 32;
@@ -187,11 +257,13 @@ struct EpiResidual {
   float* out;          // [slots][rows][n] at slot l + out_slot_offset
   CopyT* copy;         // same indexing as out, or nullptr
   int rows, n, out_slot_offset;
+  RowNormOut<CopyT> norm;
   template <class Src>
   __device__ __forceinline__ void operator()(int l, int row, bool valid, int col0, int ncols,
                                              Src& src) const {
     const long long ri = ((long long)l * rows + row) * n + col0;
     const long long oi = ((long long)(l + out_slot_offset) * rows + row) * n + col0;
+    float ss = 0.f;
     for (int c = 0; c < ncols; c += 32) {
       float a[32], r[32];
       src.template load<32>(c, a);
@@ -201,8 +273,10 @@ struct EpiResidual {
         for (int i = 0; i < 32; ++i) a[i] += r[i];
         store_row(out + oi + c, a, 32);
         if (copy != nullptr) store_row(copy + oi + c, a, 32);
+        if (norm.gain != nullptr) norm.put(l, rows, n, row, col0 + c, a, ss);
       }
     }
+    if (valid && norm.gain != nullptr) norm.finish(l, rows, row, col0, ncols, n, ss);
   }
 };
 
@@ -213,9 +287,11 @@ struct EpiSwiGLU {
   static constexpr int GROUP = 2 * GU_BLK;
   OutT* out;           // [L][rows][F]
   int rows, F;
+  RowNormIn norm;      // RMSNorm 2 row scale
   template <class Src>
   __device__ __forceinline__ void operator()(int l, int row, bool valid, int col0, int ncols,
                                              Src& src) const {
+    const float rs = valid ? norm.scale(l, rows, row) : 1.f;
     for (int b0 = 0; b0 < ncols; b0 += 2 * GU_BLK) {
       const int f0 = (col0 + b0) / 2;
       OutT* dst = out + ((long long)l * rows + row) * F + f0;
@@ -225,7 +301,7 @@ struct EpiSwiGLU {
         src.template load<32>(b0 + GU_BLK + c, u);
         if (valid) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
+          for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i] * rs) * (u[i] * rs);
           store_row(dst + c, g, 32);
         }
       }

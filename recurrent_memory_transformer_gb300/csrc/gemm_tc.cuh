@@ -16,7 +16,9 @@
 //   warp 1      MMA issuer (one thread): 4 x tcgen05.mma (K = 16 each) per
 //               stage into a 128 x BN fp32 accumulator in TMEM,
 //   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows),
-//               fused epilogue, direct stores.
+//               staged through shared memory so that the fused epilogue
+//               reads and writes global memory row by row, lanes across
+//               columns (epilogues_staged.cuh).
 // Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile
 // i+1.  Every output element is reduced in the same fixed K order no matter
 // how many groups a launch holds (no split-K, no atomics), so a cell gives
@@ -25,6 +27,7 @@
 
 #include "common.cuh"
 #include "epilogues.cuh"
+#include "epilogues_staged.cuh"
 
 namespace armt {
 
@@ -48,7 +51,8 @@ struct TcCfg {
   static constexpr uint32_t B_BYTES = BN * TC_BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
-  static constexpr size_t SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+  static constexpr uint32_t EPI_STAGE_BYTES = 4 * STAGED_FLOATS_PER_WARP * 4;  // 4 epilogue warps
+  static constexpr size_t SMEM = 1024 + STAGES * STAGE_BYTES + 256 + EPI_STAGE_BYTES;
 };
 
 template <class Epi, int BN>
@@ -56,7 +60,6 @@ __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmTcShape sh, const Epi epi) {
   using C = TcCfg<BN>;
-  static_assert(BN % Epi::GROUP == 0, "tile width must hold whole epilogue groups");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -157,6 +160,8 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    float* stage = reinterpret_cast<float*>(base + C::STAGES * C::STAGE_BYTES + 256) +
+                   quarter * STAGED_FLOATS_PER_WARP;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
@@ -165,9 +170,9 @@ __global__ void __launch_bounds__(192, 1)
       const bool got = mbar_wait_bounded(&acc_full[acc], acc_phase, sh.err, DEV_TIMEOUT_ACC_FULL);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      const int row = mt * TC_BM + quarter * 32 + lane;
-      TmemSrc src{tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16)};
-      epi(sh.g_first + g, row, row < sh.rows, nt * BN, BN, src);
+      staged_epilogue<BN>(epi, sh.g_first + g, mt * TC_BM + quarter * 32, sh.rows, nt * BN,
+                          tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16),
+                          stage);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);

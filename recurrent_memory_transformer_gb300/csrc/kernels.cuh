@@ -176,30 +176,58 @@ __global__ void __launch_bounds__(256) assoc_write_update_kernel(
   float* Al = A + (long long)l * d * P;
   AT* Aal = Aa + (long long)l * d * P;
   const float* vl = vkb + (long long)l * M * nw;
-  for (int j = j0 + warp; j < j0 + rows_per_block && j < d; j += nw_) {
-    const float vj = lane < M ? vl[(long long)lane * nw + j] : 0.f;  // lane i holds v_i[j]
-    float* arow = Al + (long long)j * P;
-    float a[MAXT];
+  // Each warp runs RW rows side by side (independent dependency chains).
+  constexpr int RW = 4;
+  const int j_end = min(j0 + rows_per_block, d);
+  for (int jb = j0 + warp * RW; jb < j_end; jb += nw_ * RW) {
+    float vj[RW];
+    float a[RW][MAXT];
 #pragma unroll
-    for (int t = 0; t < MAXT; ++t) a[t] = t < nt ? arow[lane + 32 * t] : 0.f;
+    for (int r = 0; r < RW; ++r) {
+      const int j = jb + r;
+      const bool ok = j < j_end;
+      vj[r] = (ok && lane < M) ? vl[(long long)lane * nw + j] : 0.f;  // lane i holds v_i[j]
+#pragma unroll
+      for (int t = 0; t < MAXT; ++t) a[r][t] = (ok && t < nt) ? Al[(long long)j * P + lane + 32 * t] : 0.f;
+    }
     for (int i = 0; i < M; ++i) {
       const float* pi = ps + i * P + lane;
-      float dot = 0.f;
+      float phv[MAXT];
 #pragma unroll
-      for (int t = 0; t < MAXT; ++t)
-        if (t < nt) dot += a[t] * pi[32 * t];
-      dot = warp_sum(dot);
-      const float vi = __shfl_sync(0xffffffffu, vj, i);
-      const float c = cs[2 * i] * (vi - dot / cs[2 * i + 1]);
+      for (int t = 0; t < MAXT; ++t) phv[t] = t < nt ? pi[32 * t] : 0.f;
+      float dot[RW];
 #pragma unroll
-      for (int t = 0; t < MAXT; ++t)
-        if (t < nt) a[t] += c * pi[32 * t];
+      for (int r = 0; r < RW; ++r) {
+        dot[r] = 0.f;
+#pragma unroll
+        for (int t = 0; t < MAXT; ++t)
+          if (t < nt) dot[r] += a[r][t] * phv[t];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int r = 0; r < RW; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
+      const float beta = cs[2 * i], den = cs[2 * i + 1];
+#pragma unroll
+      for (int r = 0; r < RW; ++r) {
+        const float vi = __shfl_sync(0xffffffffu, vj[r], i);
+        const float c = beta * (vi - dot[r] / den);
+#pragma unroll
+        for (int t = 0; t < MAXT; ++t)
+          if (t < nt) a[r][t] += c * phv[t];
+      }
     }
 #pragma unroll
-    for (int t = 0; t < MAXT; ++t) {
-      if (t < nt) {
-        arow[lane + 32 * t] = a[t];
-        if ((void*)Aal != (void*)Al) st_from_f32(Aal + (long long)j * P + lane + 32 * t, a[t]);
+    for (int r = 0; r < RW; ++r) {
+      const int j = jb + r;
+      if (j < j_end) {
+#pragma unroll
+        for (int t = 0; t < MAXT; ++t) {
+          if (t < nt) {
+            Al[(long long)j * P + lane + 32 * t] = a[r][t];
+            if ((void*)Aal != (void*)Al) st_from_f32(Aal + (long long)j * P + lane + 32 * t, a[r][t]);
+          }
+        }
       }
     }
   }
