@@ -262,7 +262,7 @@ struct Model : ModelBase {
   CUtensorMap tmXa, tmAWq, tmPhi, tmAa, tmNrm, tmWqkv, tmAtt, tmWo, tmWgu, tmU, tmWd, tmQK, tmVt,
       tmWw;
   size_t upd_smem = 0, feat_smem = 0, attn_smem = 0;
-  int upd_rows_per_block = 64;
+  int upd_rows_per_block = 32;
 
   armt_status copy_in(void* dst, const void* src, size_t bytes, cudaStream_t st) {
     CK(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, st));
@@ -372,10 +372,16 @@ struct Model : ModelBase {
     CK(cudaMemsetAsync(d_err, 0, sizeof(int), st));
     // kernel configuration
     upd_smem = ((size_t)c.n_mem * P + 2 * c.n_mem) * sizeof(float);
-    feat_smem = (size_t)c.n_mem * 2 * k * sizeof(float);
+    feat_smem = ((size_t)c.n_mem * 2 * k + (size_t)c.n_mem * (P + 1)) * sizeof(float);
     attn_smem = 2 * 64 * hd * sizeof(float);
-    CK(cudaFuncSetAttribute(assoc_write_update_kernel<AT>,
-                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem));
+    CK(cudaFuncSetAttribute(assoc_write_feat_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                            (int)feat_smem));
+    switch (P / 32) {
+      case 3: CK(cudaFuncSetAttribute(assoc_write_update_kernel<AT, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem)); break;
+      case 6: CK(cudaFuncSetAttribute(assoc_write_update_kernel<AT, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem)); break;
+      case 12: CK(cudaFuncSetAttribute(assoc_write_update_kernel<AT, 12>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem)); break;
+      default: return fail(ARMT_ERR_UNSUPPORTED, "2 * key_dim * dpfp_nu must be 96, 192 or 384");
+    }
     if (hd == 64)
       CK(cudaFuncSetAttribute(attn_simt_kernel<AT, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)attn_smem));
@@ -521,8 +527,15 @@ struct Model : ModelBase {
     {
       dim3 grid((d + upd_rows_per_block - 1) / upd_rows_per_block, g);
       AT* Adst = kTC ? Aa : reinterpret_cast<AT*>(A);
-      assoc_write_update_kernel<AT><<<grid, 256, upd_smem, st>>>(VKB, nw, PhiM, Coef, A, Adst, M, d,
-                                                                 P, upd_rows_per_block, lo);
+      if (P == 96)
+        assoc_write_update_kernel<AT, 3><<<grid, 128, upd_smem, st>>>(VKB, nw, PhiM, Coef, A, Adst, M,
+                                                                      d, upd_rows_per_block, lo);
+      else if (P == 192)
+        assoc_write_update_kernel<AT, 6><<<grid, 128, upd_smem, st>>>(VKB, nw, PhiM, Coef, A, Adst, M,
+                                                                      d, upd_rows_per_block, lo);
+      else
+        assoc_write_update_kernel<AT, 12><<<grid, 128, upd_smem, st>>>(VKB, nw, PhiM, Coef, A, Adst, M,
+                                                                       d, upd_rows_per_block, lo);
       CK(cudaGetLastError());
     }
     CKS(prof_end(st));
@@ -579,8 +592,11 @@ static armt_status validate(const armt_config* c) {
     return fail(ARMT_ERR_SHAPE, "n_q_heads must be a multiple of n_kv_heads");
   if (c->n_mem > 32) return fail(ARMT_ERR_UNSUPPORTED, "n_mem > 32");
   if (c->dpfp_nu >= 2 * c->key_dim) return fail(ARMT_ERR_SHAPE, "dpfp_nu must be < 2 * key_dim");
-  if ((2 * c->key_dim * c->dpfp_nu) % 32 != 0 || 2 * c->key_dim * c->dpfp_nu > 512)
-    return fail(ARMT_ERR_SHAPE, "2 * key_dim * dpfp_nu must be a multiple of 32 and <= 512");
+  {
+    const int Pf = 2 * c->key_dim * c->dpfp_nu;
+    if (Pf != 96 && Pf != 192 && Pf != 384)
+      return fail(ARMT_ERR_UNSUPPORTED, "2 * key_dim * dpfp_nu must be 96, 192 or 384");
+  }
   const int hd = c->head_dim, d = c->d_model, F = c->ffn_dim;
   const int Nq = (c->n_q_heads + 2 * c->n_kv_heads) * hd;
   const int P = 2 * c->key_dim * c->dpfp_nu;

@@ -102,20 +102,24 @@ __global__ void assoc_phi_kernel(const float* __restrict__ q, const float* __res
 // Per layer (one block), memory tokens i = 0..M-1 in order:
 //   phi_i = DPFP(k_i),  zphi_i = z_{i-1}^T phi_i,
 //   gamma_i = 1 - zphi_i / (phi_i^T phi_i + eps),  z_i = z_{i-1} + gamma_i phi_i.
-// The normaliser's recurrence does not involve A, so it runs here on its own;
-// stores phiM[l][i][:] and coef[l][i] = {beta_i, zphi_i + eps} for the row
-// update of A.  Thread t owns entries p = t, t + blockDim, ... of z (no
-// cross-thread dependence between consecutive tokens).
+// The normaliser's recurrence does not involve A.  Expanding z_{i-1} gives
+//   zphi_i = z_0^T phi_i + sum_{i' < i} gamma_i' (phi_i'^T phi_i),
+// so the block computes every z_0^T phi_i and the Gram matrix G = Phi Phi^T
+// in parallel, then one thread runs the 16-step scalar recurrence, and
+// finally z_M = z_0 + sum_i gamma_i phi_i.  Stores phiM[l][i][:] and
+// coef[l][i] = {beta_i, 1 / (zphi_i + eps)} for the row update of A.
 // vkb[l][i] = [v_i (d) | k_i (k) | beta logit | pad] (row stride nw), the
-// output of the memory-row projection GEMM.
-__global__ void assoc_write_feat_kernel(const float* __restrict__ vkb, float* __restrict__ z,
-                                        float* __restrict__ phiM, float* __restrict__ coef, int M,
-                                        int k, int nu, float eps, int d, int nw, int g_first) {
-  extern __shared__ float sm[];  // M * 2k (r rows)
-  __shared__ float red[32];
+// output of the memory-row projection GEMM.  M <= 32.
+__global__ void __launch_bounds__(256) assoc_write_feat_kernel(
+    const float* __restrict__ vkb, float* __restrict__ z, float* __restrict__ phiM,
+    float* __restrict__ coef, int M, int k, int nu, float eps, int d, int nw, int g_first) {
+  extern __shared__ float sm[];  // r: M * 2k, phi: M * (P + 1)
+  __shared__ float G[32][33];
+  __shared__ float z0phi[32], gam[32];
   const int l = g_first + blockIdx.x;
-  const int k2 = 2 * k, P = k2 * nu;
+  const int k2 = 2 * k, P = k2 * nu, Pp = P + 1;
   float* r = sm;
+  float* ph = sm + M * k2;
   for (int t = threadIdx.x; t < M * k; t += blockDim.x) {
     const int i = t / k, c = t - i * k;
     const float v = vkb[((long long)l * M + i) * nw + d + c];
@@ -123,46 +127,77 @@ __global__ void assoc_write_feat_kernel(const float* __restrict__ vkb, float* __
     r[i * k2 + c + k] = v < 0.f ? -v : 0.f;
   }
   __syncthreads();
+  for (int t = threadIdx.x; t < M * P; t += blockDim.x) {
+    const int i = t / P, p = t - i * P;
+    const int j = p / k2 + 1, c = p - (j - 1) * k2;
+    int src = c - j;
+    src = src < 0 ? src + k2 : src;
+    const float f = r[i * k2 + c] * r[i * k2 + src];
+    ph[i * Pp + p] = f;
+    phiM[((long long)l * M + i) * P + p] = f;
+  }
+  __syncthreads();
+  // G[i][i2] (i <= i2) and z_0^T phi_i: one warp per dot product
   float* zl = z + (long long)l * P;
-  for (int i = 0; i < M; ++i) {
-    float zp = 0.f, ff = 0.f;
-    float* pm = phiM + ((long long)l * M + i) * P;
-    for (int p = threadIdx.x; p < P; p += blockDim.x) {
-      const int j = p / k2 + 1, c = p - (j - 1) * k2;
-      int src = c - j;
-      src = src < 0 ? src + k2 : src;
-      const float f = r[i * k2 + c] * r[i * k2 + src];
-      pm[p] = f;
-      zp += zl[p] * f;
-      ff += f * f;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  const int npairs = M * (M + 1) / 2;
+  for (int t = warp; t < npairs + M; t += nwarp) {
+    float acc = 0.f;
+    if (t < npairs) {
+      int i = 0, rem = t;
+      while (rem >= M - i) {
+        rem -= M - i;
+        ++i;
+      }
+      const int i2 = i + rem;
+      for (int p = lane; p < P; p += 32) acc += ph[i * Pp + p] * ph[i2 * Pp + p];
+      acc = warp_sum(acc);
+      if (lane == 0) {
+        G[i][i2] = acc;
+        G[i2][i] = acc;
+      }
+    } else {
+      const int i = t - npairs;
+      for (int p = lane; p < P; p += 32) acc += zl[p] * ph[i * Pp + p];
+      acc = warp_sum(acc);
+      if (lane == 0) z0phi[i] = acc;
     }
-    zp = block_sum(zp, red);
-    ff = block_sum(ff, red);
-    const float gamma = 1.0f - zp / (ff + eps);
-    for (int p = threadIdx.x; p < P; p += blockDim.x) zl[p] += gamma * pm[p];
-    if (threadIdx.x == 0) {
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < M; ++i) {
+      float zp = z0phi[i];
+      for (int i2 = 0; i2 < i; ++i2) zp += gam[i2] * G[i2][i];
+      gam[i] = 1.0f - zp / (G[i][i] + eps);
       const float logit = vkb[((long long)l * M + i) * nw + d + k];
       coef[((long long)l * M + i) * 2 + 0] = sigmoid_f(logit);
-      coef[((long long)l * M + i) * 2 + 1] = zp + eps;
+      coef[((long long)l * M + i) * 2 + 1] = 1.0f / (zp + eps);
     }
+  }
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    float dz = 0.f;
+    for (int i = 0; i < M; ++i) dz += gam[i] * ph[i * Pp + p];
+    zl[p] += dz;
   }
 }
 
 // Delta-rule update of the rows of A_l, memory tokens applied in order.
-// Row j of A only ever needs row j of the values, so each warp keeps its row
-// of A in registers (lane owns entries lane + 32 t) and runs, for i = 0..M-1,
-//   vbar = A[j] . phi_i / (zphi_i + eps)
+// Row j of A only ever needs row j of the values, so each warp keeps rows of
+// A in registers (lane owns entries lane + 32 t, t < NT = P / 32) and runs,
+// for i = 0..M-1,
+//   vbar = A[j] . phi_i * inv_den_i,     inv_den_i = 1 / (zphi_i + eps)
 //   A[j] += beta_i (v_i[j] - vbar) phi_i,
 // reading and writing each row of A once.  v_i[j] comes from the memory-row
 // projection GEMM (vkb), phi_i and the coefficients from the feature kernel.
 // Also refreshes the activation-dtype copy Aa of the state (the next read's
-// GEMM operand) when Aa != A.  Needs P % 32 == 0, P <= 32 * MAXT, M <= 32.
-template <typename AT>
-__global__ void __launch_bounds__(256) assoc_write_update_kernel(
+// GEMM operand) when Aa != A.  M <= 32.
+template <typename AT, int NT>
+__global__ void __launch_bounds__(128) assoc_write_update_kernel(
     const float* __restrict__ vkb, int nw, const float* __restrict__ phiM,
-    const float* __restrict__ coef, float* __restrict__ A, AT* __restrict__ Aa, int M, int d, int P,
+    const float* __restrict__ coef, float* __restrict__ A, AT* __restrict__ Aa, int M, int d,
     int rows_per_block, int g_first) {
-  constexpr int MAXT = 16;
+  constexpr int P = 32 * NT;
   extern __shared__ float sm[];
   float* ps = sm;                 // [M][P]
   float* cs = ps + M * P;         // [M][2]
@@ -171,7 +206,6 @@ __global__ void __launch_bounds__(256) assoc_write_update_kernel(
   for (int t = threadIdx.x; t < 2 * M; t += blockDim.x) cs[t] = coef[(long long)l * M * 2 + t];
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw_ = blockDim.x >> 5;
-  const int nt = P >> 5;
   const int j0 = blockIdx.x * rows_per_block;
   float* Al = A + (long long)l * d * P;
   AT* Aal = Aa + (long long)l * d * P;
@@ -181,40 +215,38 @@ __global__ void __launch_bounds__(256) assoc_write_update_kernel(
   const int j_end = min(j0 + rows_per_block, d);
   for (int jb = j0 + warp * RW; jb < j_end; jb += nw_ * RW) {
     float vj[RW];
-    float a[RW][MAXT];
+    float a[RW][NT];
 #pragma unroll
     for (int r = 0; r < RW; ++r) {
       const int j = jb + r;
       const bool ok = j < j_end;
       vj[r] = (ok && lane < M) ? vl[(long long)lane * nw + j] : 0.f;  // lane i holds v_i[j]
 #pragma unroll
-      for (int t = 0; t < MAXT; ++t) a[r][t] = (ok && t < nt) ? Al[(long long)j * P + lane + 32 * t] : 0.f;
+      for (int t = 0; t < NT; ++t) a[r][t] = ok ? Al[(long long)j * P + lane + 32 * t] : 0.f;
     }
     for (int i = 0; i < M; ++i) {
       const float* pi = ps + i * P + lane;
-      float phv[MAXT];
+      float phv[NT];
 #pragma unroll
-      for (int t = 0; t < MAXT; ++t) phv[t] = t < nt ? pi[32 * t] : 0.f;
+      for (int t = 0; t < NT; ++t) phv[t] = pi[32 * t];
       float dot[RW];
 #pragma unroll
       for (int r = 0; r < RW; ++r) {
         dot[r] = 0.f;
 #pragma unroll
-        for (int t = 0; t < MAXT; ++t)
-          if (t < nt) dot[r] += a[r][t] * phv[t];
+        for (int t = 0; t < NT; ++t) dot[r] += a[r][t] * phv[t];
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
         for (int r = 0; r < RW; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
-      const float beta = cs[2 * i], den = cs[2 * i + 1];
+      const float beta = cs[2 * i], inv_den = cs[2 * i + 1];
 #pragma unroll
       for (int r = 0; r < RW; ++r) {
         const float vi = __shfl_sync(0xffffffffu, vj[r], i);
-        const float c = beta * (vi - dot[r] / den);
+        const float c = beta * (vi - dot[r] * inv_den);
 #pragma unroll
-        for (int t = 0; t < MAXT; ++t)
-          if (t < nt) a[r][t] += c * phv[t];
+        for (int t = 0; t < NT; ++t) a[r][t] += c * phv[t];
       }
     }
 #pragma unroll
@@ -222,11 +254,9 @@ __global__ void __launch_bounds__(256) assoc_write_update_kernel(
       const int j = jb + r;
       if (j < j_end) {
 #pragma unroll
-        for (int t = 0; t < MAXT; ++t) {
-          if (t < nt) {
-            Al[(long long)j * P + lane + 32 * t] = a[r][t];
-            if ((void*)Aal != (void*)Al) st_from_f32(Aal + (long long)j * P + lane + 32 * t, a[r][t]);
-          }
+        for (int t = 0; t < NT; ++t) {
+          Al[(long long)j * P + lane + 32 * t] = a[r][t];
+          if ((void*)Aal != (void*)Al) st_from_f32(Aal + (long long)j * P + lane + 32 * t, a[r][t]);
         }
       }
     }
