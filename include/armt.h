@@ -22,7 +22,7 @@
  *         each against the state the previous write left -- a delta rule):
  *         k = Wk_a h_i, v = Wv_a h_i, beta = sigmoid(wbeta_a^T h_i), p = phi(k),
  *         vbar = A_l p / (z_l^T p + assoc_eps),
- *         gamma = 1 - z_l^T p / (p^T p + assoc_eps),
+ *         gamma = clip(1 - z_l^T p / (p^T p + assoc_eps), 0, 1),
  *         A_l <- A_l + beta (v - vbar) p^T,  z_l <- z_l + gamma p
  *   phi = DPFP of order nu: r = [relu(k), relu(-k)], blocks r * roll(r, j),
  *         j = 1..nu, roll(r, j)_i = r_{(i-j) mod 2k};  P = 2 * key_dim * nu.

@@ -29,11 +29,16 @@ Oseledets, arXiv:2506.05229):
     read:  x <- x + A phi(W_Q x) / (z^T phi(W_Q x) + eps)       (every row)
     write: for the memory rows h_i, i = 0..M-1 in order, one at a time:
            k = W_K h_i, v = W_V h_i, beta = sigmoid(w_b^T h_i), p = phi(k),
-           vbar = A p / (z^T p + eps), gamma = 1 - z^T p / (p^T p + eps),
+           vbar = A p / (z^T p + eps),
+           gamma = clip(1 - z^T p / (p^T p + eps), 0, 1),
            A <- A + beta (v - vbar) p^T,  z <- z + gamma p
            (a delta rule: each write corrects against the state the previous
            write left; applying all M writes against the pre-segment state
-           instead makes the state diverge on random-init models).
+           instead makes the state diverge on random-init models).  Clipping
+           gamma to [0, 1] keeps z a non-negative combination of the
+           non-negative features, so every denominator z^T phi + eps stays
+           >= eps; unclipped, z turns negative and the state diverges within
+           ~60 segments of the 1B-shaped model.
   DPFP_nu(x): r = [relu(x), relu(-x)], phi = concat_{j=1..nu} r * roll(r, j),
   roll(r, j)_i = r_{(i - j) mod 2k}.
 * The LLaMA block run inside each cell (section 三: Llama-3-family models,
@@ -182,7 +187,7 @@ def delta_rule_update(A, z, keys, values, beta, nu, eps) -> Tuple[np.ndarray, np
     phi = dpfp(keys, nu)                                   # [R, P]
     zphi = phi @ z                                         # [R]
     vbar = (phi @ A.T) / (zphi + eps)[:, None]             # [R, d]
-    gamma = 1.0 - zphi / (np.sum(phi * phi, axis=-1) + eps)
+    gamma = np.clip(1.0 - zphi / (np.sum(phi * phi, axis=-1) + eps), 0.0, 1.0)
     dA = (beta[:, None] * (values - vbar)).T @ phi         # [d, P]
     dz = gamma @ phi                                       # [P]
     return A + dA, z + dz

@@ -101,7 +101,7 @@ __global__ void assoc_phi_kernel(const float* __restrict__ q, const float* __res
 
 // Per layer (one block), memory tokens i = 0..M-1 in order:
 //   phi_i = DPFP(k_i),  zphi_i = z_{i-1}^T phi_i,
-//   gamma_i = 1 - zphi_i / (phi_i^T phi_i + eps),  z_i = z_{i-1} + gamma_i phi_i.
+//   gamma_i = clip(1 - zphi_i / (phi_i^T phi_i + eps), 0, 1),  z_i = z_{i-1} + gamma_i phi_i.
 // The normaliser's recurrence does not involve A.  Expanding z_{i-1} gives
 //   zphi_i = z_0^T phi_i + sum_{i' < i} gamma_i' (phi_i'^T phi_i),
 // so the block computes every z_0^T phi_i and the Gram matrix G = Phi Phi^T
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(256) assoc_write_feat_kernel(
     for (int i = 0; i < M; ++i) {
       float zp = z0phi[i];
       for (int i2 = 0; i2 < i; ++i2) zp += gam[i2] * G[i2][i];
-      gam[i] = 1.0f - zp / (G[i][i] + eps);
+      gam[i] = fminf(fmaxf(1.0f - zp / (G[i][i] + eps), 0.0f), 1.0f);  // keeps z >= 0
       const float logit = vkb[((long long)l * M + i) * nw + d + k];
       coef[((long long)l * M + i) * 2 + 0] = sigmoid_f(logit);
       coef[((long long)l * M + i) * 2 + 1] = 1.0f / (zp + eps);

@@ -82,7 +82,7 @@ def run_gpu(cfg, W, tok, n_seg, schedule):
 # ------------------------------------------------------------ GEMM unit --
 
 @pytest.mark.parametrize("G,M,N,K", [(1, 128, 256, 64), (3, 1040, 512, 2048), (2, 17, 256, 384),
-                                     (1, 300, 768, 8192)])
+                                     (1, 300, 768, 8192), (2, 16, 256, 128), (1, 144, 512, 192)])
 def test_grouped_gemm_bf16_matches_fp64_matmul(G, M, N, K):
     g = torch.Generator(device="cpu").manual_seed(G * 1000 + M)
     A = torch.randn(G, M, K, generator=g).to(torch.bfloat16)
@@ -248,3 +248,45 @@ def test_armt1b_8k_matches_oracle_and_schedules_agree(armt1b):
         assert g[key]["max_abs"] <= 1.5 * m[key]["max_abs"], (key, g[key], m[key])
     for key in ("A", "z"):
         assert 1.0 - g[key]["cos"] <= 1.5 * (1.0 - m[key]["cos"]), (key, g[key], m[key])
+
+
+def _derived_bounds_hold(gpu, exact, model, S, n):
+    g = dict(hidden=stats(gpu[0], exact[0]), A=stats(gpu[1], exact[1]), z=stats(gpu[2], exact[2]))
+    m = dict(hidden=stats(model[0], exact[0]), A=stats(model[1], exact[1]), z=stats(model[2], exact[2]))
+    ok = g["hidden"]["cos"] >= 0.999
+    for key in ("hidden", "A", "z"):
+        ok &= g[key]["max_abs"] <= 1.5 * m[key]["max_abs"]
+    for key in ("A", "z"):
+        ok &= 1.0 - g[key]["cos"] <= 1.5 * (1.0 - m[key]["cos"])
+    return bool(ok), g, m
+
+
+def test_armt1b_131k_full_size_properties():
+    """The benchmark workload (128 segments, 131,072 tokens) in the benchmark's launch
+    configuration: properties that hold at any size, plus sampled outputs the
+    oracle can compute (a prefix of segments depends only on its own tokens)."""
+    cfg, n, W, tok = I.make_workload("armt-1b-131k")
+    S = cfg.seg_len
+    m = B.Model(cfg, B.device_weight_tensors(cfg, W))
+    t = torch.from_numpy(tok).cuda()
+    hd, Ad, zd = m.forward(t, n)                                   # diagonal, 128 segments
+    hs, As, zs = m.forward(t, n, schedule=B.SCHEDULE_SEQUENTIAL)
+    bitwise = bool(torch.equal(hd, hs) and torch.equal(Ad, As) and torch.equal(zd, zs))
+    del hs, As, zs
+    ha, Aa, za = m.forward(t[:64 * S].contiguous(), 64)
+    hb, Ab, zb = m.forward(t[64 * S:].contiguous(), 64, mem_A=Aa.reshape(-1), mem_z=za.reshape(-1))
+    resume = bool(torch.equal(torch.cat([ha, hb]), hd) and torch.equal(Ab, Ad) and torch.equal(zb, zd))
+    h2, A2, z2 = m.forward(t[:2 * S].contiguous(), 2)
+    prefix = bool(torch.equal(h2, hd[:2 * S]))
+    torch.cuda.synchronize()
+    m.armt_sync_status()
+    finite = bool(torch.isfinite(hd).all() and torch.isfinite(Ad).all() and torch.isfinite(zd).all())
+    gpu2 = (h2.cpu().numpy(), A2.cpu().numpy(), z2.cpu().numpy())
+    m.close()
+    exact = O.forward(cfg, W, tok[:2 * S], 2)
+    model = O.forward(cfg, W, tok[:2 * S], 2, operands="bf16")
+    ok, g, mstats = _derived_bounds_hold(gpu2, exact, model, S, 2)
+    record("armt1b_131k", bitwise_diag_seq=bitwise, resume_64_64=resume, prefix_2_segments=prefix,
+           finite=finite, gpu_vs_fp64_first2=g, model_vs_fp64_first2=mstats)
+    assert bitwise and resume and prefix and finite
+    assert ok, (g, mstats)

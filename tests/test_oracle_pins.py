@@ -252,7 +252,7 @@ def test_two_segments_one_layer_hand_expansion():
             for r in range(A.shape[0]):
                 vbar_r = float(A[r] @ phi) / (zp + eps)
                 A[r] = A[r] + beta * (val[r] - vbar_r) * phi
-            z = z + (1.0 - zp / (ff + eps)) * phi
+            z = z + min(max(1.0 - zp / (ff + eps), 0.0), 1.0) * phi
         return A, z
 
     P = cfg.phi_dim
@@ -317,6 +317,25 @@ def test_state_stays_bounded_on_a_mid_size_model():
     out, A, z = O.forward(cfg, W, tok, 12)
     assert np.isfinite(out).all()
     assert np.abs(A).max() < 1.0 and np.abs(z).max() < 10.0
+
+
+def test_normaliser_stays_nonnegative_and_denominators_positive():
+    # with the correction clipped to [0, 1], z is a non-negative combination of
+    # non-negative features: z >= 0 and z^T phi + eps >= eps for any query
+    rng = np.random.default_rng(10)
+    k, d, nu, eps = 8, 5, 3, 1e-6
+    P = 2 * k * nu
+    A, z = np.zeros((d, P)), np.zeros(P)
+    for _ in range(200):
+        keys = rng.standard_normal((1, k)) * rng.uniform(0.1, 5.0)
+        A, z = O.delta_rule_update(A, z, keys, rng.standard_normal((1, d)), rng.uniform(0, 1, 1), nu, eps)
+        assert (z >= 0).all()
+    # an over-full normaliser (z^T phi > phi^T phi) is not pushed negative
+    key = rng.standard_normal((1, k))
+    phi = _dpfp_loops(list(key[0]), nu)
+    z_big = 10.0 * phi
+    _, z2 = O.delta_rule_update(np.zeros((d, P)), z_big, key, np.ones((1, d)), np.ones(1), nu, eps)
+    np.testing.assert_array_equal(z2, z_big)      # gamma clipped to 0
 
 
 def test_tiny_workload_is_well_conditioned():
