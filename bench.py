@@ -39,6 +39,8 @@ def parse():
     p.add_argument("--no-seq", action="store_true", help="skip the sequential-schedule comparison")
     p.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-full", action="store_true",
+                   help="skip the full-causal-attention LLaMA baseline on the same weights")
     return p.parse_args()
 
 
@@ -110,6 +112,22 @@ class ClockSampler:
         reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
                 "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+def replica_throughput(ms_local, n_tok_local, steps, world, dist=None, device="cpu"):
+    """Whole-job throughput of `world` independent replicas (weak scaling).
+
+    Each rank ran `steps` steps over `n_tok_local` tokens in `ms_local` ms;
+    the job's time is the slowest rank's (all-reduce MAX), its work the sum
+    over ranks.  Returns (max_ms, tokens_per_s).
+    """
+    ms = float(ms_local)
+    if dist is not None and world > 1:
+        import torch
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * n_tok_local * steps / (ms / 1000.0)
 
 
 def load_peaks():
@@ -215,13 +233,9 @@ def main():
     kt = model.armt_kernel_times()
     model.armt_set_profiling(False)
     model.armt_sync_status()
-    if pg is not None:
-        t = torch.tensor([ms_total], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total, value = replica_throughput(ms_total, n_tok, args.steps, world, pg, "cuda")
     clocks = clk.summary()
     ms_step = ms_total / args.steps
-    value = world * n_tok * args.steps / (ms_total / 1000.0)
 
     # ---- roofline of the dominant kernel (gate-up grouped GEMM) ----------
     peaks, peak_src = load_peaks()
@@ -251,6 +265,21 @@ def main():
         seq_ms = e0.elapsed_time(e1)
         seq = {"ms_per_step": seq_ms, "tokens_per_s": n_tok / (seq_ms / 1000.0),
                "speedup_diag_over_seq": seq_ms / ms_step}
+
+    # ---- full-causal-attention LLaMA on the same weights (no memory) -----
+    full = None
+    if not args.no_full and cfg.dtype == "bf16":
+        model.armt_forward_full_attention(tokens, hidden, stream)   # grows its workspace
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        model.armt_forward_full_attention(tokens, hidden, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        model.armt_sync_status()
+        full_ms = e0.elapsed_time(e1)
+        full = {"ms_per_step": full_ms, "tokens_per_s": n_tok / (full_ms / 1000.0),
+                "speedup_diag_over_full": full_ms / ms_step}
 
     # ---- end to end through the host-buffer entry point ------------------
     e2e = None
@@ -296,6 +325,7 @@ def main():
             "model_tflops": total_flops * args.steps / (ms_total / 1000.0) / 1e12,
             "kernels": per_class,
             "sequential": seq,
+            "full_attention": full,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": int(launches),

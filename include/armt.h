@@ -175,6 +175,20 @@ ARMT_API armt_status armt_forward_host(armt_model* m, const int32_t* h_tokens, i
                               float* h_hidden_out, float* h_mem_A, float* h_mem_z,
                               int32_t mem_in_valid, int32_t schedule, void* stream);
 
+/* Full-causal-attention baseline on the same weights: the plain LLaMA stack
+ * (RMSNorm, RoPE at positions 0..n_tokens-1, causal GQA attention over the
+ * whole sequence, SwiGLU, final RMSNorm) without memory tokens and without
+ * the associative memory -- the "standard" model the ARMT forward is compared
+ * with (summary page, sections 一 and 五: diagonal-batched ARMT vs the full
+ * LLaMA-1B at 131,072 tokens).
+ *   tokens      device int32 [n_tokens] (ids clamped to [0, V))
+ *   hidden_out  device fp32 [n_tokens, d]
+ * bf16 models only (ARMT_ERR_UNSUPPORTED otherwise).  The model grows a
+ * separate activation workspace for n_tokens on first use (synchronises
+ * `stream` when it grows); n_tokens <= 2^20. */
+ARMT_API armt_status armt_forward_full_attention(armt_model* m, const int32_t* tokens,
+                                                 int64_t n_tokens, float* hidden_out, void* stream);
+
 /* Grouped matrix multiplication, the building block of the grouped layer
  * (section 三: weights stacked per group, outputs preallocated as one tensor
  * and viewed per group):  C[g] = A[g] * B[g]^T for g = 0..G-1, with

@@ -28,7 +28,7 @@ KERNEL_CLASSES = ("gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down", "attention",
 
 EXPORTED = ("armt_create", "armt_destroy", "armt_forward", "armt_forward_sequential",
             "armt_forward_host", "armt_grouped_gemm_bf16", "armt_segment_attention_bf16",
-            "armt_segment_attention_bf16_noalloc", "armt_state_sizes", "armt_launch_count",
+            "armt_segment_attention_bf16_noalloc", "armt_forward_full_attention", "armt_state_sizes", "armt_launch_count",
             "armt_set_profiling", "armt_kernel_times", "armt_sync_status", "armt_status_string",
             "armt_last_error")
 
@@ -77,6 +77,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     for fn in (lib.armt_forward, lib.armt_forward_sequential):
         fn.argtypes = [P, P, I64, P, P, P, I32, P]
     lib.armt_forward_host.argtypes = [P, P, I64, P, P, P, I32, I32, P]
+    lib.armt_forward_full_attention.argtypes = [P, P, I64, P, P]
     lib.armt_grouped_gemm_bf16.argtypes = [P, P, P, I32, I32, I32, I32, P]
     lib.armt_segment_attention_bf16.argtypes = [P, P, P, I32, I32, I32, I32, I32, P]
     lib.armt_segment_attention_bf16_noalloc.argtypes = [P, P, I32, I32, I32, I32, I32, P]
@@ -213,6 +214,12 @@ class Model:
         self.armt_forward(tokens, n_segments, hidden, A, z, 1 if valid else 0, stream, schedule)
         L, d, P = self.cfg.n_layers, self.cfg.d_model, self.cfg.phi_dim
         return hidden, A.view(L, d, P), z.view(L, P)
+
+    def armt_forward_full_attention(self, tokens, hidden_out, stream=None):
+        """Plain causal LLaMA over all tokens (no memory), same weights."""
+        _check(_lib.armt_forward_full_attention(self._h, _ptr(tokens), int(tokens.numel()),
+                                                _ptr(hidden_out), _stream_ptr(stream)),
+               "armt_forward_full_attention")
 
     def armt_launch_count(self, n_segments, schedule=SCHEDULE_DIAGONAL) -> int:
         n = ctypes.c_int64()

@@ -173,6 +173,8 @@ struct ModelBase {
   virtual armt_status create(const armt_weights* w, cudaStream_t st) = 0;
   virtual armt_status forward(const int32_t* tokens, int64_t n, float* hidden, float* A, float* z,
                               int mem_in_valid, int schedule, cudaStream_t st) = 0;
+  virtual armt_status forward_full(const int32_t* tokens, int64_t T, float* hidden,
+                                   cudaStream_t st) = 0;
 
   int rows() const { return cfg.seg_len + cfg.n_mem; }
   int phi_dim() const { return 2 * cfg.key_dim * cfg.dpfp_nu; }
@@ -262,6 +264,14 @@ struct Model : ModelBase {
   CUtensorMap tmXa, tmAWq, tmPhi, tmAa, tmNrm, tmWqkv, tmAtt, tmWo, tmWgu, tmU, tmWd, tmQK, tmVt,
       tmWw;
   size_t upd_smem = 0, feat_smem = 0, attn_smem = 0;
+  // full-causal-attention LLaMA over a whole sequence (baseline): one
+  // activation slot, grown on demand
+  DevAllocs full_mem;
+  int64_t full_T = 0;
+  float *Xf = nullptr, *Resf = nullptr, *Ssqf = nullptr, *cosF = nullptr, *sinF = nullptr;
+  AT *Nrmf = nullptr, *QKVf = nullptr, *Vtf = nullptr, *Attf = nullptr, *Uf = nullptr;
+  CUtensorMap tmNrmf, tmQKf, tmVtf, tmAttf, tmUf;
+  ~Model() override { full_mem.free_all(); }
   int upd_rows_per_block = 32;
 
   armt_status copy_in(void* dst, const void* src, size_t bytes, cudaStream_t st) {
@@ -550,6 +560,123 @@ struct Model : ModelBase {
     return ARMT_OK;
   }
 
+  // Workspace of the full-attention baseline for T tokens.
+  armt_status ensure_full(int64_t T, cudaStream_t st) {
+    if (T <= full_T) return ARMT_OK;
+    CK(cudaStreamSynchronize(st));
+    full_mem.free_all();
+    full_T = 0;
+    const armt_config& c = cfg;
+    const size_t d = c.d_model, hd = c.head_dim, F = c.ffn_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
+    const size_t tp = (size_t)((T + 7) / 8 * 8);
+    CKS(full_mem.alloc_n(&Xf, T * d));
+    CKS(full_mem.alloc_n(&Resf, T * d));
+    CKS(full_mem.alloc_n(&Ssqf, T * (size_t)npart));
+    CKS(full_mem.alloc_n(&Nrmf, T * d));
+    CKS(full_mem.alloc_n(&QKVf, T * (Hq + Hkv) * hd));
+    CKS(full_mem.alloc_n(&Vtf, Hkv * hd * tp));
+    CKS(full_mem.alloc_n(&Attf, T * Hq * hd));
+    CKS(full_mem.alloc_n(&Uf, T * F));
+    {
+      std::vector<float> hc((size_t)T * (hd / 2)), hs((size_t)T * (hd / 2));
+      for (int64_t t = 0; t < T; ++t)
+        for (size_t i = 0; i < hd / 2; ++i) {
+          const double ang = (double)t * std::pow(c.rope_base, -2.0 * (double)i / (double)hd);
+          hc[t * (hd / 2) + i] = (float)std::cos(ang);
+          hs[t * (hd / 2) + i] = (float)std::sin(ang);
+        }
+      CKS(full_mem.alloc_n(&cosF, hc.size()));
+      CKS(full_mem.alloc_n(&sinF, hs.size()));
+      CK(cudaMemcpy(cosF, hc.data(), hc.size() * 4, cudaMemcpyHostToDevice));
+      CK(cudaMemcpy(sinF, hs.data(), hs.size() * 4, cudaMemcpyHostToDevice));
+    }
+    bool ok = true;
+    ok &= encode_tmap_bf16_3d(&tmNrmf, Nrmf, (int)d, (int)T, 1, TC_BM);
+    ok &= encode_tmap_bf16_3d(&tmQKf, QKVf, (int)((Hq + Hkv) * hd), (int)T, 1, 128);
+    ok &= encode_tmap_bf16_3d(&tmVtf, Vtf, (int)tp, (int)hd, (int)Hkv, (int)hd);
+    ok &= encode_tmap_bf16_3d(&tmAttf, Attf, (int)(Hq * hd), (int)T, 1, TC_BM);
+    ok &= encode_tmap_bf16_3d(&tmUf, Uf, (int)F, (int)T, 1, TC_BM);
+    if (!ok) return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    full_T = T;
+    return ARMT_OK;
+  }
+
+  // Plain causal LLaMA over T tokens with the same weights: no memory tokens,
+  // no associative memory, one attention over the whole sequence.  Layers run
+  // one after another; each launch reads activation slot 0 and weight slot l.
+  armt_status forward_full(const int32_t* tokens, int64_t T64, float* hidden,
+                           cudaStream_t st) override {
+    if constexpr (!kTC) {
+      return fail(ARMT_ERR_UNSUPPORTED, "the full-attention baseline needs a bf16 model");
+    } else {
+      if (T64 > (1 << 20)) return fail(ARMT_ERR_SHAPE, "n_tokens > 1048576");
+      CKS(ensure_full(T64, st));
+      const armt_config& c = cfg;
+      const int T = (int)T64, L = c.n_layers, d = c.d_model, hd = c.head_dim, F = c.ffn_dim;
+      const int Hq = c.n_q_heads, Hkv = c.n_kv_heads, Nq = n_qkv();
+      const int tp = (T + 7) / 8 * 8;
+      const long long Td = (long long)T * d;
+      CKS(prof_begin(ARMT_KC_OTHER, st));
+      embed_gather_kernel<WT><<<T, 256, 0, st>>>(tokens, embed, memtok, Xf, (WT*)nullptr, T, d, c.vocab);
+      CK(cudaGetLastError());
+      CKS(prof_end(st));
+      const RowNormIn no_scale{nullptr, 0, 0.f, 0.f};
+      const RowNormIn norm_in{Ssqf, npart, 1.0f / (float)d, c.norm_eps};
+      for (int l = 0; l < L; ++l) {
+        CKS(prof_begin(ARMT_KC_NORM, st));
+        rmsnorm_kernel<AT><<<dim3(T, 1), 256, 0, st>>>(Xf, 0, g1 + (long long)l * d, 0, Nrmf, 0, d,
+                                                      c.norm_eps, 0);
+        CK(cudaGetLastError());
+        CKS(prof_end(st));
+        CKS(prof_begin(ARMT_KC_GEMM_QKV, st));
+        CK((launch_gemm_tc<FQkv, 256>(tmNrmf, tmWqkv, T, Nq, d, 0, 1, d_err,
+                                      FQkv{QKVf, cosF, sinF, T, hd, (Hq + Hkv) * hd, (Hq + Hkv) * hd,
+                                           Vtf, Hkv, tp, no_scale},
+                                      num_sms, st, 0, 0, l)));
+        CKS(prof_end(st));
+        CKS(prof_begin(ARMT_KC_ATTENTION, st));
+        {
+          AttnArgs aa;
+          aa.out = Attf;
+          aa.T = T;
+          aa.Hq = Hq;
+          aa.Hkv = Hkv;
+          aa.g_first = 0;
+          aa.n_qtiles = (T + 127) / 128;
+          aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
+          aa.err = d_err;
+          if (hd == 64)
+            CK(launch_attn_tc<64>(tmQKf, tmVtf, aa, 1, st));
+          else
+            CK(launch_attn_tc<128>(tmQKf, tmVtf, aa, 1, st));
+        }
+        CKS(prof_end(st));
+        CKS(prof_begin(ARMT_KC_GEMM_O, st));
+        CK((launch_gemm_tc<FRes, 256>(tmAttf, tmWo, T, d, Hq * hd, 0, 1, d_err,
+                                      FRes{Xf, Resf, nullptr, T, d, 0,
+                                           RowNormOut<AT>{g2 + (long long)l * d, Nrmf, Ssqf}},
+                                      num_sms, st, 0, 0, l)));
+        CKS(prof_end(st));
+        CKS(prof_begin(ARMT_KC_GEMM_GATEUP, st));
+        CK((launch_gemm_tc<FSwi, 256>(tmNrmf, tmWgu, T, 2 * F, d, 0, 1, d_err, FSwi{Uf, T, F, norm_in},
+                                      num_sms, st, 0, 0, l)));
+        CKS(prof_end(st));
+        CKS(prof_begin(ARMT_KC_GEMM_DOWN, st));
+        CK((launch_gemm_tc<FRes, 256>(tmUf, tmWd, T, d, F, 0, 1, d_err,
+                                      FRes{Resf, Xf, nullptr, T, d, 0,
+                                           RowNormOut<AT>{nullptr, nullptr, nullptr}},
+                                      num_sms, st, 0, 0, l)));
+        CKS(prof_end(st));
+      }
+      CKS(prof_begin(ARMT_KC_NORM, st));
+      rmsnorm_kernel<float><<<dim3(T, 1), 256, 0, st>>>(Xf, 0, gf, 0, hidden, 0, d, c.norm_eps, 0);
+      CK(cudaGetLastError());
+      CKS(prof_end(st));
+      (void)Td;
+      return ARMT_OK;
+    }
+  }
+
   armt_status forward(const int32_t* tokens, int64_t n, float* hidden, float* A, float* z,
                       int mem_in_valid, int schedule, cudaStream_t st) override {
     const int L = cfg.n_layers, d = cfg.d_model, P = phi_dim();
@@ -762,6 +889,14 @@ armt_status armt_forward_host(armt_model* m, const int32_t* h_tokens, int64_t n,
   CK(cudaMemcpyAsync(h_z, b->st_z, nz * sizeof(float), cudaMemcpyDeviceToHost, st));
   CK(cudaStreamSynchronize(st));
   return ARMT_OK;
+}
+
+armt_status armt_forward_full_attention(armt_model* m, const int32_t* tokens, int64_t n_tokens,
+                                       float* hidden_out, void* stream) {
+  if (m == nullptr || tokens == nullptr || hidden_out == nullptr)
+    return fail(ARMT_ERR_ARG, "NULL argument");
+  if (n_tokens <= 0) return fail(ARMT_ERR_ARG, "n_tokens must be positive");
+  return m->impl->forward_full(tokens, n_tokens, hidden_out, reinterpret_cast<cudaStream_t>(stream));
 }
 
 armt_status armt_grouped_gemm_bf16(const void* A, const void* B, float* C, int32_t G, int32_t M,

@@ -38,6 +38,7 @@ struct GemmTcShape {
   int rows;       // valid rows per group (M), counted from row0
   int row0;       // first A row read (TMA row coordinate of output row 0)
   int a_slot_off; // A is read from layer slot (layer + a_slot_off)
+  int b_slot_off; // B (weights) from layer slot (layer + b_slot_off)
   int N, K;
   int g_first, g_count;
   int m_tiles, n_tiles, k_blocks;
@@ -112,7 +113,8 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
           tma_load_3d(sA + stage * C::A_BYTES, &tmA, kb * TC_BK, sh.row0 + mt * TC_BM,
                       layer + sh.a_slot_off, &full[stage]);
-          tma_load_3d(sB + stage * C::B_BYTES, &tmB, kb * TC_BK, nt * BN, layer, &full[stage]);
+          tma_load_3d(sB + stage * C::B_BYTES, &tmB, kb * TC_BK, nt * BN, layer + sh.b_slot_off,
+                      &full[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -200,7 +202,8 @@ bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int K, int rows, in
 template <class Epi, int BN>
 cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int rows, int N, int K,
                            int g_first, int g_count, int* err, const Epi& epi, int num_sms,
-                           cudaStream_t stream, int row0 = 0, int a_slot_off = 0) {
+                           cudaStream_t stream, int row0 = 0, int a_slot_off = 0,
+                           int b_slot_off = 0) {
   using C = TcCfg<BN>;
   static bool configured = false;
   if (!configured) {
@@ -213,6 +216,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int r
   sh.rows = rows;
   sh.row0 = row0;
   sh.a_slot_off = a_slot_off;
+  sh.b_slot_off = b_slot_off;
   sh.N = N;
   sh.K = K;
   sh.g_first = g_first;

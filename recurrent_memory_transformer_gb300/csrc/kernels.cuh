@@ -20,7 +20,8 @@ namespace armt {
 // ------------------------------------------------------- layer-0 input --
 
 // X[0] = [E[tokens of the segment]; memory embeddings] (fp32 residual stream)
-// plus the activation-dtype copy Xa[0] (used as a GEMM operand).
+// plus the activation-dtype copy Xa[0] (used as a GEMM operand; nullptr or
+// equal to X when not needed).
 template <typename WT>
 __global__ void embed_gather_kernel(const int32_t* __restrict__ tokens, const WT* __restrict__ embed,
                                     const WT* __restrict__ mem, float* __restrict__ X,
@@ -39,7 +40,7 @@ __global__ void embed_gather_kernel(const int32_t* __restrict__ tokens, const WT
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
     const float v = ld_as_f32(src + i);
     xo[i] = v;
-    if ((void*)Xa != (void*)X) xa[i] = src[i];
+    if (Xa != nullptr && (void*)Xa != (void*)X) xa[i] = src[i];
   }
 }
 

@@ -293,3 +293,53 @@ def test_armt1b_131k_full_size_properties():
            finite=finite, gpu_vs_fp64_first2=g, model_vs_fp64_first2=mstats)
     assert bitwise and resume and prefix and finite
     assert ok, (g, mstats)
+
+
+# ------------------------------------------- full-attention LLaMA baseline --
+
+def _plain_llama_oracle(cfg, W, tok, operands=None):
+    rnd = O.ROUNDING[operands]
+    W64 = O.widen_weights(W)
+    x = W64["embed"][tok]
+    for l in range(cfg.n_layers):
+        x = O.llama_block(x, cfg, W64, l, rnd)
+    return O.rmsnorm(x, W64["norm_f"], cfg.norm_eps)
+
+
+@pytest.mark.parametrize("T", [1040, 300])
+def test_full_attention_baseline_matches_oracle(T):
+    cfg = dataclasses.replace(I.ARMT_1B, n_layers=2)
+    W = I.make_weights(cfg, seed=31, norm_jitter=0.1)
+    tok = np.random.default_rng(31).integers(0, cfg.vocab, size=T).astype(np.int32)
+    m = B.Model(cfg, B.device_weight_tensors(cfg, W))
+    h = torch.empty((T, cfg.d_model), dtype=torch.float32, device="cuda")
+    m.armt_forward_full_attention(torch.from_numpy(tok).cuda(), h)
+    torch.cuda.synchronize()
+    m.armt_sync_status()
+    got = h.cpu().numpy()
+    m.close()
+    exact = _plain_llama_oracle(cfg, W, tok)
+    model = _plain_llama_oracle(cfg, W, tok, "bf16")
+    g, mm = stats(got, exact), stats(model, exact)
+    record(f"full_attention_T{T}", gpu_vs_fp64=g, model_vs_fp64=mm)
+    assert g["finite"] and g["cos"] >= 0.999, g
+    assert g["max_abs"] <= 2.0 * mm["max_abs"], (g, mm)
+
+
+def test_full_attention_baseline_equals_armt_first_segment_up_to_rounding():
+    # With an empty memory the read adds zero and the memory rows come after
+    # the segment, so segment 0 of the ARMT forward is the plain causal model
+    # over the segment's tokens.
+    cfg = dataclasses.replace(I.ARMT_1B, n_layers=2)
+    W = I.make_weights(cfg, seed=32)
+    tok = I.make_tokens(cfg, 1, seed=32)
+    m = B.Model(cfg, B.device_weight_tensors(cfg, W))
+    t = torch.from_numpy(tok).cuda()
+    ha, _, _ = m.forward(t, 1)
+    hf = torch.empty_like(ha)
+    m.armt_forward_full_attention(t, hf)
+    torch.cuda.synchronize()
+    s = stats(ha.cpu().numpy(), hf.cpu().numpy())
+    m.close()
+    record("full_vs_armt_segment0", **s)
+    assert s["cos"] >= 0.9999 and s["max_abs"] <= 0.05, s
