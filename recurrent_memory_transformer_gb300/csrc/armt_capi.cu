@@ -370,7 +370,7 @@ struct Model : ModelBase {
     CKS(mem.alloc_n(&Qa, L * T * k));
     CKS(mem.alloc_n(&Phi, L * T * P));
     CKS(mem.alloc_n(&Den, L * T));
-    npart = (int)(kTC ? d / 256 : d / 32);
+    npart = (int)(kTC ? d / 128 : d / 32);  // one partial per 128 columns (two epilogue halves)
     CKS(mem.alloc_n(&Ssq, L * T * (size_t)npart));
     CKS(mem.alloc_n(&VKB, L * c.n_mem * (size_t)nw));
     CKS(mem.alloc_n(&PhiM, L * c.n_mem * P));
@@ -425,15 +425,15 @@ struct Model : ModelBase {
   // One grouped GEMM over layers [lo, lo+g): tensor cores for bf16, SIMT +
   // row epilogue for fp32.  Output rows 0..rows-1 read A rows row0.. of layer
   // slot (layer + a_slot_off).
-  template <int BN, class Epi>
+  template <int BN, class Epi, int EPI_WG = 1>
   armt_status gemm(int cls, const CUtensorMap& ta, const CUtensorMap& tb, const AT* a, long long a_gs,
                    const WT* b, int N, int K, const Epi& epi, int lo, int g, cudaStream_t st,
                    int rows = -1, int row0 = 0, int a_slot_off = 0) {
     if (rows < 0) rows = this->rows();
     CKS(prof_begin(cls, st));
     if constexpr (kTC) {
-      CK((launch_gemm_tc<Epi, BN>(ta, tb, rows, N, K, lo, g, d_err, epi, num_sms, st, row0,
-                                  a_slot_off)));
+      CK((launch_gemm_tc<Epi, BN, EPI_WG>(ta, tb, rows, N, K, lo, g, d_err, epi, num_sms, st, row0,
+                                          a_slot_off)));
     } else {
       const float* a0 = reinterpret_cast<const float*>(a) + a_slot_off * a_gs + (long long)row0 * K;
       dim3 grid((N + 63) / 64, (rows + 63) / 64, g);
@@ -477,11 +477,11 @@ struct Model : ModelBase {
     CKS(prof_end(st));
     const AT* Asrc = kTC ? Aa : reinterpret_cast<const AT*>(A);
     const RowNormIn norm_in{Ssq, npart, 1.0f / (float)d, c.norm_eps};
-    CKS((gemm<256>(ARMT_KC_ASSOC_READ, tmPhi, tmAa, Phi, (long long)T * P,
-                   reinterpret_cast<const WT*>(Asrc), d, P,
-                   FRead{X, Den, Res, T, d, RowNormOut<AT>{g1, Nrm, Ssq}}, lo, g, st)));
+    CKS((gemm<256, FRead, 2>(ARMT_KC_ASSOC_READ, tmPhi, tmAa, Phi, (long long)T * P,
+                             reinterpret_cast<const WT*>(Asrc), d, P,
+                             FRead{X, Den, Res, T, d, RowNormOut<AT>{g1, Nrm, Ssq}}, lo, g, st)));
     // attention sub-layer (RMSNorm 1 completes in the QKV epilogue)
-    CKS((gemm<256>(ARMT_KC_GEMM_QKV, tmNrm, tmWqkv, Nrm, Td, Wqkv, Nq, d,
+    CKS((gemm<256, FQkv, 1>(ARMT_KC_GEMM_QKV, tmNrm, tmWqkv, Nrm, Td, Wqkv, Nq, d,
                    FQkv{QKV, cosT, sinT, T, hd, (Hq + Hkv) * hd, qkv_ld, Vt, Hkv, t_pad,
                                   norm_in},
                    lo, g, st)));
@@ -512,7 +512,7 @@ struct Model : ModelBase {
       CK(cudaGetLastError());
     }
     CKS(prof_end(st));
-    CKS((gemm<256>(ARMT_KC_GEMM_O, tmAtt, tmWo, Att, (long long)T * Hq * hd, Wo, d, Hq * hd,
+    CKS((gemm<256, FRes, 2>(ARMT_KC_GEMM_O, tmAtt, tmWo, Att, (long long)T * Hq * hd, Wo, d, Hq * hd,
                    FRes{Res, Res, nullptr, T, d, 0, RowNormOut<AT>{g2, Nrm, Ssq}}, lo, g,
                    st)));
     // MLP sub-layer (RMSNorm 2 completes in the gate-up epilogue)
@@ -629,7 +629,7 @@ struct Model : ModelBase {
         CK(cudaGetLastError());
         CKS(prof_end(st));
         CKS(prof_begin(ARMT_KC_GEMM_QKV, st));
-        CK((launch_gemm_tc<FQkv, 256>(tmNrmf, tmWqkv, T, Nq, d, 0, 1, d_err,
+        CK((launch_gemm_tc<FQkv, 256, 1>(tmNrmf, tmWqkv, T, Nq, d, 0, 1, d_err,
                                       FQkv{QKVf, cosF, sinF, T, hd, (Hq + Hkv) * hd, (Hq + Hkv) * hd,
                                            Vtf, Hkv, tp, no_scale},
                                       num_sms, st, 0, 0, l)));
@@ -652,7 +652,7 @@ struct Model : ModelBase {
         }
         CKS(prof_end(st));
         CKS(prof_begin(ARMT_KC_GEMM_O, st));
-        CK((launch_gemm_tc<FRes, 256>(tmAttf, tmWo, T, d, Hq * hd, 0, 1, d_err,
+        CK((launch_gemm_tc<FRes, 256, 2>(tmAttf, tmWo, T, d, Hq * hd, 0, 1, d_err,
                                       FRes{Xf, Resf, nullptr, T, d, 0,
                                            RowNormOut<AT>{g2 + (long long)l * d, Nrmf, Ssqf}},
                                       num_sms, st, 0, 0, l)));

@@ -308,21 +308,28 @@ __device__ __forceinline__ void epi_unit(const SEpiQkvRope<T>& e, int u, int& a,
 // All 32 lanes call this.
 constexpr int STAGED_FLOATS_PER_WARP = 32 * 64 + 32;
 
-template <int BN, class Epi>
+// With EPI_WG warpgroups, warp part p handles units [p*U/EPI_WG, (p+1)*U/EPI_WG)
+// of the tile's U = BN/64 units, and its row sums cover BN/EPI_WG columns.
+template <int BN, int EPI_WG, class Epi>
 __device__ __forceinline__ void staged_epilogue(const Epi& epi, int l, int row0, int rows,
-                                                int tile_col0, uint32_t tbase, float* stage) {
+                                                int tile_col0, int part, uint32_t tbase,
+                                                float* stage) {
   const int lane = threadIdx.x & 31;
+  constexpr int U = BN / 64, UP = U / EPI_WG, NCOLS = BN / EPI_WG;
   if (epi.direct_tile(tile_col0)) {
-    TmemSrc src{tbase};
-    const int row = row0 + lane;
-    epi.direct(l, row, row < rows, tile_col0, BN, src);
+    // thread-per-row tiles: the first warpgroup does the whole tile
+    if (part == 0) {
+      TmemSrc src{tbase};
+      const int row = row0 + lane;
+      epi.direct(l, row, row < rows, tile_col0, BN, src);
+    }
     return;
   }
   const float ctx = epi.row_ctx(l, row0 + lane, row0 + lane < rows);
   float* rowsum = stage + 32 * 64;
   if (Epi::ROWSUM) rowsum[lane] = 0.f;
 #pragma unroll 1
-  for (int u = 0; u < BN / 64; ++u) {
+  for (int u = part * UP; u < (part + 1) * UP; ++u) {
     int ca, cb;
     epi_unit(epi, u, ca, cb);
     {
@@ -344,7 +351,7 @@ __device__ __forceinline__ void staged_epilogue(const Epi& epi, int l, int row0,
   }
   if (Epi::ROWSUM) {
     const int row = row0 + lane;
-    if (row < rows) epi.finish(l, row, tile_col0, BN, rowsum[lane]);
+    if (row < rows) epi.finish(l, row, tile_col0 + part * NCOLS, NCOLS, rowsum[lane]);
     __syncwarp();
   }
 }

@@ -15,7 +15,7 @@
 //   warp 0      TMA producer: A tile 128 x 64 and B tile BN x 64 per stage,
 //   warp 1      MMA issuer (one thread): 4 x tcgen05.mma (K = 16 each) per
 //               stage into a 128 x BN fp32 accumulator in TMEM,
-//   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows),
+//   warps 2..    epilogue (4 or 8 warps): tcgen05.ld of their 32 TMEM lanes (= tile rows),
 //               staged through shared memory so that the fused epilogue
 //               reads and writes global memory row by row, lanes across
 //               columns (epilogues_staged.cuh).
@@ -45,22 +45,28 @@ struct GemmTcShape {
   int* err;       // device error word
 };
 
-template <int BN>
+// EPI_WG epilogue warpgroups (1 or 2); with 2, each takes half of the tile's
+// columns (for GEMMs whose short K loop leaves the epilogue exposed) and the
+// pipeline keeps one stage less to make room for their shared-memory stages.
+template <int BN, int EPI_WG>
 struct TcCfg {
-  static constexpr int STAGES = BN >= 256 ? 4 : 8;
+  static constexpr int STAGES = BN >= 256 ? (EPI_WG == 2 ? 3 : 4) : 8;
   static constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
   static constexpr uint32_t B_BYTES = BN * TC_BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
-  static constexpr uint32_t EPI_STAGE_BYTES = 4 * STAGED_FLOATS_PER_WARP * 4;  // 4 epilogue warps
+  static constexpr int EPI_WARPS = 4 * EPI_WG;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr uint32_t EPI_STAGE_BYTES = EPI_WARPS * STAGED_FLOATS_PER_WARP * 4;
   static constexpr size_t SMEM = 1024 + STAGES * STAGE_BYTES + 256 + EPI_STAGE_BYTES;
+  static_assert(SMEM <= 232448, "shared memory");
 };
 
-template <class Epi, int BN>
-__global__ void __launch_bounds__(192, 1)
+template <class Epi, int BN, int EPI_WG>
+__global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmTcShape sh, const Epi epi) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, EPI_WG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -80,7 +86,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);  // one arrival per epilogue warp
+      mbar_init(&acc_empty[a], C::EPI_WARPS);  // one arrival per epilogue warp
     }
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -162,8 +168,10 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int ew = warp - 2;       // epilogue warp index
+    const int part = ew / 4;       // column part of the tile this warp handles
     float* stage = reinterpret_cast<float*>(base + C::STAGES * C::STAGE_BYTES + 256) +
-                   quarter * STAGED_FLOATS_PER_WARP;
+                   ew * STAGED_FLOATS_PER_WARP;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
@@ -172,9 +180,9 @@ __global__ void __launch_bounds__(192, 1)
       const bool got = mbar_wait_bounded(&acc_full[acc], acc_phase, sh.err, DEV_TIMEOUT_ACC_FULL);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      staged_epilogue<BN>(epi, sh.g_first + g, mt * TC_BM + quarter * 32, sh.rows, nt * BN,
-                          tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16),
-                          stage);
+      staged_epilogue<BN, EPI_WG>(epi, sh.g_first + g, mt * TC_BM + quarter * 32, sh.rows, nt * BN,
+                                  part, tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16),
+                                  stage);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -199,15 +207,15 @@ __global__ void __launch_bounds__(192, 1)
 bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int K, int rows, int layers,
                          int box_rows);
 
-template <class Epi, int BN>
+template <class Epi, int BN, int EPI_WG = 1>
 cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int rows, int N, int K,
                            int g_first, int g_count, int* err, const Epi& epi, int num_sms,
                            cudaStream_t stream, int row0 = 0, int a_slot_off = 0,
                            int b_slot_off = 0) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, EPI_WG>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<Epi, BN>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<Epi, BN, EPI_WG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
@@ -228,7 +236,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int r
   const int tiles = g_count * sh.m_tiles * sh.n_tiles;
   const int grid = tiles < num_sms ? tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
-  gemm_tc_kernel<Epi, BN><<<grid, 192, C::SMEM, stream>>>(tmA, tmB, sh, epi);
+  gemm_tc_kernel<Epi, BN, EPI_WG><<<grid, C::THREADS, C::SMEM, stream>>>(tmA, tmB, sh, epi);
   return cudaGetLastError();
 }
 

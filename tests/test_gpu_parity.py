@@ -342,4 +342,7 @@ def test_full_attention_baseline_equals_armt_first_segment_up_to_rounding():
     s = stats(ha.cpu().numpy(), hf.cpu().numpy())
     m.close()
     record("full_vs_armt_segment0", **s)
-    assert s["cos"] >= 0.9999 and s["max_abs"] <= 0.05, s
+    # both paths are ~0.045 max-abs from fp64 at 2 layers (bf16 operands, see
+    # the baseline test), and they round the norms at different points, so
+    # they may differ by up to about twice that
+    assert s["cos"] >= 0.9999 and s["max_abs"] <= 0.1, s
