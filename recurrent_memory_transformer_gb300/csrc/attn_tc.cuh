@@ -9,15 +9,17 @@
 //
 // One CTA = (query head, layer, 128-row query tile m); it walks key tiles
 // j = 0..m (causal block skipping):
-//   warp 0      TMA: Q tile once; K_j and V_j tiles (single-buffered each, K_j+1
-//               streams in while P_j V_j runs),
-//   warp 1      MMA issue: S_j = Q K_j^T (M=128, N=128) into TMEM, then
-//               O_j = P_j V_j (M=128, N=hd) into TMEM,
-//   warps 2..5  softmax, one thread per query row (= TMEM lane): two passes
-//               over S_j from TMEM (row max, then exp2 and row sum), P_j
-//               written as bf16 into shared memory in the 128-byte-swizzled
-//               K-major layout the MMA reads, then O_j folded into registers
-//               with the running-max correction.
+//   warp 0      TMA: Q tile once; K_j and V_j tiles (single-buffered each),
+//   warp 1      MMA issue: S_j = Q K_j^T (M=128, N=128) into TMEM buffer j%2,
+//               O_j = P_j V_j (M=128, N=hd) into the first hd columns of the
+//               same buffer once the softmax has read S_j,
+//   warps 2..5  softmax, one thread per query row (= TMEM lane): a max pass
+//               over S_j, then O_{j-1} folded into registers with the
+//               running-max correction (which frees its buffer for S_{j+1}),
+//               then an exp2 pass writing P_j as bf16 into shared memory in
+//               the 128-byte-swizzled K-major layout the MMA reads.
+// With two S buffers the MMA computes S_{j+1} while the softmax works on
+// S_j; 256 TMEM columns per CTA keep two CTAs resident per SM.
 // V comes pre-transposed (Vt[l][g][hd][T], written by the QKV epilogue) so
 // that every MMA operand is K-major.  fp32 accumulation and softmax.
 #pragma once
@@ -34,7 +36,7 @@ struct AttnCfg {
   static constexpr uint32_t K_BYTES = BN * HD * 2;  // HD_ATOMS x [128 keys x 128 B]
   static constexpr uint32_t V_BYTES = HD * BN * 2;  // 2 x [HD rows x 128 B] (keys 0-63, 64-127)
   static constexpr uint32_t P_BYTES = BM * BN * 2;  // 2 x [128 rows x 128 B]
-  static constexpr uint32_t TMEM_COLS = 256;        // S at column 0, O at column 128
+  static constexpr uint32_t TMEM_COLS = 256;        // two 128-column S/O buffers
   static constexpr size_t SMEM = 1024 + Q_BYTES + K_BYTES + V_BYTES + P_BYTES + 256;
   static constexpr int MIN_BLOCKS = HD == 64 ? 2 : 1;
 };
@@ -48,7 +50,11 @@ struct AttnArgs {
   int* err;
 };
 
-enum AttnBar { B_Q = 0, B_KF, B_KE, B_VF, B_VE, B_SF, B_PF, B_OF, B_OE, B_COUNT };
+// S_FULL/O_FULL/BUF_FREE come in pairs, one per TMEM buffer.
+enum AttnBar {
+  B_Q = 0, B_KF, B_KE, B_VF, B_VE, B_PF,
+  B_SF0, B_SF1, B_OF0, B_OF1, B_FREE0, B_FREE1, B_COUNT
+};
 
 template <int HD>
 __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
@@ -78,10 +84,12 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
     mbar_init(&bar[B_KE], 1);
     mbar_init(&bar[B_VF], 1);
     mbar_init(&bar[B_VE], 1);
-    mbar_init(&bar[B_SF], 1);
     mbar_init(&bar[B_PF], 4);
-    mbar_init(&bar[B_OF], 1);
-    mbar_init(&bar[B_OE], 4);
+    for (int bb = 0; bb < 2; ++bb) {
+      mbar_init(&bar[B_SF0 + bb], 1);
+      mbar_init(&bar[B_OF0 + bb], 1);
+      mbar_init(&bar[B_FREE0 + bb], 4);
+    }
     fence_barrier_init();
     fence_proxy_async_smem();
     tma_prefetch_desc(&tmQK);
@@ -91,8 +99,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 128;
+  const uint32_t tmem = *tmem_slot;  // buffer b at columns 128 b .. 128 b + 127
 
   if (warp == 0) {
     if (lane == 0) {
@@ -114,42 +121,43 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128);
       constexpr uint32_t idO = idesc_bf16_f32(128, HD);
-      auto issue_S = [&]() {
+      // S_j = Q K_j^T into buffer j % 2 (K_j must have arrived)
+      auto issue_S = [&](int j) -> bool {
+        if (!mbar_wait_bounded(&bar[B_KF], j & 1, a.err, DEV_TIMEOUT_FULL)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + 128u * (uint32_t)(j & 1);
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
           const int at = ks >> 2, w = ks & 3;
-          tc_mma_bf16(tS, smem_desc_sw128(smem_u32(sQ + at * 16384)) + 2 * w,
+          tc_mma_bf16(d, smem_desc_sw128(smem_u32(sQ + at * 16384)) + 2 * w,
                       smem_desc_sw128(smem_u32(sK + at * 16384)) + 2 * w, idS, ks > 0 ? 1u : 0u);
         }
-        tc_commit(&bar[B_SF]);
+        tc_commit(&bar[B_SF0 + (j & 1)]);
         tc_commit(&bar[B_KE]);
+        return true;
       };
-      bool ok = mbar_wait_bounded(&bar[B_Q], 0, a.err, DEV_TIMEOUT_FULL) &&
-                mbar_wait_bounded(&bar[B_KF], 0, a.err, DEV_TIMEOUT_FULL);
-      if (ok) {
-        tc_fence_after();
-        issue_S();
-      }
+      bool ok = mbar_wait_bounded(&bar[B_Q], 0, a.err, DEV_TIMEOUT_FULL) && issue_S(0) &&
+                (nj < 2 || issue_S(1));
       for (int j = 0; ok && j < nj; ++j) {
+        // P_j written (the softmax has read S_j) and V_j loaded
         ok = mbar_wait_bounded(&bar[B_PF], j & 1, a.err, DEV_TIMEOUT_ACC_FULL) &&
-             mbar_wait_bounded(&bar[B_VF], j & 1, a.err, DEV_TIMEOUT_FULL) &&
-             (j == 0 || mbar_wait_bounded(&bar[B_OE], (j - 1) & 1, a.err, DEV_TIMEOUT_ACC_EMPTY));
+             mbar_wait_bounded(&bar[B_VF], j & 1, a.err, DEV_TIMEOUT_FULL);
         if (!ok) break;
         tc_fence_after();
+        const uint32_t d = tmem + 128u * (uint32_t)(j & 1);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const int at = ks >> 2, w = ks & 3;
-          tc_mma_bf16(tO, smem_desc_sw128(smem_u32(sP + at * 16384)) + 2 * w,
+          tc_mma_bf16(d, smem_desc_sw128(smem_u32(sP + at * 16384)) + 2 * w,
                       smem_desc_sw128(smem_u32(sV + at * (HD * 128))) + 2 * w, idO,
                       ks > 0 ? 1u : 0u);
         }
-        tc_commit(&bar[B_OF]);
+        tc_commit(&bar[B_OF0 + (j & 1)]);
         tc_commit(&bar[B_VE]);
-        if (j + 1 < nj) {
-          ok = mbar_wait_bounded(&bar[B_KF], (j + 1) & 1, a.err, DEV_TIMEOUT_FULL);
-          if (!ok) break;
-          tc_fence_after();
-          issue_S();
+        if (j + 2 < nj) {
+          // buffer j % 2 is reused once the softmax has taken O_j out of it
+          ok = mbar_wait_bounded(&bar[B_FREE0 + (j & 1)], (j >> 1) & 1, a.err, DEV_TIMEOUT_ACC_EMPTY) &&
+               issue_S(j + 2);
         }
       }
     }
@@ -161,12 +169,35 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
     float o[HD];
 #pragma unroll
     for (int i = 0; i < HD; ++i) o[i] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_run = 0.f, corr_prev = 1.f;
     uint8_t* prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
-    for (int j = 0; j < nj; ++j) {
-      const bool got = mbar_wait_bounded(&bar[B_SF], j & 1, a.err, DEV_TIMEOUT_ACC_FULL);
-      if (!__all_sync(0xffffffffu, got)) break;
+    bool ok = true;
+    // o = o * corr + O_t (O_t = P_t V_t, in buffer t % 2), then free the buffer
+    auto fold = [&](int t, float corr) -> bool {
+      const bool got = mbar_wait_bounded(&bar[B_OF0 + (t & 1)], (t >> 1) & 1, a.err, DEV_TIMEOUT_ACC_FULL);
+      if (!__all_sync(0xffffffffu, got)) return false;
       tc_fence_after();
+      const uint32_t tO = tmem + 128u * (uint32_t)(t & 1) + lane_off;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        float ov[32];
+        tmem_ld32(tO + 32 * c, ov);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[32 * c + i] = o[32 * c + i] * corr + ov[i];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_FREE0 + (t & 1)]);
+      return true;
+    };
+    for (int j = 0; j < nj; ++j) {
+      const bool got = mbar_wait_bounded(&bar[B_SF0 + (j & 1)], (j >> 1) & 1, a.err, DEV_TIMEOUT_ACC_FULL);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tS = tmem + 128u * (uint32_t)(j & 1) + lane_off;
       // Only the diagonal tile j == m is masked (key index > query index);
       // keys of earlier tiles are all visible.  lim = last visible key
       // column of this row within the tile.
@@ -176,69 +207,63 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        float s[32];
-        tmem_ld32(tS + lane_off + 32 * c, s);
+        float sv[32];
+        tmem_ld32(tS + 32 * c, sv);
         if (diag) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = (32 * c + i <= lim) ? fmaxf(mx, s[i]) : mx;
+          for (int i = 0; i < 32; ++i) mx = (32 * c + i <= lim) ? fmaxf(mx, sv[i]) : mx;
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, s[i]);
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, sv[i]);
         }
       }
       const float m_new = fmaxf(m_run, mx * a.scale_log2);
       const float corr = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      // O_{j-1} (relative to the previous max) joins the running output; its
+      // P.V has finished, so P may be overwritten below
+      if (j > 0 && !fold(j - 1, corr_prev)) {
+        ok = false;
+        break;
+      }
       // pass 2: p = 2^(s * scale - m), row sum, bf16 P into shared memory
       float rs = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        float s[32];
-        tmem_ld32(tS + lane_off + 32 * c, s);
+        float sv[32];
+        tmem_ld32(tS + 32 * c, sv);
         if (diag) {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            s[i] = (32 * c + i <= lim) ? fast_exp2(fmaf(s[i], a.scale_log2, -m_use)) : 0.f;
+            sv[i] = (32 * c + i <= lim) ? fast_exp2(fmaf(sv[i], a.scale_log2, -m_use)) : 0.f;
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[i] = fast_exp2(fmaf(s[i], a.scale_log2, -m_use));
+          for (int i = 0; i < 32; ++i) sv[i] = fast_exp2(fmaf(sv[i], a.scale_log2, -m_use));
         }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) rs += s[i];
+        for (int i = 0; i < 32; ++i) rs += sv[i];
         uint8_t* atom = prow + (c >> 1) * 16384;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const int chunk = 4 * (c & 1) + v;  // 16-byte chunk within the 128-byte row
           uint4 pk;
-          pk.x = pack_bf16x2(s[8 * v + 0], s[8 * v + 1]);
-          pk.y = pack_bf16x2(s[8 * v + 2], s[8 * v + 3]);
-          pk.z = pack_bf16x2(s[8 * v + 4], s[8 * v + 5]);
-          pk.w = pack_bf16x2(s[8 * v + 6], s[8 * v + 7]);
+          pk.x = pack_bf16x2(sv[8 * v + 0], sv[8 * v + 1]);
+          pk.y = pack_bf16x2(sv[8 * v + 2], sv[8 * v + 3]);
+          pk.z = pack_bf16x2(sv[8 * v + 4], sv[8 * v + 5]);
+          pk.w = pack_bf16x2(sv[8 * v + 6], sv[8 * v + 7]);
           *reinterpret_cast<uint4*>(atom + ((chunk ^ (r & 7)) << 4)) = pk;
         }
       }
       l_run = l_run * corr + rs;
       m_run = m_new;
+      corr_prev = corr;
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[B_PF]);
-      // fold O_j = P_j V_j into the running output
-      const bool got2 = mbar_wait_bounded(&bar[B_OF], j & 1, a.err, DEV_TIMEOUT_ACC_FULL);
-      if (!__all_sync(0xffffffffu, got2)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        float ov[32];
-        tmem_ld32(tO + lane_off + 32 * c, ov);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[32 * c + i] = o[32 * c + i] * corr + ov[i];
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_OE]);
     }
-    if (qi < a.T) {
+    if (ok) ok = fold(nj - 1, corr_prev);
+    if (ok && qi < a.T) {
       const float inv = 1.0f / l_run;
       bf16* dst = a.out + ((long long)l * a.T + qi) * (a.Hq * HD) + h * HD;
 #pragma unroll
