@@ -244,6 +244,13 @@ def main():
     gu_launches, gu_ms = kt["gemm_gateup"]
     gu_tflops = fl["gemm_gateup"] * cells / (gu_ms / 1000.0) / 1e12 if gu_ms > 0 else None
     peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    # DRAM bytes of the gate-up GEMM per cell from one ncu capture of an 8-cell
+    # launch (profiles/gemm_gateup_armt1b_8k.md): traffic scales with cells
+    # (each cell's layer weights + activations), so per launch it is this
+    # times the launch's cells.
+    GATEUP_DRAM_BYTES_PER_CELL_1B = 86.4e6
+    gu_traffic = (GATEUP_DRAM_BYTES_PER_CELL_1B * cells / gu_launches
+                  if (gu_launches and args.workload.startswith("armt-1b")) else None)
     gemm_keys = ("gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down")
     gemm_ms = sum(kt[k][1] for k in gemm_keys)
     gemm_tflops = sum(fl[k] for k in gemm_keys) * cells / (gemm_ms / 1000.0) / 1e12 if gemm_ms else None
@@ -318,7 +325,8 @@ def main():
                              "~1 GB of activations, far above the 129 MB L2"},
             "roofline": {"bound": "tensor", "kernel": "grouped GEMM gate-up + SwiGLU (tcgen05)",
                          "achieved": gu_tflops, "peak": peak, "unit": "TFLOP/s",
-                         "frac": (gu_tflops / peak) if gu_tflops else None, "traffic": None,
+                         "frac": (gu_tflops / peak) if gu_tflops else None, "traffic": gu_traffic,
+                         "traffic_unit": "bytes per launch (ncu dram__bytes_read+write, scaled by cells)",
                          "peak_source": f"bf16_tflops_sustained ({peak_src})",
                          "all_gemms_tflops": gemm_tflops,
                          "all_gemms_frac": (gemm_tflops / peak) if gemm_tflops else None},

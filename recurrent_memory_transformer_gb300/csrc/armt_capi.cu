@@ -497,9 +497,9 @@ struct Model : ModelBase {
       aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
       aa.err = d_err;
       if (hd == 64)
-        CK(launch_attn_tc<64>(tmQK, tmVt, aa, g, st));
+        CK(launch_attn_tc<64>(tmQK, tmVt, aa, g, num_sms, st));
       else
-        CK(launch_attn_tc<128>(tmQK, tmVt, aa, g, st));
+        CK(launch_attn_tc<128>(tmQK, tmVt, aa, g, num_sms, st));
     } else {
       dim3 grid((T + 63) / 64, Hq, g);
       const float scale = 1.0f / sqrtf((float)hd);
@@ -646,9 +646,9 @@ struct Model : ModelBase {
           aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
           aa.err = d_err;
           if (hd == 64)
-            CK(launch_attn_tc<64>(tmQKf, tmVtf, aa, 1, st));
+            CK(launch_attn_tc<64>(tmQKf, tmVtf, aa, 1, num_sms, st));
           else
-            CK(launch_attn_tc<128>(tmQKf, tmVtf, aa, 1, st));
+            CK(launch_attn_tc<128>(tmQKf, tmVtf, aa, 1, num_sms, st));
         }
         CKS(prof_end(st));
         CKS(prof_begin(ARMT_KC_GEMM_O, st));
@@ -958,9 +958,9 @@ armt_status armt_segment_attention_bf16(const void* qk, const void* vt, void* ou
   aa.err = err;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (hd == 64)
-    CK(launch_attn_tc<64>(tq, tv, aa, G, st));
+    CK(launch_attn_tc<64>(tq, tv, aa, G, g_num_sms(dev), st));
   else
-    CK(launch_attn_tc<128>(tq, tv, aa, G, st));
+    CK(launch_attn_tc<128>(tq, tv, aa, G, g_num_sms(dev), st));
   return ARMT_OK;
 }
 

@@ -7,8 +7,9 @@
 // 0..T-1 (segment tokens, then memory tokens) attend causally to rows <= their
 // own; query head h reads kv head h / (Hq / Hkv).
 //
-// One CTA = (query head, layer, 128-row query tile m); it walks key tiles
-// j = 0..m (causal block skipping):
+// Persistent CTAs (two per SM) take work items (query head, layer, 128-row
+// query tile m) round-robin, heaviest tiles first; per item a CTA walks key
+// tiles j = 0..m (causal block skipping):
 //   warp 0      TMA: Q tile once; K_j and V_j tiles (single-buffered each),
 //   warp 1      MMA issue: S_j = Q K_j^T (M=128, N=128) into TMEM buffer j%2,
 //               O_j = P_j V_j (M=128, N=hd) into the first hd columns of the
@@ -19,7 +20,10 @@
 //               then an exp2 pass writing P_j as bf16 into shared memory in
 //               the 128-byte-swizzled K-major layout the MMA reads.
 // With two S buffers the MMA computes S_{j+1} while the softmax works on
-// S_j; 256 TMEM columns per CTA keep two CTAs resident per SM.
+// S_j; 256 TMEM columns per CTA keep two CTAs resident per SM.  TMEM and the
+// barriers are set up once per CTA; a running tile count c (across items)
+// gives every barrier's phase: per-tile barriers complete once per tile,
+// buffer c % 2 holds tile c, and its barriers complete once every 2 tiles.
 // V comes pre-transposed (Vt[l][g][hd][T], written by the QKV epilogue) so
 // that every MMA operand is K-major.  fp32 accumulation and softmax.
 #pragma once
@@ -44,11 +48,26 @@ struct AttnCfg {
 struct AttnArgs {
   bf16* out;        // [L][T][Hq*HD]
   int T, Hq, Hkv;
-  int g_first;
+  int g_first, g_count;
   int n_qtiles;
   float scale_log2;  // log2(e) / sqrt(HD)
   int* err;
 };
+
+// Work item i (heaviest query tiles first): m = n_qtiles - 1 - i / (Hq * G),
+// then cell, then head.
+struct AttnItem {
+  int h, l, m;
+};
+__device__ __forceinline__ AttnItem attn_item(const AttnArgs& a, int i) {
+  const int per_m = a.Hq * a.g_count;
+  const int mi = i / per_m, rem = i - mi * per_m;
+  AttnItem it;
+  it.m = a.n_qtiles - 1 - mi;
+  it.l = a.g_first + rem / a.Hq;
+  it.h = rem % a.Hq;
+  return it;
+}
 
 // S_FULL/O_FULL/BUF_FREE come in pairs, one per TMEM buffer.
 enum AttnBar {
@@ -71,11 +90,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
   uint64_t* bar = reinterpret_cast<uint64_t*>(sP + C::P_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + B_COUNT);
 
-  const int h = blockIdx.x;
-  const int l = a.g_first + blockIdx.y;
-  const int m = a.n_qtiles - 1 - (int)blockIdx.z;  // heavy tiles first
-  const int g = h / (a.Hq / a.Hkv);
-  const int nj = m + 1;
+  const int n_items = a.Hq * a.g_count * a.n_qtiles;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (warp == 0 && lane == 0) {
@@ -103,75 +118,92 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(&bar[B_Q], C::Q_BYTES);
-      for (int at = 0; at < C::HD_ATOMS; ++at)
-        tma_load_3d(sQ + at * 16384, &tmQK, h * HD + 64 * at, m * 128, l, &bar[B_Q]);
-      for (int j = 0; j < nj; ++j) {
-        if (j > 0 && !mbar_wait_bounded(&bar[B_KE], (j - 1) & 1, a.err, DEV_TIMEOUT_EMPTY)) break;
-        mbar_arrive_expect_tx(&bar[B_KF], C::K_BYTES);
+      int c = 0;  // running tile count
+      bool ok = true;
+      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+        const AttnItem it = attn_item(a, i);
+        const int g = it.h / (a.Hq / a.Hkv);
+        // Q is reused once every S of the previous item has run
+        if (c > 0 && !mbar_wait_bounded(&bar[B_KE], (c - 1) & 1, a.err, DEV_TIMEOUT_EMPTY)) break;
+        mbar_arrive_expect_tx(&bar[B_Q], C::Q_BYTES);
         for (int at = 0; at < C::HD_ATOMS; ++at)
-          tma_load_3d(sK + at * 16384, &tmQK, (a.Hq + g) * HD + 64 * at, j * 128, l, &bar[B_KF]);
-        if (j > 0 && !mbar_wait_bounded(&bar[B_VE], (j - 1) & 1, a.err, DEV_TIMEOUT_EMPTY)) break;
-        mbar_arrive_expect_tx(&bar[B_VF], C::V_BYTES);
-        for (int at = 0; at < 2; ++at)
-          tma_load_3d(sV + at * (HD * 128), &tmV, j * 128 + 64 * at, 0, l * a.Hkv + g, &bar[B_VF]);
+          tma_load_3d(sQ + at * 16384, &tmQK, it.h * HD + 64 * at, it.m * 128, it.l, &bar[B_Q]);
+        for (int j = 0; j <= it.m; ++j, ++c) {
+          if (j > 0 && !mbar_wait_bounded(&bar[B_KE], (c - 1) & 1, a.err, DEV_TIMEOUT_EMPTY)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bar[B_KF], C::K_BYTES);
+          for (int at = 0; at < C::HD_ATOMS; ++at)
+            tma_load_3d(sK + at * 16384, &tmQK, (a.Hq + g) * HD + 64 * at, j * 128, it.l, &bar[B_KF]);
+          if (c > 0 && !mbar_wait_bounded(&bar[B_VE], (c - 1) & 1, a.err, DEV_TIMEOUT_EMPTY)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bar[B_VF], C::V_BYTES);
+          for (int at = 0; at < 2; ++at)
+            tma_load_3d(sV + at * (HD * 128), &tmV, j * 128 + 64 * at, 0, it.l * a.Hkv + g, &bar[B_VF]);
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128);
       constexpr uint32_t idO = idesc_bf16_f32(128, HD);
-      // S_j = Q K_j^T into buffer j % 2 (K_j must have arrived)
-      auto issue_S = [&](int j) -> bool {
-        if (!mbar_wait_bounded(&bar[B_KF], j & 1, a.err, DEV_TIMEOUT_FULL)) return false;
+      // S for running tile cc = Q K^T into buffer cc % 2, once the buffer's
+      // previous tile (cc - 2) has been folded by the softmax and K arrived
+      auto issue_S = [&](int cc) -> bool {
+        if (cc >= 2 && !mbar_wait_bounded(&bar[B_FREE0 + (cc & 1)], ((cc - 2) >> 1) & 1, a.err,
+                                          DEV_TIMEOUT_ACC_EMPTY))
+          return false;
+        if (!mbar_wait_bounded(&bar[B_KF], cc & 1, a.err, DEV_TIMEOUT_FULL)) return false;
         tc_fence_after();
-        const uint32_t d = tmem + 128u * (uint32_t)(j & 1);
+        const uint32_t d = tmem + 128u * (uint32_t)(cc & 1);
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
           const int at = ks >> 2, w = ks & 3;
           tc_mma_bf16(d, smem_desc_sw128(smem_u32(sQ + at * 16384)) + 2 * w,
                       smem_desc_sw128(smem_u32(sK + at * 16384)) + 2 * w, idS, ks > 0 ? 1u : 0u);
         }
-        tc_commit(&bar[B_SF0 + (j & 1)]);
+        tc_commit(&bar[B_SF0 + (cc & 1)]);
         tc_commit(&bar[B_KE]);
         return true;
       };
-      bool ok = mbar_wait_bounded(&bar[B_Q], 0, a.err, DEV_TIMEOUT_FULL) && issue_S(0) &&
-                (nj < 2 || issue_S(1));
-      for (int j = 0; ok && j < nj; ++j) {
-        // P_j written (the softmax has read S_j) and V_j loaded
-        ok = mbar_wait_bounded(&bar[B_PF], j & 1, a.err, DEV_TIMEOUT_ACC_FULL) &&
-             mbar_wait_bounded(&bar[B_VF], j & 1, a.err, DEV_TIMEOUT_FULL);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t d = tmem + 128u * (uint32_t)(j & 1);
+      int c = 0, k = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
+        const AttnItem it = attn_item(a, i);
+        const int nj = it.m + 1;
+        ok = mbar_wait_bounded(&bar[B_Q], k & 1, a.err, DEV_TIMEOUT_FULL) && issue_S(c) &&
+             (nj < 2 || issue_S(c + 1));
+        for (int j = 0; ok && j < nj; ++j) {
+          const int cj = c + j;
+          // P written (the softmax has read S) and V arrived
+          ok = mbar_wait_bounded(&bar[B_PF], cj & 1, a.err, DEV_TIMEOUT_ACC_FULL) &&
+               mbar_wait_bounded(&bar[B_VF], cj & 1, a.err, DEV_TIMEOUT_FULL);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d = tmem + 128u * (uint32_t)(cj & 1);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const int at = ks >> 2, w = ks & 3;
-          tc_mma_bf16(d, smem_desc_sw128(smem_u32(sP + at * 16384)) + 2 * w,
-                      smem_desc_sw128(smem_u32(sV + at * (HD * 128))) + 2 * w, idO,
-                      ks > 0 ? 1u : 0u);
+          for (int ks = 0; ks < 8; ++ks) {
+            const int at = ks >> 2, w = ks & 3;
+            tc_mma_bf16(d, smem_desc_sw128(smem_u32(sP + at * 16384)) + 2 * w,
+                        smem_desc_sw128(smem_u32(sV + at * (HD * 128))) + 2 * w, idO,
+                        ks > 0 ? 1u : 0u);
+          }
+          tc_commit(&bar[B_OF0 + (cj & 1)]);
+          tc_commit(&bar[B_VE]);
+          if (j + 2 < nj) ok = issue_S(cj + 2);
         }
-        tc_commit(&bar[B_OF0 + (j & 1)]);
-        tc_commit(&bar[B_VE]);
-        if (j + 2 < nj) {
-          // buffer j % 2 is reused once the softmax has taken O_j out of it
-          ok = mbar_wait_bounded(&bar[B_FREE0 + (j & 1)], (j >> 1) & 1, a.err, DEV_TIMEOUT_ACC_EMPTY) &&
-               issue_S(j + 2);
-        }
+        c += nj;
       }
     }
   } else {
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;            // row within the tile = TMEM lane
-    const int qi = m * 128 + r;                   // query index within the cell
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    float o[HD];
-#pragma unroll
-    for (int i = 0; i < HD; ++i) o[i] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f, corr_prev = 1.f;
     uint8_t* prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
-    bool ok = true;
+    float o[HD];
     // o = o * corr + O_t (O_t = P_t V_t, in buffer t % 2), then free the buffer
     auto fold = [&](int t, float corr) -> bool {
       const bool got = mbar_wait_bounded(&bar[B_OF0 + (t & 1)], (t >> 1) & 1, a.err, DEV_TIMEOUT_ACC_FULL);
@@ -179,102 +211,114 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
       tc_fence_after();
       const uint32_t tO = tmem + 128u * (uint32_t)(t & 1) + lane_off;
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int cc = 0; cc < HD / 32; ++cc) {
         float ov[32];
-        tmem_ld32(tO + 32 * c, ov);
+        tmem_ld32(tO + 32 * cc, ov);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[32 * c + i] = o[32 * c + i] * corr + ov[i];
+        for (int i = 0; i < 32; ++i) o[32 * cc + i] = o[32 * cc + i] * corr + ov[i];
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[B_FREE0 + (t & 1)]);
       return true;
     };
-    for (int j = 0; j < nj; ++j) {
-      const bool got = mbar_wait_bounded(&bar[B_SF0 + (j & 1)], (j >> 1) & 1, a.err, DEV_TIMEOUT_ACC_FULL);
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t tS = tmem + 128u * (uint32_t)(j & 1) + lane_off;
-      // Only the diagonal tile j == m is masked (key index > query index);
-      // keys of earlier tiles are all visible.  lim = last visible key
-      // column of this row within the tile.
-      const bool diag = (j == m);
-      const int lim = qi - j * 128;
-      // pass 1: row max of the raw scores (the scale is positive)
-      float mx = -INFINITY;
+    int c = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      const AttnItem it = attn_item(a, item);
+      const int m = it.m, nj = m + 1;
+      const int qi = m * 128 + r;                 // query index within the cell
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float sv[32];
-        tmem_ld32(tS + 32 * c, sv);
-        if (diag) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) mx = (32 * c + i <= lim) ? fmaxf(mx, sv[i]) : mx;
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, sv[i]);
+      for (int i = 0; i < HD; ++i) o[i] = 0.f;
+      float m_run = -INFINITY, l_run = 0.f, corr_prev = 1.f;
+      for (int j = 0; j < nj; ++j) {
+        const int cj = c + j;
+        const bool got = mbar_wait_bounded(&bar[B_SF0 + (cj & 1)], (cj >> 1) & 1, a.err, DEV_TIMEOUT_ACC_FULL);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
         }
-      }
-      const float m_new = fmaxf(m_run, mx * a.scale_log2);
-      const float corr = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      // O_{j-1} (relative to the previous max) joins the running output; its
-      // P.V has finished, so P may be overwritten below
-      if (j > 0 && !fold(j - 1, corr_prev)) {
-        ok = false;
-        break;
-      }
-      // pass 2: p = 2^(s * scale - m), row sum, bf16 P into shared memory
-      float rs = 0.f;
+        tc_fence_after();
+        const uint32_t tS = tmem + 128u * (uint32_t)(cj & 1) + lane_off;
+        // Only the diagonal tile j == m is masked (key index > query index);
+        // keys of earlier tiles are all visible.  lim = last visible key
+        // column of this row within the tile.
+        const bool diag = (j == m);
+        const int lim = qi - j * 128;
+        // pass 1: row max of the raw scores (the scale is positive)
+        float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float sv[32];
-        tmem_ld32(tS + 32 * c, sv);
-        if (diag) {
+        for (int cc = 0; cc < 4; ++cc) {
+          float sv[32];
+          tmem_ld32(tS + 32 * cc, sv);
+          if (diag) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            sv[i] = (32 * c + i <= lim) ? fast_exp2(fmaf(sv[i], a.scale_log2, -m_use)) : 0.f;
-        } else {
+            for (int i = 0; i < 32; ++i) mx = (32 * cc + i <= lim) ? fmaxf(mx, sv[i]) : mx;
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sv[i] = fast_exp2(fmaf(sv[i], a.scale_log2, -m_use));
+            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, sv[i]);
+          }
         }
+        const float m_new = fmaxf(m_run, mx * a.scale_log2);
+        const float corr = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        // O of the previous tile (relative to the previous max) joins the
+        // running output; its P.V has finished, so P may be overwritten below
+        if (j > 0 && !fold(cj - 1, corr_prev)) {
+          ok = false;
+          break;
+        }
+        // pass 2: p = 2^(s * scale - m), row sum, bf16 P into shared memory
+        float rs = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) rs += sv[i];
-        uint8_t* atom = prow + (c >> 1) * 16384;
+        for (int cc = 0; cc < 4; ++cc) {
+          float sv[32];
+          tmem_ld32(tS + 32 * cc, sv);
+          if (diag) {
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int chunk = 4 * (c & 1) + v;  // 16-byte chunk within the 128-byte row
+            for (int i = 0; i < 32; ++i)
+              sv[i] = (32 * cc + i <= lim) ? fast_exp2(fmaf(sv[i], a.scale_log2, -m_use)) : 0.f;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sv[i] = fast_exp2(fmaf(sv[i], a.scale_log2, -m_use));
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rs += sv[i];
+          uint8_t* atom = prow + (cc >> 1) * 16384;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int chunk = 4 * (cc & 1) + v;  // 16-byte chunk within the 128-byte row
+            uint4 pk;
+            pk.x = pack_bf16x2(sv[8 * v + 0], sv[8 * v + 1]);
+            pk.y = pack_bf16x2(sv[8 * v + 2], sv[8 * v + 3]);
+            pk.z = pack_bf16x2(sv[8 * v + 4], sv[8 * v + 5]);
+            pk.w = pack_bf16x2(sv[8 * v + 6], sv[8 * v + 7]);
+            *reinterpret_cast<uint4*>(atom + ((chunk ^ (r & 7)) << 4)) = pk;
+          }
+        }
+        l_run = l_run * corr + rs;
+        m_run = m_new;
+        corr_prev = corr;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[B_PF]);
+      }
+      if (ok) ok = fold(c + nj - 1, corr_prev);
+      if (ok && qi < a.T) {
+        const float inv = 1.0f / l_run;
+        bf16* dst = a.out + ((long long)it.l * a.T + qi) * (a.Hq * HD) + it.h * HD;
+#pragma unroll
+        for (int cc = 0; cc < HD; cc += 8) {
           uint4 pk;
-          pk.x = pack_bf16x2(sv[8 * v + 0], sv[8 * v + 1]);
-          pk.y = pack_bf16x2(sv[8 * v + 2], sv[8 * v + 3]);
-          pk.z = pack_bf16x2(sv[8 * v + 4], sv[8 * v + 5]);
-          pk.w = pack_bf16x2(sv[8 * v + 6], sv[8 * v + 7]);
-          *reinterpret_cast<uint4*>(atom + ((chunk ^ (r & 7)) << 4)) = pk;
+          pk.x = pack_bf16x2(o[cc + 0] * inv, o[cc + 1] * inv);
+          pk.y = pack_bf16x2(o[cc + 2] * inv, o[cc + 3] * inv);
+          pk.z = pack_bf16x2(o[cc + 4] * inv, o[cc + 5] * inv);
+          pk.w = pack_bf16x2(o[cc + 6] * inv, o[cc + 7] * inv);
+          *reinterpret_cast<uint4*>(dst + cc) = pk;
         }
       }
-      l_run = l_run * corr + rs;
-      m_run = m_new;
-      corr_prev = corr;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_PF]);
-    }
-    if (ok) ok = fold(nj - 1, corr_prev);
-    if (ok && qi < a.T) {
-      const float inv = 1.0f / l_run;
-      bf16* dst = a.out + ((long long)l * a.T + qi) * (a.Hq * HD) + h * HD;
-#pragma unroll
-      for (int c = 0; c < HD; c += 8) {
-        uint4 pk;
-        pk.x = pack_bf16x2(o[c + 0] * inv, o[c + 1] * inv);
-        pk.y = pack_bf16x2(o[c + 2] * inv, o[c + 3] * inv);
-        pk.z = pack_bf16x2(o[c + 4] * inv, o[c + 5] * inv);
-        pk.w = pack_bf16x2(o[c + 6] * inv, o[c + 7] * inv);
-        *reinterpret_cast<uint4*>(dst + c) = pk;
-      }
+      c += nj;
     }
   }
   tc_fence_before();
@@ -287,7 +331,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
 
 template <int HD>
 cudaError_t launch_attn_tc(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnArgs& a,
-                           int g_count, cudaStream_t stream) {
+                           int g_count, int num_sms, cudaStream_t stream) {
   using C = AttnCfg<HD>;
   static bool configured = false;
   if (!configured) {
@@ -296,8 +340,11 @@ cudaError_t launch_attn_tc(const CUtensorMap& tmQK, const CUtensorMap& tmV, cons
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(a.Hq, g_count, a.n_qtiles);
-  attn_tc_kernel<HD><<<grid, 192, C::SMEM, stream>>>(tmQK, tmV, a);
+  AttnArgs aa = a;
+  aa.g_count = g_count;
+  const int n_items = a.Hq * g_count * a.n_qtiles;
+  const int grid = n_items < C::MIN_BLOCKS * num_sms ? n_items : C::MIN_BLOCKS * num_sms;
+  attn_tc_kernel<HD><<<grid, 192, C::SMEM, stream>>>(tmQK, tmV, aa);
   return cudaGetLastError();
 }
 

@@ -122,7 +122,12 @@ extern "C" ARMT_API armt_status armt_segment_attention_bf16_noalloc(const void* 
   aa.n_qtiles = (T + 127) / 128;
   aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
   aa.err = err;
-  e = hd == 64 ? launch_attn_tc<64>(tq, tv, aa, G, st) : launch_attn_tc<128>(tq, tv, aa, G, st);
+  int nsm = 0;
+  if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0) {
+    cudaGetLastError();
+    nsm = 148;
+  }
+  e = hd == 64 ? launch_attn_tc<64>(tq, tv, aa, G, nsm, st) : launch_attn_tc<128>(tq, tv, aa, G, nsm, st);
   if (e != cudaSuccess) return nfail(ARMT_ERR_CUDA, std::string("attention: ") + cudaGetErrorString(e));
   return ARMT_OK;
 }
