@@ -204,18 +204,25 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     uint8_t* prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
     float o[HD];
+    // A warp whose 32 rows all lie at or past T (the short last query tile)
+    // keeps the barrier protocol -- the same waits and arrivals in the same
+    // order, so no arrival can run ahead into another tile's phase -- but
+    // reads no TMEM and writes no P.  Its rows of P and O are never stored.
+    bool idle = false;
     // o = o * corr + O_t (O_t = P_t V_t, in buffer t % 2), then free the buffer
     auto fold = [&](int t, float corr) -> bool {
       const bool got = mbar_wait_bounded(&bar[B_OF0 + (t & 1)], (t >> 1) & 1, a.err, DEV_TIMEOUT_ACC_FULL);
       if (!__all_sync(0xffffffffu, got)) return false;
       tc_fence_after();
-      const uint32_t tO = tmem + 128u * (uint32_t)(t & 1) + lane_off;
+      if (!idle) {
+        const uint32_t tO = tmem + 128u * (uint32_t)(t & 1) + lane_off;
 #pragma unroll
-      for (int cc = 0; cc < HD / 32; ++cc) {
-        float ov[32];
-        tmem_ld32(tO + 32 * cc, ov);
+        for (int cc = 0; cc < HD / 32; ++cc) {
+          float ov[32];
+          tmem_ld32(tO + 32 * cc, ov);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[32 * cc + i] = o[32 * cc + i] * corr + ov[i];
+          for (int i = 0; i < 32; ++i) o[32 * cc + i] = o[32 * cc + i] * corr + ov[i];
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -228,6 +235,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
       const AttnItem it = attn_item(a, item);
       const int m = it.m, nj = m + 1;
       const int qi = m * 128 + r;                 // query index within the cell
+      idle = m * 128 + quarter * 32 >= a.T;
 #pragma unroll
       for (int i = 0; i < HD; ++i) o[i] = 0.f;
       float m_run = -INFINITY, l_run = 0.f, corr_prev = 1.f;
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
         // pass 1: row max of the raw scores (the scale is positive)
         float mx = -INFINITY;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 4 && !idle; ++cc) {
           float sv[32];
           tmem_ld32(tS + 32 * cc, sv);
           if (diag) {
@@ -271,7 +279,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
         // pass 2: p = 2^(s * scale - m), row sum, bf16 P into shared memory
         float rs = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 4 && !idle; ++cc) {
           float sv[32];
           tmem_ld32(tS + 32 * cc, sv);
           if (diag) {
