@@ -14,6 +14,7 @@ Under torchrun each rank runs an independent replica (weak scaling); the
 path has no exchange step, so there is no collective in the data path.
 """
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -27,6 +28,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "tokens/sec ARMT-1B @131072 tok (1 GB300)"
 UNIT = "tokens/s"
+
+
+def metric_name(workload):
+    return METRIC if workload == "armt-1b-131k" else f"tokens/sec {workload} (1 GB300)"
 
 
 def parse():
@@ -151,18 +156,26 @@ def run_reference(args, rank):
     if rank != 0:
         return
     cfg, n_seg, seed = I.WORKLOADS[args.workload]
-    W = I.make_weights(cfg, seed)
+    # 3B/8B: one layer of the same shape, timed and scaled by the layer count
+    # (every layer costs the same), so that a step stays within seconds
+    big = args.workload in I.DEVICE_WEIGHT_WORKLOADS
+    cfg_s = dataclasses.replace(cfg, n_layers=1) if big else cfg
+    scale = cfg.n_layers if big else 1
+    W = I.make_weights(cfg_s, seed)
     tok = I.make_tokens(cfg, n_seg, seed)
     for _ in range(args.warmup):
-        oracle_sample_seconds(cfg, W, tok)
-    ts = [oracle_sample_seconds(cfg, W, tok) for _ in range(args.steps)]
+        oracle_sample_seconds(cfg_s, W, tok)
+    ts = [oracle_sample_seconds(cfg_s, W, tok) * scale for _ in range(args.steps)]
     tok_per_step = cfg.seg_len
     value = tok_per_step * len(ts) / sum(ts)
     cores = os.cpu_count()
     sample = (f"fp64 oracle, segment 0 ({cfg.seg_len} tokens) through all {cfg.n_layers} layers per step; "
               "per-segment cost is constant in the segment recurrence")
+    if big:
+        sample = (f"fp64 oracle, segment 0 ({cfg.seg_len} tokens) through one layer of this shape, "
+                  f"x {cfg.n_layers} layers per step; per-segment cost is constant in the recurrence")
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric_name(args.workload), "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * sum(ts) / len(ts),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": args.workload, "tokens": n_seg * cfg.seg_len},
@@ -197,9 +210,14 @@ def main():
     B.load_library()
 
     cfg, n_seg, seed = I.WORKLOADS[args.workload]
-    W = I.make_weights(cfg, seed)
     tok_np = I.make_tokens(cfg, n_seg, seed)
-    model = B.Model(cfg, B.device_weight_tensors(cfg, W))
+    if args.workload in I.DEVICE_WEIGHT_WORKLOADS:
+        W = None   # drawn on the GPU; the oracle baseline needs host weights
+        model = B.Model(cfg, I.make_weights_device(cfg, seed))
+    else:
+        W = I.make_weights(cfg, seed)
+        model = B.Model(cfg, B.device_weight_tensors(cfg, W))
+    torch.cuda.empty_cache()   # the caller's weight copies are no longer needed
     tokens = torch.from_numpy(tok_np).cuda()
     n_tok = n_seg * cfg.seg_len
     hidden = torch.empty((n_tok, cfg.d_model), dtype=torch.float32, device="cuda")
@@ -273,6 +291,30 @@ def main():
         seq = {"ms_per_step": seq_ms, "tokens_per_s": n_tok / (seq_ms / 1000.0),
                "speedup_diag_over_seq": seq_ms / ms_step}
 
+    # ---- ideal-uniform-load bound ---------------------------------------
+    # Both runs share the same ramp-up and ramp-down diagonals, so the time
+    # difference between n and n/2 segments is n/2 full diagonals (every
+    # layer busy).  A full diagonal advances one segment through the whole
+    # model, so S / t_full is the throughput with no ramp at all.
+    uniform = None
+    if n_seg // 2 >= cfg.n_layers:
+        h2 = n_seg // 2
+        step_half = lambda: model.armt_forward(tokens[:h2 * cfg.seg_len], h2, hidden, A, z, 0, stream,
+                                               B.SCHEDULE_DIAGONAL)
+        step_half()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step_half()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        half_ms = e0.elapsed_time(e1)
+        t_full = (ms_step - half_ms) / (n_seg - h2)
+        uniform = {"ms_per_full_diagonal": t_full,
+                   "tokens_per_s": cfg.seg_len / (t_full / 1000.0) if t_full > 0 else None,
+                   "ramp_overhead_frac": 1.0 - n_seg * t_full / ms_step,
+                   "method": f"(t({n_seg} segments) - t({h2})) / {n_seg - h2} full diagonals"}
+
     # ---- full-causal-attention LLaMA on the same weights (no memory) -----
     full = None
     if not args.no_full and cfg.dtype == "bf16":
@@ -306,16 +348,28 @@ def main():
 
     # ---- oracle on the host cores (rank 0, N=1 only) ---------------------
     cpu = None
-    if not args.no_cpu and rank == 0 and world == 1:
+    if not args.no_cpu and rank == 0 and world == 1 and W is not None:
         t = oracle_sample_seconds(cfg, W, tok_np)
         cpu = {"value": cfg.seg_len / t, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"fp64 oracle, segment 0 ({cfg.seg_len} tokens) through all {cfg.n_layers} "
                          f"layers ({t:.1f} s); per-segment cost is constant in the segment recurrence"}
 
+    # ---- device memory: recurrent state vs a full-attention KV cache -----
+    w_bytes, ws_bytes, fw_bytes = model.armt_memory_bytes()
+    state_bytes = (model.a_elems + model.z_elems) * 4
+    kv_bytes = 2 * cfg.n_layers * n_tok * cfg.n_kv_heads * cfg.head_dim * 2
+    memory = {"weights_bytes": w_bytes, "armt_workspace_bytes": ws_bytes,
+              "armt_state_bytes": state_bytes, "full_attention_workspace_bytes": fw_bytes or None,
+              "kv_cache_bytes_full_llama": kv_bytes,
+              "kv_cache_over_armt_state": kv_bytes / state_bytes,
+              "note": "ARMT workspace is fixed at create (one activation slot per layer) and its "
+                      "state is O(L d P) whatever the length; a full-attention model holds a bf16 "
+                      "KV cache of 2 L T Hkv hd entries at context T"}
+
     launches = model.armt_launch_count(n_seg, B.SCHEDULE_DIAGONAL) * args.steps
     if rank == 0:
         out = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "metric": metric_name(args.workload), "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
             "config": {"workload": args.workload, "tokens": n_tok, "segments": n_seg,
@@ -333,7 +387,9 @@ def main():
             "model_tflops": total_flops * args.steps / (ms_total / 1000.0) / 1e12,
             "kernels": per_class,
             "sequential": seq,
+            "uniform_bound": uniform,
             "full_attention": full,
+            "memory": memory,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": int(launches),

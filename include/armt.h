@@ -242,6 +242,21 @@ ARMT_API armt_status armt_segment_attention_bf16_noalloc(const void* qkv, void* 
 /* Sizes of the memory state buffers for this model (elements). */
 ARMT_API armt_status armt_state_sizes(const armt_model* m, int64_t* a_elems, int64_t* z_elems);
 
+/* Device memory the library holds for this model, in bytes (its own
+ * cudaMalloc calls; the caller's tokens, outputs and memory state are not
+ * counted -- armt_state_sizes gives the state):
+ *   weights         stacked per-layer weights, embeddings and norm gains
+ *   workspace       the cell engine's activations and scratch, one slot per
+ *                   layer: fixed at armt_create, independent of the number of
+ *                   segments (the recurrence's constant-memory property,
+ *                   section 一 of the summary page)
+ *   full_workspace  the full-attention baseline's workspace, 0 until
+ *                   armt_forward_full_attention has run; it grows with the
+ *                   sequence length
+ * Any pointer may be NULL to skip that figure.  ARMT_ERR_ARG if m is NULL. */
+ARMT_API armt_status armt_memory_bytes(const armt_model* m, int64_t* weights, int64_t* workspace,
+                                       int64_t* full_workspace);
+
 /* Number of kernel launches one forward of n_segments makes with `schedule`. */
 ARMT_API armt_status armt_launch_count(const armt_model* m, int64_t n_segments, int32_t schedule,
                               int64_t* launches);

@@ -150,6 +150,7 @@ struct ModelBase {
   armt_config cfg{};
   int device = 0, num_sms = 148;
   DevAllocs mem;
+  long long weight_bytes = 0;  // part of mem.total holding the weights
   int* d_err = nullptr;
   // profiling
   bool profiling = false;
@@ -175,6 +176,7 @@ struct ModelBase {
                               int mem_in_valid, int schedule, cudaStream_t st) = 0;
   virtual armt_status forward_full(const int32_t* tokens, int64_t T, float* hidden,
                                    cudaStream_t st) = 0;
+  virtual long long full_workspace_bytes() const = 0;
 
   int rows() const { return cfg.seg_len + cfg.n_mem; }
   int phi_dim() const { return 2 * cfg.key_dim * cfg.dpfp_nu; }
@@ -272,6 +274,7 @@ struct Model : ModelBase {
   AT *Nrmf = nullptr, *QKVf = nullptr, *Vtf = nullptr, *Attf = nullptr, *Uf = nullptr;
   CUtensorMap tmNrmf, tmQKf, tmVtf, tmAttf, tmUf;
   ~Model() override { full_mem.free_all(); }
+  long long full_workspace_bytes() const override { return full_mem.total; }
   int upd_rows_per_block = 32;
 
   armt_status copy_in(void* dst, const void* src, size_t bytes, cudaStream_t st) {
@@ -337,6 +340,7 @@ struct Model : ModelBase {
     CKS(gain_to_f32(&g1, w->norm1, L * d, st));
     CKS(gain_to_f32(&g2, w->norm2, L * d, st));
     CKS(gain_to_f32(&gf, w->norm_f, d, st));
+    weight_bytes = mem.total;
     // RoPE tables (double precision on the host, stored fp32)
     {
       std::vector<float> hc(T * (hd / 2)), hs(T * (hd / 2));
@@ -969,6 +973,16 @@ armt_status armt_state_sizes(const armt_model* m, int64_t* a_elems, int64_t* z_e
   const armt_config& c = m->impl->cfg;
   *a_elems = (int64_t)c.n_layers * c.d_model * m->impl->phi_dim();
   *z_elems = (int64_t)c.n_layers * m->impl->phi_dim();
+  return ARMT_OK;
+}
+
+armt_status armt_memory_bytes(const armt_model* m, int64_t* weights, int64_t* workspace,
+                              int64_t* full_workspace) {
+  if (m == nullptr) return fail(ARMT_ERR_ARG, "NULL model");
+  const ModelBase& b = *m->impl;
+  if (weights) *weights = b.weight_bytes;
+  if (workspace) *workspace = b.mem.total - b.weight_bytes;
+  if (full_workspace) *full_workspace = b.full_workspace_bytes();
   return ARMT_OK;
 }
 

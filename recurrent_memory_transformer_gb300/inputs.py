@@ -93,8 +93,19 @@ WORKLOADS = {
     "armt-1b-8k": (ARMT_1B, 8, 1),
     "armt-1b-131k": (ARMT_1B, 128, 1),
     "armt-3b-32k": (ARMT_3B, 32, 2),
+    "armt-3b-131k": (ARMT_3B, 128, 2),
+    # 8B at 131,072 tokens with segment lengths 512 / 1024 / 2048 (the
+    # segment-size sweep of section 三), 16 memory tokens each
+    "armt-8b-131k-s512": (dataclasses.replace(ARMT_8B, seg_len=512), 256, 3),
     "armt-8b-131k": (ARMT_8B, 128, 3),
+    "armt-8b-131k-s2048": (dataclasses.replace(ARMT_8B, seg_len=2048), 64, 3),
 }
+
+# Workloads whose weights are drawn on the GPU (make_weights_device): the 3B
+# and 8B shapes need no oracle parity, and a host draw of 6-15 GB of normals
+# would dominate a benchmark run.
+DEVICE_WEIGHT_WORKLOADS = ("armt-3b-32k", "armt-3b-131k", "armt-8b-131k-s512", "armt-8b-131k",
+                           "armt-8b-131k-s2048")
 
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
@@ -151,6 +162,38 @@ def make_weights(cfg: ArmtConfig, seed: int, std: float = 0.02,
     if cfg.dtype == "bf16":
         for key in WEIGHT_KEYS:
             w[key] = round_to_bf16(w[key])
+    return w
+
+
+def make_weights_device(cfg: ArmtConfig, seed: int, std: float = 0.02, device="cuda"):
+    """Random-init weights drawn on the GPU, for shapes too large to draw on the host.
+
+    Same keys, shapes and key order as ``make_weights`` (norm gains 1), but the
+    normals come from a torch CUDA generator seeded with ``seed``, so the
+    values differ from the host draw.  Returns torch tensors on ``device`` in
+    the model's element type (bf16 or fp32).
+    """
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    L, d, hd, F = cfg.n_layers, cfg.d_model, cfg.head_dim, cfg.ffn_dim
+
+    def normal(*shape):
+        a = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        a.mul_(std)
+        return a.to(dt)
+
+    shapes = (("embed", (cfg.vocab, d)), ("mem", (cfg.n_mem, d)),
+              ("wq", (L, cfg.n_q_heads * hd, d)), ("wk", (L, cfg.n_kv_heads * hd, d)),
+              ("wv", (L, cfg.n_kv_heads * hd, d)), ("wo", (L, d, cfg.n_q_heads * hd)),
+              ("w_gate", (L, F, d)), ("w_up", (L, F, d)), ("w_down", (L, d, F)),
+              ("a_wq", (L, cfg.key_dim, d)), ("a_wk", (L, cfg.key_dim, d)), ("a_wv", (L, d, d)),
+              ("a_wbeta", (L, d)))
+    w = {k: normal(*shape) for k, shape in shapes}
+    w["norm1"] = torch.ones((L, d), device=device, dtype=dt)
+    w["norm2"] = torch.ones((L, d), device=device, dtype=dt)
+    w["norm_f"] = torch.ones((d,), device=device, dtype=dt)
     return w
 
 

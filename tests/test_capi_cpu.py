@@ -96,6 +96,7 @@ def test_forward_and_gemm_reject_null_arguments(lib):
     i64 = ctypes.c_int64()
     assert lib.armt_launch_count(None, 1, 0, ctypes.byref(i64)) == 1
     assert lib.armt_state_sizes(None, ctypes.byref(i64), ctypes.byref(i64)) == 1
+    assert lib.armt_memory_bytes(None, ctypes.byref(i64), None, None) == 1
     assert lib.armt_destroy(None) == 0
 
 

@@ -346,3 +346,31 @@ def test_full_attention_baseline_equals_armt_first_segment_up_to_rounding():
     # the baseline test), and they round the norms at different points, so
     # they may differ by up to about twice that
     assert s["cos"] >= 0.9999 and s["max_abs"] <= 0.1, s
+
+
+def test_memory_bytes_workspace_is_independent_of_sequence_length():
+    # The recurrence keeps one activation slot per layer however many
+    # segments run; the full-attention baseline's workspace grows with T.
+    cfg = dataclasses.replace(I.ARMT_1B, n_layers=2)
+    W = I.make_weights(cfg, seed=33)
+    m = B.Model(cfg, B.device_weight_tensors(cfg, W))
+    w0, ws0, fw0 = m.armt_memory_bytes()
+    n_par = sum(int(np.prod(W[k].shape)) for k in I.WEIGHT_KEYS if not k.startswith("norm"))
+    assert 2 * n_par <= w0 <= int(2.05 * n_par) + 4 * 3 * cfg.n_layers * cfg.d_model, (w0, n_par)
+    assert ws0 > 0 and fw0 == 0
+    for n_seg in (1, 3):
+        tok = torch.from_numpy(I.make_tokens(cfg, n_seg, seed=33)).cuda()
+        m.forward(tok, n_seg)
+        torch.cuda.synchronize()
+        assert m.armt_memory_bytes()[:2] == (w0, ws0)
+    sizes = []
+    for T in (1024, 3072):
+        tok = torch.from_numpy(I.make_tokens(cfg, T // cfg.seg_len, seed=33)).cuda()
+        h = torch.empty((T, cfg.d_model), dtype=torch.float32, device="cuda")
+        m.armt_forward_full_attention(tok, h)
+        torch.cuda.synchronize()
+        sizes.append(m.armt_memory_bytes()[2])
+    m.armt_sync_status()
+    m.close()
+    assert 0 < sizes[0] < sizes[1], sizes
+    record("memory_bytes", weights=w0, workspace=ws0, full_workspace=sizes)
