@@ -295,6 +295,32 @@ def test_armt1b_131k_full_size_properties():
     assert ok, (g, mstats)
 
 
+@pytest.mark.parametrize("base,n_layers,n_seg,seed", [(I.ARMT_3B, 2, 2, 41), (I.ARMT_8B, 1, 2, 42)])
+def test_3b_8b_cell_shapes_match_oracle(base, n_layers, n_seg, seed):
+    """The 3B and 8B cell shapes (head_dim 128, d 3072 / 4096, F 8192 / 14336)
+    at reduced depth: oracle parity under the derived bf16 bounds, and the
+    diagonal and sequential schedules bitwise equal."""
+    # a 4096-token vocabulary keeps the host draw short; it does not change the cell
+    cfg = dataclasses.replace(base, n_layers=n_layers, vocab=4096)
+    W = I.make_weights(cfg, seed, norm_jitter=0.1)
+    tok = I.make_tokens(cfg, n_seg, seed)
+    m = B.Model(cfg, B.device_weight_tensors(cfg, W))
+    t = torch.from_numpy(tok).cuda()
+    hd, Ad, zd = m.forward(t, n_seg)
+    hs, As, zs = m.forward(t, n_seg, schedule=B.SCHEDULE_SEQUENTIAL)
+    torch.cuda.synchronize()
+    m.armt_sync_status()
+    bitwise = bool(torch.equal(hd, hs) and torch.equal(Ad, As) and torch.equal(zd, zs))
+    gpu = (hd.cpu().numpy(), Ad.cpu().numpy(), zd.cpu().numpy())
+    m.close()
+    exact = O.forward(cfg, W, tok, n_seg)
+    model = O.forward(cfg, W, tok, n_seg, operands="bf16")
+    ok, g, mstats = _derived_bounds_hold(gpu, exact, model, cfg.seg_len, n_seg)
+    record(f"cell_shape_d{cfg.d_model}", bitwise_diag_seq=bitwise, gpu_vs_fp64=g, model_vs_fp64=mstats)
+    assert bitwise
+    assert ok, (g, mstats)
+
+
 # ------------------------------------------- full-attention LLaMA baseline --
 
 def _plain_llama_oracle(cfg, W, tok, operands=None):
