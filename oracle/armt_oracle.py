@@ -48,6 +48,9 @@ Oseledets, arXiv:2506.05229):
   segment (the write-memory position of the RMT form in section 二).
 * Output: the last layer's segment rows after the final RMSNorm, and the
   final A_l, z_l of every layer.
+* LM head and error measure (section 四: the drift of diagonal batching from
+  the sequential recurrence, read through the logits): logits = hidden
+  head^T, compared as a relative Frobenius norm.
 
 Everything is float64 with no intermediate rounding; bf16 models arrive as
 float32 arrays holding bf16 values and are widened exactly.  numpy matmul is
@@ -288,3 +291,22 @@ def forward(cfg, W, tokens, n_segments, order="seq", A0=None, z0=None, W64=None,
                 acts[(l, s)] = h
     return out, np.stack(A), np.stack(z)
 
+
+
+# --------------------------------------------------------------------------
+# LM head and the relative-logits error (summary page, section 四)
+# --------------------------------------------------------------------------
+def lm_head_logits(hidden, head):
+    """Logits of hidden rows against a head matrix [V, d]: logits = hidden head^T.
+
+    The summary page (section 四) measures how far diagonal batching drifts
+    from the sequential recurrence through the logits of the final hidden
+    states; with a tied head the matrix is the token embedding.
+    """
+    return _f64(hidden) @ _f64(head).T
+
+
+def relative_logits_error(logits, ref):
+    """||logits - ref||_F / ||ref||_F, in fp64 (the section 四 error measure, as a relative norm)."""
+    logits, ref = _f64(logits), _f64(ref)
+    return float(np.linalg.norm(logits - ref) / np.linalg.norm(ref))

@@ -376,3 +376,27 @@ def test_bf16_precision_model_is_close_to_fp64_and_rounds():
     model_d = O.forward(cfg, W, tok, 3, order="diag", operands="bf16")
     for a, b in zip(model, model_d):
         np.testing.assert_array_equal(a, b)
+
+
+def test_lm_head_logits_closed_forms():
+    # with an identity head (V = d) the logits are the hidden rows themselves;
+    # with a permutation head they are those rows permuted -- a transposed or
+    # swapped operand fails one of the two
+    rng = np.random.default_rng(5)
+    h = rng.standard_normal((3, 6))
+    np.testing.assert_array_equal(O.lm_head_logits(h, np.eye(6)), h)
+    perm = np.array([2, 0, 5, 1, 4, 3])
+    head = np.eye(6)[perm]                       # row v picks coordinate perm[v]
+    np.testing.assert_array_equal(O.lm_head_logits(h, head), h[:, perm])
+    # a tied head and a hidden row equal to embedding row j: logit j is ||e_j||^2
+    E = rng.standard_normal((10, 6))
+    lg = O.lm_head_logits(E[[7]], E)
+    assert lg.shape == (1, 10)
+    assert abs(lg[0, 7] - float(E[7] @ E[7])) < 1e-12
+
+
+def test_relative_logits_error_closed_forms():
+    ref = np.random.default_rng(6).standard_normal((4, 9))
+    assert O.relative_logits_error(ref, ref) == 0.0
+    assert abs(O.relative_logits_error(1.01 * ref, ref) - 0.01) < 1e-12
+    assert abs(O.relative_logits_error(np.zeros_like(ref), ref) - 1.0) < 1e-15
