@@ -315,6 +315,26 @@ def main():
                    "ramp_overhead_frac": 1.0 - n_seg * t_full / ms_step,
                    "method": f"(t({n_seg} segments) - t({h2})) / {n_seg - h2} full diagonals"}
 
+    # ---- LM head (tied embedding) over one 8192-token chunk of the output --
+    lm = None
+    if cfg.dtype == "bf16" and cfg.vocab % 256 == 0:
+        r = min(8192, n_tok)
+        logits = torch.empty((r, cfg.vocab), dtype=torch.float32, device="cuda")
+        model.armt_lm_head(hidden[:r], logits, stream=stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(3):
+            model.armt_lm_head(hidden[:r], logits, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        model.armt_sync_status()
+        lm_ms = e0.elapsed_time(e1) / 3
+        lm = {"rows": r, "vocab": cfg.vocab, "ms": lm_ms,
+              "tflops": 2.0 * r * cfg.d_model * cfg.vocab / (lm_ms / 1000.0) / 1e12}
+        del logits
+        torch.cuda.empty_cache()
+
     # ---- full-causal-attention LLaMA on the same weights (no memory) -----
     full = None
     if not args.no_full and cfg.dtype == "bf16":
@@ -388,6 +408,7 @@ def main():
             "kernels": per_class,
             "sequential": seq,
             "uniform_bound": uniform,
+            "lm_head": lm,
             "full_attention": full,
             "memory": memory,
             "e2e": e2e,

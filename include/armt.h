@@ -239,6 +239,23 @@ ARMT_API armt_status armt_segment_attention_bf16_noalloc(const void* qkv, void* 
                                                          int32_t T, int32_t Hq, int32_t Hkv,
                                                          int32_t hd, void* stream);
 
+/* LM head over hidden states (the logits behind the error-accumulation
+ * study of section 四 of the summary page: diagonal batching vs the
+ * sequential recurrence):
+ *   logits[r][v] = sum_c hidden[r][c] * head[v][c],  r < n_rows, v < vocab
+ *   hidden  device fp32 [n_rows][d_model] (e.g. armt_forward's output)
+ *   w_head  device [vocab][d_model] in the model's dtype, or NULL for the
+ *           model's own token embedding (tied head)
+ *   logits  device fp32 [n_rows][vocab], caller-owned
+ * bf16 models: the hidden rows are rounded to bf16 and the product runs on
+ * the tensor cores (fp32 accumulation, the grouped GEMM), 8192 rows per
+ * launch; vocab % 256 == 0 (ARMT_ERR_UNSUPPORTED otherwise).  fp32 models:
+ * fp32 SIMT product.  16-byte aligned pointers.  Asynchronous on `stream`;
+ * the first call allocates a 8192 x d_model bf16 staging buffer owned by the
+ * model. */
+ARMT_API armt_status armt_lm_head(armt_model* m, const float* hidden, int64_t n_rows,
+                                  const void* w_head, float* logits, void* stream);
+
 /* Sizes of the memory state buffers for this model (elements). */
 ARMT_API armt_status armt_state_sizes(const armt_model* m, int64_t* a_elems, int64_t* z_elems);
 

@@ -29,7 +29,7 @@ KERNEL_CLASSES = ("gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down", "attention",
 EXPORTED = ("armt_create", "armt_destroy", "armt_forward", "armt_forward_sequential",
             "armt_forward_host", "armt_grouped_gemm_bf16", "armt_segment_attention_bf16",
             "armt_segment_attention_bf16_noalloc", "armt_forward_full_attention", "armt_state_sizes",
-            "armt_memory_bytes", "armt_launch_count",
+            "armt_memory_bytes", "armt_lm_head", "armt_launch_count",
             "armt_set_profiling", "armt_kernel_times", "armt_sync_status", "armt_status_string",
             "armt_last_error")
 
@@ -83,6 +83,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.armt_segment_attention_bf16.argtypes = [P, P, P, I32, I32, I32, I32, I32, P]
     lib.armt_segment_attention_bf16_noalloc.argtypes = [P, P, I32, I32, I32, I32, I32, P]
     lib.armt_state_sizes.argtypes = [P, ctypes.POINTER(I64), ctypes.POINTER(I64)]
+    lib.armt_lm_head.argtypes = [P, P, I64, P, P, P]
     lib.armt_memory_bytes.argtypes = [P, ctypes.POINTER(I64), ctypes.POINTER(I64), ctypes.POINTER(I64)]
     lib.armt_launch_count.argtypes = [P, I64, I32, ctypes.POINTER(I64)]
     lib.armt_set_profiling.argtypes = [P, I32]
@@ -222,6 +223,12 @@ class Model:
         _check(_lib.armt_forward_full_attention(self._h, _ptr(tokens), int(tokens.numel()),
                                                 _ptr(hidden_out), _stream_ptr(stream)),
                "armt_forward_full_attention")
+
+    def armt_lm_head(self, hidden, logits, w_head=None, stream=None):
+        """logits fp32 [rows, vocab] = hidden fp32 [rows, d] @ head^T (head: w_head or the tied embedding)."""
+        _check(_lib.armt_lm_head(self._h, _ptr(hidden), int(hidden.shape[0]),
+                                 None if w_head is None else _ptr(w_head), _ptr(logits),
+                                 _stream_ptr(stream)), "armt_lm_head")
 
     def armt_memory_bytes(self):
         """(weights, workspace, full_workspace): device bytes the library holds for this model."""

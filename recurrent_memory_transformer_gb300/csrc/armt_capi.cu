@@ -177,6 +177,8 @@ struct ModelBase {
   virtual armt_status forward_full(const int32_t* tokens, int64_t T, float* hidden,
                                    cudaStream_t st) = 0;
   virtual long long full_workspace_bytes() const = 0;
+  virtual armt_status lm_head(const float* hidden, int64_t n_rows, const void* w_head, float* logits,
+                              cudaStream_t st) = 0;
 
   int rows() const { return cfg.seg_len + cfg.n_mem; }
   int phi_dim() const { return 2 * cfg.key_dim * cfg.dpfp_nu; }
@@ -270,10 +272,17 @@ struct Model : ModelBase {
   // activation slot, grown on demand
   DevAllocs full_mem;
   int64_t full_T = 0;
+  // LM head: bf16 copy of a chunk of hidden rows (tensor-core path)
+  DevAllocs lm_mem;
+  AT* lm_rows = nullptr;
+  static constexpr int64_t kLmChunk = 8192;
   float *Xf = nullptr, *Resf = nullptr, *Ssqf = nullptr, *cosF = nullptr, *sinF = nullptr;
   AT *Nrmf = nullptr, *QKVf = nullptr, *Vtf = nullptr, *Attf = nullptr, *Uf = nullptr;
   CUtensorMap tmNrmf, tmQKf, tmVtf, tmAttf, tmUf;
-  ~Model() override { full_mem.free_all(); }
+  ~Model() override {
+    full_mem.free_all();
+    lm_mem.free_all();
+  }
   long long full_workspace_bytes() const override { return full_mem.total; }
   int upd_rows_per_block = 32;
 
@@ -608,6 +617,44 @@ struct Model : ModelBase {
   // Plain causal LLaMA over T tokens with the same weights: no memory tokens,
   // no associative memory, one attention over the whole sequence.  Layers run
   // one after another; each launch reads activation slot 0 and weight slot l.
+  // logits[r][v] = hidden[r] . head[v], head = w_head or the token embedding
+  // (tied); rows in chunks of kLmChunk.  Tensor cores for bf16 models: the
+  // fp32 hidden rows are rounded to bf16 first (the head's operand type).
+  armt_status lm_head(const float* hidden, int64_t n_rows, const void* w_head, float* logits,
+                      cudaStream_t st) override {
+    const armt_config& c = cfg;
+    const int d = c.d_model, V = c.vocab;
+    const WT* head = w_head != nullptr ? reinterpret_cast<const WT*>(w_head) : embed;
+    if (kTC && V % 256 != 0) return fail(ARMT_ERR_UNSUPPORTED, "bf16 LM head needs vocab % 256 == 0");
+    if (kTC && lm_rows == nullptr) CKS(lm_mem.alloc_n(&lm_rows, (size_t)kLmChunk * d));
+    CKS(prof_begin(ARMT_KC_OTHER, st));
+    if constexpr (kTC) {
+      CUtensorMap tb;
+      if (!encode_tmap_bf16_3d(&tb, head, d, V, 1, 256)) return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+      for (int64_t r0 = 0; r0 < n_rows; r0 += kLmChunk) {
+        const int rows_c = (int)std::min<int64_t>(kLmChunk, n_rows - r0);
+        convert_state_kernel<AT><<<num_sms * 4, 256, 0, st>>>(hidden + r0 * d, lm_rows, (long long)rows_c * d);
+        CK(cudaGetLastError());
+        CUtensorMap ta;
+        if (!encode_tmap_bf16_3d(&ta, lm_rows, d, rows_c, 1, TC_BM))
+          return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        SEpiStore epi{logits + r0 * V, (long long)V, 0};
+        CK((launch_gemm_tc<SEpiStore, 256>(ta, tb, rows_c, V, d, 0, 1, d_err, epi, num_sms, st)));
+      }
+    } else {
+      for (int64_t r0 = 0; r0 < n_rows; r0 += kLmChunk) {
+        const int rows_c = (int)std::min<int64_t>(kLmChunk, n_rows - r0);
+        dim3 grid((V + 63) / 64, (rows_c + 63) / 64, 1);
+        gemm_simt_f32_kernel<<<grid, 256, 0, st>>>(hidden + r0 * d, 0, d,
+                                                   reinterpret_cast<const float*>(head), 0,
+                                                   logits + r0 * V, 0, V, rows_c, V, d, 0);
+        CK(cudaGetLastError());
+      }
+    }
+    CKS(prof_end(st));
+    return ARMT_OK;
+  }
+
   armt_status forward_full(const int32_t* tokens, int64_t T64, float* hidden,
                            cudaStream_t st) override {
     if constexpr (!kTC) {
@@ -901,6 +948,16 @@ armt_status armt_forward_full_attention(armt_model* m, const int32_t* tokens, in
     return fail(ARMT_ERR_ARG, "NULL argument");
   if (n_tokens <= 0) return fail(ARMT_ERR_ARG, "n_tokens must be positive");
   return m->impl->forward_full(tokens, n_tokens, hidden_out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+armt_status armt_lm_head(armt_model* m, const float* hidden, int64_t n_rows, const void* w_head,
+                         float* logits, void* stream) {
+  if (m == nullptr || hidden == nullptr || logits == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
+  if (n_rows <= 0) return fail(ARMT_ERR_ARG, "n_rows must be positive");
+  if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(logits) |
+       reinterpret_cast<uintptr_t>(w_head)) & 15)
+    return fail(ARMT_ERR_ARG, "pointers must be 16-byte aligned");
+  return m->impl->lm_head(hidden, n_rows, w_head, logits, reinterpret_cast<cudaStream_t>(stream));
 }
 
 armt_status armt_grouped_gemm_bf16(const void* A, const void* B, float* C, int32_t G, int32_t M,

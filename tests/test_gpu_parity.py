@@ -223,19 +223,39 @@ def armt1b():
 
 def test_armt1b_8k_matches_oracle_and_schedules_agree(armt1b):
     cfg, n, W, tok = armt1b
+    S = cfg.seg_len
     m = B.Model(cfg, B.device_weight_tensors(cfg, W))
     t = torch.from_numpy(tok).cuda()
     hd, Ad, zd = m.forward(t, n, schedule=B.SCHEDULE_DIAGONAL)
     hs, As, zs = m.forward(t, n, schedule=B.SCHEDULE_SEQUENTIAL)
+    # logits (tied head) of 32 evenly spaced rows per segment, both schedules
+    rows = np.concatenate([s * S + np.arange(0, S, S // 32) for s in range(n)])
+    ri = torch.from_numpy(rows).cuda()
+    lg_d = torch.empty((len(rows), cfg.vocab), dtype=torch.float32, device="cuda")
+    lg_s = torch.empty_like(lg_d)
+    m.armt_lm_head(hd[ri].contiguous(), lg_d)
+    m.armt_lm_head(hs[ri].contiguous(), lg_s)
     torch.cuda.synchronize()
     m.armt_sync_status()
     bitwise = bool(torch.equal(hd, hs) and torch.equal(Ad, As) and torch.equal(zd, zs))
+    logits_bitwise = bool(torch.equal(lg_d, lg_s))
     hd, Ad, zd = hd.cpu().numpy(), Ad.cpu().numpy(), zd.cpu().numpy()
+    lg_d = lg_d.cpu().numpy()
     m.close()
-    S = cfg.seg_len
-    res = {"bitwise_diag_seq": bitwise}
+    res = {"bitwise_diag_seq": bitwise, "logits_bitwise_diag_seq": logits_bitwise}
     ho, Ao, zo = O.forward(cfg, W, tok, n)
     hm, Am, zm = O.forward(cfg, W, tok, n, operands="bf16")
+    # relative logits error per segment (the error-accumulation measure of
+    # section 四), GPU and the bf16 precision model against fp64
+    E = W["embed"]
+    lo = O.lm_head_logits(ho[rows], E)
+    lm = O.lm_head_logits(O.round_bf16(hm[rows]), E)
+    per = len(rows) // n
+    res["relative_logits_error"] = {
+        "gpu": [O.relative_logits_error(lg_d[s * per:(s + 1) * per], lo[s * per:(s + 1) * per]) for s in range(n)],
+        "bf16_model": [O.relative_logits_error(lm[s * per:(s + 1) * per], lo[s * per:(s + 1) * per])
+                       for s in range(n)],
+        "diag_vs_seq": 0.0 if logits_bitwise else None}
     res["gpu_vs_fp64"] = dict(hidden=stats(hd, ho), A=stats(Ad, Ao), z=stats(zd, zo),
                               per_segment_max_abs=[float(np.abs(hd[s * S:(s + 1) * S] - ho[s * S:(s + 1) * S]).max())
                                                    for s in range(n)])
@@ -244,7 +264,10 @@ def test_armt1b_8k_matches_oracle_and_schedules_agree(armt1b):
                                                      for s in range(n)])
     res["gpu_vs_model"] = dict(hidden=stats(hd, hm), A=stats(Ad, Am), z=stats(zd, zm))
     record("armt1b_8k", **res)
-    assert bitwise
+    assert bitwise and logits_bitwise
+    rle = res["relative_logits_error"]
+    for s in range(n):
+        assert rle["gpu"][s] <= 2.0 * rle["bf16_model"][s], (s, rle)
     g, m = res["gpu_vs_fp64"], res["model_vs_fp64"]
     assert g["hidden"]["finite"] and g["hidden"]["cos"] >= 0.999, g["hidden"]
     for key in ("hidden", "A", "z"):
@@ -400,3 +423,42 @@ def test_memory_bytes_workspace_is_independent_of_sequence_length():
     m.close()
     assert 0 < sizes[0] < sizes[1], sizes
     record("memory_bytes", weights=w0, workspace=ws0, full_workspace=sizes)
+
+
+
+@pytest.mark.parametrize("n_rows,tied", [(300, True), (8192 + 100, False)])
+def test_lm_head_bf16_matches_fp64(n_rows, tied):
+    cfg = dataclasses.replace(I.ARMT_1B, n_layers=1, vocab=4096)
+    W = I.make_weights(cfg, seed=51)
+    m = B.Model(cfg, B.device_weight_tensors(cfg, W))
+    rng = np.random.default_rng(51)
+    h = rng.standard_normal((n_rows, cfg.d_model)).astype(np.float32)
+    head = W["embed"] if tied else I.round_to_bf16(0.02 * rng.standard_normal((cfg.vocab, cfg.d_model)).astype(np.float32))
+    lg = torch.empty((n_rows, cfg.vocab), dtype=torch.float32, device="cuda")
+    wh = None if tied else torch.from_numpy(head).cuda().to(torch.bfloat16)
+    m.armt_lm_head(torch.from_numpy(h).cuda(), lg, w_head=wh)
+    torch.cuda.synchronize()
+    m.armt_sync_status()
+    got = lg.cpu().numpy()
+    m.close()
+    hb = O.round_bf16(h)                        # the head's operand type
+    ref = O.lm_head_logits(hb, head)
+    # fp32 accumulation of 2048 exact bf16 products: a few ulps of the sum of |terms|
+    bound = 4e-6 * (np.abs(hb) @ np.abs(head.astype(np.float64)).T) + 1e-7
+    err = np.abs(got - ref)
+    record(f"lm_head_{n_rows}", max_abs=float(err.max()), worst_ratio=float((err / bound).max()))
+    assert (err <= bound).all(), float((err / bound).max())
+
+
+def test_lm_head_fp32_tiny_matches_fp64():
+    cfg, n, W, tok = I.make_workload("tiny")
+    m = B.Model(cfg, W)
+    h = np.random.default_rng(52).standard_normal((37, cfg.d_model)).astype(np.float32)
+    lg = torch.empty((37, cfg.vocab), dtype=torch.float32, device="cuda")
+    m.armt_lm_head(torch.from_numpy(h).cuda(), lg)
+    torch.cuda.synchronize()
+    m.armt_sync_status()
+    got = lg.cpu().numpy()
+    m.close()
+    ref = O.lm_head_logits(h, W["embed"])
+    assert np.abs(got - ref).max() <= 1e-5 * max(1.0, np.abs(ref).max())
