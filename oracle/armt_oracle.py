@@ -236,13 +236,13 @@ def cell_forward(x, cfg, W, l, A, z, rnd=_identity):
     nu, eps = cfg.dpfp_nu, cfg.assoc_eps
     x = assoc_read(x, W["a_wq"][l], A, z, nu, eps, rnd)
     h = llama_block(x, cfg, W, l, rnd)
-    S = cfg.seg_len
-    A2, z2 = assoc_write(h[S:], W["a_wk"][l], W["a_wv"][l], W["a_wbeta"][l], A, z, nu, eps, rnd)
+    m0 = h.shape[0] - cfg.n_mem               # the memory rows close the cell
+    A2, z2 = assoc_write(h[m0:], W["a_wk"][l], W["a_wv"][l], W["a_wbeta"][l], A, z, nu, eps, rnd)
     return h, A2, z2
 
 
 def layer0_input(cfg, W, tokens, s):
-    """[E[tokens of segment s]; memory embeddings] -> [T_c, d]."""
+    """[E[tokens of segment s]; memory embeddings] -> [T_c, d] (fewer rows for a short last segment)."""
     S = cfg.seg_len
     return np.concatenate([W["embed"][tokens[s * S:(s + 1) * S]], W["mem"]], axis=0)
 
@@ -266,7 +266,12 @@ def schedule(n_layers: int, n_segments: int, order: str):
 def forward(cfg, W, tokens, n_segments, order="seq", A0=None, z0=None, W64=None, operands=None):
     """ARMT forward over n_segments segments.
 
-    Returns (hidden [n*S, d], A [L, d, P], z [L, P]) in float64.  ``A0``/``z0``
+    ``tokens`` holds N ids with (n_segments - 1) * S < N <= n_segments * S.
+    The last segment may be short: it takes the remaining S' = N - (n - 1) S
+    tokens, followed as usual by the M memory tokens (S' + M rows, positions
+    0..S'+M-1).  The pages do not discuss a partial segment; this is the
+    plainest reading (the segment is just shorter).
+    Returns (hidden [N, d], A [L, d, P], z [L, P]) in float64.  ``A0``/``z0``
     give an initial memory state (zeros when None).  ``operands="bf16"``
     selects the bf16 operand-rounding precision model (module docstring).
     """
@@ -274,19 +279,21 @@ def forward(cfg, W, tokens, n_segments, order="seq", A0=None, z0=None, W64=None,
     L, d, P, S = cfg.n_layers, cfg.d_model, cfg.phi_dim, cfg.seg_len
     W = W64 if W64 is not None else widen_weights(W)
     tokens = np.asarray(tokens)
-    assert tokens.shape[0] == n_segments * S
+    N = tokens.shape[0]
+    assert (n_segments - 1) * S < N <= n_segments * S
     A = [(_f64(A0[l]).copy() if A0 is not None else np.zeros((d, P), F64)) for l in range(L)]
     z = [(_f64(z0[l]).copy() if z0 is not None else np.zeros((P,), F64)) for l in range(L)]
     # outputs of each layer per segment; in a real run only the live wavefront
     # is kept, here a dict keyed by (l, s) is plain and small enough.
     acts = {}
-    out = np.zeros((n_segments * S, d), F64)
+    out = np.zeros((N, d), F64)
     for step in schedule(L, n_segments, order):
         for (l, s) in step:
             x = layer0_input(cfg, W, tokens, s) if l == 0 else acts.pop((l - 1, s))
             h, A[l], z[l] = cell_forward(x, cfg, W, l, A[l], z[l], rnd)
             if l == L - 1:
-                out[s * S:(s + 1) * S] = rmsnorm(h[:S], W["norm_f"], cfg.norm_eps)
+                seg = h.shape[0] - cfg.n_mem
+                out[s * S:s * S + seg] = rmsnorm(h[:seg], W["norm_f"], cfg.norm_eps)
             else:
                 acts[(l, s)] = h
     return out, np.stack(A), np.stack(z)

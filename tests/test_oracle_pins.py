@@ -214,13 +214,15 @@ def test_schedule_covers_grid_in_dependency_order():
                 assert seen[(l, s - 1)] < i
 
 
-@pytest.mark.parametrize("over", [{}, {"n_q_heads": 4, "n_kv_heads": 2, "head_dim": 16}])
-def test_one_segment_empty_memory_equals_plain_transformer(over):
+@pytest.mark.parametrize("over,short", [({}, 0), ({"n_q_heads": 4, "n_kv_heads": 2, "head_dim": 16}, 0),
+                                        ({}, 7)])
+def test_one_segment_empty_memory_equals_plain_transformer(over, short):
     cfg = _tiny(**over)
     W = I.make_weights(cfg, seed=12, norm_jitter=0.1)
     tok = I.make_tokens(cfg, 1, seed=12)
+    tok = tok[:tok.shape[0] - short]             # short > 0: a partial segment
     out, _, _ = O.forward(cfg, W, tok, 1)
-    S = cfg.seg_len
+    S = cfg.seg_len - short
     X = np.concatenate([W["embed"][tok], W["mem"]]).astype(np.float64)
     ref = plain_stack(X, W, cfg)
     np.testing.assert_allclose(out, ref[:S], rtol=1e-10, atol=1e-12)
@@ -230,12 +232,17 @@ def test_one_segment_empty_memory_equals_plain_transformer(over):
     np.testing.assert_allclose(out, ref_s, rtol=1e-10, atol=1e-12)
 
 
-def test_two_segments_one_layer_hand_expansion():
+@pytest.mark.parametrize("short", [0, 5])
+def test_two_segments_one_layer_hand_expansion(short):
+    # short > 0: the second segment is `short` tokens shorter (a partial last
+    # segment: its memory rows follow its S - short tokens)
     cfg = _tiny(n_layers=1)
     W = I.make_weights(cfg, seed=13, norm_jitter=0.1)
     tok = I.make_tokens(cfg, 2, seed=13)
+    tok = tok[:tok.shape[0] - short]
     out, A, z = O.forward(cfg, W, tok, 2)
     S, k, nu, eps = cfg.seg_len, cfg.key_dim, cfg.dpfp_nu, cfg.assoc_eps
+    S1 = S - short
     W64 = {kk: np.asarray(v, np.float64) for kk, v in W.items()}
     gf = W64["norm_f"]
 
@@ -263,10 +270,12 @@ def test_two_segments_one_layer_hand_expansion():
     for t in range(X1.shape[0]):
         phi = _dpfp_loops(list(W64["a_wq"][0] @ X1[t]), nu)
         X1[t] = X1[t] + (A1 @ phi) / (float(z1 @ phi) + eps)
+    assert X1.shape[0] == S1 + cfg.n_mem
     H1 = plain_layer(X1, W64, 0, cfg)
-    A2, z2 = write(H1[S:], A1, z1)
+    A2, z2 = write(H1[S1:], A1, z1)
     ms = lambda r: r / math.sqrt(float(np.mean(r * r)) + cfg.norm_eps) * gf
-    ref = np.stack([ms(r) for r in np.concatenate([H0[:S], H1[:S]])])
+    ref = np.stack([ms(r) for r in np.concatenate([H0[:S], H1[:S1]])])
+    assert out.shape == (S + S1, cfg.d_model)
     np.testing.assert_allclose(out, ref, rtol=1e-9, atol=1e-11)
     np.testing.assert_allclose(A[0], A2, rtol=1e-9, atol=1e-11)
     np.testing.assert_allclose(z[0], z2, rtol=1e-9, atol=1e-11)
