@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-full", action="store_true",
                    help="skip the full-causal-attention LLaMA baseline on the same weights")
+    p.add_argument("--no-microbatch", action="store_true",
+                   help="skip the diagonal-batching vs micro-batching comparison")
     return p.parse_args()
 
 
@@ -224,6 +226,7 @@ def main():
     A = torch.empty(model.a_elems, dtype=torch.float32, device="cuda")
     z = torch.empty(model.z_elems, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
+    ws_create = model.armt_memory_bytes()[1]
 
     def step(schedule=B.SCHEDULE_DIAGONAL):
         model.armt_forward(tokens, n_seg, hidden, A, z, 0, stream, schedule)
@@ -350,6 +353,41 @@ def main():
         full = {"ms_per_step": full_ms, "tokens_per_s": n_tok / (full_ms / 1000.0),
                 "speedup_diag_over_full": full_ms / ms_step}
 
+    # ---- diagonal batching vs micro-batching (per-segment time) ----------
+    # Section 三 of the summary page compares the time per segment of
+    # diagonal batching with micro-batching (the sequential schedule run over
+    # a batch of B sequences at once).  Same weights; 16 segments per
+    # sequence; time per segment of one sequence = t / (segments x B).
+    microbatch = None
+    if not args.no_microbatch and cfg.dtype == "bf16":
+        mb_seg = min(16, n_seg)
+        mb_tok = mb_seg * cfg.seg_len
+        rng = np.random.default_rng(seed + 1000)
+        rows = []
+        for sched, bs in ((B.SCHEDULE_SEQUENTIAL, 1), (B.SCHEDULE_SEQUENTIAL, 2), (B.SCHEDULE_SEQUENTIAL, 4),
+                          (B.SCHEDULE_SEQUENTIAL, 8), (B.SCHEDULE_SEQUENTIAL, 16),
+                          (B.SCHEDULE_DIAGONAL, 1), (B.SCHEDULE_DIAGONAL, 4)):
+            tb = torch.from_numpy(rng.integers(0, cfg.vocab, size=(bs, mb_tok)).astype(np.int32)).cuda()
+            hb = torch.empty((bs, mb_tok, cfg.d_model), dtype=torch.float32, device="cuda")
+            Ab = torch.empty((cfg.n_layers, bs, model.a_elems // cfg.n_layers), dtype=torch.float32, device="cuda")
+            zb = torch.empty((cfg.n_layers, bs, model.z_elems // cfg.n_layers), dtype=torch.float32, device="cuda")
+            model.armt_forward_batch(tb, hb, Ab, zb, 0, sched, stream)   # sizes the batch workspace
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            model.armt_forward_batch(tb, hb, Ab, zb, 0, sched, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            model.armt_sync_status()
+            t_ms = e0.elapsed_time(e1)
+            rows.append({"schedule": "diagonal" if sched == B.SCHEDULE_DIAGONAL else "sequential",
+                         "batch": bs, "ms": t_ms, "ms_per_segment": t_ms / (mb_seg * bs),
+                         "tokens_per_s": bs * mb_tok / (t_ms / 1000.0)})
+            del tb, hb, Ab, zb
+        microbatch = {"segments_per_sequence": mb_seg, "runs": rows,
+                      "batch_workspace_bytes": model.armt_memory_bytes()[1] - ws_create}
+        torch.cuda.empty_cache()
+
     # ---- end to end through the host-buffer entry point ------------------
     e2e = None
     if not args.no_e2e:
@@ -375,7 +413,8 @@ def main():
                          f"layers ({t:.1f} s); per-segment cost is constant in the segment recurrence"}
 
     # ---- device memory: recurrent state vs a full-attention KV cache -----
-    w_bytes, ws_bytes, fw_bytes = model.armt_memory_bytes()
+    w_bytes, _, fw_bytes = model.armt_memory_bytes()
+    ws_bytes = ws_create
     state_bytes = (model.a_elems + model.z_elems) * 4
     kv_bytes = 2 * cfg.n_layers * n_tok * cfg.n_kv_heads * cfg.head_dim * 2
     memory = {"weights_bytes": w_bytes, "armt_workspace_bytes": ws_bytes,
@@ -410,6 +449,7 @@ def main():
             "uniform_bound": uniform,
             "lm_head": lm,
             "full_attention": full,
+            "microbatch": microbatch,
             "memory": memory,
             "e2e": e2e,
             "cpu_baseline": cpu,

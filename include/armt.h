@@ -167,6 +167,41 @@ ARMT_API armt_status armt_forward_sequential(armt_model* m, const int32_t* token
                                     float* hidden_out, float* mem_A, float* mem_z,
                                     int32_t mem_in_valid, void* stream);
 
+/* Largest batch armt_forward_batch accepts (also batch * n_layers <= 65535). */
+#define ARMT_MAX_BATCH 1024
+
+/* Batched forward over `batch` independent sequences of n_tokens tokens each,
+ * with the diagonal or the sequential schedule.  Every cell (l, s) runs the
+ * batch's sequences side by side: the weight GEMMs of a layer see the
+ * batch * (S + M) rows of its cells as one matrix, while attention and the
+ * memory read / write run per (layer, sequence) with that sequence's own
+ * state.  With the sequential schedule this is the micro-batching the
+ * summary page compares diagonal batching with (section 三: per-segment
+ * time of diagonal batching vs micro-batching); with the diagonal schedule
+ * the two kinds of batching combine.
+ * A short last segment is allowed: n_tokens need not be a multiple of S.
+ * The last segment then holds the remaining S' = n_tokens - (n - 1) S
+ * tokens (n = ceil(n_tokens / S)) followed as usual by the M memory tokens,
+ * at positions 0 .. S' + M - 1; the page does not discuss partial segments,
+ * this is the plain reading (the segment is just shorter).
+ *   tokens      device int32 [batch][n_tokens] (ids clamped to [0, V))
+ *   hidden_out  device fp32 [batch][n_tokens][d]
+ *   mem_A       device fp32 [L][batch][d][P] (layer-major: the state of
+ *               layer l, sequence b is at (l * batch + b) * d * P)
+ *   mem_z       device fp32 [L][batch][P]
+ *   mem_in_valid, schedule: as for armt_forward / armt_forward_sequential.
+ * batch == 1 uses the workspace built by armt_create; batch > 1 uses a second
+ * workspace of about batch times that size, allocated on the first call with
+ * that batch size and re-allocated when the batch size changes (the
+ * re-allocation synchronises `stream`; ARMT_ERR_OOM if it does not fit).
+ * Per sequence the results are bit-identical to a batch-1 call with the same
+ * tokens and state, and the diagonal and sequential schedules agree bitwise.
+ * batch <= ARMT_MAX_BATCH and batch * L <= 65535 (ARMT_ERR_SHAPE). */
+ARMT_API armt_status armt_forward_batch(armt_model* m, const int32_t* tokens, int32_t batch,
+                                        int64_t n_tokens, float* hidden_out, float* mem_A,
+                                        float* mem_z, int32_t mem_in_valid, int32_t schedule,
+                                        void* stream);
+
 /* End-to-end variant with HOST buffers (pinned or pageable): copies tokens
  * (and the state when mem_in_valid) to the device, runs `schedule`, copies
  * hidden states and state back, and synchronises `stream` before returning.
@@ -256,7 +291,8 @@ ARMT_API armt_status armt_segment_attention_bf16_noalloc(const void* qkv, void* 
 ARMT_API armt_status armt_lm_head(armt_model* m, const float* hidden, int64_t n_rows,
                                   const void* w_head, float* logits, void* stream);
 
-/* Sizes of the memory state buffers for this model (elements). */
+/* Sizes of the memory state buffers of one sequence (elements); a batch of
+ * B sequences needs B times these. */
 ARMT_API armt_status armt_state_sizes(const armt_model* m, int64_t* a_elems, int64_t* z_elems);
 
 /* Device memory the library holds for this model, in bytes (its own
@@ -266,7 +302,9 @@ ARMT_API armt_status armt_state_sizes(const armt_model* m, int64_t* a_elems, int
  *   workspace       the cell engine's activations and scratch, one slot per
  *                   layer: fixed at armt_create, independent of the number of
  *                   segments (the recurrence's constant-memory property,
- *                   section 一 of the summary page)
+ *                   section 一 of the summary page); plus, once
+ *                   armt_forward_batch has run with batch > 1, the batched
+ *                   workspace for the last batch size used
  *   full_workspace  the full-attention baseline's workspace, 0 until
  *                   armt_forward_full_attention has run; it grows with the
  *                   sequence length

@@ -27,7 +27,7 @@ KERNEL_CLASSES = ("gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down", "attention",
                   "assoc_write", "norm", "other")
 
 EXPORTED = ("armt_create", "armt_destroy", "armt_forward", "armt_forward_sequential",
-            "armt_forward_host", "armt_grouped_gemm_bf16", "armt_segment_attention_bf16",
+            "armt_forward_batch", "armt_forward_host", "armt_grouped_gemm_bf16", "armt_segment_attention_bf16",
             "armt_segment_attention_bf16_noalloc", "armt_forward_full_attention", "armt_state_sizes",
             "armt_memory_bytes", "armt_lm_head", "armt_launch_count",
             "armt_set_profiling", "armt_kernel_times", "armt_sync_status", "armt_status_string",
@@ -77,6 +77,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.armt_destroy.argtypes = [P]
     for fn in (lib.armt_forward, lib.armt_forward_sequential):
         fn.argtypes = [P, P, I64, P, P, P, I32, P]
+    lib.armt_forward_batch.argtypes = [P, P, I32, I64, P, P, P, I32, I32, P]
     lib.armt_forward_host.argtypes = [P, P, I64, P, P, P, I32, I32, P]
     lib.armt_forward_full_attention.argtypes = [P, P, I64, P, P]
     lib.armt_grouped_gemm_bf16.argtypes = [P, P, P, I32, I32, I32, I32, P]
@@ -193,6 +194,29 @@ class Model:
                                 stream=None):
         self.armt_forward(tokens, n_segments, hidden_out, mem_A, mem_z, mem_in_valid, stream,
                           SCHEDULE_SEQUENTIAL)
+
+    def armt_forward_batch(self, tokens, hidden_out, mem_A, mem_z, mem_in_valid=0,
+                           schedule=SCHEDULE_DIAGONAL, stream=None):
+        """tokens int32 [B, N] (device), hidden fp32 [B, N, d], state [L, B, d, P] and [L, B, P]."""
+        B_, N = tokens.shape
+        _check(_lib.armt_forward_batch(self._h, _ptr(tokens), int(B_), int(N), _ptr(hidden_out),
+                                       _ptr(mem_A), _ptr(mem_z), int(mem_in_valid), int(schedule),
+                                       _stream_ptr(stream)), "armt_forward_batch")
+
+    def forward_batch(self, tokens, schedule=SCHEDULE_DIAGONAL, mem_A=None, mem_z=None, stream=None):
+        """Allocates outputs with torch; tokens int32 [B, N] on the device (N any
+        positive count: a short last segment is allowed).  Returns (hidden
+        [B, N, d], A [L, B, d, P], z [L, B, P])."""
+        import torch
+        dev = tokens.device
+        B_, N = tokens.shape
+        L, d, P = self.cfg.n_layers, self.cfg.d_model, self.cfg.phi_dim
+        hidden = torch.empty((B_, N, d), dtype=torch.float32, device=dev)
+        valid = mem_A is not None
+        A = mem_A.clone() if valid else torch.empty((L, B_, d, P), dtype=torch.float32, device=dev)
+        z = mem_z.clone() if valid else torch.empty((L, B_, P), dtype=torch.float32, device=dev)
+        self.armt_forward_batch(tokens, hidden, A, z, 1 if valid else 0, schedule, stream)
+        return hidden, A.view(L, B_, d, P), z.view(L, B_, P)
 
     def armt_forward_host(self, tokens: np.ndarray, n_segments, hidden_out: np.ndarray,
                           mem_A: np.ndarray, mem_z: np.ndarray, mem_in_valid=0,

@@ -172,8 +172,11 @@ struct ModelBase {
     mem.free_all();
   }
   virtual armt_status create(const armt_weights* w, cudaStream_t st) = 0;
-  virtual armt_status forward(const int32_t* tokens, int64_t n, float* hidden, float* A, float* z,
-                              int mem_in_valid, int schedule, cudaStream_t st) = 0;
+  // n_tok tokens per sequence, nb sequences ([nb][n_tok] tokens, [nb][n_tok][d]
+  // hidden states, state [L][nb][d][P] and [L][nb][P]).
+  virtual armt_status forward(const int32_t* tokens, int64_t n_tok, int nb, float* hidden, float* A,
+                              float* z, int mem_in_valid, int schedule, cudaStream_t st) = 0;
+  virtual long long batch_workspace_bytes() const = 0;
   virtual armt_status forward_full(const int32_t* tokens, int64_t T, float* hidden,
                                    cudaStream_t st) = 0;
   virtual long long full_workspace_bytes() const = 0;
@@ -254,19 +257,33 @@ struct Model : ModelBase {
   // weights (library layout)
   WT *embed = nullptr, *memtok = nullptr, *Wqkv = nullptr, *Wo = nullptr, *Wgu = nullptr,
      *Wd = nullptr, *aWq = nullptr, *Ww = nullptr;  // Ww: per layer [Wv_a; Wk_a; wbeta_a; 0]
-  float *g1 = nullptr, *g2 = nullptr, *gf = nullptr, *cosT = nullptr, *sinT = nullptr;
-  // activations, all [layer or slot][rows][width]
-  float *X = nullptr, *Res = nullptr, *Qa = nullptr, *Den = nullptr, *VKB = nullptr,
-        *PhiM = nullptr, *Coef = nullptr, *Cscr = nullptr, *Ssq = nullptr;
+  float *g1 = nullptr, *g2 = nullptr, *gf = nullptr;
   int npart = 0;  // partial sums of squares per row (one per epilogue column tile)
   int nw = 0;  // rows of Ww per layer (d + k + 1 rounded up to the tile width)
-  AT *Xa = nullptr, *Nrm = nullptr, *QKV = nullptr, *Att = nullptr, *U = nullptr, *Phi = nullptr,
-     *Aa = nullptr, *Vt = nullptr;
   int qkv_ld = 0, t_pad = 0;  // row stride of QKV; padded row count of Vt
   int nmax = 0;  // widest GEMM output (fp32 scratch row stride)
-  // tensor maps (bf16 path)
-  CUtensorMap tmXa, tmAWq, tmPhi, tmAa, tmNrm, tmWqkv, tmAtt, tmWo, tmWgu, tmU, tmWd, tmQK, tmVt,
-      tmWw;
+  // weight tensor maps (bf16 path)
+  CUtensorMap tmAWq, tmWqkv, tmWo, tmWgu, tmWd, tmWw;
+  // The cell engine's activations for nb sequences run side by side (a
+  // batch of requests).  With T = S + M rows per cell and R = nb * T rows per
+  // layer, the per-layer tensors are [layer or slot][R][width]: cell b of a
+  // layer owns rows [b T, (b + 1) T), so the weight GEMMs see one R-row
+  // matrix per layer, while the per-(layer, sequence) tensors -- memory state,
+  // attention, write projections -- are addressed as groups l * nb + b of T
+  // rows (the same memory, a finer view).
+  struct Work {
+    int nb = 0;
+    float *X = nullptr, *Res = nullptr, *Qa = nullptr, *Den = nullptr, *VKB = nullptr,
+          *PhiM = nullptr, *Coef = nullptr, *Cscr = nullptr, *Ssq = nullptr, *cosT = nullptr,
+          *sinT = nullptr;
+    AT *Xa = nullptr, *Nrm = nullptr, *QKV = nullptr, *Att = nullptr, *U = nullptr,
+       *Phi = nullptr, *Aa = nullptr, *Vt = nullptr;
+    // row views {width, R, layers}; group views {width, T, layers * nb}
+    CUtensorMap tmXa, tmNrm, tmAtt, tmU, tmXaW, tmPhi, tmAa, tmQK, tmVt;
+  };
+  Work w1;             // one sequence: allocated by armt_create
+  Work wb;             // armt_forward_batch with nb > 1, sized on first use
+  DevAllocs wb_mem;
   size_t upd_smem = 0, feat_smem = 0, attn_smem = 0;
   // full-causal-attention LLaMA over a whole sequence (baseline): one
   // activation slot, grown on demand
@@ -282,8 +299,10 @@ struct Model : ModelBase {
   ~Model() override {
     full_mem.free_all();
     lm_mem.free_all();
+    wb_mem.free_all();
   }
   long long full_workspace_bytes() const override { return full_mem.total; }
+  long long batch_workspace_bytes() const override { return wb_mem.total; }
   int upd_rows_per_block = 32;
 
   armt_status copy_in(void* dst, const void* src, size_t bytes, cudaStream_t st) {
@@ -350,47 +369,23 @@ struct Model : ModelBase {
     CKS(gain_to_f32(&g2, w->norm2, L * d, st));
     CKS(gain_to_f32(&gf, w->norm_f, d, st));
     weight_bytes = mem.total;
-    // RoPE tables (double precision on the host, stored fp32)
-    {
-      std::vector<float> hc(T * (hd / 2)), hs(T * (hd / 2));
-      for (size_t t = 0; t < T; ++t)
-        for (size_t i = 0; i < hd / 2; ++i) {
-          const double ang = (double)t * std::pow(c.rope_base, -2.0 * (double)i / (double)hd);
-          hc[t * (hd / 2) + i] = (float)std::cos(ang);
-          hs[t * (hd / 2) + i] = (float)std::sin(ang);
-        }
-      CKS(mem.alloc_n(&cosT, hc.size()));
-      CKS(mem.alloc_n(&sinT, hs.size()));
-      CK(cudaMemcpy(cosT, hc.data(), hc.size() * 4, cudaMemcpyHostToDevice));
-      CK(cudaMemcpy(sinT, hs.data(), hs.size() * 4, cudaMemcpyHostToDevice));
-    }
-    // activations
-    CKS(mem.alloc_n(&X, (L + 1) * T * d));
-    if (kTC) {
-      CKS(mem.alloc_n(&Xa, (L + 1) * T * d));
-    } else {
-      Xa = reinterpret_cast<AT*>(X);
-    }
-    CKS(mem.alloc_n(&Res, L * T * d));
-    CKS(mem.alloc_n(&Nrm, L * T * d));
-    // bf16: q|k rows in QKV, v transposed into Vt; fp32: q|k|v rows in QKV
     qkv_ld = kTC ? (int)((Hq + Hkv) * hd) : (int)Nq;
     t_pad = (int)((T + 7) / 8 * 8);
-    CKS(mem.alloc_n(&QKV, L * T * (size_t)qkv_ld));
-    if (kTC) CKS(mem.alloc_n(&Vt, L * Hkv * hd * (size_t)t_pad));
-    CKS(mem.alloc_n(&Att, L * T * Hq * hd));
-    CKS(mem.alloc_n(&U, L * T * F));
-    CKS(mem.alloc_n(&Qa, L * T * k));
-    CKS(mem.alloc_n(&Phi, L * T * P));
-    CKS(mem.alloc_n(&Den, L * T));
     npart = (int)(kTC ? d / 128 : d / 32);  // one partial per 128 columns (two epilogue halves)
-    CKS(mem.alloc_n(&Ssq, L * T * (size_t)npart));
-    CKS(mem.alloc_n(&VKB, L * c.n_mem * (size_t)nw));
-    CKS(mem.alloc_n(&PhiM, L * c.n_mem * P));
-    CKS(mem.alloc_n(&Coef, L * c.n_mem * 2));
-    if (kTC) CKS(mem.alloc_n(&Aa, L * d * P));
     nmax = (int)std::max(std::max(Nq, d), std::max(2 * F, std::max(k, (size_t)nw)));
-    if (!kTC) CKS(mem.alloc_n(&Cscr, L * T * (size_t)nmax));
+    if (kTC && ((Hq + Hkv) * hd) % 256 != 0)
+      return fail(ARMT_ERR_UNSUPPORTED, "(Hq + Hkv) * head_dim must be a multiple of 256");
+    if (kTC) {
+      bool ok = true;
+      ok &= encode_tmap_bf16_3d(&tmAWq, aWq, (int)d, (int)k, (int)L, 64);
+      ok &= encode_tmap_bf16_3d(&tmWqkv, Wqkv, (int)d, (int)Nq, (int)L, 256);
+      ok &= encode_tmap_bf16_3d(&tmWo, Wo, (int)(Hq * hd), (int)d, (int)L, 256);
+      ok &= encode_tmap_bf16_3d(&tmWgu, Wgu, (int)d, (int)(2 * F), (int)L, 256);
+      ok &= encode_tmap_bf16_3d(&tmWd, Wd, (int)F, (int)d, (int)L, 256);
+      ok &= encode_tmap_bf16_3d(&tmWw, Ww, (int)d, nw, (int)L, 256);
+      if (!ok) return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    }
+    CKS(alloc_work(w1, 1, mem, st));
     CKS(mem.alloc_n(&d_err, 1));
     CK(cudaMemsetAsync(d_err, 0, sizeof(int), st));
     // kernel configuration
@@ -411,162 +406,250 @@ struct Model : ModelBase {
     else if (hd == 128)
       CK(cudaFuncSetAttribute(attn_simt_kernel<AT, 128>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem));
-    if (kTC && ((Hq + Hkv) * hd) % 256 != 0)
-      return fail(ARMT_ERR_UNSUPPORTED, "(Hq + Hkv) * head_dim must be a multiple of 256");
-    if (kTC) {
-      bool ok = true;
-      ok &= encode_tmap_bf16_3d(&tmXa, Xa, (int)d, (int)T, (int)L + 1, TC_BM);
-      ok &= encode_tmap_bf16_3d(&tmAWq, aWq, (int)d, (int)k, (int)L, 64);
-      ok &= encode_tmap_bf16_3d(&tmPhi, Phi, (int)P, (int)T, (int)L, TC_BM);
-      ok &= encode_tmap_bf16_3d(&tmAa, Aa, (int)P, (int)d, (int)L, 256);
-      ok &= encode_tmap_bf16_3d(&tmNrm, Nrm, (int)d, (int)T, (int)L, TC_BM);
-      ok &= encode_tmap_bf16_3d(&tmWqkv, Wqkv, (int)d, (int)Nq, (int)L, 256);
-      ok &= encode_tmap_bf16_3d(&tmAtt, Att, (int)(Hq * hd), (int)T, (int)L, TC_BM);
-      ok &= encode_tmap_bf16_3d(&tmWo, Wo, (int)(Hq * hd), (int)d, (int)L, 256);
-      ok &= encode_tmap_bf16_3d(&tmWgu, Wgu, (int)d, (int)(2 * F), (int)L, 256);
-      ok &= encode_tmap_bf16_3d(&tmU, U, (int)F, (int)T, (int)L, TC_BM);
-      ok &= encode_tmap_bf16_3d(&tmWd, Wd, (int)F, (int)d, (int)L, 256);
-      ok &= encode_tmap_bf16_3d(&tmQK, QKV, qkv_ld, (int)T, (int)L, 128);
-      ok &= encode_tmap_bf16_3d(&tmVt, Vt, t_pad, (int)hd, (int)(L * Hkv), (int)hd);
-      ok &= encode_tmap_bf16_3d(&tmWw, Ww, (int)d, nw, (int)L, 256);
-      if (!ok) return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    }
     CK(cudaStreamSynchronize(st));
     return ARMT_OK;
   }
 
-  // One grouped GEMM over layers [lo, lo+g): tensor cores for bf16, SIMT +
-  // row epilogue for fp32.  Output rows 0..rows-1 read A rows row0.. of layer
-  // slot (layer + a_slot_off).
+  // Activations for nb sequences per cell, from `pool`.
+  armt_status alloc_work(Work& w, int nb, DevAllocs& pool, cudaStream_t st) {
+    const armt_config& c = cfg;
+    const size_t L = c.n_layers, d = c.d_model, hd = c.head_dim, F = c.ffn_dim, T = rows();
+    const size_t Hq = c.n_q_heads, Hkv = c.n_kv_heads, k = c.key_dim, P = phi_dim();
+    const size_t R = (size_t)nb * T, M = c.n_mem;
+    w = Work();
+    // RoPE tables over the R rows of a layer: row r sits at position r % T
+    // (double precision on the host, stored fp32)
+    {
+      std::vector<float> hc(R * (hd / 2)), hs(R * (hd / 2));
+      for (size_t t = 0; t < T; ++t)
+        for (size_t i = 0; i < hd / 2; ++i) {
+          const double ang = (double)t * std::pow(c.rope_base, -2.0 * (double)i / (double)hd);
+          hc[t * (hd / 2) + i] = (float)std::cos(ang);
+          hs[t * (hd / 2) + i] = (float)std::sin(ang);
+        }
+      for (size_t b = 1; b < (size_t)nb; ++b) {
+        std::copy(hc.begin(), hc.begin() + T * (hd / 2), hc.begin() + b * T * (hd / 2));
+        std::copy(hs.begin(), hs.begin() + T * (hd / 2), hs.begin() + b * T * (hd / 2));
+      }
+      CKS(pool.alloc_n(&w.cosT, hc.size()));
+      CKS(pool.alloc_n(&w.sinT, hs.size()));
+      CK(cudaMemcpy(w.cosT, hc.data(), hc.size() * 4, cudaMemcpyHostToDevice));
+      CK(cudaMemcpy(w.sinT, hs.data(), hs.size() * 4, cudaMemcpyHostToDevice));
+    }
+    CKS(pool.alloc_n(&w.X, (L + 1) * R * d));
+    if (kTC) {
+      CKS(pool.alloc_n(&w.Xa, (L + 1) * R * d));
+    } else {
+      w.Xa = reinterpret_cast<AT*>(w.X);
+    }
+    CKS(pool.alloc_n(&w.Res, L * R * d));
+    CKS(pool.alloc_n(&w.Nrm, L * R * d));
+    // bf16: q|k rows in QKV, v transposed into Vt; fp32: q|k|v rows in QKV
+    CKS(pool.alloc_n(&w.QKV, L * R * (size_t)qkv_ld));
+    if (kTC) CKS(pool.alloc_n(&w.Vt, L * nb * Hkv * hd * (size_t)t_pad));
+    CKS(pool.alloc_n(&w.Att, L * R * Hq * hd));
+    CKS(pool.alloc_n(&w.U, L * R * F));
+    CKS(pool.alloc_n(&w.Qa, L * R * k));
+    CKS(pool.alloc_n(&w.Phi, L * R * P));
+    CKS(pool.alloc_n(&w.Den, L * R));
+    CKS(pool.alloc_n(&w.Ssq, L * R * (size_t)npart));
+    CKS(pool.alloc_n(&w.VKB, L * nb * M * (size_t)nw));
+    CKS(pool.alloc_n(&w.PhiM, L * nb * M * P));
+    CKS(pool.alloc_n(&w.Coef, L * nb * M * 2));
+    if (kTC) CKS(pool.alloc_n(&w.Aa, L * nb * d * P));
+    if (!kTC) CKS(pool.alloc_n(&w.Cscr, L * R * (size_t)nmax));
+    if (kTC) {
+      const int iR = (int)R, iT = (int)T, iL = (int)L, G = (int)L * nb;
+      bool ok = true;
+      ok &= encode_tmap_bf16_3d(&w.tmXa, w.Xa, (int)d, iR, iL + 1, TC_BM);
+      ok &= encode_tmap_bf16_3d(&w.tmNrm, w.Nrm, (int)d, iR, iL, TC_BM);
+      ok &= encode_tmap_bf16_3d(&w.tmAtt, w.Att, (int)(Hq * hd), iR, iL, TC_BM);
+      ok &= encode_tmap_bf16_3d(&w.tmU, w.U, (int)F, iR, iL, TC_BM);
+      ok &= encode_tmap_bf16_3d(&w.tmXaW, w.Xa, (int)d, iT, (iL + 1) * nb, TC_BM);
+      ok &= encode_tmap_bf16_3d(&w.tmPhi, w.Phi, (int)P, iT, G, TC_BM);
+      ok &= encode_tmap_bf16_3d(&w.tmAa, w.Aa, (int)P, (int)d, G, 256);
+      ok &= encode_tmap_bf16_3d(&w.tmQK, w.QKV, qkv_ld, iT, G, 128);
+      ok &= encode_tmap_bf16_3d(&w.tmVt, w.Vt, t_pad, (int)hd, G * (int)Hkv, (int)hd);
+      if (!ok) return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    }
+    (void)st;
+    w.nb = nb;
+    return ARMT_OK;
+  }
+
+  // The batched workspace for exactly nb sequences (re-sized when nb changes).
+  armt_status ensure_batch(int nb, cudaStream_t st) {
+    if (wb.nb == nb) return ARMT_OK;
+    CK(cudaStreamSynchronize(st));
+    wb_mem.free_all();
+    wb = Work();
+    armt_status s = alloc_work(wb, nb, wb_mem, st);
+    if (s != ARMT_OK) {
+      wb_mem.free_all();
+      wb = Work();
+    }
+    return s;
+  }
+
+  // One grouped GEMM over groups [lo, lo+g): tensor cores for bf16, SIMT +
+  // row epilogue for fp32.  `rows` output rows per group; `map` places each
+  // group's A rows and B slot (GemmGroupMap).  The fp32 path stages raw
+  // products in w.Cscr.
   template <int BN, class Epi, int EPI_WG = 1>
-  armt_status gemm(int cls, const CUtensorMap& ta, const CUtensorMap& tb, const AT* a, long long a_gs,
-                   const WT* b, int N, int K, const Epi& epi, int lo, int g, cudaStream_t st,
-                   int rows = -1, int row0 = 0, int a_slot_off = 0) {
-    if (rows < 0) rows = this->rows();
+  armt_status gemm(int cls, Work& w, const CUtensorMap& ta, const CUtensorMap& tb, const AT* a,
+                   long long a_gs, const WT* b, int N, int K, const Epi& epi, int lo, int g,
+                   cudaStream_t st, int rows, const GemmGroupMap& map = GemmGroupMap()) {
     CKS(prof_begin(cls, st));
     if constexpr (kTC) {
-      CK((launch_gemm_tc<Epi, BN, EPI_WG>(ta, tb, rows, N, K, lo, g, d_err, epi, num_sms, st, row0,
-                                          a_slot_off)));
+      CK((launch_gemm_tc<Epi, BN, EPI_WG>(ta, tb, rows, N, K, lo, g, d_err, epi, num_sms, st, map)));
     } else {
-      const float* a0 = reinterpret_cast<const float*>(a) + a_slot_off * a_gs + (long long)row0 * K;
+      const SimtAMap am{map.row0, map.a_slot_off, map.b_div, map.alt_lo, map.alt_hi, map.alt_row0};
+      const float* b0 = reinterpret_cast<const float*>(b) + (long long)map.b_slot_off * N * K;
       dim3 grid((N + 63) / 64, (rows + 63) / 64, g);
-      gemm_simt_f32_kernel<<<grid, 256, 0, st>>>(a0, a_gs, K, reinterpret_cast<const float*>(b),
-                                                 (long long)N * K, Cscr,
-                                                 (long long)this->rows() * nmax, nmax, rows, N, K, lo);
+      gemm_simt_f32_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float*>(a), a_gs, K, b0,
+                                                 (long long)N * K, w.Cscr, (long long)rows * nmax,
+                                                 nmax, rows, N, K, lo, am);
       CK(cudaGetLastError());
-      epi_rows_kernel<Epi><<<dim3(rows, g), 128, 0, st>>>(Cscr, (long long)this->rows() * nmax, nmax,
-                                                          N, lo, epi);
+      epi_rows_kernel<Epi><<<dim3(rows, g), 128, 0, st>>>(w.Cscr, (long long)rows * nmax, nmax, N,
+                                                          lo, epi);
       CK(cudaGetLastError());
     }
     CKS(prof_end(st));
     return ARMT_OK;
   }
 
-  // All kernels of one grouped step over layers [lo, hi].  seg0: segment of
-  // the layer-0 cell (when lo == 0); segL: segment of the last-layer cell
-  // (when hi == L-1).
-  armt_status step(int lo, int hi, int64_t seg0, int64_t segL, const int32_t* tokens, float* hidden,
-                   float* A, float* z, cudaStream_t st) {
+  // All kernels of one grouped step: the cells (l, s_lo - (l - lo)) for l in
+  // [lo, hi], each for the w.nb sequences of the batch.  The sequences hold
+  // n_tok tokens each (n_seg segments; the last one may be short).
+  armt_status step(Work& w, int lo, int hi, int64_t s_lo, const int32_t* tokens, int64_t n_tok,
+                   int64_t n_seg, float* hidden, float* A, float* z, cudaStream_t st) {
     const armt_config& c = cfg;
     const int L = c.n_layers, d = c.d_model, hd = c.head_dim, F = c.ffn_dim, T = rows();
     const int Hq = c.n_q_heads, Hkv = c.n_kv_heads, k = c.key_dim, P = phi_dim(), M = c.n_mem;
     const int S = c.seg_len, Nq = n_qkv();
-    const int g = hi - lo + 1;
-    const long long Td = (long long)T * d;
+    const int g = hi - lo + 1, nb = w.nb, R = nb * T;
+    const long long Rd = (long long)R * d;
+    // the last segment holds last_len <= S tokens; its memory rows follow them
+    const int last_len = (int)(n_tok - (n_seg - 1) * S);
+    const int64_t l_last = lo + (s_lo - (n_seg - 1));  // layer of the last segment's cell
+    const bool short_here = last_len < S && l_last >= lo && l_last <= hi;
     if (lo == 0) {
+      const int n_rows = s_lo == n_seg - 1 ? last_len : S;
       CKS(prof_begin(ARMT_KC_OTHER, st));
-      embed_gather_kernel<WT><<<T, 256, 0, st>>>(tokens + seg0 * S, embed, memtok, X, Xa, S, d,
-                                                 c.vocab);
+      embed_gather_kernel<WT><<<dim3(T, nb), 256, 0, st>>>(tokens + s_lo * S, n_tok, embed, memtok,
+                                                           w.X, w.Xa, T, n_rows, M, d, c.vocab);
       CK(cudaGetLastError());
       CKS(prof_end(st));
     }
     // associative read: q = Wq_a x, phi, den, then x' = x + A phi / den
-    CKS((gemm<64>(ARMT_KC_ASSOC_READ, tmXa, tmAWq, Xa, Td, aWq, k, d,
-                  FStore{Qa, (long long)k, (long long)T * k}, lo, g, st)));
+    CKS((gemm<64>(ARMT_KC_ASSOC_READ, w, w.tmXa, tmAWq, w.Xa, Rd, aWq, k, d,
+                  FStore{w.Qa, (long long)k, (long long)R * k}, lo, g, st, R)));
     CKS(prof_begin(ARMT_KC_ASSOC_READ, st));
-    assoc_phi_kernel<AT><<<dim3(T, g), 128, 2 * k * sizeof(float), st>>>(Qa, z, Phi, Den, T, k,
-                                                                        c.dpfp_nu, c.assoc_eps, lo);
+    assoc_phi_kernel<AT><<<dim3(R, g), 128, 2 * k * sizeof(float), st>>>(
+        w.Qa, z, w.Phi, w.Den, R, k, c.dpfp_nu, c.assoc_eps, lo, T, nb);
     CK(cudaGetLastError());
     CKS(prof_end(st));
-    const AT* Asrc = kTC ? Aa : reinterpret_cast<const AT*>(A);
-    const RowNormIn norm_in{Ssq, npart, 1.0f / (float)d, c.norm_eps};
-    CKS((gemm<256, FRead, 2>(ARMT_KC_ASSOC_READ, tmPhi, tmAa, Phi, (long long)T * P,
-                             reinterpret_cast<const WT*>(Asrc), d, P,
-                             FRead{X, Den, Res, T, d, RowNormOut<AT>{g1, Nrm, Ssq}}, lo, g, st)));
+    // the read GEMM runs per (layer, sequence): groups lo*nb .. (hi+1)*nb - 1
+    // of T rows, each with its own state
+    const AT* Asrc = kTC ? w.Aa : reinterpret_cast<const AT*>(A);
+    const RowNormIn norm_in{w.Ssq, npart, 1.0f / (float)d, c.norm_eps};
+    {
+      RowNormOut<AT> n1{g1, w.Nrm, w.Ssq};
+      n1.gdiv = nb;
+      CKS((gemm<256, FRead, 2>(ARMT_KC_ASSOC_READ, w, w.tmPhi, w.tmAa, w.Phi, (long long)T * P,
+                               reinterpret_cast<const WT*>(Asrc), d, P,
+                               FRead{w.X, w.Den, w.Res, T, d, n1}, lo * nb, g * nb, st, T)));
+    }
     // attention sub-layer (RMSNorm 1 completes in the QKV epilogue)
-    CKS((gemm<256, FQkv, 1>(ARMT_KC_GEMM_QKV, tmNrm, tmWqkv, Nrm, Td, Wqkv, Nq, d,
-                   FQkv{QKV, cosT, sinT, T, hd, (Hq + Hkv) * hd, qkv_ld, Vt, Hkv, t_pad,
-                                  norm_in},
-                   lo, g, st)));
+    CKS((gemm<256, FQkv, 1>(ARMT_KC_GEMM_QKV, w, w.tmNrm, tmWqkv, w.Nrm, Rd, Wqkv, Nq, d,
+                            FQkv{w.QKV, w.cosT, w.sinT, R, hd, (Hq + Hkv) * hd, qkv_ld, w.Vt, Hkv,
+                                 t_pad, norm_in, T, nb},
+                            lo, g, st, R)));
     CKS(prof_begin(ARMT_KC_ATTENTION, st));
     if constexpr (kTC) {
       AttnArgs aa;
-      aa.out = Att;
+      aa.out = w.Att;
       aa.T = T;
       aa.Hq = Hq;
       aa.Hkv = Hkv;
-      aa.g_first = lo;
+      aa.g_first = lo * nb;
       aa.n_qtiles = (T + 127) / 128;
       aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
       aa.err = d_err;
       if (hd == 64)
-        CK(launch_attn_tc<64>(tmQK, tmVt, aa, g, num_sms, st));
+        CK(launch_attn_tc<64>(w.tmQK, w.tmVt, aa, g * nb, num_sms, st));
       else
-        CK(launch_attn_tc<128>(tmQK, tmVt, aa, g, num_sms, st));
+        CK(launch_attn_tc<128>(w.tmQK, w.tmVt, aa, g * nb, num_sms, st));
     } else {
-      dim3 grid((T + 63) / 64, Hq, g);
+      dim3 grid((T + 63) / 64, Hq, g * nb);
       const float scale = 1.0f / sqrtf((float)hd);
       if (hd == 64)
-        attn_simt_kernel<AT, 64><<<grid, 256, attn_smem, st>>>(QKV, Att, T, Hq, Hkv, scale, lo);
+        attn_simt_kernel<AT, 64><<<grid, 256, attn_smem, st>>>(w.QKV, w.Att, T, Hq, Hkv, scale, lo * nb);
       else if (hd == 128)
-        attn_simt_kernel<AT, 128><<<grid, 256, attn_smem, st>>>(QKV, Att, T, Hq, Hkv, scale, lo);
+        attn_simt_kernel<AT, 128><<<grid, 256, attn_smem, st>>>(w.QKV, w.Att, T, Hq, Hkv, scale, lo * nb);
       else
-        attn_simt_kernel<AT, 32><<<grid, 256, attn_smem, st>>>(QKV, Att, T, Hq, Hkv, scale, lo);
+        attn_simt_kernel<AT, 32><<<grid, 256, attn_smem, st>>>(w.QKV, w.Att, T, Hq, Hkv, scale, lo * nb);
       CK(cudaGetLastError());
     }
     CKS(prof_end(st));
-    CKS((gemm<256, FRes, 2>(ARMT_KC_GEMM_O, tmAtt, tmWo, Att, (long long)T * Hq * hd, Wo, d, Hq * hd,
-                   FRes{Res, Res, nullptr, T, d, 0, RowNormOut<AT>{g2, Nrm, Ssq}}, lo, g,
-                   st)));
+    CKS((gemm<256, FRes, 2>(ARMT_KC_GEMM_O, w, w.tmAtt, tmWo, w.Att, (long long)R * Hq * hd, Wo, d,
+                            Hq * hd, FRes{w.Res, w.Res, nullptr, R, d, 0, RowNormOut<AT>{g2, w.Nrm, w.Ssq}},
+                            lo, g, st, R)));
     // MLP sub-layer (RMSNorm 2 completes in the gate-up epilogue)
-    CKS((gemm<256>(ARMT_KC_GEMM_GATEUP, tmNrm, tmWgu, Nrm, Td, Wgu, 2 * F, d,
-                   FSwi{U, T, F, norm_in}, lo, g, st)));
-    CKS((gemm<256>(ARMT_KC_GEMM_DOWN, tmU, tmWd, U, (long long)T * F, Wd, d, F,
-                   FRes{Res, X, kTC ? Xa : nullptr, T, d, 1,
-                                   RowNormOut<AT>{nullptr, nullptr, nullptr}},
-                   lo, g, st)));
+    CKS((gemm<256>(ARMT_KC_GEMM_GATEUP, w, w.tmNrm, tmWgu, w.Nrm, Rd, Wgu, 2 * F, d,
+                   FSwi{w.U, R, F, norm_in}, lo, g, st, R)));
+    CKS((gemm<256>(ARMT_KC_GEMM_DOWN, w, w.tmU, tmWd, w.U, (long long)R * F, Wd, d, F,
+                   FRes{w.Res, w.X, kTC ? w.Xa : nullptr, R, d, 1,
+                        RowNormOut<AT>{nullptr, nullptr, nullptr}},
+                   lo, g, st, R)));
     // delta-rule write from the memory-token rows of this layer's output:
-    // [v | k | beta] = h_mem [Wv_a; Wk_a; wbeta_a]^T on the tensor cores (A =
-    // rows S..S+M-1 of layer slot l+1), then the normaliser recurrence and
-    // the row-wise update of A.
-    CKS((gemm<256>(ARMT_KC_ASSOC_WRITE, tmXa, tmWw, Xa, Td, Ww, nw, d,
-                   FStore{VKB, (long long)nw, (long long)M * nw}, lo, g, st, M, S, 1)));
+    // [v | k | beta] = h_mem [Wv_a; Wk_a; wbeta_a]^T on the tensor cores, per
+    // (layer, sequence) group: A = the M memory rows of the cell in layer
+    // slot l + 1 (rows S..S+M-1, or last_len.. after a short last segment),
+    // B = layer l's projections.  Then the normaliser recurrence and the
+    // row-wise update of A.
+    {
+      GemmGroupMap wm;
+      wm.row0 = S;
+      wm.a_slot_off = nb;
+      wm.b_div = nb;
+      if (short_here) {
+        wm.alt_lo = (int)l_last * nb;
+        wm.alt_hi = (int)(l_last + 1) * nb;
+        wm.alt_row0 = last_len;
+      }
+      CKS((gemm<256>(ARMT_KC_ASSOC_WRITE, w, w.tmXaW, tmWw, w.Xa, (long long)T * d, Ww, nw, d,
+                     FStore{w.VKB, (long long)nw, (long long)M * nw}, lo * nb, g * nb, st, M, wm)));
+    }
     CKS(prof_begin(ARMT_KC_ASSOC_WRITE, st));
-    assoc_write_feat_kernel<<<g, 256, feat_smem, st>>>(VKB, z, PhiM, Coef, M, k, c.dpfp_nu,
-                                                       c.assoc_eps, d, nw, lo);
+    assoc_write_feat_kernel<<<g * nb, 256, feat_smem, st>>>(w.VKB, z, w.PhiM, w.Coef, M, k, c.dpfp_nu,
+                                                            c.assoc_eps, d, nw, lo * nb);
     CK(cudaGetLastError());
     CKS(prof_end(st));
     CKS(prof_begin(ARMT_KC_ASSOC_WRITE, st));
     {
-      dim3 grid((d + upd_rows_per_block - 1) / upd_rows_per_block, g);
-      AT* Adst = kTC ? Aa : reinterpret_cast<AT*>(A);
+      dim3 grid((d + upd_rows_per_block - 1) / upd_rows_per_block, g * nb);
+      AT* Adst = kTC ? w.Aa : reinterpret_cast<AT*>(A);
+      const int gf0 = lo * nb;
       if (P == 96)
-        assoc_write_update_kernel<AT, 3><<<grid, 128, upd_smem, st>>>(VKB, nw, PhiM, Coef, A, Adst, M,
-                                                                      d, upd_rows_per_block, lo);
+        assoc_write_update_kernel<AT, 3><<<grid, 128, upd_smem, st>>>(w.VKB, nw, w.PhiM, w.Coef, A, Adst,
+                                                                      M, d, upd_rows_per_block, gf0);
       else if (P == 192)
-        assoc_write_update_kernel<AT, 6><<<grid, 128, upd_smem, st>>>(VKB, nw, PhiM, Coef, A, Adst, M,
-                                                                      d, upd_rows_per_block, lo);
+        assoc_write_update_kernel<AT, 6><<<grid, 128, upd_smem, st>>>(w.VKB, nw, w.PhiM, w.Coef, A, Adst,
+                                                                      M, d, upd_rows_per_block, gf0);
       else
-        assoc_write_update_kernel<AT, 12><<<grid, 128, upd_smem, st>>>(VKB, nw, PhiM, Coef, A, Adst, M,
-                                                                       d, upd_rows_per_block, lo);
+        assoc_write_update_kernel<AT, 12><<<grid, 128, upd_smem, st>>>(w.VKB, nw, w.PhiM, w.Coef, A, Adst,
+                                                                       M, d, upd_rows_per_block, gf0);
       CK(cudaGetLastError());
     }
     CKS(prof_end(st));
     if (hi == L - 1) {
+      const int64_t segL = s_lo - (hi - lo);
+      const int n_rows = segL == n_seg - 1 ? last_len : S;
       CKS(prof_begin(ARMT_KC_NORM, st));
-      rmsnorm_kernel<float><<<dim3(S, 1), 256, 0, st>>>(X + (long long)L * Td, 0, gf, 0,
-                                                        hidden + segL * S * (long long)d, 0, d,
-                                                        c.norm_eps, 0);
+      rmsnorm_kernel<float><<<dim3(n_rows, nb), 256, 0, st>>>(
+          w.X + (long long)L * Rd, (long long)T * d, gf, 0, hidden + segL * S * (long long)d,
+          n_tok * (long long)d, d, c.norm_eps, 0);
       CK(cudaGetLastError());
       CKS(prof_end(st));
     }
@@ -647,12 +730,19 @@ struct Model : ModelBase {
         dim3 grid((V + 63) / 64, (rows_c + 63) / 64, 1);
         gemm_simt_f32_kernel<<<grid, 256, 0, st>>>(hidden + r0 * d, 0, d,
                                                    reinterpret_cast<const float*>(head), 0,
-                                                   logits + r0 * V, 0, V, rows_c, V, d, 0);
+                                                   logits + r0 * V, 0, V, rows_c, V, d, 0,
+                                                   SimtAMap{0, 0, 1, 0, 0, 0});
         CK(cudaGetLastError());
       }
     }
     CKS(prof_end(st));
     return ARMT_OK;
+  }
+
+  static GemmGroupMap layer_map(int l) {
+    GemmGroupMap m;
+    m.b_slot_off = l;
+    return m;
   }
 
   armt_status forward_full(const int32_t* tokens, int64_t T64, float* hidden,
@@ -668,7 +758,8 @@ struct Model : ModelBase {
       const int tp = (T + 7) / 8 * 8;
       const long long Td = (long long)T * d;
       CKS(prof_begin(ARMT_KC_OTHER, st));
-      embed_gather_kernel<WT><<<T, 256, 0, st>>>(tokens, embed, memtok, Xf, (WT*)nullptr, T, d, c.vocab);
+      embed_gather_kernel<WT><<<dim3(T, 1), 256, 0, st>>>(tokens, 0, embed, memtok, Xf, (WT*)nullptr, T, T, 0,
+                                                         d, c.vocab);
       CK(cudaGetLastError());
       CKS(prof_end(st));
       const RowNormIn no_scale{nullptr, 0, 0.f, 0.f};
@@ -682,8 +773,8 @@ struct Model : ModelBase {
         CKS(prof_begin(ARMT_KC_GEMM_QKV, st));
         CK((launch_gemm_tc<FQkv, 256, 1>(tmNrmf, tmWqkv, T, Nq, d, 0, 1, d_err,
                                       FQkv{QKVf, cosF, sinF, T, hd, (Hq + Hkv) * hd, (Hq + Hkv) * hd,
-                                           Vtf, Hkv, tp, no_scale},
-                                      num_sms, st, 0, 0, l)));
+                                           Vtf, Hkv, tp, no_scale, T, 1},
+                                      num_sms, st, layer_map(l))));
         CKS(prof_end(st));
         CKS(prof_begin(ARMT_KC_ATTENTION, st));
         {
@@ -706,17 +797,17 @@ struct Model : ModelBase {
         CK((launch_gemm_tc<FRes, 256, 2>(tmAttf, tmWo, T, d, Hq * hd, 0, 1, d_err,
                                       FRes{Xf, Resf, nullptr, T, d, 0,
                                            RowNormOut<AT>{g2 + (long long)l * d, Nrmf, Ssqf}},
-                                      num_sms, st, 0, 0, l)));
+                                      num_sms, st, layer_map(l))));
         CKS(prof_end(st));
         CKS(prof_begin(ARMT_KC_GEMM_GATEUP, st));
         CK((launch_gemm_tc<FSwi, 256>(tmNrmf, tmWgu, T, 2 * F, d, 0, 1, d_err, FSwi{Uf, T, F, norm_in},
-                                      num_sms, st, 0, 0, l)));
+                                      num_sms, st, layer_map(l))));
         CKS(prof_end(st));
         CKS(prof_begin(ARMT_KC_GEMM_DOWN, st));
         CK((launch_gemm_tc<FRes, 256>(tmUf, tmWd, T, d, F, 0, 1, d_err,
                                       FRes{Resf, Xf, nullptr, T, d, 0,
                                            RowNormOut<AT>{nullptr, nullptr, nullptr}},
-                                      num_sms, st, 0, 0, l)));
+                                      num_sms, st, layer_map(l))));
         CKS(prof_end(st));
       }
       CKS(prof_begin(ARMT_KC_NORM, st));
@@ -728,17 +819,20 @@ struct Model : ModelBase {
     }
   }
 
-  armt_status forward(const int32_t* tokens, int64_t n, float* hidden, float* A, float* z,
-                      int mem_in_valid, int schedule, cudaStream_t st) override {
-    const int L = cfg.n_layers, d = cfg.d_model, P = phi_dim();
-    const size_t a_n = (size_t)L * d * P, z_n = (size_t)L * P;
+  armt_status forward(const int32_t* tokens, int64_t n_tok, int nb, float* hidden, float* A,
+                      float* z, int mem_in_valid, int schedule, cudaStream_t st) override {
+    const int L = cfg.n_layers, d = cfg.d_model, P = phi_dim(), S = cfg.seg_len;
+    const int64_t n = (n_tok + S - 1) / S;
+    if (nb > 1) CKS(ensure_batch(nb, st));
+    Work& w = nb == 1 ? w1 : wb;
+    const size_t a_n = (size_t)L * nb * d * P, z_n = (size_t)L * nb * P;
     if (!mem_in_valid) {
       CK(cudaMemsetAsync(A, 0, a_n * sizeof(float), st));
       CK(cudaMemsetAsync(z, 0, z_n * sizeof(float), st));
-      if (kTC) CK(cudaMemsetAsync(Aa, 0, a_n * sizeof(AT), st));
+      if (kTC) CK(cudaMemsetAsync(w.Aa, 0, a_n * sizeof(AT), st));
     } else if (kTC) {
       CKS(prof_begin(ARMT_KC_OTHER, st));
-      convert_state_kernel<AT><<<4 * num_sms, 256, 0, st>>>(A, Aa, (long long)a_n);
+      convert_state_kernel<AT><<<4 * num_sms, 256, 0, st>>>(A, w.Aa, (long long)a_n);
       CK(cudaGetLastError());
       CKS(prof_end(st));
     }
@@ -746,11 +840,11 @@ struct Model : ModelBase {
       for (int64_t i = 0; i < L + n - 1; ++i) {
         const int lo = (int)(i - n + 1 > 0 ? i - n + 1 : 0);
         const int hi = (int)(i < L - 1 ? i : L - 1);
-        CKS(step(lo, hi, i, i - (L - 1), tokens, hidden, A, z, st));
+        CKS(step(w, lo, hi, i - lo, tokens, n_tok, n, hidden, A, z, st));
       }
     } else {
       for (int64_t s = 0; s < n; ++s)
-        for (int l = 0; l < L; ++l) CKS(step(l, l, s, s, tokens, hidden, A, z, st));
+        for (int l = 0; l < L; ++l) CKS(step(w, l, l, s, tokens, n_tok, n, hidden, A, z, st));
     }
     return ARMT_OK;
   }
@@ -880,7 +974,24 @@ static armt_status forward_common(armt_model* m, const int32_t* tokens, int64_t 
   if (n <= 0) return fail(ARMT_ERR_ARG, "n_segments must be positive");
   if (mem_in_valid != 0 && mem_in_valid != 1) return fail(ARMT_ERR_ARG, "mem_in_valid must be 0 or 1");
   if (n > ((int64_t)1 << 24)) return fail(ARMT_ERR_SHAPE, "n_segments too large");
-  return m->impl->forward(tokens, n, hidden, A, z, mem_in_valid, schedule,
+  return m->impl->forward(tokens, n * m->impl->cfg.seg_len, 1, hidden, A, z, mem_in_valid, schedule,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+armt_status armt_forward_batch(armt_model* m, const int32_t* tokens, int32_t batch, int64_t n_tokens,
+                               float* hidden_out, float* mem_A, float* mem_z, int32_t mem_in_valid,
+                               int32_t schedule, void* stream) {
+  if (m == nullptr || tokens == nullptr || hidden_out == nullptr || mem_A == nullptr || mem_z == nullptr)
+    return fail(ARMT_ERR_ARG, "NULL argument");
+  if (batch <= 0 || n_tokens <= 0) return fail(ARMT_ERR_ARG, "batch and n_tokens must be positive");
+  if (mem_in_valid != 0 && mem_in_valid != 1) return fail(ARMT_ERR_ARG, "mem_in_valid must be 0 or 1");
+  if (schedule != ARMT_SCHEDULE_DIAGONAL && schedule != ARMT_SCHEDULE_SEQUENTIAL)
+    return fail(ARMT_ERR_ARG, "unknown schedule");
+  const armt_config& c = m->impl->cfg;
+  if (n_tokens > ((int64_t)1 << 24) * c.seg_len) return fail(ARMT_ERR_SHAPE, "n_tokens too large");
+  if (batch > ARMT_MAX_BATCH || (int64_t)batch * c.n_layers > 65535)
+    return fail(ARMT_ERR_SHAPE, "batch > ARMT_MAX_BATCH or batch * n_layers > 65535");
+  return m->impl->forward(tokens, n_tokens, batch, hidden_out, mem_A, mem_z, mem_in_valid, schedule,
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -1038,7 +1149,7 @@ armt_status armt_memory_bytes(const armt_model* m, int64_t* weights, int64_t* wo
   if (m == nullptr) return fail(ARMT_ERR_ARG, "NULL model");
   const ModelBase& b = *m->impl;
   if (weights) *weights = b.weight_bytes;
-  if (workspace) *workspace = b.mem.total - b.weight_bytes;
+  if (workspace) *workspace = b.mem.total - b.weight_bytes + b.batch_workspace_bytes();
   if (full_workspace) *full_workspace = b.full_workspace_bytes();
   return ARMT_OK;
 }

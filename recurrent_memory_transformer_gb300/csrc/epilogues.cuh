@@ -95,14 +95,15 @@ struct RowNormIn {
 template <typename AT>
 struct RowNormOut {
   const float* gain;  // [L][d] stacked gains, or nullptr (no norm output)
-  AT* out;            // [L][rows][d] gain-weighted row
-  float* ssq;         // [L][rows][npart]
+  AT* out;            // [groups][rows][d] gain-weighted row
+  float* ssq;         // [groups][rows][npart]
+  int gdiv = 1;       // group g uses the gains of layer g / gdiv
   // v: 32 fp32 values of row `row` at columns col..col+31 (col0 = start of
   // this call's columns; the call's partial index is col0 / ncols).
   __device__ __forceinline__ void put(int l, int rows, int d, int row, int col, const float* v,
                                       float& acc) const {
     float w[32];
-    const float* g = gain + (long long)l * d + col;
+    const float* g = gain + (long long)(l / gdiv) * d + col;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       w[i] = v[i] * g[i];
@@ -179,7 +180,9 @@ struct EpiAssocRead {
 // q and k go to `out` (row stride `ld`); v goes to `out` too when vt is null
 // (fp32 path), else transposed into vt[l][g][c][t] (row stride t_pad) so the
 // tensor-core attention reads it K-major.  cos/sin tables are [rows][hd/2]
-// (position = row within the cell).
+// (the position of each row within its cell).  With nb sequences per layer
+// the rows of a layer are nb cells of cell_rows rows; cell b of layer l
+// keeps its values at vt[l * nb + b].
 template <typename OutT>
 struct EpiQkvRope {
   static constexpr int GROUP = 64;  // callers pass whole heads (ncols a multiple of hd)
@@ -190,6 +193,7 @@ struct EpiQkvRope {
   OutT* vt;                         // nullptr: v stays in `out`
   int n_kv, t_pad;
   RowNormIn norm;                   // RMSNorm 1 row scale
+  int cell_rows = 0, nb = 1;        // rows per cell, cells per layer (rows = nb * cell_rows)
 
   template <int CH, class Src>
   __device__ __forceinline__ void rope_chunk(int l, int row, bool valid, int hcol, int h0, int i0,
@@ -217,7 +221,8 @@ struct EpiQkvRope {
       }
     } else if (vt != nullptr) {
       const int g = (hcol - n_rope_cols) / hd;
-      OutT* col0 = vt + ((long long)(l * n_kv + g) * hd) * t_pad + row;
+      const int b = nb > 1 ? row / cell_rows : 0;
+      OutT* col0 = vt + ((long long)((l * nb + b) * n_kv + g) * hd) * t_pad + (row - b * cell_rows);
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
         st_from_f32(col0 + (long long)(i0 + i) * t_pad, x1[i]);

@@ -167,7 +167,7 @@ struct SEpiAssocRead {
   }
   __device__ __forceinline__ void process(int l, int row0, int rows_, int colA, int colB,
                                           const float* stage, float ctx, float* rowsum) const {
-    const float4 g = lane_gain4(norm.gain, l, d, colA, colB);
+    const float4 g = lane_gain4(norm.gain, l / norm.gdiv, d, colA, colB);
     staged_rows_elementwise(stage, row0, rows_, colA, colB, ctx,
                             [&](int row, int col) { return ld4(x + ((long long)l * rows + row) * d + col); },
                             [&](int row, int col, float4 v, float4 xv, float inv) {
@@ -198,7 +198,7 @@ struct SEpiResidual {
   __device__ float row_ctx(int, int, bool) const { return 0.f; }
   __device__ __forceinline__ void process(int l, int row0, int rows_, int colA, int colB,
                                           const float* stage, float, float* rowsum) const {
-    const float4 g = norm.gain != nullptr ? lane_gain4(norm.gain, l, n, colA, colB)
+    const float4 g = norm.gain != nullptr ? lane_gain4(norm.gain, l / norm.gdiv, n, colA, colB)
                                           : make_float4(0.f, 0.f, 0.f, 0.f);
     staged_rows_elementwise(stage, row0, rows_, colA, colB, 0.f,
                             [&](int row, int col) { return ld4(res + ((long long)l * rows + row) * n + col); },
@@ -230,6 +230,7 @@ struct SEpiQkvRope {
   OutT* vt;
   int n_kv, t_pad;
   RowNormIn norm;
+  int cell_rows = 0, nb = 1;
   // unit u: 32 rotation pairs (i0 + i, i0 + i + hd/2) of one head
   __device__ void unit_hd(int u, int& a, int& b) const {
     const int half = hd >> 1, per_head = half / 32;
@@ -241,7 +242,8 @@ struct SEpiQkvRope {
   __device__ bool direct_tile(int col0) const { return col0 >= n_rope_cols; }
   template <class Src>
   __device__ void direct(int l, int row, bool valid, int col0, int ncols, Src& src) const {
-    EpiQkvRope<OutT> e{out, cosT, sinT, rows, hd, n_rope_cols, ld, vt, n_kv, t_pad, norm};
+    EpiQkvRope<OutT> e{out, cosT, sinT, rows, hd, n_rope_cols, ld, vt, n_kv, t_pad, norm,
+                       cell_rows, nb};
     e(l, row, valid, col0, ncols, src);
   }
   __device__ float row_ctx(int l, int row, bool ok) const {

@@ -34,11 +34,21 @@ namespace armt {
 constexpr int TC_BM = 128;
 constexpr int TC_BK = 64;  // one 128-byte swizzle row of bf16
 
+// How a group index gi of a launch addresses its operands:
+//   A rows  [r0, r0 + rows) of A slot gi + a_slot_off, with r0 = alt_row0
+//           for gi in [alt_lo, alt_hi) and row0 otherwise (a cell whose
+//           memory rows sit elsewhere, e.g. after a short last segment);
+//   B       slot gi / b_div + b_slot_off (b_div = sequences per layer when
+//           the groups are (layer, sequence) pairs sharing a layer's weights).
+struct GemmGroupMap {
+  int row0 = 0, a_slot_off = 0, b_slot_off = 0, b_div = 1;
+  int alt_lo = 0, alt_hi = 0, alt_row0 = 0;
+  __host__ __device__ int a_row0(int gi) const { return gi >= alt_lo && gi < alt_hi ? alt_row0 : row0; }
+};
+
 struct GemmTcShape {
-  int rows;       // valid rows per group (M), counted from row0
-  int row0;       // first A row read (TMA row coordinate of output row 0)
-  int a_slot_off; // A is read from layer slot (layer + a_slot_off)
-  int b_slot_off; // B (weights) from layer slot (layer + b_slot_off)
+  int rows;       // valid rows per group (M), counted from the group's first A row
+  GemmGroupMap map;
   int N, K;
   int g_first, g_count;
   int m_tiles, n_tiles, k_blocks;
@@ -111,16 +121,17 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
         const int g = t / tiles_per_g, r = t - g * tiles_per_g;
         const int nt = r / sh.m_tiles, mt = r - nt * sh.m_tiles;
         const int layer = sh.g_first + g;
+        const int a_row = sh.map.a_row0(layer) + mt * TC_BM;
+        const int b_slot = layer / sh.map.b_div + sh.map.b_slot_off;
         for (int kb = 0; kb < sh.k_blocks; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, sh.err, DEV_TIMEOUT_EMPTY)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_3d(sA + stage * C::A_BYTES, &tmA, kb * TC_BK, sh.row0 + mt * TC_BM,
-                      layer + sh.a_slot_off, &full[stage]);
-          tma_load_3d(sB + stage * C::B_BYTES, &tmB, kb * TC_BK, nt * BN, layer + sh.b_slot_off,
+          tma_load_3d(sA + stage * C::A_BYTES, &tmA, kb * TC_BK, a_row, layer + sh.map.a_slot_off,
                       &full[stage]);
+          tma_load_3d(sB + stage * C::B_BYTES, &tmB, kb * TC_BK, nt * BN, b_slot, &full[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -210,8 +221,7 @@ bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int K, int rows, in
 template <class Epi, int BN, int EPI_WG = 1>
 cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int rows, int N, int K,
                            int g_first, int g_count, int* err, const Epi& epi, int num_sms,
-                           cudaStream_t stream, int row0 = 0, int a_slot_off = 0,
-                           int b_slot_off = 0) {
+                           cudaStream_t stream, const GemmGroupMap& map = GemmGroupMap()) {
   using C = TcCfg<BN, EPI_WG>;
   static bool configured = false;
   if (!configured) {
@@ -222,9 +232,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int r
   }
   GemmTcShape sh;
   sh.rows = rows;
-  sh.row0 = row0;
-  sh.a_slot_off = a_slot_off;
-  sh.b_slot_off = b_slot_off;
+  sh.map = map;
   sh.N = N;
   sh.K = K;
   sh.g_first = g_first;

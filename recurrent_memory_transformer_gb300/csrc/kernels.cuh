@@ -21,26 +21,33 @@ namespace armt {
 
 // X[0] = [E[tokens of the segment]; memory embeddings] (fp32 residual stream)
 // plus the activation-dtype copy Xa[0] (used as a GEMM operand; nullptr or
-// equal to X when not needed).
+// equal to X when not needed).  Cell b (blockIdx.y) of the launch takes its
+// tokens from tokens + b * tok_stride and fills rows [b * T, (b + 1) * T):
+// n_seg token rows, then the M memory rows, then zero rows up to T (a short
+// last segment; the zero rows come after every real row, so under the causal
+// mask no real row ever sees them).
 template <typename WT>
-__global__ void embed_gather_kernel(const int32_t* __restrict__ tokens, const WT* __restrict__ embed,
-                                    const WT* __restrict__ mem, float* __restrict__ X,
-                                    WT* __restrict__ Xa, int S, int d, int vocab) {
-  const int t = blockIdx.x;
-  const WT* src;
-  if (t < S) {
-    int id = tokens[t];
+__global__ void embed_gather_kernel(const int32_t* __restrict__ tokens, long long tok_stride,
+                                    const WT* __restrict__ embed, const WT* __restrict__ mem,
+                                    float* __restrict__ X, WT* __restrict__ Xa, int T, int n_seg,
+                                    int M, int d, int vocab) {
+  const int t = blockIdx.x, b = blockIdx.y;
+  const WT* src = nullptr;
+  if (t < n_seg) {
+    int id = tokens[b * tok_stride + t];
     id = id < 0 ? 0 : (id >= vocab ? vocab - 1 : id);
     src = embed + (long long)id * d;
-  } else {
-    src = mem + (long long)(t - S) * d;
+  } else if (t < n_seg + M) {
+    src = mem + (long long)(t - n_seg) * d;
   }
-  float* xo = X + (long long)t * d;
-  WT* xa = Xa + (long long)t * d;
+  const long long row = (long long)b * T + t;
+  float* xo = X + row * d;
+  WT* xa = Xa + row * d;
+  const bool copy = Xa != nullptr && (void*)Xa != (void*)X;
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const float v = ld_as_f32(src + i);
+    const float v = src != nullptr ? ld_as_f32(src + i) : 0.f;
     xo[i] = v;
-    if (Xa != nullptr && (void*)Xa != (void*)X) xa[i] = src[i];
+    if (copy) st_from_f32(xa + i, v);
   }
 }
 
@@ -67,11 +74,13 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, long long x_gs, cons
 // ----------------------------------------------- associative read side --
 
 // From q = Wq_a x (fp32 [rows][k] per layer): phi = DPFP_nu(q) (act dtype,
-// [rows][P]) and den = z^T phi + eps.  One block per (row, layer).
+// [rows][P]) and den = z^T phi + eps.  One block per (row, layer).  A layer's
+// rows are nb cells of cell_rows rows; cell b of layer l reads the
+// normaliser z[l * nb + b].
 template <typename PhiT>
 __global__ void assoc_phi_kernel(const float* __restrict__ q, const float* __restrict__ z,
                                  PhiT* __restrict__ phi, float* __restrict__ den, int rows, int k,
-                                 int nu, float eps, int g_first) {
+                                 int nu, float eps, int g_first, int cell_rows, int nb) {
   extern __shared__ float r[];  // 2k
   __shared__ float red[32];
   const int l = g_first + blockIdx.y, row = blockIdx.x;
@@ -83,7 +92,7 @@ __global__ void assoc_phi_kernel(const float* __restrict__ q, const float* __res
     r[i + k] = v < 0.f ? -v : 0.f;
   }
   __syncthreads();
-  const float* zl = z + (long long)l * P;
+  const float* zl = z + ((long long)l * nb + row / cell_rows) * P;
   PhiT* pr = phi + ((long long)l * rows + row) * P;
   float acc = 0.f;
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
@@ -351,19 +360,24 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const T* __restrict__ qk
 
 // --------------------------------------------------- fp32 SIMT GEMM ----
 
-// C[l] = A[l] * B[l]^T, fp32, for l = g_first + blockIdx.z.  A [rows][K]
-// (row stride lda), B [N][K], C [rows][N] (row stride ldc).  64 x 64 tiles,
-// 16-wide K steps, 4 x 4 outputs per thread, fixed K order.
+// C[l] = A[l] * B[l / b_div]^T, fp32, for l = g_first + blockIdx.z.  A
+// [rows][K] (row stride lda) starting at row a_row0(l) of slot l + a_slot_off,
+// B [N][K], C [rows][N] (row stride ldc).  64 x 64 tiles, 16-wide K steps,
+// 4 x 4 outputs per thread, fixed K order.
+struct SimtAMap {
+  int row0, a_slot_off, b_div, alt_lo, alt_hi, alt_row0;
+};
 __global__ void __launch_bounds__(256) gemm_simt_f32_kernel(const float* __restrict__ A, long long a_gs,
                                                             int lda, const float* __restrict__ B,
                                                             long long b_gs, float* __restrict__ C,
                                                             long long c_gs, int ldc, int rows, int N,
-                                                            int K, int g_first) {
+                                                            int K, int g_first, SimtAMap am) {
   __shared__ float As[16][64 + 4];
   __shared__ float Bs[16][64 + 4];
   const int l = g_first + blockIdx.z;
-  const float* Al = A + l * a_gs;
-  const float* Bl = B + l * b_gs;
+  const int r0 = (l >= am.alt_lo && l < am.alt_hi) ? am.alt_row0 : am.row0;
+  const float* Al = A + (l + am.a_slot_off) * a_gs + (long long)r0 * lda;
+  const float* Bl = B + (l / am.b_div) * b_gs;
   float* Cl = C + l * c_gs;
   const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;

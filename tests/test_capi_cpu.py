@@ -92,6 +92,7 @@ def test_forward_and_gemm_reject_null_arguments(lib):
     assert lib.armt_forward(None, None, 1, None, None, None, 0, None) == 1
     assert lib.armt_forward_sequential(None, None, 1, None, None, None, 0, None) == 1
     assert lib.armt_forward_host(None, None, 1, None, None, None, 0, 0, None) == 1
+    assert lib.armt_forward_batch(None, None, 1, 1, None, None, None, 0, 0, None) == 1
     assert lib.armt_grouped_gemm_bf16(None, None, None, 1, 1, 256, 64, None) == 1
     i64 = ctypes.c_int64()
     assert lib.armt_launch_count(None, 1, 0, ctypes.byref(i64)) == 1
