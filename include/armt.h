@@ -205,7 +205,13 @@ ARMT_API armt_status armt_forward_batch(armt_model* m, const int32_t* tokens, in
 /* End-to-end variant with HOST buffers (pinned or pageable): copies tokens
  * (and the state when mem_in_valid) to the device, runs `schedule`, copies
  * hidden states and state back, and synchronises `stream` before returning.
- * Device staging buffers are owned by the model and grow on demand. */
+ * Device staging buffers are owned by the model and grow on demand.  When
+ * h_hidden_out, h_mem_A and h_mem_z are all pinned (cudaHostAlloc /
+ * cudaHostRegister) the results leave while the forward still runs: on a
+ * second, library-owned stream, hidden rows in chunks of 8 segments as soon
+ * as their segments have left the last layer, and each layer's state once
+ * that layer has run its last segment.  Pageable buffers are copied after
+ * the forward.  Either way everything has arrived when the call returns. */
 ARMT_API armt_status armt_forward_host(armt_model* m, const int32_t* h_tokens, int64_t n_segments,
                               float* h_hidden_out, float* h_mem_A, float* h_mem_z,
                               int32_t mem_in_valid, int32_t schedule, void* stream);
@@ -317,7 +323,8 @@ ARMT_API armt_status armt_launch_count(const armt_model* m, int64_t n_segments, 
                               int64_t* launches);
 
 /* Per-kernel timing with CUDA events recorded on the launch stream around
- * every launch of each kernel class (off by default).  armt_kernel_times
+ * every launch of each kernel class (off by default; enable != 0 times all
+ * classes).  armt_kernel_times
  * synchronises, then returns for class c (see armt_kernel_class) the number
  * of launches and total milliseconds since the last reset, and resets. */
 typedef enum armt_kernel_class {
@@ -326,6 +333,11 @@ typedef enum armt_kernel_class {
   ARMT_KC_OTHER = 8, ARMT_KC_COUNT = 9
 } armt_kernel_class;
 ARMT_API armt_status armt_set_profiling(armt_model* m, int32_t enable);
+/* Same, for the classes whose bit (1 << armt_kernel_class) is set in
+ * class_mask only (0 = off): the other launches get no events, so timing one
+ * class disturbs the rest of the forward as little as possible.  Resets the
+ * recorded times.  ARMT_ERR_ARG for bits at or past ARMT_KC_COUNT. */
+ARMT_API armt_status armt_set_profiling_mask(armt_model* m, uint32_t class_mask);
 ARMT_API armt_status armt_kernel_times(armt_model* m, int64_t* launches, double* ms, int32_t n_classes);
 
 /* Waits for `stream` and reports a device-side error recorded since the last

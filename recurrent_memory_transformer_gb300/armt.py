@@ -30,7 +30,7 @@ EXPORTED = ("armt_create", "armt_destroy", "armt_forward", "armt_forward_sequent
             "armt_forward_batch", "armt_forward_host", "armt_grouped_gemm_bf16", "armt_segment_attention_bf16",
             "armt_segment_attention_bf16_noalloc", "armt_forward_full_attention", "armt_state_sizes",
             "armt_memory_bytes", "armt_lm_head", "armt_launch_count",
-            "armt_set_profiling", "armt_kernel_times", "armt_sync_status", "armt_status_string",
+            "armt_set_profiling", "armt_set_profiling_mask", "armt_kernel_times", "armt_sync_status", "armt_status_string",
             "armt_last_error")
 
 
@@ -88,6 +88,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.armt_memory_bytes.argtypes = [P, ctypes.POINTER(I64), ctypes.POINTER(I64), ctypes.POINTER(I64)]
     lib.armt_launch_count.argtypes = [P, I64, I32, ctypes.POINTER(I64)]
     lib.armt_set_profiling.argtypes = [P, I32]
+    lib.armt_set_profiling_mask.argtypes = [P, ctypes.c_uint32]
     lib.armt_kernel_times.argtypes = [P, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double), I32]
     lib.armt_sync_status.argtypes = [P, P]
     for name in EXPORTED:
@@ -269,6 +270,13 @@ class Model:
 
     def armt_set_profiling(self, enable: bool):
         _check(_lib.armt_set_profiling(self._h, 1 if enable else 0), "armt_set_profiling")
+
+    def armt_set_profiling_mask(self, classes):
+        """Time only the launches of the named kernel classes (KERNEL_CLASSES); [] turns it off."""
+        mask = 0
+        for c in classes:
+            mask |= 1 << KERNEL_CLASSES.index(c)
+        _check(_lib.armt_set_profiling_mask(self._h, mask), "armt_set_profiling_mask")
 
     def armt_kernel_times(self):
         n = len(KERNEL_CLASSES)

@@ -33,6 +33,7 @@
 #include "epilogues.cuh"
 #include "attn_tc.cuh"
 #include "gemm_tc.cuh"
+#include "gemm_tc2.cuh"
 #include "kernels.cuh"
 
 using namespace armt;
@@ -152,8 +153,10 @@ struct ModelBase {
   DevAllocs mem;
   long long weight_bytes = 0;  // part of mem.total holding the weights
   int* d_err = nullptr;
-  // profiling
+  // profiling: launches of the classes in prof_mask get an event pair
   bool profiling = false;
+  uint32_t prof_mask = 0;
+  bool prof_open = false;
   std::vector<cudaEvent_t> ev_start, ev_stop;
   std::vector<int> ev_class;
   size_t ev_used = 0;
@@ -161,10 +164,28 @@ struct ModelBase {
   int32_t* st_tokens = nullptr;
   float *st_hidden = nullptr, *st_A = nullptr, *st_z = nullptr;
   size_t st_tokens_n = 0, st_hidden_n = 0;
+  // Results leave for the host while the forward still runs: once the
+  // last-layer cell of a segment is done its hidden rows are final, and once
+  // layer l has run its last cell its state is final.  forward() reports that
+  // progress after every step; sink_progress() then queues the device-to-host
+  // copies of what became final on a second stream (copy_stream), ordered
+  // after the step by one event.  Set only inside armt_forward_host.
+  struct HostSink {
+    float *h_hidden, *h_A, *h_z;              // host destinations
+    const float *d_hidden, *d_A, *d_z;        // device sources (the staging buffers)
+    int64_t rows_done, rows_total;            // hidden rows queued / to queue
+    int layers_done;                          // layers whose state is queued
+    int64_t chunk_rows;                       // queue hidden rows in chunks of at least this
+  };
+  HostSink* sink = nullptr;
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t copy_event = nullptr;
 
   virtual ~ModelBase() {
     for (cudaEvent_t e : ev_start) cudaEventDestroy(e);
     for (cudaEvent_t e : ev_stop) cudaEventDestroy(e);
+    if (copy_stream) cudaStreamDestroy(copy_stream);
+    if (copy_event) cudaEventDestroy(copy_event);
     if (st_tokens) cudaFree(st_tokens);
     if (st_hidden) cudaFree(st_hidden);
     if (st_A) cudaFree(st_A);
@@ -184,6 +205,35 @@ struct ModelBase {
                               cudaStream_t st) = 0;
 
   int rows() const { return cfg.seg_len + cfg.n_mem; }
+
+  // Queues the copies of everything that is final after a step: hidden rows
+  // [rows_done, rows_final) and the states of layers [layers_done,
+  // layers_final) (single sequence: the state is [L][d][P], [L][P]).
+  armt_status sink_progress(int64_t rows_final, int layers_final, cudaStream_t st) {
+    HostSink& k = *sink;
+    const bool last = rows_final >= k.rows_total && layers_final >= cfg.n_layers;
+    const bool rows_due = rows_final - k.rows_done >= k.chunk_rows || (last && rows_final > k.rows_done);
+    const bool layers_due = layers_final > k.layers_done;
+    if (!rows_due && !layers_due) return ARMT_OK;
+    CK(cudaEventRecord(copy_event, st));
+    CK(cudaStreamWaitEvent(copy_stream, copy_event, 0));
+    const size_t d = cfg.d_model, P = phi_dim();
+    if (rows_due) {
+      CK(cudaMemcpyAsync(k.h_hidden + k.rows_done * d, k.d_hidden + k.rows_done * d,
+                         (size_t)(rows_final - k.rows_done) * d * sizeof(float), cudaMemcpyDeviceToHost,
+                         copy_stream));
+      k.rows_done = rows_final;
+    }
+    if (layers_due) {
+      const size_t l0 = (size_t)k.layers_done, nl = (size_t)(layers_final - k.layers_done);
+      CK(cudaMemcpyAsync(k.h_A + l0 * d * P, k.d_A + l0 * d * P, nl * d * P * sizeof(float),
+                         cudaMemcpyDeviceToHost, copy_stream));
+      CK(cudaMemcpyAsync(k.h_z + l0 * P, k.d_z + l0 * P, nl * P * sizeof(float),
+                         cudaMemcpyDeviceToHost, copy_stream));
+      k.layers_done = layers_final;
+    }
+    return ARMT_OK;
+  }
   int phi_dim() const { return 2 * cfg.key_dim * cfg.dpfp_nu; }
   int n_qkv() const { return (cfg.n_q_heads + 2 * cfg.n_kv_heads) * cfg.head_dim; }
 
@@ -217,7 +267,8 @@ struct ModelBase {
 
   // Event pair around one launch when profiling.
   armt_status prof_begin(int cls, cudaStream_t st) {
-    if (!profiling) return ARMT_OK;
+    prof_open = profiling && ((prof_mask >> cls) & 1u) != 0;
+    if (!prof_open) return ARMT_OK;
     if (ev_used == ev_start.size()) {
       cudaEvent_t a, b;
       CK(cudaEventCreate(&a));
@@ -231,7 +282,8 @@ struct ModelBase {
     return ARMT_OK;
   }
   armt_status prof_end(cudaStream_t st) {
-    if (!profiling) return ARMT_OK;
+    if (!prof_open) return ARMT_OK;
+    prof_open = false;
     CK(cudaEventRecord(ev_stop[ev_used], st));
     ++ev_used;
     return ARMT_OK;
@@ -262,8 +314,8 @@ struct Model : ModelBase {
   int nw = 0;  // rows of Ww per layer (d + k + 1 rounded up to the tile width)
   int qkv_ld = 0, t_pad = 0;  // row stride of QKV; padded row count of Vt
   int nmax = 0;  // widest GEMM output (fp32 scratch row stride)
-  // weight tensor maps (bf16 path)
-  CUtensorMap tmAWq, tmWqkv, tmWo, tmWgu, tmWd, tmWw;
+  // weight tensor maps (bf16 path); the *2 maps have 128-row boxes for CTA-pair tiles
+  CUtensorMap tmAWq, tmWqkv, tmWo, tmWgu, tmWd, tmWw, tmWqkv2, tmWo2, tmWgu2, tmWd2;
   // The cell engine's activations for nb sequences run side by side (a
   // batch of requests).  With T = S + M rows per cell and R = nb * T rows per
   // layer, the per-layer tensors are [layer or slot][R][width]: cell b of a
@@ -382,6 +434,11 @@ struct Model : ModelBase {
       ok &= encode_tmap_bf16_3d(&tmWo, Wo, (int)(Hq * hd), (int)d, (int)L, 256);
       ok &= encode_tmap_bf16_3d(&tmWgu, Wgu, (int)d, (int)(2 * F), (int)L, 256);
       ok &= encode_tmap_bf16_3d(&tmWd, Wd, (int)F, (int)d, (int)L, 256);
+      // CTA-pair tiles: each CTA loads 128 of a tile's 256 B rows
+      ok &= encode_tmap_bf16_3d(&tmWqkv2, Wqkv, (int)d, (int)Nq, (int)L, 128);
+      ok &= encode_tmap_bf16_3d(&tmWo2, Wo, (int)(Hq * hd), (int)d, (int)L, 128);
+      ok &= encode_tmap_bf16_3d(&tmWgu2, Wgu, (int)d, (int)(2 * F), (int)L, 128);
+      ok &= encode_tmap_bf16_3d(&tmWd2, Wd, (int)F, (int)d, (int)L, 128);
       ok &= encode_tmap_bf16_3d(&tmWw, Ww, (int)d, nw, (int)L, 256);
       if (!ok) return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     }
@@ -495,13 +552,25 @@ struct Model : ModelBase {
   // row epilogue for fp32.  `rows` output rows per group; `map` places each
   // group's A rows and B slot (GemmGroupMap).  The fp32 path stages raw
   // products in w.Cscr.
+  // tb2 != nullptr: a 128-row-box map of the same B, so that the product
+  // may run as 256 x 256 tiles on CTA pairs (gemm_tc2.cuh) -- chosen when
+  // `rows` pads to 256-row tiles almost as tightly as to 128-row ones
+  // (pair_tiles_pay_off); otherwise 128 x BN tiles on single CTAs.
   template <int BN, class Epi, int EPI_WG = 1>
   armt_status gemm(int cls, Work& w, const CUtensorMap& ta, const CUtensorMap& tb, const AT* a,
                    long long a_gs, const WT* b, int N, int K, const Epi& epi, int lo, int g,
-                   cudaStream_t st, int rows, const GemmGroupMap& map = GemmGroupMap()) {
+                   cudaStream_t st, int rows, const GemmGroupMap& map = GemmGroupMap(),
+                   const CUtensorMap* tb2 = nullptr) {
     CKS(prof_begin(cls, st));
     if constexpr (kTC) {
-      CK((launch_gemm_tc<Epi, BN, EPI_WG>(ta, tb, rows, N, K, lo, g, d_err, epi, num_sms, st, map)));
+      bool done = false;
+      if constexpr (BN == 256) {
+        if (tb2 != nullptr && pair_tiles_pay_off(rows)) {
+          CK((launch_gemm_tc2<Epi, EPI_WG>(ta, *tb2, rows, N, K, lo, g, d_err, epi, num_sms, st, map)));
+          done = true;
+        }
+      }
+      if (!done) CK((launch_gemm_tc<Epi, BN, EPI_WG>(ta, tb, rows, N, K, lo, g, d_err, epi, num_sms, st, map)));
     } else {
       const SimtAMap am{map.row0, map.a_slot_off, map.b_div, map.alt_lo, map.alt_hi, map.alt_row0};
       const float* b0 = reinterpret_cast<const float*>(b) + (long long)map.b_slot_off * N * K;
@@ -564,7 +633,7 @@ struct Model : ModelBase {
     CKS((gemm<256, FQkv, 1>(ARMT_KC_GEMM_QKV, w, w.tmNrm, tmWqkv, w.Nrm, Rd, Wqkv, Nq, d,
                             FQkv{w.QKV, w.cosT, w.sinT, R, hd, (Hq + Hkv) * hd, qkv_ld, w.Vt, Hkv,
                                  t_pad, norm_in, T, nb},
-                            lo, g, st, R)));
+                            lo, g, st, R, GemmGroupMap(), &tmWqkv2)));
     CKS(prof_begin(ARMT_KC_ATTENTION, st));
     if constexpr (kTC) {
       AttnArgs aa;
@@ -594,14 +663,14 @@ struct Model : ModelBase {
     CKS(prof_end(st));
     CKS((gemm<256, FRes, 2>(ARMT_KC_GEMM_O, w, w.tmAtt, tmWo, w.Att, (long long)R * Hq * hd, Wo, d,
                             Hq * hd, FRes{w.Res, w.Res, nullptr, R, d, 0, RowNormOut<AT>{g2, w.Nrm, w.Ssq}},
-                            lo, g, st, R)));
+                            lo, g, st, R, GemmGroupMap(), &tmWo2)));
     // MLP sub-layer (RMSNorm 2 completes in the gate-up epilogue)
-    CKS((gemm<256>(ARMT_KC_GEMM_GATEUP, w, w.tmNrm, tmWgu, w.Nrm, Rd, Wgu, 2 * F, d,
-                   FSwi{w.U, R, F, norm_in}, lo, g, st, R)));
-    CKS((gemm<256>(ARMT_KC_GEMM_DOWN, w, w.tmU, tmWd, w.U, (long long)R * F, Wd, d, F,
-                   FRes{w.Res, w.X, kTC ? w.Xa : nullptr, R, d, 1,
-                        RowNormOut<AT>{nullptr, nullptr, nullptr}},
-                   lo, g, st, R)));
+    CKS((gemm<256, FSwi, 1>(ARMT_KC_GEMM_GATEUP, w, w.tmNrm, tmWgu, w.Nrm, Rd, Wgu, 2 * F, d,
+                            FSwi{w.U, R, F, norm_in}, lo, g, st, R, GemmGroupMap(), &tmWgu2)));
+    CKS((gemm<256, FRes, 1>(ARMT_KC_GEMM_DOWN, w, w.tmU, tmWd, w.U, (long long)R * F, Wd, d, F,
+                            FRes{w.Res, w.X, kTC ? w.Xa : nullptr, R, d, 1,
+                                 RowNormOut<AT>{nullptr, nullptr, nullptr}},
+                            lo, g, st, R, GemmGroupMap(), &tmWd2)));
     // delta-rule write from the memory-token rows of this layer's output:
     // [v | k | beta] = h_mem [Wv_a; Wk_a; wbeta_a]^T on the tensor cores, per
     // (layer, sequence) group: A = the M memory rows of the cell in layer
@@ -713,7 +782,9 @@ struct Model : ModelBase {
     CKS(prof_begin(ARMT_KC_OTHER, st));
     if constexpr (kTC) {
       CUtensorMap tb;
-      if (!encode_tmap_bf16_3d(&tb, head, d, V, 1, 256)) return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+      CUtensorMap tb1;
+      if (!encode_tmap_bf16_3d(&tb, head, d, V, 1, 128) || !encode_tmap_bf16_3d(&tb1, head, d, V, 1, 256))
+        return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
       for (int64_t r0 = 0; r0 < n_rows; r0 += kLmChunk) {
         const int rows_c = (int)std::min<int64_t>(kLmChunk, n_rows - r0);
         convert_state_kernel<AT><<<num_sms * 4, 256, 0, st>>>(hidden + r0 * d, lm_rows, (long long)rows_c * d);
@@ -722,7 +793,10 @@ struct Model : ModelBase {
         if (!encode_tmap_bf16_3d(&ta, lm_rows, d, rows_c, 1, TC_BM))
           return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         SEpiStore epi{logits + r0 * V, (long long)V, 0};
-        CK((launch_gemm_tc<SEpiStore, 256>(ta, tb, rows_c, V, d, 0, 1, d_err, epi, num_sms, st)));
+        if (pair_tiles_pay_off(rows_c))
+          CK((launch_gemm_tc2<SEpiStore, 1>(ta, tb, rows_c, V, d, 0, 1, d_err, epi, num_sms, st)));
+        else
+          CK((launch_gemm_tc<SEpiStore, 256>(ta, tb1, rows_c, V, d, 0, 1, d_err, epi, num_sms, st)));
       }
     } else {
       for (int64_t r0 = 0; r0 < n_rows; r0 += kLmChunk) {
@@ -737,6 +811,15 @@ struct Model : ModelBase {
     }
     CKS(prof_end(st));
     return ARMT_OK;
+  }
+
+  template <class Epi, int EPI_WG>
+  cudaError_t launch_weight_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
+                                 int rows, int N, int K, int g_first, int g_count, int* err,
+                                 const Epi& epi, int nsm, cudaStream_t st, const GemmGroupMap& map) {
+    if (pair_tiles_pay_off(rows))
+      return launch_gemm_tc2<Epi, EPI_WG>(ta, tb2, rows, N, K, g_first, g_count, err, epi, nsm, st, map);
+    return launch_gemm_tc<Epi, 256, EPI_WG>(ta, tb, rows, N, K, g_first, g_count, err, epi, nsm, st, map);
   }
 
   static GemmGroupMap layer_map(int l) {
@@ -771,7 +854,7 @@ struct Model : ModelBase {
         CK(cudaGetLastError());
         CKS(prof_end(st));
         CKS(prof_begin(ARMT_KC_GEMM_QKV, st));
-        CK((launch_gemm_tc<FQkv, 256, 1>(tmNrmf, tmWqkv, T, Nq, d, 0, 1, d_err,
+        CK((launch_weight_gemm<FQkv, 1>(tmNrmf, tmWqkv, tmWqkv2, T, Nq, d, 0, 1, d_err,
                                       FQkv{QKVf, cosF, sinF, T, hd, (Hq + Hkv) * hd, (Hq + Hkv) * hd,
                                            Vtf, Hkv, tp, no_scale, T, 1},
                                       num_sms, st, layer_map(l))));
@@ -794,17 +877,17 @@ struct Model : ModelBase {
         }
         CKS(prof_end(st));
         CKS(prof_begin(ARMT_KC_GEMM_O, st));
-        CK((launch_gemm_tc<FRes, 256, 2>(tmAttf, tmWo, T, d, Hq * hd, 0, 1, d_err,
+        CK((launch_weight_gemm<FRes, 2>(tmAttf, tmWo, tmWo2, T, d, Hq * hd, 0, 1, d_err,
                                       FRes{Xf, Resf, nullptr, T, d, 0,
                                            RowNormOut<AT>{g2 + (long long)l * d, Nrmf, Ssqf}},
                                       num_sms, st, layer_map(l))));
         CKS(prof_end(st));
         CKS(prof_begin(ARMT_KC_GEMM_GATEUP, st));
-        CK((launch_gemm_tc<FSwi, 256>(tmNrmf, tmWgu, T, 2 * F, d, 0, 1, d_err, FSwi{Uf, T, F, norm_in},
+        CK((launch_weight_gemm<FSwi, 1>(tmNrmf, tmWgu, tmWgu2, T, 2 * F, d, 0, 1, d_err, FSwi{Uf, T, F, norm_in},
                                       num_sms, st, layer_map(l))));
         CKS(prof_end(st));
         CKS(prof_begin(ARMT_KC_GEMM_DOWN, st));
-        CK((launch_gemm_tc<FRes, 256>(tmUf, tmWd, T, d, F, 0, 1, d_err,
+        CK((launch_weight_gemm<FRes, 1>(tmUf, tmWd, tmWd2, T, d, F, 0, 1, d_err,
                                       FRes{Resf, Xf, nullptr, T, d, 0,
                                            RowNormOut<AT>{nullptr, nullptr, nullptr}},
                                       num_sms, st, layer_map(l))));
@@ -836,15 +919,24 @@ struct Model : ModelBase {
       CK(cudaGetLastError());
       CKS(prof_end(st));
     }
+    const bool report = sink != nullptr && nb == 1;
     if (schedule == ARMT_SCHEDULE_DIAGONAL) {
       for (int64_t i = 0; i < L + n - 1; ++i) {
         const int lo = (int)(i - n + 1 > 0 ? i - n + 1 : 0);
         const int hi = (int)(i < L - 1 ? i : L - 1);
         CKS(step(w, lo, hi, i - lo, tokens, n_tok, n, hidden, A, z, st));
+        if (report) {
+          // after step i: segments 0..i-L+1 have left the last layer, and
+          // layers 0..i-n+1 have run their last segment
+          const int64_t segs = std::max<int64_t>(0, i - L + 2);
+          CKS(sink_progress(std::min<int64_t>(n_tok, segs * S), (int)std::max<int64_t>(0, i - n + 2), st));
+        }
       }
     } else {
-      for (int64_t s = 0; s < n; ++s)
+      for (int64_t s = 0; s < n; ++s) {
         for (int l = 0; l < L; ++l) CKS(step(w, l, l, s, tokens, n_tok, n, hidden, A, z, st));
+        if (report) CKS(sink_progress(std::min<int64_t>(n_tok, (s + 1) * S), s == n - 1 ? L : 0, st));
+      }
     }
     return ARMT_OK;
   }
@@ -1008,6 +1100,15 @@ armt_status armt_forward_sequential(armt_model* m, const int32_t* tokens, int64_
                         ARMT_SCHEDULE_SEQUENTIAL, stream);
 }
 
+static bool is_pinned(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
 armt_status armt_forward_host(armt_model* m, const int32_t* h_tokens, int64_t n, float* h_hidden,
                               float* h_A, float* h_z, int32_t mem_in_valid, int32_t schedule,
                               void* stream) {
@@ -1044,12 +1145,37 @@ armt_status armt_forward_host(armt_model* m, const int32_t* h_tokens, int64_t n,
     CK(cudaMemcpyAsync(b->st_A, h_A, na * sizeof(float), cudaMemcpyHostToDevice, st));
     CK(cudaMemcpyAsync(b->st_z, h_z, nz * sizeof(float), cudaMemcpyHostToDevice, st));
   }
-  CKS(forward_common(m, b->st_tokens, n, b->st_hidden, b->st_A, b->st_z, mem_in_valid, schedule,
-                     stream));
-  CK(cudaMemcpyAsync(h_hidden, b->st_hidden, nh * sizeof(float), cudaMemcpyDeviceToHost, st));
-  CK(cudaMemcpyAsync(h_A, b->st_A, na * sizeof(float), cudaMemcpyDeviceToHost, st));
-  CK(cudaMemcpyAsync(h_z, b->st_z, nz * sizeof(float), cudaMemcpyDeviceToHost, st));
+  if (b->copy_stream == nullptr) {
+    CK(cudaStreamCreateWithFlags(&b->copy_stream, cudaStreamNonBlocking));
+    CK(cudaEventCreateWithFlags(&b->copy_event, cudaEventDisableTiming));
+  }
+  // Pinned destinations: results stream back to the host while later
+  // diagonals still run.  Pageable ones: a copy into pageable memory returns
+  // only when it has finished, which would stall the launches, so they are
+  // copied once the forward is done.
+  const bool pinned = is_pinned(h_hidden) && is_pinned(h_A) && is_pinned(h_z);
+  ModelBase::HostSink sink{h_hidden, h_A, h_z, b->st_hidden, b->st_A, b->st_z, 0, (int64_t)ntok, 0,
+                           (int64_t)8 * c.seg_len};
+  b->sink = pinned ? &sink : nullptr;
+  const armt_status fs = forward_common(m, b->st_tokens, n, b->st_hidden, b->st_A, b->st_z,
+                                        mem_in_valid, schedule, stream);
+  b->sink = nullptr;
+  if (fs == ARMT_OK && !pinned) {
+    CK(cudaEventRecord(b->copy_event, st));
+    CK(cudaStreamWaitEvent(b->copy_stream, b->copy_event, 0));
+    CK(cudaMemcpyAsync(h_hidden, b->st_hidden, nh * sizeof(float), cudaMemcpyDeviceToHost, b->copy_stream));
+    CK(cudaMemcpyAsync(h_A, b->st_A, na * sizeof(float), cudaMemcpyDeviceToHost, b->copy_stream));
+    CK(cudaMemcpyAsync(h_z, b->st_z, nz * sizeof(float), cudaMemcpyDeviceToHost, b->copy_stream));
+    sink.rows_done = (int64_t)ntok;
+    sink.layers_done = c.n_layers;
+  }
+  // drain the copy stream whatever happened, so no copy outlives the call
+  const cudaError_t e1 = cudaStreamSynchronize(b->copy_stream);
+  CKS(fs);
+  if (e1 != cudaSuccess) return fail(ARMT_ERR_CUDA, std::string("copy stream: ") + cudaGetErrorString(e1));
   CK(cudaStreamSynchronize(st));
+  if (sink.rows_done != (int64_t)ntok || sink.layers_done != c.n_layers)
+    return fail(ARMT_ERR_CUDA, "internal: results not fully copied");
   return ARMT_OK;
 }
 
@@ -1089,11 +1215,15 @@ armt_status armt_grouped_gemm_bf16(const void* A, const void* B, float* C, int32
     CK(cudaMemset(err, 0, sizeof(int)));
   }
   CUtensorMap ta, tb;
-  if (!encode_tmap_bf16_3d(&ta, A, K, M, G, TC_BM) || !encode_tmap_bf16_3d(&tb, B, K, N, G, 256))
+  const bool pairs = pair_tiles_pay_off(M);
+  if (!encode_tmap_bf16_3d(&ta, A, K, M, G, TC_BM) || !encode_tmap_bf16_3d(&tb, B, K, N, G, pairs ? 128 : 256))
     return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   SEpiStore epi{C, (long long)N, (long long)M * N};
-  CK((launch_gemm_tc<SEpiStore, 256>(ta, tb, M, N, K, 0, G, err, epi, g_num_sms(dev),
-                                    reinterpret_cast<cudaStream_t>(stream))));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (pairs)
+    CK((launch_gemm_tc2<SEpiStore, 1>(ta, tb, M, N, K, 0, G, err, epi, g_num_sms(dev), st)));
+  else
+    CK((launch_gemm_tc<SEpiStore, 256>(ta, tb, M, N, K, 0, G, err, epi, g_num_sms(dev), st)));
   return ARMT_OK;
 }
 
@@ -1164,8 +1294,14 @@ armt_status armt_launch_count(const armt_model* m, int64_t n, int32_t schedule, 
 }
 
 armt_status armt_set_profiling(armt_model* m, int32_t enable) {
+  return armt_set_profiling_mask(m, enable != 0 ? (1u << ARMT_KC_COUNT) - 1u : 0u);
+}
+
+armt_status armt_set_profiling_mask(armt_model* m, uint32_t class_mask) {
   if (m == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
-  m->impl->profiling = enable != 0;
+  if (class_mask >> ARMT_KC_COUNT) return fail(ARMT_ERR_ARG, "class_mask has bits past ARMT_KC_COUNT");
+  m->impl->prof_mask = class_mask;
+  m->impl->profiling = class_mask != 0;
   m->impl->ev_used = 0;
   return ARMT_OK;
 }

@@ -216,12 +216,23 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
       tc_fence_after();
       if (!idle) {
         const uint32_t tO = tmem + 128u * (uint32_t)(t & 1) + lane_off;
+        const float2 c2 = make_float2(corr, corr);
 #pragma unroll
         for (int cc = 0; cc < HD / 32; ++cc) {
           float ov[32];
           tmem_ld32(tO + 32 * cc, ov);
+          if constexpr (HD == 64) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[32 * cc + i] = o[32 * cc + i] * corr + ov[i];
+            for (int i = 0; i < 32; i += 2) {
+              const float2 r2 = __ffma2_rn(make_float2(o[32 * cc + i], o[32 * cc + i + 1]), c2,
+                                           make_float2(ov[i], ov[i + 1]));
+              o[32 * cc + i] = r2.x;
+              o[32 * cc + i + 1] = r2.y;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[32 * cc + i] = o[32 * cc + i] * corr + ov[i];
+          }
         }
       }
       tc_fence_before();
@@ -253,20 +264,25 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
         // column of this row within the tile.
         const bool diag = (j == m);
         const int lim = qi - j * 128;
-        // pass 1: row max of the raw scores (the scale is positive)
-        float mx = -INFINITY;
+        // pass 1: row max of the raw scores (the scale is positive); NMX
+        // independent partial maxima keep the dependency chains short
+        constexpr int NMX = HD == 64 ? 8 : 4;  // fewer where o[] already fills the registers
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
 #pragma unroll
         for (int cc = 0; cc < 4 && !idle; ++cc) {
           float sv[32];
           tmem_ld32(tS + 32 * cc, sv);
           if (diag) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) mx = (32 * cc + i <= lim) ? fmaxf(mx, sv[i]) : mx;
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, sv[i]);
+            for (int i = 0; i < 32; ++i) sv[i] = (32 * cc + i <= lim) ? sv[i] : -INFINITY;
           }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx8[i % NMX] = fmaxf(mx8[i % NMX], sv[i]);
         }
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_new = fmaxf(m_run, mx * a.scale_log2);
         const float corr = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
@@ -276,22 +292,27 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
           ok = false;
           break;
         }
-        // pass 2: p = 2^(s * scale - m), row sum, bf16 P into shared memory
-        float rs = 0.f;
+        // pass 2: p = 2^(s * scale - m) (masked keys: 2^-inf = 0), row sum
+        // in four independent pairs, bf16 P into shared memory
+        float2 rs4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rs4[i] = make_float2(0.f, 0.f);
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
         for (int cc = 0; cc < 4 && !idle; ++cc) {
           float sv[32];
           tmem_ld32(tS + 32 * cc, sv);
           if (diag) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              sv[i] = (32 * cc + i <= lim) ? fast_exp2(fmaf(sv[i], a.scale_log2, -m_use)) : 0.f;
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) sv[i] = fast_exp2(fmaf(sv[i], a.scale_log2, -m_use));
+            for (int i = 0; i < 32; ++i) sv[i] = (32 * cc + i <= lim) ? sv[i] : -INFINITY;
           }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) rs += sv[i];
+          for (int i = 0; i < 32; i += 2) {
+            const float2 x2 = __ffma2_rn(make_float2(sv[i], sv[i + 1]), sc2, nm2);
+            sv[i] = fast_exp2(x2.x);
+            sv[i + 1] = fast_exp2(x2.y);
+            rs4[(i >> 1) % (NMX / 2)] = __fadd2_rn(rs4[(i >> 1) % (NMX / 2)], make_float2(sv[i], sv[i + 1]));
+          }
           uint8_t* atom = prow + (cc >> 1) * 16384;
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
@@ -304,6 +325,8 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
             *reinterpret_cast<uint4*>(atom + ((chunk ^ (r & 7)) << 4)) = pk;
           }
         }
+        const float rs = ((rs4[0].x + rs4[0].y) + (rs4[1].x + rs4[1].y)) +
+                         ((rs4[2].x + rs4[2].y) + (rs4[3].x + rs4[3].y));
         l_run = l_run * corr + rs;
         m_run = m_new;
         corr_prev = corr;

@@ -1,0 +1,258 @@
+// Grouped bf16 GEMM on CTA pairs (tcgen05 cta_group::2): 256 x 256 tiles.
+//
+// The same grouped layer as gemm_tc.cuh (summary page of "Diagonal Batching
+// Unlocks Parallelism in Recurrent Memory Transformers for Long Contexts",
+// section 三: one grouped product per linear layer over the cells of a
+// diagonal, out[g] = epilogue(A[g] B[g]^T)), for the wide projections.
+//
+// Why pairs: with one CTA a 128 x 256 x 16 MMA reads 12 KB of operands from
+// shared memory and TMA writes the same 12 KB into it, about 192 bytes per
+// clock against the tensor core's rate -- more than shared memory delivers,
+// so a single-CTA tile cannot keep the tensor core busy.  A CTA pair runs one
+// 256 x 256 tile: each CTA loads its 128 rows of A and 128 of the 256 B rows
+// and each SM reads only its own halves, 128 bytes per clock in all.
+//
+// Cluster of 2 CTAs (rank 0 = leader), persistent over pair tiles
+// (group-major, then N tile, then 256-row M tile):
+//   warp 0      TMA producer in both CTAs: A rows [m0 + 128 r, +128) and B rows
+//               [n0 + 128 r, +128) of each 64-wide K block into its own
+//               shared memory; completion counted on the LEADER's full barrier
+//               (which expects both CTAs' bytes).
+//   warp 1      leader only: one thread issues the pair MMAs (4 per K block)
+//               into TMEM accumulator (acc) of both CTAs, commits the stage's
+//               empty barrier and, per tile, the accumulator-full barrier of
+//               both CTAs (multicast).
+//   warps 2..   epilogue in both CTAs, as in gemm_tc.cuh, on the CTA's 128
+//               rows x 256 columns; each warp then arrives on the leader's
+//               accumulator-empty barrier (remote arrive).
+// Every wait is bounded; an error word stops both CTAs, which then meet at
+// the final cluster barrier.  Same fixed K order per element as gemm_tc.cuh.
+#pragma once
+
+#include "common.cuh"
+#include "epilogues.cuh"
+#include "epilogues_staged.cuh"
+#include "gemm_tc.cuh"
+
+namespace armt {
+
+template <int EPI_WG>
+struct Tc2Cfg {
+  static constexpr int BN = 256;                     // N per pair tile (each CTA loads BN/2 B rows)
+  static constexpr int STAGES = EPI_WG == 2 ? 4 : 6;
+  static constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;        // 16 KB
+  static constexpr uint32_t B_BYTES = (BN / 2) * TC_BK * 2;     // 16 KB
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;    // per CTA
+  static constexpr uint32_t TMEM_COLS = 2 * BN;                 // two accumulators
+  static constexpr int EPI_WARPS = 4 * EPI_WG;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr uint32_t EPI_STAGE_BYTES = EPI_WARPS * STAGED_FLOATS_PER_WARP * 4;
+  static constexpr size_t SMEM = 1024 + STAGES * STAGE_BYTES + 256 + EPI_STAGE_BYTES;
+  static_assert(SMEM <= 232448, "shared memory");
+};
+
+template <class Epi, int EPI_WG>
+__global__ void __launch_bounds__(Tc2Cfg<EPI_WG>::THREADS, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmTcShape sh, const Epi epi) {
+  using C = Tc2Cfg<EPI_WG>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + C::STAGES * C::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);   // the leader's producer arrival (+ both CTAs' bytes)
+      mbar_init(&empty[s], 1);  // the pair commit
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);                  // the pair commit
+      mbar_init(&acc_empty[a], 2 * C::EPI_WARPS);  // every epilogue warp of both CTAs
+    }
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int m_pairs = (sh.rows + 2 * TC_BM - 1) / (2 * TC_BM);
+  const int tiles_per_g = m_pairs * sh.n_tiles;
+  const int num_tiles = sh.g_count * tiles_per_g;
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = cid; ok && t < num_tiles; t += ncl) {
+        const int g = t / tiles_per_g, r = t - g * tiles_per_g;
+        const int nt = r / m_pairs, mp = r - nt * m_pairs;
+        const int layer = sh.g_first + g;
+        const int a_row = sh.map.a_row0(layer) + mp * 2 * TC_BM + (int)rank * TC_BM;
+        const int b_row = nt * C::BN + (int)rank * (C::BN / 2);
+        const int b_slot = layer / sh.map.b_div + sh.map.b_slot_off;
+        for (int kb = 0; kb < sh.k_blocks; ++kb) {
+          if (!mbar_wait_bounded_cluster(&empty[stage], phase ^ 1u, sh.err, DEV_TIMEOUT_EMPTY)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+          const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+          tma_load_3d_pair(sA + stage * C::A_BYTES, &tmA, kb * TC_BK, a_row, layer + sh.map.a_slot_off, fb);
+          tma_load_3d_pair(sB + stage * C::B_BYTES, &tmB, kb * TC_BK, b_row, b_slot, fb);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (leader && lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * TC_BM, C::BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = cid; ok && t < num_tiles; t += ncl) {
+        if (!mbar_wait_bounded_cluster(&acc_empty[acc], acc_phase ^ 1u, sh.err, DEV_TIMEOUT_ACC_EMPTY))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::BN);
+        for (int kb = 0; kb < sh.k_blocks; ++kb) {
+          if (!mbar_wait_bounded_cluster(&full[stage], phase, sh.err, DEV_TIMEOUT_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES));
+          const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + stage * C::B_BYTES));
+#pragma unroll
+          for (int k = 0; k < TC_BK / 16; ++k)
+            tc_mma_bf16_pair(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
+                             (kb | k) != 0 ? 1u : 0u);
+          tc_commit_pair(&empty[stage]);  // the stage is free in both CTAs once these finish
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair(&acc_full[acc]);  // both CTAs' accumulators ready
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int ew = warp - 2;
+    const int part = ew / 4;
+    float* stage = reinterpret_cast<float*>(base + C::STAGES * C::STAGE_BYTES + 256) +
+                   ew * STAGED_FLOATS_PER_WARP;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = cid; t < num_tiles; t += ncl) {
+      const int g = t / tiles_per_g, r = t - g * tiles_per_g;
+      const int nt = r / m_pairs, mp = r - nt * m_pairs;
+      const bool got =
+          mbar_wait_bounded_cluster(&acc_full[acc], acc_phase, sh.err, DEV_TIMEOUT_ACC_FULL);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const int row0 = mp * 2 * TC_BM + (int)rank * TC_BM + quarter * 32;
+      staged_epilogue<C::BN, EPI_WG>(epi, sh.g_first + g, row0, sh.rows, nt * C::BN, part,
+                                     tmem_base + (uint32_t)(acc * C::BN) + ((uint32_t)(quarter * 32) << 16),
+                                     stage);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&acc_empty[acc]), 0));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no remote arrival or pair MMA is still aimed at this CTA
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// Pair tiles cover 256 rows, single-CTA tiles 128: for a product of `rows`
+// rows the pair kernel computes up to 255 padding rows against 127.  Where
+// that padding is a few percent of the work the pair kernel is faster; for
+// short cells (1040 rows: 1280 vs 1152 computed) the extra tensor work costs
+// more than the pair saves.  Pairs are used when they pad at most 3 % more.
+inline bool pair_tiles_pay_off(long long rows) {
+  const long long p = (rows + 255) / 256 * 256, s1 = (rows + 127) / 128 * 128;
+  return p * 100 <= s1 * 103;
+}
+
+// Launch with clusters of two; the grid is the number of co-resident pairs
+// (queried once per kernel), at most the number of pair tiles.
+template <class Epi, int EPI_WG = 1>
+cudaError_t launch_gemm_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, int rows, int N, int K,
+                            int g_first, int g_count, int* err, const Epi& epi, int num_sms,
+                            cudaStream_t stream, const GemmGroupMap& map = GemmGroupMap()) {
+  using C = Tc2Cfg<EPI_WG>;
+  static int max_clusters = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters == 0) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel<Epi, EPI_WG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel<Epi, EPI_WG>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    max_clusters = n;
+  }
+  GemmTcShape sh;
+  sh.rows = rows;
+  sh.map = map;
+  sh.N = N;
+  sh.K = K;
+  sh.g_first = g_first;
+  sh.g_count = g_count;
+  sh.m_tiles = (rows + TC_BM - 1) / TC_BM;
+  sh.n_tiles = N / C::BN;
+  sh.k_blocks = K / TC_BK;
+  sh.err = err;
+  const int tiles = g_count * ((rows + 2 * TC_BM - 1) / (2 * TC_BM)) * sh.n_tiles;
+  const int clusters = tiles < max_clusters ? tiles : max_clusters;
+  if (clusters <= 0) return cudaSuccess;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  return cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<Epi, EPI_WG>, tmA, tmB, sh, epi);
+}
+
+}  // namespace armt

@@ -162,3 +162,27 @@ def test_armt1b_shape_batch_with_short_last_segment():
     record("armt1b_shape_batch2_short", **res)
     assert bitwise and all(alone)
     assert ok_all, res
+
+
+def test_armt1b_shape_batch8_pair_tiles_equal_each_sequence_alone():
+    """A batch of 8 cells per layer (8 x 1040 rows) runs the weight GEMMs on
+    CTA-pair tiles, a single sequence on single-CTA tiles: every sequence of
+    the batch must still equal its batch-1 run bitwise (same per-element
+    reduction order), in both schedules."""
+    cfg = dataclasses.replace(I.ARMT_1B, n_layers=2, vocab=4096)
+    W = I.make_weights(cfg, 66, norm_jitter=0.1)
+    n_tok = cfg.seg_len + 100
+    tok = _tokens(cfg, n_tok, 66, 8)
+    m = B.Model(cfg, B.device_weight_tensors(cfg, W))
+    t = torch.from_numpy(tok).cuda()
+    hd, Ad, zd = m.forward_batch(t)
+    hs, As, zs = m.forward_batch(t, schedule=B.SCHEDULE_SEQUENTIAL)
+    torch.cuda.synchronize()
+    assert _equal(hd, hs) and _equal(Ad, As) and _equal(zd, zs)
+    for b in (0, 5, 7):
+        h1, A1, z1 = m.forward_batch(t[b:b + 1].contiguous())
+        torch.cuda.synchronize()
+        assert _equal(h1[0], hd[b]) and _equal(A1[:, 0], Ad[:, b]) and _equal(z1[:, 0], zd[:, b]), b
+    m.armt_sync_status()
+    assert torch.isfinite(hd).all()
+    m.close()

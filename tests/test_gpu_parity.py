@@ -84,8 +84,11 @@ def run_gpu(cfg, W, tok, n_seg, schedule):
 
 # ------------------------------------------------------------ GEMM unit --
 
+# M = 144, 512 and 2304 pad to 256-row tiles as tightly as to 128-row ones and
+# run on CTA pairs; the others on single CTAs
 @pytest.mark.parametrize("G,M,N,K", [(1, 128, 256, 64), (3, 1040, 512, 2048), (2, 17, 256, 384),
-                                     (1, 300, 768, 8192), (2, 16, 256, 128), (1, 144, 512, 192)])
+                                     (1, 300, 768, 8192), (2, 16, 256, 128), (1, 144, 512, 192),
+                                     (2, 512, 768, 256), (1, 2304, 1024, 1024)])
 def test_grouped_gemm_bf16_matches_fp64_matmul(G, M, N, K):
     g = torch.Generator(device="cpu").manual_seed(G * 1000 + M)
     A = torch.randn(G, M, K, generator=g).to(torch.bfloat16)
@@ -196,6 +199,27 @@ def test_tiny_host_entry_point_matches_device():
     m.armt_forward_host(tok, 4, hh, Ah, zh)
     assert np.array_equal(hh, h.cpu().numpy())
     assert np.array_equal(Ah, A.cpu().numpy().ravel()) and np.array_equal(zh, z.cpu().numpy().ravel())
+    m.close()
+
+
+@pytest.mark.parametrize("n_layers,n_seg", [(2, 4), (2, 19)])
+def test_host_entry_point_pinned_streams_results_during_forward(n_layers, n_seg):
+    # pinned host buffers take the overlapped path (copies queued as segments
+    # and layers finish); the result must equal the device path bitwise
+    cfg = dataclasses.replace(I.ARMT_1B, n_layers=n_layers, vocab=4096)
+    W = I.make_weights(cfg, seed=25)
+    tok = I.make_tokens(cfg, n_seg, seed=25)
+    m = B.Model(cfg, B.device_weight_tensors(cfg, W))
+    for schedule in (B.SCHEDULE_DIAGONAL, B.SCHEDULE_SEQUENTIAL):
+        h, A, z = m.forward(torch.from_numpy(tok).cuda(), n_seg, schedule=schedule)
+        torch.cuda.synchronize()
+        hh = torch.full((n_seg * cfg.seg_len, cfg.d_model), float("nan")).pin_memory()
+        Ah = torch.full((m.a_elems,), float("nan")).pin_memory()
+        zh = torch.full((m.z_elems,), float("nan")).pin_memory()
+        m.armt_forward_host(torch.from_numpy(tok).pin_memory(), n_seg, hh, Ah, zh, schedule=schedule)
+        assert torch.equal(hh, h.cpu()), schedule
+        assert torch.equal(Ah, A.cpu().reshape(-1)) and torch.equal(zh, z.cpu().reshape(-1)), schedule
+    m.armt_sync_status()
     m.close()
 
 
@@ -355,7 +379,7 @@ def _plain_llama_oracle(cfg, W, tok, operands=None):
     return O.rmsnorm(x, W64["norm_f"], cfg.norm_eps)
 
 
-@pytest.mark.parametrize("T", [1040, 300])
+@pytest.mark.parametrize("T", [1040, 300, 2048])   # 2048 rows: CTA-pair GEMM tiles
 def test_full_attention_baseline_matches_oracle(T):
     cfg = dataclasses.replace(I.ARMT_1B, n_layers=2)
     W = I.make_weights(cfg, seed=31, norm_jitter=0.1)
