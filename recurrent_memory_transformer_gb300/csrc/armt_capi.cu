@@ -242,7 +242,7 @@ struct ModelBase {
     const int per_gemm = cfg.dtype == ARMT_BF16 ? 1 : 2;
     int64_t n = 0;
     if (lo == 0) n += 1;                    // layer-0 input gather
-    n += per_gemm + 1 + per_gemm;           // associative query GEMM, phi, read GEMM
+    n += per_gemm + (per_gemm == 1 ? 0 : 1) + per_gemm;  // query GEMM (+ phi on the fp32 path), read GEMM
     n += per_gemm + 1 + per_gemm;           // QKV GEMM, attention, O GEMM (norms fused)
     n += per_gemm + per_gemm;               // gate-up GEMM, down GEMM
     n += per_gemm + 2;                      // delta-rule write: projection GEMM, z, A rows
@@ -447,7 +447,7 @@ struct Model : ModelBase {
     CK(cudaMemsetAsync(d_err, 0, sizeof(int), st));
     // kernel configuration
     upd_smem = ((size_t)c.n_mem * P + 2 * c.n_mem) * sizeof(float);
-    feat_smem = ((size_t)c.n_mem * 2 * k + (size_t)c.n_mem * (P + 1)) * sizeof(float);
+    feat_smem = ((size_t)c.n_mem * 2 * k + (size_t)c.n_mem * (P + 1) + P) * sizeof(float);
     attn_smem = 2 * 64 * hd * sizeof(float);
     CK(cudaFuncSetAttribute(assoc_write_feat_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                             (int)feat_smem));
@@ -610,14 +610,20 @@ struct Model : ModelBase {
       CK(cudaGetLastError());
       CKS(prof_end(st));
     }
-    // associative read: q = Wq_a x, phi, den, then x' = x + A phi / den
-    CKS((gemm<64>(ARMT_KC_ASSOC_READ, w, w.tmXa, tmAWq, w.Xa, Rd, aWq, k, d,
-                  FStore{w.Qa, (long long)k, (long long)R * k}, lo, g, st, R)));
-    CKS(prof_begin(ARMT_KC_ASSOC_READ, st));
-    assoc_phi_kernel<AT><<<dim3(R, g), 128, 2 * k * sizeof(float), st>>>(
-        w.Qa, z, w.Phi, w.Den, R, k, c.dpfp_nu, c.assoc_eps, lo, T, nb);
-    CK(cudaGetLastError());
-    CKS(prof_end(st));
+    // associative read: q = Wq_a x, phi, den, then x' = x + A phi / den.  On the
+    // tensor-core path phi and den come out of the query GEMM's epilogue.
+    if constexpr (kTC) {
+      CKS((gemm<64, SEpiPhi<AT>>(ARMT_KC_ASSOC_READ, w, w.tmXa, tmAWq, w.Xa, Rd, aWq, k, d,
+                                 SEpiPhi<AT>{w.Phi, w.Den, z, R, T, nb, c.assoc_eps}, lo, g, st, R)));
+    } else {
+      CKS((gemm<64>(ARMT_KC_ASSOC_READ, w, w.tmXa, tmAWq, w.Xa, Rd, aWq, k, d,
+                    FStore{w.Qa, (long long)k, (long long)R * k}, lo, g, st, R)));
+      CKS(prof_begin(ARMT_KC_ASSOC_READ, st));
+      assoc_phi_kernel<AT><<<dim3(R, g), 128, 2 * k * sizeof(float), st>>>(
+          w.Qa, z, w.Phi, w.Den, R, k, c.dpfp_nu, c.assoc_eps, lo, T, nb);
+      CK(cudaGetLastError());
+      CKS(prof_end(st));
+    }
     // the read GEMM runs per (layer, sequence): groups lo*nb .. (hi+1)*nb - 1
     // of T rows, each with its own state
     const AT* Asrc = kTC ? w.Aa : reinterpret_cast<const AT*>(A);
@@ -973,7 +979,8 @@ static armt_status validate(const armt_config* c) {
     if (hd == 32) return fail(ARMT_ERR_UNSUPPORTED, "bf16 models need head_dim 64 or 128");
     if (d % 256 != 0 || Nq % 256 != 0)
       return fail(ARMT_ERR_SHAPE, "bf16: d_model and (Hq+2Hkv)*head_dim must be multiples of 256");
-    if (c->key_dim != 64) return fail(ARMT_ERR_UNSUPPORTED, "bf16: key_dim must be 64");
+    if (c->key_dim != 64 || c->dpfp_nu != 3)
+      return fail(ARMT_ERR_UNSUPPORTED, "bf16: key_dim must be 64 and dpfp_nu 3");
     if (P % 64 != 0 || (c->n_q_heads * hd) % 64 != 0 || F % 64 != 0)
       return fail(ARMT_ERR_SHAPE, "bf16: P, Hq*head_dim, ffn_dim must be multiples of 64");
   }

@@ -293,6 +293,56 @@ struct SEpiSwiGLU {
   __device__ void finish(int, int, int, int, float) const {}
 };
 
+// DPFP features and the read denominator straight from the associative
+// query GEMM, whose 64-wide tile holds the whole query q = Wq_a x of a row
+// (key_dim 64, nu 3, P = 384; the tensor-core path supports only that):
+//   r = [relu(q), relu(-q)],  phi_{128 (j-1) + c} = r_c r_{(c-j) mod 128}, j = 1..3,
+//   den = z^T phi + eps with z of the row's (layer, sequence) group,
+// phi stored in the activation dtype, den in fp32 (from the unrounded phi).
+// Per row, lane L computes p = L + 32 t, t < 12 (c = L + 32 (t mod 4), j = t / 4 + 1).
+template <typename AT>
+struct SEpiPhi {
+  static constexpr bool ROWSUM = false;
+  AT* phi;         // [groups][rows][384]
+  float* den;      // [groups][rows]
+  const float* z;  // [L * nb][384]
+  int rows, cell_rows, nb;
+  float eps;
+  __device__ static void unit(int u, int& a, int& b) { a = 64 * u; b = 64 * u + 32; }
+  __device__ bool direct_tile(int) const { return false; }
+  template <class Src> __device__ void direct(int, int, bool, int, int, Src&) const {}
+  __device__ float row_ctx(int, int, bool) const { return 0.f; }
+  // r_c of stage row `r` (stage columns 0..63 = q_0..q_63, 16-byte chunks swizzled by row & 7)
+  __device__ __forceinline__ static float r_at(const float* stage, int r, int c) {
+    const int e = c & 63;
+    const float q = stage[r * 64 + (((e >> 2) ^ (r & 7)) << 2) + (e & 3)];
+    return c < 64 ? fmaxf(q, 0.f) : fmaxf(-q, 0.f);
+  }
+  __device__ __forceinline__ void process(int l, int row0, int rows_, int, int, const float* stage,
+                                          float, float*) const {
+    const int lane = threadIdx.x & 31;
+#pragma unroll 1
+    for (int r = 0; r < 32; ++r) {
+      const int row = row0 + r;
+      if (row >= rows_) break;  // warp-uniform
+      const float* zr = z + ((long long)l * nb + row / cell_rows) * 384;
+      AT* out = phi + ((long long)l * rows + row) * 384;
+      float acc = 0.f;
+#pragma unroll
+      for (int t = 0; t < 12; ++t) {
+        const int j = t / 4 + 1;
+        const int c = lane + 32 * (t % 4);
+        const float f = r_at(stage, r, c) * r_at(stage, r, (c - j) & 127);
+        st_from_f32(out + 32 * t + lane, f);
+        acc = fmaf(zr[32 * t + lane], f, acc);
+      }
+      acc = warp_sum(acc);
+      if (lane == 0) den[(long long)l * rows + row] = acc + eps;
+    }
+  }
+  __device__ void finish(int, int, int, int, float) const {}
+};
+
 // Unit enumeration: functors with a runtime layout (RoPE heads) provide
 // unit_hd(); the rest a static unit().
 template <class E>

@@ -115,41 +115,49 @@ __global__ void assoc_phi_kernel(const float* __restrict__ q, const float* __res
 // The normaliser's recurrence does not involve A.  Expanding z_{i-1} gives
 //   zphi_i = z_0^T phi_i + sum_{i' < i} gamma_i' (phi_i'^T phi_i),
 // so the block computes every z_0^T phi_i and the Gram matrix G = Phi Phi^T
-// in parallel, then one thread runs the 16-step scalar recurrence, and
-// finally z_M = z_0 + sum_i gamma_i phi_i.  Stores phiM[l][i][:] and
-// coef[l][i] = {beta_i, 1 / (zphi_i + eps)} for the row update of A.
+// in parallel, then one thread runs the 16-step scalar recurrence on shared
+// memory, and finally z_M = z_0 + sum_i gamma_i phi_i.  Stores phiM[l][i][:]
+// and coef[l][i] = {beta_i, 1 / (zphi_i + eps)} for the row update of A.
 // vkb[l][i] = [v_i (d) | k_i (k) | beta logit | pad] (row stride nw), the
-// output of the memory-row projection GEMM.  M <= 32.
+// output of the memory-row projection GEMM.  Index arithmetic uses no
+// division: a warp takes one token, its lanes the feature columns.  M <= 32.
 __global__ void __launch_bounds__(256) assoc_write_feat_kernel(
     const float* __restrict__ vkb, float* __restrict__ z, float* __restrict__ phiM,
     float* __restrict__ coef, int M, int k, int nu, float eps, int d, int nw, int g_first) {
-  extern __shared__ float sm[];  // r: M * 2k, phi: M * (P + 1)
+  extern __shared__ float sm[];  // r: M * 2k, phi: M * (P + 1), z0: P
   __shared__ float G[32][33];
-  __shared__ float z0phi[32], gam[32];
+  __shared__ float z0phi[32], gam[32], logit[32];
   const int l = g_first + blockIdx.x;
   const int k2 = 2 * k, P = k2 * nu, Pp = P + 1;
   float* r = sm;
   float* ph = sm + M * k2;
-  for (int t = threadIdx.x; t < M * k; t += blockDim.x) {
-    const int i = t / k, c = t - i * k;
-    const float v = vkb[((long long)l * M + i) * nw + d + c];
-    r[i * k2 + c] = v > 0.f ? v : 0.f;
-    r[i * k2 + c + k] = v < 0.f ? -v : 0.f;
+  float* zs = ph + M * Pp;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  float* zl = z + (long long)l * P;
+  for (int i = warp; i < M; i += nwarp) {
+    const float* src = vkb + ((long long)l * M + i) * nw + d;
+    for (int c = lane; c < k; c += 32) {
+      const float v = src[c];
+      r[i * k2 + c] = v > 0.f ? v : 0.f;
+      r[i * k2 + c + k] = v < 0.f ? -v : 0.f;
+    }
+    if (lane == 0) logit[i] = src[k];
   }
+  for (int p = threadIdx.x; p < P; p += blockDim.x) zs[p] = zl[p];
   __syncthreads();
-  for (int t = threadIdx.x; t < M * P; t += blockDim.x) {
-    const int i = t / P, p = t - i * P;
-    const int j = p / k2 + 1, c = p - (j - 1) * k2;
-    int src = c - j;
-    src = src < 0 ? src + k2 : src;
-    const float f = r[i * k2 + c] * r[i * k2 + src];
-    ph[i * Pp + p] = f;
-    phiM[((long long)l * M + i) * P + p] = f;
+  for (int i = warp; i < M; i += nwarp) {
+    const float* ri = r + i * k2;
+    float* out = phiM + ((long long)l * M + i) * P;
+    for (int j = 1; j <= nu; ++j)
+      for (int c = lane; c < k2; c += 32) {
+        const int src = c - j < 0 ? c - j + k2 : c - j;
+        const float f = ri[c] * ri[src];
+        ph[i * Pp + (j - 1) * k2 + c] = f;
+        out[(j - 1) * k2 + c] = f;
+      }
   }
   __syncthreads();
   // G[i][i2] (i <= i2) and z_0^T phi_i: one warp per dot product
-  float* zl = z + (long long)l * P;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
   const int npairs = M * (M + 1) / 2;
   for (int t = warp; t < npairs + M; t += nwarp) {
     float acc = 0.f;
@@ -168,7 +176,7 @@ __global__ void __launch_bounds__(256) assoc_write_feat_kernel(
       }
     } else {
       const int i = t - npairs;
-      for (int p = lane; p < P; p += 32) acc += zl[p] * ph[i * Pp + p];
+      for (int p = lane; p < P; p += 32) acc += zs[p] * ph[i * Pp + p];
       acc = warp_sum(acc);
       if (lane == 0) z0phi[i] = acc;
     }
@@ -179,16 +187,19 @@ __global__ void __launch_bounds__(256) assoc_write_feat_kernel(
       float zp = z0phi[i];
       for (int i2 = 0; i2 < i; ++i2) zp += gam[i2] * G[i2][i];
       gam[i] = fminf(fmaxf(1.0f - zp / (G[i][i] + eps), 0.0f), 1.0f);  // keeps z >= 0
-      const float logit = vkb[((long long)l * M + i) * nw + d + k];
-      coef[((long long)l * M + i) * 2 + 0] = sigmoid_f(logit);
-      coef[((long long)l * M + i) * 2 + 1] = 1.0f / (zp + eps);
+      z0phi[i] = zp;  // now z_{i-1}^T phi_i
     }
   }
   __syncthreads();
+  if (threadIdx.x < M) {
+    const int i = threadIdx.x;
+    coef[((long long)l * M + i) * 2 + 0] = sigmoid_f(logit[i]);
+    coef[((long long)l * M + i) * 2 + 1] = 1.0f / (z0phi[i] + eps);
+  }
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
     float dz = 0.f;
     for (int i = 0; i < M; ++i) dz += gam[i] * ph[i * Pp + p];
-    zl[p] += dz;
+    zl[p] = zs[p] + dz;
   }
 }
 
