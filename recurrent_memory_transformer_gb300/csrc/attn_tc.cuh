@@ -360,8 +360,10 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
   }
 }
 
+// Internal linkage: every translation unit that launches the kernel configures
+// (shared-memory opt-in) and launches its own copy of it.
 template <int HD>
-cudaError_t launch_attn_tc(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnArgs& a,
+static cudaError_t launch_attn_tc(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnArgs& a,
                            int g_count, int num_sms, cudaStream_t stream) {
   using C = AttnCfg<HD>;
   static bool configured = false;

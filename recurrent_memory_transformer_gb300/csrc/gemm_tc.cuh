@@ -218,8 +218,9 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
 bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int K, int rows, int layers,
                          int box_rows);
 
+// Internal linkage: each translation unit configures and launches its own copy.
 template <class Epi, int BN, int EPI_WG = 1>
-cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int rows, int N, int K,
+static cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int rows, int N, int K,
                            int g_first, int g_count, int* err, const Epi& epi, int num_sms,
                            cudaStream_t stream, const GemmGroupMap& map = GemmGroupMap()) {
   using C = TcCfg<BN, EPI_WG>;

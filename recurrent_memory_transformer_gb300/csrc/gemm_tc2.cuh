@@ -210,7 +210,7 @@ inline bool pair_tiles_pay_off(long long rows) {
 // Launch with clusters of two; the grid is the number of co-resident pairs
 // (queried once per kernel), at most the number of pair tiles.
 template <class Epi, int EPI_WG = 1>
-cudaError_t launch_gemm_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, int rows, int N, int K,
+static cudaError_t launch_gemm_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, int rows, int N, int K,
                             int g_first, int g_count, int* err, const Epi& epi, int num_sms,
                             cudaStream_t stream, const GemmGroupMap& map = GemmGroupMap()) {
   using C = Tc2Cfg<EPI_WG>;
