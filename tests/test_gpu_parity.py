@@ -105,6 +105,31 @@ def test_grouped_gemm_bf16_matches_fp64_matmul(G, M, N, K):
     assert err <= 1e-5 * K * 4, err
 
 
+def test_grouped_gemm_reproduces_printed_integer_example():
+    # The two chained linear layers printed as a worked example
+    # (tests/golden/two_linear_layers_small_integers.txt), zero-padded to the
+    # kernel's tiling (K % 64, N % 256); every value is exact in bf16/fp32,
+    # so the grouped GEMM must reproduce the printed numbers exactly.
+    from tests.golden.load import read_matrices
+    g = read_matrices("two_linear_layers_small_integers.txt")
+
+    def gemm(a, w_in_out):
+        M, K = a.shape
+        N = w_in_out.shape[1]
+        A = torch.zeros(1, M, 64, dtype=torch.bfloat16)
+        A[0, :, :K] = torch.from_numpy(a).to(torch.bfloat16)
+        Bm = torch.zeros(1, 256, 64, dtype=torch.bfloat16)
+        Bm[0, :N, :K] = torch.from_numpy(w_in_out.T.copy()).to(torch.bfloat16)
+        C = torch.full((1, M, 256), float("nan"), device="cuda")
+        B.armt_grouped_gemm_bf16(A.cuda(), Bm.cuda(), C)
+        torch.cuda.synchronize()
+        return C[0, :, :N].double().cpu().numpy()
+
+    inter = gemm(g["x"], g["weights_A"])
+    np.testing.assert_array_equal(inter, g["intermediate"])
+    np.testing.assert_array_equal(gemm(inter, g["weights_B"]), g["output"])
+
+
 def test_grouped_gemm_each_group_independent():
     # a group's result does not depend on how many groups share the launch
     g = torch.Generator(device="cpu").manual_seed(7)

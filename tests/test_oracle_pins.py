@@ -409,3 +409,18 @@ def test_relative_logits_error_closed_forms():
     assert O.relative_logits_error(ref, ref) == 0.0
     assert abs(O.relative_logits_error(1.01 * ref, ref) - 0.01) < 1e-12
     assert abs(O.relative_logits_error(np.zeros_like(ref), ref) - 1.0) < 1e-15
+
+
+def test_linear_map_matches_printed_two_layer_example():
+    # A worked example printed on a page of the same bundle (two chained linear
+    # layers on small integers, tests/golden/two_linear_layers_small_integers.txt):
+    # the oracle's linear map (rows times the transpose of an (out, in) matrix,
+    # the form of every projection and of the LM head) reproduces it exactly.
+    from tests.golden.load import read_matrices
+    g = read_matrices("two_linear_layers_small_integers.txt")
+    inter = O.lm_head_logits(g["x"], g["weights_A"].T)        # (out, in) = transpose of (in, out)
+    np.testing.assert_array_equal(inter, g["intermediate"])
+    out = O.lm_head_logits(inter, g["weights_B"].T)
+    np.testing.assert_array_equal(out, g["output"])
+    # a transposed operand would give a different (or ill-shaped) product
+    assert not np.array_equal(O.lm_head_logits(g["x"].T, g["weights_A"].T), g["intermediate"])
