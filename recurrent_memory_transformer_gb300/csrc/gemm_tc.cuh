@@ -141,11 +141,18 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      // A last row tile with at most 16 valid rows (the memory rows that close
+      // a 1040-row cell, or a 16-row write projection) runs as an M = 64 MMA:
+      // half the tensor work of M = 128 for the same 16 rows, which land in
+      // TMEM lanes 0..15 with either M -- the lanes the epilogue reads for them.
       constexpr uint32_t idesc = idesc_bf16_f32(TC_BM, BN);
+      constexpr uint32_t idesc64 = idesc_bf16_f32(64, BN);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        const int mt = (t % tiles_per_g) % sh.m_tiles;
+        const uint32_t id = sh.rows - mt * TC_BM <= 16 ? idesc64 : idesc;
         if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, sh.err, DEV_TIMEOUT_ACC_EMPTY)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -160,7 +167,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
 #pragma unroll
           for (int k = 0; k < TC_BK / 16; ++k) {
             // advance 16 bf16 = 32 bytes along K inside the swizzled row
-            tc_mma_bf16(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
+            tc_mma_bf16(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), id,
                         (kb | k) != 0 ? 1u : 0u);
           }
           tc_commit(&empty[stage]);  // stage reusable once these MMAs finish
