@@ -276,7 +276,7 @@ def main():
     # traffic scales with cells (each cell's layer weights + activations), so
     # per launch it is this times the launch's cells.  None until a capture
     # of the current kernel exists.
-    GATEUP_DRAM_BYTES_PER_CELL_1B = None
+    GATEUP_DRAM_BYTES_PER_CELL_1B = 86.4e6
     gu_traffic = (GATEUP_DRAM_BYTES_PER_CELL_1B * cells / gu_launches
                   if (GATEUP_DRAM_BYTES_PER_CELL_1B and gu_launches and args.workload.startswith("armt-1b"))
                   else None)
