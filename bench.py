@@ -445,7 +445,7 @@ def main():
                        "batch": 1, "schedule": "diagonal", "parallelism": "replicas" if world > 1 else "single",
                        "l2": "no flush: every diagonal re-reads all layers' weights (~2 GB) and "
                              "~1 GB of activations, far above the 129 MB L2"},
-            "roofline": {"bound": "tensor", "kernel": "grouped GEMM gate-up + SwiGLU (tcgen05, CTA pairs)",
+            "roofline": {"bound": "tensor", "kernel": "grouped GEMM gate-up + SwiGLU (tcgen05)",
                          "achieved": gu_tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": (gu_tflops / peak) if gu_tflops else None, "traffic": gu_traffic,
                          "traffic_unit": "bytes per launch (ncu dram__bytes_read+write, scaled by cells)",

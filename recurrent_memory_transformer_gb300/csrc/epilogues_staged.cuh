@@ -299,9 +299,12 @@ struct SEpiSwiGLU {
 //   r = [relu(q), relu(-q)],  phi_{128 (j-1) + c} = r_c r_{(c-j) mod 128}, j = 1..3,
 //   den = z^T phi + eps with z of the row's (layer, sequence) group,
 // phi stored in the activation dtype, den in fp32 (from the unrounded phi).
-// Per row, lane L computes p = L + 32 t, t < 12 (c = L + 32 (t mod 4), j = t / 4 + 1).
+// Per row, lane L computes the pairs p, p + 1 with p = 64 t + 2 L, t < 6
+// (c = 2 L + 64 (t mod 2), j = t / 2 + 1) and stores them as one bf16 pair; z
+// is reloaded only when the rows pass into another sequence's cell.
 template <typename AT>
 struct SEpiPhi {
+  static_assert(sizeof(AT) == 2, "bf16 features");
   static constexpr bool ROWSUM = false;
   AT* phi;         // [groups][rows][384]
   float* den;      // [groups][rows]
@@ -321,20 +324,30 @@ struct SEpiPhi {
   __device__ __forceinline__ void process(int l, int row0, int rows_, int, int, const float* stage,
                                           float, float*) const {
     const int lane = threadIdx.x & 31;
+    int cell = -1;
+    float2 zz[6];
 #pragma unroll 1
     for (int r = 0; r < 32; ++r) {
       const int row = row0 + r;
       if (row >= rows_) break;  // warp-uniform
-      const float* zr = z + ((long long)l * nb + row / cell_rows) * 384;
-      AT* out = phi + ((long long)l * rows + row) * 384;
+      const int cb = row / cell_rows;
+      if (cb != cell) {
+        cell = cb;
+        const float* zr = z + ((long long)l * nb + cb) * 384 + 2 * lane;
+#pragma unroll
+        for (int t = 0; t < 6; ++t) zz[t] = *reinterpret_cast<const float2*>(zr + 64 * t);
+      }
+      uint32_t* out = reinterpret_cast<uint32_t*>(phi + ((long long)l * rows + row) * 384) + lane;
       float acc = 0.f;
 #pragma unroll
-      for (int t = 0; t < 12; ++t) {
-        const int j = t / 4 + 1;
-        const int c = lane + 32 * (t % 4);
-        const float f = r_at(stage, r, c) * r_at(stage, r, (c - j) & 127);
-        st_from_f32(out + 32 * t + lane, f);
-        acc = fmaf(zr[32 * t + lane], f, acc);
+      for (int t = 0; t < 6; ++t) {
+        const int j = t / 2 + 1;
+        const int c = 2 * lane + 64 * (t % 2);
+        const float f0 = r_at(stage, r, c) * r_at(stage, r, (c - j) & 127);
+        const float f1 = r_at(stage, r, c + 1) * r_at(stage, r, (c + 1 - j) & 127);
+        out[32 * t] = pack_bf16x2(f0, f1);
+        acc = fmaf(zz[t].x, f0, acc);
+        acc = fmaf(zz[t].y, f1, acc);
       }
       acc = warp_sum(acc);
       if (lane == 0) den[(long long)l * rows + row] = acc + eps;
