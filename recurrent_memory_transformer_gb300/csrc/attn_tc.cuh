@@ -366,7 +366,7 @@ template <int HD>
 static cudaError_t launch_attn_tc(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnArgs& a,
                            int g_count, int num_sms, cudaStream_t stream) {
   using C = AttnCfg<HD>;
-  static bool configured = false;
+  static std::atomic<bool> configured{false};  // once per translation unit (set-up is idempotent)
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);

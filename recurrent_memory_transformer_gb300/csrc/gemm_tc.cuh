@@ -231,7 +231,7 @@ static cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB
                            int g_first, int g_count, int* err, const Epi& epi, int num_sms,
                            cudaStream_t stream, const GemmGroupMap& map = GemmGroupMap()) {
   using C = TcCfg<BN, EPI_WG>;
-  static bool configured = false;
+  static std::atomic<bool> configured{false};  // once per translation unit (set-up is idempotent)
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<Epi, BN, EPI_WG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);

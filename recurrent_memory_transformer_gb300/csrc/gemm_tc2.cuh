@@ -214,7 +214,7 @@ static cudaError_t launch_gemm_tc2(const CUtensorMap& tmA, const CUtensorMap& tm
                             int g_first, int g_count, int* err, const Epi& epi, int num_sms,
                             cudaStream_t stream, const GemmGroupMap& map = GemmGroupMap()) {
   using C = Tc2Cfg<EPI_WG>;
-  static int max_clusters = 0;
+  static std::atomic<int> max_clusters{0};  // once per translation unit (the query is idempotent)
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -249,7 +249,8 @@ static cudaError_t launch_gemm_tc2(const CUtensorMap& tmA, const CUtensorMap& tm
   sh.k_blocks = K / TC_BK;
   sh.err = err;
   const int tiles = g_count * ((rows + 2 * TC_BM - 1) / (2 * TC_BM)) * sh.n_tiles;
-  const int clusters = tiles < max_clusters ? tiles : max_clusters;
+  const int mc = max_clusters.load();
+  const int clusters = tiles < mc ? tiles : mc;
   if (clusters <= 0) return cudaSuccess;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   return cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<Epi, EPI_WG>, tmA, tmB, sh, epi);
