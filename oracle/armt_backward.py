@@ -1,0 +1,168 @@
+"""fp64 gradients of the ARMT forward pass: the reference for a backward pass.
+
+TEST INFRASTRUCTURE ONLY, like ``armt_oracle``: only the tests may import
+this module; the library and its binding never do, and it imports nothing
+from them.
+
+The summary page of "Diagonal Batching Unlocks Parallelism in Recurrent
+Memory Transformers for Long Contexts" (section 四) reports that diagonal
+batching was also carried over to the backward pass so that training and
+inference share one schedule.  The backward of the recurrence is the adjoint
+of the forward that ``armt_oracle.forward`` defines: every cell (l, s) passes
+gradients back to its input rows (cell (l-1, s)) and to the state it read
+(cell (l, s-1)), and each layer's weights collect the gradients of all of its
+cells.  Here that forward is restated term by term on torch float64 CPU
+tensors -- the same definitions, in the same order: associative read, LLaMA
+block, delta-rule writes of the memory rows one after another, final RMSNorm
+of the segment rows -- and differentiated with torch's reverse-mode autograd,
+used as a library primitive.  Nothing is fused or reordered; a short last
+segment and an initial state are handled as in the oracle.
+
+The loss is the inner product of the outputs with fixed cotangents:
+    loss = <hidden, R_h> + <A_final, R_A> + <z_final, R_z>,
+so its gradient is the vector-Jacobian product a backward kernel computes.
+Pinned in tests/test_backward_oracle.py: the restated forward agrees with
+``armt_oracle.forward``; directional derivatives agree with central finite
+differences of ``armt_oracle.forward`` for every weight group and the initial
+state; the diagonal and sequential cell orders give the same gradients;
+gradients respect causality (later segments do not influence earlier
+outputs) and vanish for embedding rows no token uses.
+"""
+from typing import Dict, Optional, Tuple
+
+import numpy as np
+import torch
+
+from . import armt_oracle as O
+
+F64 = torch.float64
+WEIGHT_KEYS = ("embed", "mem", "wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "a_wq", "a_wk",
+               "a_wv", "a_wbeta", "norm1", "norm2", "norm_f")
+
+
+def _t(a, grad=False):
+    t = torch.as_tensor(np.asarray(a, dtype=np.float64), dtype=F64).clone()
+    return t.requires_grad_(grad)
+
+
+def rmsnorm(x, gain, eps):
+    return x / torch.sqrt((x * x).mean(dim=-1, keepdim=True) + eps) * gain
+
+
+def dpfp(x, nu):
+    r = torch.cat([torch.relu(x), torch.relu(-x)], dim=-1)
+    return torch.cat([r * torch.roll(r, j, dims=-1) for j in range(1, nu + 1)], dim=-1)
+
+
+def rope_rotate_half(x, base):
+    T, _, hd = x.shape
+    half = hd // 2
+    inv_freq = base ** (-(2.0 * torch.arange(half, dtype=F64)) / hd)
+    ang = torch.arange(T, dtype=F64)[:, None] * inv_freq[None, :]
+    cos, sin = torch.cos(ang)[:, None, :], torch.sin(ang)[:, None, :]
+    x1, x2 = x[..., :half], x[..., half:]
+    return torch.cat([x1 * cos - x2 * sin, x2 * cos + x1 * sin], dim=-1)
+
+
+def causal_gqa_attention(q, k, v):
+    T, Hq, hd = q.shape
+    Hkv = k.shape[1]
+    mask = torch.triu(torch.ones((T, T), dtype=torch.bool), diagonal=1)
+    heads = []
+    for h in range(Hq):
+        g = (h * Hkv) // Hq
+        s = (q[:, h, :] @ k[:, g, :].T) / np.sqrt(hd)
+        p = torch.softmax(s.masked_fill(mask, float("-inf")), dim=-1)
+        heads.append(p @ v[:, g, :])
+    return torch.stack(heads, dim=1).reshape(T, Hq * hd)
+
+
+def assoc_read(x, wq_a, A, z, nu, eps):
+    phi = dpfp(x @ wq_a.T, nu)
+    return x + (phi @ A.T) / (phi @ z + eps)[:, None]
+
+
+def delta_rule_write(A, z, key, value, beta, nu, eps):
+    """One write (key [k], value [d], beta scalar) against the current state."""
+    phi = dpfp(key, nu)
+    zphi = phi @ z
+    vbar = (A @ phi) / (zphi + eps)
+    gamma = torch.clamp(1.0 - zphi / (phi @ phi + eps), 0.0, 1.0)
+    return A + torch.outer(beta * (value - vbar), phi), z + gamma * phi
+
+
+def llama_block(x, cfg, W, l):
+    T = x.shape[0]
+    Hq, Hkv, hd = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    n = rmsnorm(x, W["norm1"][l], cfg.norm_eps)
+    q = rope_rotate_half((n @ W["wq"][l].T).reshape(T, Hq, hd), cfg.rope_base)
+    k = rope_rotate_half((n @ W["wk"][l].T).reshape(T, Hkv, hd), cfg.rope_base)
+    v = (n @ W["wv"][l].T).reshape(T, Hkv, hd)
+    y = x + causal_gqa_attention(q, k, v) @ W["wo"][l].T
+    n2 = rmsnorm(y, W["norm2"][l], cfg.norm_eps)
+    u = torch.nn.functional.silu(n2 @ W["w_gate"][l].T) * (n2 @ W["w_up"][l].T)
+    return y + u @ W["w_down"][l].T
+
+
+def cell_forward(x, cfg, W, l, A, z):
+    nu, eps = cfg.dpfp_nu, cfg.assoc_eps
+    x = assoc_read(x, W["a_wq"][l], A, z, nu, eps)
+    h = llama_block(x, cfg, W, l)
+    m0 = h.shape[0] - cfg.n_mem
+    hm = h[m0:]
+    keys, values = hm @ W["a_wk"][l].T, hm @ W["a_wv"][l].T
+    beta = torch.sigmoid(hm @ W["a_wbeta"][l])
+    for i in range(hm.shape[0]):
+        A, z = delta_rule_write(A, z, keys[i], values[i], beta[i], nu, eps)
+    return h, A, z
+
+
+def forward(cfg, W, tokens, n_segments, order="seq", A0=None, z0=None):
+    """The oracle's forward on torch tensors; W: dict of float64 tensors
+    (leaves that may require grad), A0 [L, d, P] / z0 [L, P] tensors or None.
+    Returns (hidden [N, d], A [L, d, P], z [L, P])."""
+    L, d, P, S = cfg.n_layers, cfg.d_model, cfg.phi_dim, cfg.seg_len
+    tokens = np.asarray(tokens)
+    N = tokens.shape[0]
+    assert (n_segments - 1) * S < N <= n_segments * S
+    A = [A0[l] if A0 is not None else torch.zeros((d, P), dtype=F64) for l in range(L)]
+    z = [z0[l] if z0 is not None else torch.zeros((P,), dtype=F64) for l in range(L)]
+    acts, rows = {}, [None] * n_segments
+    for step in O.schedule(L, n_segments, order):
+        for (l, s) in step:
+            if l == 0:
+                ids = torch.as_tensor(tokens[s * S:(s + 1) * S], dtype=torch.long)
+                x = torch.cat([W["embed"][ids], W["mem"]], dim=0)
+            else:
+                x = acts.pop((l - 1, s))
+            h, A[l], z[l] = cell_forward(x, cfg, W, l, A[l], z[l])
+            if l == L - 1:
+                seg = h.shape[0] - cfg.n_mem
+                rows[s] = rmsnorm(h[:seg], W["norm_f"], cfg.norm_eps)
+            else:
+                acts[(l, s)] = h
+    return torch.cat(rows, dim=0), torch.stack(A), torch.stack(z)
+
+
+def loss_value(out: Tuple, cot: Dict[str, np.ndarray]) -> float:
+    """<hidden, R_h> + <A, R_A> + <z, R_z> for numpy outputs (fp64)."""
+    h, A, z = (np.asarray(o, np.float64) for o in out)
+    return float(np.sum(h * cot["hidden"]) + np.sum(A * cot["A"]) + np.sum(z * cot["z"]))
+
+
+def gradients(cfg, W: Dict[str, np.ndarray], tokens, n_segments, cot: Dict[str, np.ndarray],
+              order="seq", A0: Optional[np.ndarray] = None, z0: Optional[np.ndarray] = None):
+    """Gradient of the loss above with respect to every weight (and to the
+    initial state A0, z0 when given).  Returns (loss, {name: fp64 array})."""
+    Wt = {k: _t(W[k], grad=True) for k in WEIGHT_KEYS}
+    A0t = _t(A0, grad=True) if A0 is not None else None
+    z0t = _t(z0, grad=True) if z0 is not None else None
+    h, A, z = forward(cfg, Wt, tokens, n_segments, order, A0t, z0t)
+    loss = (h * _t(cot["hidden"])).sum() + (A * _t(cot["A"])).sum() + (z * _t(cot["z"])).sum()
+    leaves = [Wt[k] for k in WEIGHT_KEYS] + [t for t in (A0t, z0t) if t is not None]
+    grads = torch.autograd.grad(loss, leaves, allow_unused=True)
+    names = list(WEIGHT_KEYS) + [n for n, t in (("A0", A0t), ("z0", z0t)) if t is not None]
+    out = {}
+    for n, g, leaf in zip(names, grads, leaves):
+        out[n] = (g if g is not None else torch.zeros_like(leaf)).detach().numpy()
+    return float(loss.detach()), out
