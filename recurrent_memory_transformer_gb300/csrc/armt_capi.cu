@@ -35,6 +35,7 @@
 #include "gemm_tc.cuh"
 #include "gemm_tc2.cuh"
 #include "kernels.cuh"
+#include "schedule.h"
 
 using namespace armt;
 
@@ -253,10 +254,9 @@ struct ModelBase {
     const int L = cfg.n_layers;
     int64_t total = (mem_in_valid && cfg.dtype == ARMT_BF16) ? 1 : 0;  // state copy
     if (schedule == ARMT_SCHEDULE_DIAGONAL) {
-      for (int64_t i = 0; i < L + n_seg - 1; ++i) {
-        const int lo = (int)(i - n_seg + 1 > 0 ? i - n_seg + 1 : 0);
-        const int hi = (int)(i < L - 1 ? i : L - 1);
-        total += step_launches(lo, hi);
+      for (int64_t i = 0; i < diagonal_steps(L, n_seg); ++i) {
+        const CellRange c = diagonal_step(i, L, n_seg);
+        total += step_launches(c.lo, c.hi);
       }
     } else {
       for (int64_t s = 0; s < n_seg; ++s)
@@ -599,8 +599,8 @@ struct Model : ModelBase {
     const int g = hi - lo + 1, nb = w.nb, R = nb * T;
     const long long Rd = (long long)R * d;
     // the last segment holds last_len <= S tokens; its memory rows follow them
-    const int last_len = (int)(n_tok - (n_seg - 1) * S);
-    const int64_t l_last = lo + (s_lo - (n_seg - 1));  // layer of the last segment's cell
+    const int last_len = last_segment_len(n_tok, S);
+    const int64_t l_last = last_segment_layer(lo, s_lo, n_seg);  // layer of the last segment's cell
     const bool short_here = last_len < S && l_last >= lo && l_last <= hi;
     if (lo == 0) {
       const int n_rows = s_lo == n_seg - 1 ? last_len : S;
@@ -911,7 +911,7 @@ struct Model : ModelBase {
   armt_status forward(const int32_t* tokens, int64_t n_tok, int nb, float* hidden, float* A,
                       float* z, int mem_in_valid, int schedule, cudaStream_t st) override {
     const int L = cfg.n_layers, d = cfg.d_model, P = phi_dim(), S = cfg.seg_len;
-    const int64_t n = (n_tok + S - 1) / S;
+    const int64_t n = n_segments_for(n_tok, S);
     if (nb > 1) CKS(ensure_batch(nb, st));
     Work& w = nb == 1 ? w1 : wb;
     const size_t a_n = (size_t)L * nb * d * P, z_n = (size_t)L * nb * P;
@@ -927,21 +927,16 @@ struct Model : ModelBase {
     }
     const bool report = sink != nullptr && nb == 1;
     if (schedule == ARMT_SCHEDULE_DIAGONAL) {
-      for (int64_t i = 0; i < L + n - 1; ++i) {
-        const int lo = (int)(i - n + 1 > 0 ? i - n + 1 : 0);
-        const int hi = (int)(i < L - 1 ? i : L - 1);
-        CKS(step(w, lo, hi, i - lo, tokens, n_tok, n, hidden, A, z, st));
-        if (report) {
-          // after step i: segments 0..i-L+1 have left the last layer, and
-          // layers 0..i-n+1 have run their last segment
-          const int64_t segs = std::max<int64_t>(0, i - L + 2);
-          CKS(sink_progress(std::min<int64_t>(n_tok, segs * S), (int)std::max<int64_t>(0, i - n + 2), st));
-        }
+      for (int64_t i = 0; i < diagonal_steps(L, n); ++i) {
+        const CellRange c = diagonal_step(i, L, n);
+        CKS(step(w, c.lo, c.hi, c.s_lo, tokens, n_tok, n, hidden, A, z, st));
+        if (report)
+          CKS(sink_progress(diagonal_rows_final(i, L, S, n_tok), diagonal_layers_final(i, n), st));
       }
     } else {
       for (int64_t s = 0; s < n; ++s) {
         for (int l = 0; l < L; ++l) CKS(step(w, l, l, s, tokens, n_tok, n, hidden, A, z, st));
-        if (report) CKS(sink_progress(std::min<int64_t>(n_tok, (s + 1) * S), s == n - 1 ? L : 0, st));
+        if (report) CKS(sink_progress(sequential_rows_final(s, S, n_tok), sequential_layers_final(s, n, L), st));
       }
     }
     return ARMT_OK;

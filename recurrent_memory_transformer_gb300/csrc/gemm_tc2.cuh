@@ -33,6 +33,7 @@
 #include "epilogues.cuh"
 #include "epilogues_staged.cuh"
 #include "gemm_tc.cuh"
+#include "schedule.h"  // pair_tiles_pay_off
 
 namespace armt {
 
@@ -195,16 +196,6 @@ __global__ void __launch_bounds__(Tc2Cfg<EPI_WG>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
   }
-}
-
-// Pair tiles cover 256 rows, single-CTA tiles 128: for a product of `rows`
-// rows the pair kernel computes up to 255 padding rows against 127.  Where
-// that padding is a few percent of the work the pair kernel is faster; for
-// short cells (1040 rows: 1280 vs 1152 computed) the extra tensor work costs
-// more than the pair saves.  Pairs are used when they pad at most 3 % more.
-inline bool pair_tiles_pay_off(long long rows) {
-  const long long p = (rows + 255) / 256 * 256, s1 = (rows + 127) / 128 * 128;
-  return p * 100 <= s1 * 103;
 }
 
 // Launch with clusters of two; the grid is the number of co-resident pairs
