@@ -112,3 +112,18 @@ def test_valid_config_reports_missing_device_without_gpu(lib):
     w, keep = _weights_struct(I.TINY)
     h = ctypes.c_void_p()
     assert lib.armt_create(ctypes.byref(c), ctypes.byref(w), None, ctypes.byref(h)) == 7
+
+
+def test_binding_argument_counts_match_the_header(lib):
+    # every entry point the header declares takes as many arguments as the
+    # ctypes binding passes (a mismatch would only surface on a GPU)
+    src = open(os.path.join(ROOT, "include", "armt.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    for m in re.finditer(r"ARMT_API\s+[\w\s\*]+?\b(armt_\w+)\s*\(([^)]*)\)", src):
+        name, params = m.group(1), m.group(2).strip()
+        n = 0 if params in ("", "void") else len(params.split(","))
+        argtypes = getattr(lib, name).argtypes
+        if argtypes is None:
+            assert n == 0, name
+        else:
+            assert len(argtypes) == n, (name, len(argtypes), n)
