@@ -27,6 +27,12 @@ differences of ``armt_oracle.forward`` for every weight group and the initial
 state; the diagonal and sequential cell orders give the same gradients;
 gradients respect causality (later segments do not influence earlier
 outputs) and vanish for embedding rows no token uses.
+
+``backward_by_diagonals`` computes the same gradients in the order a
+diagonal-batched backward pass would: anti-diagonals in reverse, each cell's
+vector-Jacobian product handing adjoints to the cell below it (same segment)
+and to the cell before it (same layer); pinned against the whole-graph
+gradient.
 """
 from typing import Dict, Optional, Tuple
 
@@ -166,3 +172,83 @@ def gradients(cfg, W: Dict[str, np.ndarray], tokens, n_segments, cot: Dict[str, 
     for n, g, leaf in zip(names, grads, leaves):
         out[n] = (g if g is not None else torch.zeros_like(leaf)).detach().numpy()
     return float(loss.detach()), out
+
+
+def backward_by_diagonals(cfg, W: Dict[str, np.ndarray], tokens, n_segments, cot: Dict[str, np.ndarray],
+                          A0: Optional[np.ndarray] = None, z0: Optional[np.ndarray] = None):
+    """The same gradients, computed the way a diagonal-batched backward pass
+    runs: anti-diagonals in reverse order (i = L + n - 2 down to 0), every
+    cell (l, s) of a diagonal taking the adjoints of its outputs -- its rows
+    from cell (l+1, s) (or the final RMSNorm when l = L-1) and its written
+    state from cell (l, s+1) (or the final-state cotangent) -- and returning
+    the adjoints of its input rows (to cell (l-1, s), or to the embeddings)
+    and of the state it read (to cell (l, s-1), or to A0/z0), plus its share
+    of layer l's weight gradients.  The cell's vector-Jacobian product is
+    taken on a recomputed forward of that one cell (the forward keeps only
+    cell inputs and states).  Returns {name: fp64 array} like ``gradients``."""
+    L, d, P, S, M = cfg.n_layers, cfg.d_model, cfg.phi_dim, cfg.seg_len, cfg.n_mem
+    tokens = np.asarray(tokens)
+    n = n_segments
+    Wt = {k: _t(W[k]) for k in WEIGHT_KEYS}
+    # forward, keeping what each cell read: its input rows and the state before it
+    x_in, state_in = {}, {}
+    A = [_t(A0[l]) if A0 is not None else torch.zeros((d, P), dtype=F64) for l in range(L)]
+    z = [_t(z0[l]) if z0 is not None else torch.zeros((P,), dtype=F64) for l in range(L)]
+    acts = {}
+    with torch.no_grad():
+        for step in O.schedule(L, n, "diag"):
+            for (l, s) in step:
+                if l == 0:
+                    ids = torch.as_tensor(tokens[s * S:(s + 1) * S], dtype=torch.long)
+                    x = torch.cat([Wt["embed"][ids], Wt["mem"]], dim=0)
+                else:
+                    x = acts.pop((l - 1, s))
+                x_in[(l, s)], state_in[(l, s)] = x, (A[l], z[l])
+                h, A[l], z[l] = cell_forward(x, cfg, Wt, l, A[l], z[l])
+                if l < L - 1:
+                    acts[(l, s)] = h
+    grads = {k: torch.zeros_like(Wt[k]) for k in WEIGHT_KEYS}
+    gA0, gz0 = torch.zeros((L, d, P), dtype=F64), torch.zeros((L, P), dtype=F64)
+    h_bar = {}                                             # adjoint of each cell's output rows
+    st_bar = {l: (_t(cot["A"][l]), _t(cot["z"][l])) for l in range(L)}  # adjoint of the state a cell wrote
+    R_h = _t(cot["hidden"])
+    for i in reversed(range(L + n - 1)):
+        for l in range(L):
+            s = i - l
+            if not 0 <= s < n:
+                continue
+            x = x_in[(l, s)].clone().requires_grad_(True)
+            Ain = state_in[(l, s)][0].clone().requires_grad_(True)
+            zin = state_in[(l, s)][1].clone().requires_grad_(True)
+            Wl = {k: (Wt[k].clone().requires_grad_(True) if k != "embed" else Wt[k]) for k in WEIGHT_KEYS}
+            h, A_out, z_out = cell_forward(x, cfg, Wl, l, Ain, zin)
+            Abar, zbar = st_bar[l]
+            terms = (A_out * Abar).sum() + (z_out * zbar).sum()
+            if l == L - 1:
+                seg = h.shape[0] - M
+                lo_row = s * S
+                terms = terms + (rmsnorm(h[:seg], Wl["norm_f"], cfg.norm_eps) * R_h[lo_row:lo_row + seg]).sum()
+            else:
+                terms = terms + (h * h_bar.pop((l, s))).sum()
+            leaves = [x, Ain, zin] + [Wl[k] for k in WEIGHT_KEYS if k != "embed"]
+            g = torch.autograd.grad(terms, leaves, allow_unused=True)
+            gx, gA, gz = g[0], g[1], g[2]
+            for k, gk in zip([k for k in WEIGHT_KEYS if k != "embed"], g[3:]):
+                if gk is not None:
+                    grads[k] += gk
+            st_bar[l] = (gA, gz)                            # to cell (l, s - 1)
+            if l > 0:
+                h_bar[(l - 1, s)] = gx                      # to cell (l - 1, s)
+            else:
+                seg = x.shape[0] - M                        # the embedding rows and the memory rows
+                ids = torch.as_tensor(tokens[s * S:s * S + seg], dtype=torch.long)
+                grads["embed"].index_add_(0, ids, gx[:seg])
+                grads["mem"] += gx[seg:]
+    for l in range(L):
+        gA0[l], gz0[l] = st_bar[l]
+    out = {k: v.numpy() for k, v in grads.items()}
+    if A0 is not None:
+        out["A0"] = gA0.numpy()
+    if z0 is not None:
+        out["z0"] = gz0.numpy()
+    return out

@@ -102,3 +102,19 @@ def test_gradients_respect_causality_and_unused_embedding_rows():
     unused = np.setdiff1d(np.arange(cfg.vocab), np.unique(tok))
     assert unused.size > 0 and np.all(g["embed"][unused] == 0.0)
     assert np.abs(g["embed"][np.unique(tok)]).max() > 0.0
+
+
+@pytest.mark.parametrize("short,over", [(0, {"n_layers": 3}), (5, {})])
+def test_backward_by_reverse_diagonals_equals_whole_graph_gradient(short, over):
+    # the schedule a diagonal-batched backward pass follows -- reverse
+    # anti-diagonals, per-cell vector-Jacobian products passing adjoints to
+    # (l-1, s) and (l, s-1) -- gives the gradient of the whole graph
+    cfg, W, tok, n, cot, rng = _setup(short, seed=75, n_seg=4, over=over)
+    A0 = 0.01 * np.abs(rng.standard_normal((cfg.n_layers, cfg.d_model, cfg.phi_dim)))
+    z0 = 0.05 * np.abs(rng.standard_normal((cfg.n_layers, cfg.phi_dim)))
+    _, whole = G.gradients(cfg, W, tok, n, cot, "diag", A0, z0)
+    diag = G.backward_by_diagonals(cfg, W, tok, n, cot, A0, z0)
+    assert set(diag) == set(whole)
+    for k in whole:
+        np.testing.assert_allclose(diag[k], whole[k], rtol=1e-10,
+                                   atol=1e-12 * max(1.0, float(np.abs(whole[k]).max())), err_msg=k)
