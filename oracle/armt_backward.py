@@ -252,3 +252,95 @@ def backward_by_diagonals(cfg, W: Dict[str, np.ndarray], tokens, n_segments, cot
     if z0 is not None:
         out["z0"] = gz0.numpy()
     return out
+
+
+# --------------------------------------------------------------------------
+# Explicit adjoints of the associative block (numpy fp64), the per-op
+# reference for backward kernels: each function takes the forward inputs and
+# the adjoints of the outputs and returns the adjoints of the inputs, derived
+# step by step from the forward definitions in armt_oracle.
+# --------------------------------------------------------------------------
+
+def dpfp_backward(x, phi_bar, nu):
+    """Adjoint of phi = DPFP_nu(x) for x [..., k]: with r = [relu(x), relu(-x)]
+    and phi_{(j-1) 2k + c} = r_c r_{(c-j) mod 2k}, each product sends
+    phi_bar * (other factor) to both factors; relu passes where its input > 0."""
+    x = np.asarray(x, np.float64)
+    k = x.shape[-1]
+    k2 = 2 * k
+    r = np.concatenate([np.maximum(x, 0.0), np.maximum(-x, 0.0)], axis=-1)
+    r_bar = np.zeros_like(r)
+    for j in range(1, nu + 1):
+        blk = phi_bar[..., (j - 1) * k2:j * k2]
+        rolled = np.roll(r, j, axis=-1)                  # rolled_c = r_{(c-j) mod 2k}
+        r_bar += blk * rolled
+        r_bar += np.roll(blk * r, -j, axis=-1)           # to r_{(c-j)}: index c' = c - j
+    return r_bar[..., :k] * (x > 0) - r_bar[..., k:] * (x < 0)
+
+
+def assoc_read_backward(x, wq_a, A, z, nu, eps, y_bar):
+    """Adjoint of y = x + A phi / (z^T phi + eps), phi = DPFP(W_Q x), rows x [R, d].
+    Returns (x_bar, wq_bar, A_bar, z_bar)."""
+    x = np.asarray(x, np.float64)
+    q = x @ wq_a.T
+    phi = O.dpfp(q, nu)
+    D = phi @ z + eps                                    # [R]
+    r = (phi @ A.T) / D[:, None]                         # [R, d] the read
+    coef = np.sum(y_bar * r, axis=-1) / D                # (y_bar . r) / D per row
+    A_bar = (y_bar / D[:, None]).T @ phi                 # sum_rows y_bar phi^T / D
+    z_bar = -(coef[:, None] * phi).sum(axis=0)
+    phi_bar = (y_bar @ A) / D[:, None] - coef[:, None] * z[None, :]
+    q_bar = dpfp_backward(q, phi_bar, nu)
+    return y_bar + q_bar @ wq_a, q_bar.T @ x, A_bar, z_bar
+
+
+def assoc_write_backward(h_mem, wk_a, wv_a, wb_a, A0, z0, nu, eps, A_bar, z_bar):
+    """Adjoint of the in-order delta-rule writes of the memory rows h_mem [M, d]
+    from state (A0, z0) (armt_oracle.assoc_write), given the adjoints of the
+    final state.  The writes are undone in reverse order, carrying the state's
+    adjoint back through each one.  Returns (h_bar, wk_bar, wv_bar, wb_bar,
+    A0_bar, z0_bar)."""
+    h_mem = np.asarray(h_mem, np.float64)
+    M = h_mem.shape[0]
+    keys, values = h_mem @ wk_a.T, h_mem @ wv_a.T
+    beta = 1.0 / (1.0 + np.exp(-(h_mem @ wb_a)))
+    states = [(np.asarray(A0, np.float64), np.asarray(z0, np.float64))]
+    for i in range(M):                                   # forward, keeping the state before each write
+        states.append(O.delta_rule_update(states[-1][0], states[-1][1], keys[i:i + 1], values[i:i + 1],
+                                          beta[i:i + 1], nu, eps))
+    A_bar, z_bar = np.array(A_bar, np.float64), np.array(z_bar, np.float64)
+    k_bar, v_bar, b_bar = np.zeros_like(keys), np.zeros_like(values), np.zeros(M)
+    for i in reversed(range(M)):
+        A, z = states[i]
+        phi = O.dpfp(keys[i], nu)
+        zphi = phi @ z
+        D = zphi + eps
+        vbar = (A @ phi) / D
+        Q = phi @ phi + eps
+        gu = 1.0 - zphi / Q
+        gamma = min(max(gu, 0.0), 1.0)
+        c = beta[i] * (values[i] - vbar)
+        # A' = A + c phi^T,  z' = z + gamma phi
+        c_bar = A_bar @ phi
+        phi_bar = A_bar.T @ c + gamma * z_bar
+        gamma_bar = z_bar @ phi
+        # c = beta (v - vbar)
+        b_bar[i] = c_bar @ (values[i] - vbar)
+        v_bar[i] = beta[i] * c_bar
+        vbar_bar = -beta[i] * c_bar
+        # vbar = A phi / D
+        A_prev_bar = A_bar + np.outer(vbar_bar / D, phi)
+        phi_bar += A.T @ vbar_bar / D
+        zphi_bar = -(vbar_bar @ vbar) / D
+        # gamma = clip(1 - zphi / Q, 0, 1), Q = phi^T phi + eps
+        gu_bar = gamma_bar if 0.0 <= gu <= 1.0 else 0.0
+        zphi_bar += -gu_bar / Q
+        phi_bar += 2.0 * (gu_bar * zphi / (Q * Q)) * phi
+        # zphi = z^T phi
+        z_prev_bar = z_bar + zphi_bar * phi
+        phi_bar += zphi_bar * z
+        k_bar[i] = dpfp_backward(keys[i], phi_bar, nu)
+        A_bar, z_bar = A_prev_bar, z_prev_bar
+    logit_bar = b_bar * beta * (1.0 - beta)
+    h_bar = k_bar @ wk_a + v_bar @ wv_a + np.outer(logit_bar, wb_a)
+    return h_bar, k_bar.T @ h_mem, v_bar.T @ h_mem, logit_bar @ h_mem, A_bar, z_bar

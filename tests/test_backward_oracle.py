@@ -118,3 +118,54 @@ def test_backward_by_reverse_diagonals_equals_whole_graph_gradient(short, over):
     for k in whole:
         np.testing.assert_allclose(diag[k], whole[k], rtol=1e-10,
                                    atol=1e-12 * max(1.0, float(np.abs(whole[k]).max())), err_msg=k)
+
+
+def _t64(a):
+    return torch.tensor(np.asarray(a, np.float64), dtype=torch.float64, requires_grad=True)
+
+
+def test_explicit_adjoints_of_dpfp_and_the_read_match_autograd():
+    rng = np.random.default_rng(76)
+    R, d, k, nu, eps = 7, 24, 8, 3, 1e-6
+    P = 2 * k * nu
+    x = rng.standard_normal((R, d))
+    wq = 0.3 * rng.standard_normal((k, d))
+    A = 0.2 * rng.standard_normal((d, P))
+    z = np.abs(rng.standard_normal(P))
+    y_bar = rng.standard_normal((R, d))
+    q = x @ wq.T
+    phi_bar = rng.standard_normal((R, P))
+    qt = _t64(q)
+    (G.dpfp(qt, nu) * torch.tensor(phi_bar)).sum().backward()
+    np.testing.assert_allclose(G.dpfp_backward(q, phi_bar, nu), qt.grad.numpy(), rtol=1e-12, atol=1e-12)
+    xt, wt, At, zt = _t64(x), _t64(wq), _t64(A), _t64(z)
+    (G.assoc_read(xt, wt, At, zt, nu, eps) * torch.tensor(y_bar)).sum().backward()
+    got = G.assoc_read_backward(x, wq, A, z, nu, eps, y_bar)
+    for g, t in zip(got, (xt, wt, At, zt)):
+        np.testing.assert_allclose(g, t.grad.numpy(), rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("z_scale", [0.0, 0.05, 5.0])   # zero state (gamma = 1), interior, clipped (gamma = 0)
+def test_explicit_adjoint_of_the_in_order_writes_matches_autograd(z_scale):
+    rng = np.random.default_rng(77)
+    M, d, k, nu, eps = 5, 16, 8, 3, 1e-6
+    P = 2 * k * nu
+    h = rng.standard_normal((M, d))
+    wk, wv = 0.4 * rng.standard_normal((k, d)), 0.3 * rng.standard_normal((d, d))
+    wb = 0.3 * rng.standard_normal(d)
+    A0 = 0.1 * rng.standard_normal((d, P))
+    z0 = z_scale * np.abs(rng.standard_normal(P))
+    A_bar, z_bar = rng.standard_normal((d, P)), rng.standard_normal(P)
+    ht, wkt, wvt, wbt, At, zt = (_t64(a) for a in (h, wk, wv, wb, A0, z0))
+    keys, values = ht @ wkt.T, ht @ wvt.T
+    beta = torch.sigmoid(ht @ wbt)
+    Aw, zw = At, zt
+    for i in range(M):
+        Aw, zw = G.delta_rule_write(Aw, zw, keys[i], values[i], beta[i], nu, eps)
+    ((Aw * torch.tensor(A_bar)).sum() + (zw * torch.tensor(z_bar)).sum()).backward()
+    got = G.assoc_write_backward(h, wk, wv, wb, A0, z0, nu, eps, A_bar, z_bar)
+    for g, t in zip(got, (ht, wkt, wvt, wbt, At, zt)):
+        np.testing.assert_allclose(g, t.grad.numpy(), rtol=1e-9, atol=1e-9 * max(1.0, float(np.abs(g).max())))
+    # the forward the adjoint walks back is the oracle's own
+    A1, z1 = O.assoc_write(h, wk, wv, wb, A0, z0, nu, eps)
+    np.testing.assert_allclose(A1, Aw.detach().numpy(), rtol=1e-12, atol=1e-12)
