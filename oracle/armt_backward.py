@@ -32,7 +32,10 @@ outputs) and vanish for embedding rows no token uses.
 diagonal-batched backward pass would: anti-diagonals in reverse, each cell's
 vector-Jacobian product handing adjoints to the cell below it (same segment)
 and to the cell before it (same layer); pinned against the whole-graph
-gradient.
+gradient.  ``backward_explicit`` does the same with every adjoint written out
+in numpy (``rmsnorm_backward``, ``rope_backward``, ``attention_backward``,
+``dpfp_backward``, ``assoc_read_backward``, ``assoc_write_backward``,
+``cell_backward``): the per-op reference for backward kernels.
 """
 from typing import Dict, Optional, Tuple
 
@@ -344,3 +347,165 @@ def assoc_write_backward(h_mem, wk_a, wv_a, wb_a, A0, z0, nu, eps, A_bar, z_bar)
     logit_bar = b_bar * beta * (1.0 - beta)
     h_bar = k_bar @ wk_a + v_bar @ wv_a + np.outer(logit_bar, wb_a)
     return h_bar, k_bar.T @ h_mem, v_bar.T @ h_mem, logit_bar @ h_mem, A_bar, z_bar
+
+
+def rmsnorm_backward(x, gain, eps, y_bar):
+    """Adjoint of y = x s gain, s = 1 / sqrt(mean(x^2) + eps), rows x [R, d].
+    Returns (x_bar, gain_bar)."""
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    s = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    g_bar = np.sum(y_bar * x * s, axis=0)
+    t = y_bar * gain                                     # adjoint of x s
+    x_bar = s * t - (s ** 3) * np.sum(t * x, axis=-1, keepdims=True) * x / d
+    return x_bar, g_bar
+
+
+def rope_backward(y_bar, base):
+    """Adjoint of the rotate-half rotation (a rotation per pair: its transpose)."""
+    T, _, hd = y_bar.shape
+    half = hd // 2
+    inv_freq = base ** (-(2.0 * np.arange(half, dtype=np.float64)) / hd)
+    ang = np.arange(T, dtype=np.float64)[:, None] * inv_freq[None, :]
+    cos, sin = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    y1, y2 = y_bar[..., :half], y_bar[..., half:]
+    return np.concatenate([y1 * cos + y2 * sin, -y1 * sin + y2 * cos], axis=-1)
+
+
+def attention_backward(q, k, v, o_bar):
+    """Adjoint of causal GQA attention (armt_oracle.causal_gqa_attention):
+    q [T, Hq, hd], k/v [T, Hkv, hd], o_bar [T, Hq*hd].  Per query head:
+    v_bar += P^T O_bar, P_bar = O_bar v^T, S_bar = P (P_bar - rowsum(P_bar P)),
+    q_bar = S_bar k / sqrt(hd), k_bar += S_bar^T q / sqrt(hd)."""
+    T, Hq, hd = q.shape
+    Hkv = k.shape[1]
+    o_bar = o_bar.reshape(T, Hq, hd)
+    q_bar, k_bar, v_bar = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    mask = np.triu(np.ones((T, T), dtype=bool), k=1)
+    for h in range(Hq):
+        g = (h * Hkv) // Hq
+        s = np.where(mask, -np.inf, (q[:, h, :] @ k[:, g, :].T) / np.sqrt(hd))
+        p = np.exp(s - s.max(axis=-1, keepdims=True))
+        p /= p.sum(axis=-1, keepdims=True)
+        v_bar[:, g, :] += p.T @ o_bar[:, h, :]
+        p_bar = o_bar[:, h, :] @ v[:, g, :].T
+        s_bar = p * (p_bar - np.sum(p_bar * p, axis=-1, keepdims=True))
+        q_bar[:, h, :] = s_bar @ k[:, g, :] / np.sqrt(hd)
+        k_bar[:, g, :] += s_bar.T @ q[:, h, :] / np.sqrt(hd)
+    return q_bar, k_bar, v_bar
+
+
+def cell_backward(x, cfg, W, l, A, z, h_bar, A_bar, z_bar):
+    """Explicit adjoint of armt_oracle.cell_forward (read, LLaMA block, writes)
+    for one cell: inputs x [T, d] and state (A, z), adjoints of the output rows
+    h_bar [T, d] and of the written state (A_bar, z_bar).  Returns (x_bar,
+    A_in_bar, z_in_bar, {weight name: layer-l gradient})."""
+    W = {kk: np.asarray(v, np.float64) for kk, v in W.items()}
+    nu, eps, ne = cfg.dpfp_nu, cfg.assoc_eps, cfg.norm_eps
+    T = x.shape[0]
+    Hq, Hkv, hd = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    g = {}
+    # forward, keeping the intermediates
+    x1 = O.assoc_read(x, W["a_wq"][l], A, z, nu, eps)
+    n1 = O.rmsnorm(x1, W["norm1"][l], ne)
+    q0 = (n1 @ W["wq"][l].T).reshape(T, Hq, hd)
+    k0 = (n1 @ W["wk"][l].T).reshape(T, Hkv, hd)
+    v = (n1 @ W["wv"][l].T).reshape(T, Hkv, hd)
+    q, k = O.rope_rotate_half(q0, cfg.rope_base), O.rope_rotate_half(k0, cfg.rope_base)
+    att = O.causal_gqa_attention(q, k, v)
+    y = x1 + att @ W["wo"][l].T
+    n2 = O.rmsnorm(y, W["norm2"][l], ne)
+    a, b = n2 @ W["w_gate"][l].T, n2 @ W["w_up"][l].T
+    sa = 1.0 / (1.0 + np.exp(-a))
+    u = a * sa * b
+    h = y + u @ W["w_down"][l].T
+    m0 = T - cfg.n_mem
+    # the writes (from the state the read used)
+    hw_bar, g["a_wk"], g["a_wv"], g["a_wbeta"], A_in_bar, z_in_bar = assoc_write_backward(
+        h[m0:], W["a_wk"][l], W["a_wv"][l], W["a_wbeta"][l], A, z, nu, eps, A_bar, z_bar)
+    h_bar = np.array(h_bar, np.float64)
+    h_bar[m0:] += hw_bar
+    # h = y + u Wd^T
+    y_bar = h_bar.copy()
+    u_bar = h_bar @ W["w_down"][l]
+    g["w_down"] = h_bar.T @ u
+    # u = silu(a) b
+    a_bar = u_bar * b * sa * (1.0 + a * (1.0 - sa))
+    b_bar = u_bar * a * sa
+    g["w_gate"], g["w_up"] = a_bar.T @ n2, b_bar.T @ n2
+    n2_bar = a_bar @ W["w_gate"][l] + b_bar @ W["w_up"][l]
+    dy, g["norm2"] = rmsnorm_backward(y, W["norm2"][l], ne, n2_bar)
+    y_bar += dy
+    # y = x1 + att Wo^T
+    x1_bar = y_bar.copy()
+    att_bar = y_bar @ W["wo"][l]
+    g["wo"] = y_bar.T @ att
+    q_bar, k_bar, v_bar = attention_backward(q, k, v, att_bar)
+    q0_bar, k0_bar = rope_backward(q_bar, cfg.rope_base), rope_backward(k_bar, cfg.rope_base)
+    q0_bar, k0_bar, v_bar = q0_bar.reshape(T, -1), k0_bar.reshape(T, -1), v_bar.reshape(T, -1)
+    g["wq"], g["wk"], g["wv"] = q0_bar.T @ n1, k0_bar.T @ n1, v_bar.T @ n1
+    n1_bar = q0_bar @ W["wq"][l] + k0_bar @ W["wk"][l] + v_bar @ W["wv"][l]
+    dx1, g["norm1"] = rmsnorm_backward(x1, W["norm1"][l], ne, n1_bar)
+    x1_bar += dx1
+    # the read
+    x_bar, g["a_wq"], Ar_bar, zr_bar = assoc_read_backward(x, W["a_wq"][l], A, z, nu, eps, x1_bar)
+    return x_bar, A_in_bar + Ar_bar, z_in_bar + zr_bar, g
+
+
+def backward_explicit(cfg, W: Dict[str, np.ndarray], tokens, n_segments, cot: Dict[str, np.ndarray],
+                      A0: Optional[np.ndarray] = None, z0: Optional[np.ndarray] = None):
+    """backward_by_diagonals with the explicit numpy adjoints above in place
+    of autograd: the complete backward pass written out, cell by cell, in
+    reverse diagonal order.  Returns {name: fp64 array}."""
+    L, d, P, S, M = cfg.n_layers, cfg.d_model, cfg.phi_dim, cfg.seg_len, cfg.n_mem
+    W64 = O.widen_weights(W)
+    tokens = np.asarray(tokens)
+    n = n_segments
+    x_in, state_in, acts = {}, {}, {}
+    A = [np.asarray(A0[l], np.float64).copy() if A0 is not None else np.zeros((d, P)) for l in range(L)]
+    z = [np.asarray(z0[l], np.float64).copy() if z0 is not None else np.zeros(P) for l in range(L)]
+    h_last = {}
+    for step in O.schedule(L, n, "diag"):
+        for (l, s) in step:
+            x = O.layer0_input(cfg, W64, tokens, s) if l == 0 else acts.pop((l - 1, s))
+            x_in[(l, s)], state_in[(l, s)] = x, (A[l], z[l])
+            h, A[l], z[l] = O.cell_forward(x, cfg, W64, l, A[l], z[l])
+            if l < L - 1:
+                acts[(l, s)] = h
+            else:
+                h_last[s] = h
+    grads = {kk: np.zeros_like(W64[kk]) for kk in WEIGHT_KEYS}
+    st_bar = {l: (np.asarray(cot["A"][l], np.float64), np.asarray(cot["z"][l], np.float64)) for l in range(L)}
+    h_bar = {}
+    for i in reversed(range(L + n - 1)):
+        for l in range(L):
+            s = i - l
+            if not 0 <= s < n:
+                continue
+            x = x_in[(l, s)]
+            if l == L - 1:
+                h = h_last[s]
+                seg = h.shape[0] - M
+                hb = np.zeros_like(h)
+                hb[:seg], gf = rmsnorm_backward(h[:seg], W64["norm_f"], cfg.norm_eps,
+                                                np.asarray(cot["hidden"][s * S:s * S + seg], np.float64))
+                grads["norm_f"] += gf
+            else:
+                hb = h_bar.pop((l, s))
+            A_, z_ = state_in[(l, s)]
+            x_bar, Ab, zb, g = cell_backward(x, cfg, W64, l, A_, z_, hb, *st_bar[l])
+            st_bar[l] = (Ab, zb)
+            for kk, v in g.items():
+                grads[kk][l] += v
+            if l > 0:
+                h_bar[(l - 1, s)] = x_bar
+            else:
+                seg = x.shape[0] - M
+                np.add.at(grads["embed"], tokens[s * S:s * S + seg], x_bar[:seg])
+                grads["mem"] += x_bar[seg:]
+    out = dict(grads)
+    if A0 is not None:
+        out["A0"] = np.stack([st_bar[l][0] for l in range(L)])
+    if z0 is not None:
+        out["z0"] = np.stack([st_bar[l][1] for l in range(L)])
+    return out

@@ -169,3 +169,20 @@ def test_explicit_adjoint_of_the_in_order_writes_matches_autograd(z_scale):
     # the forward the adjoint walks back is the oracle's own
     A1, z1 = O.assoc_write(h, wk, wv, wb, A0, z0, nu, eps)
     np.testing.assert_allclose(A1, Aw.detach().numpy(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("short,over", [(0, {"n_layers": 3}), (5, {}),
+                                        (0, {"n_q_heads": 4, "n_kv_heads": 2, "head_dim": 16})])
+def test_explicit_backward_equals_whole_graph_gradient(short, over):
+    # the whole backward pass written out with explicit adjoints (RMSNorm,
+    # RoPE, causal GQA attention, SwiGLU, read, in-order writes), cell by cell
+    # in reverse diagonal order
+    cfg, W, tok, n, cot, rng = _setup(short, seed=78, n_seg=3, over=over)
+    A0 = 0.01 * np.abs(rng.standard_normal((cfg.n_layers, cfg.d_model, cfg.phi_dim)))
+    z0 = 0.05 * np.abs(rng.standard_normal((cfg.n_layers, cfg.phi_dim)))
+    _, whole = G.gradients(cfg, W, tok, n, cot, "diag", A0, z0)
+    expl = G.backward_explicit(cfg, W, tok, n, cot, A0, z0)
+    assert set(expl) == set(whole)
+    for k in whole:
+        np.testing.assert_allclose(expl[k], whole[k], rtol=1e-9,
+                                   atol=1e-11 * max(1.0, float(np.abs(whole[k]).max())), err_msg=k)
