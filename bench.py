@@ -6,7 +6,15 @@ One step = one forward pass over the whole workload (default: ARMT-1B shape,
 inputs already resident in HBM.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl ours|reference] [--no-seq] [--no-cpu]
+                  [--impl ours|reference] [--no-seq] [--no-cpu] [--no-e2e]
+                  [--no-full] [--no-microbatch]
+
+Inside the timed region only the roofline kernel (the gate-up GEMM) carries
+per-launch CUDA events; the per-kernel-class table comes from one more forward
+after it.  Besides the timed forward the line reports the sequential schedule,
+the uniform-load bound, the LM head, the full-attention LLaMA on the same
+weights, diagonal batching vs micro-batching, the end-to-end host-buffer path,
+device memory, and the oracle on the host cores.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
 sample of the same workload (one segment through every layer per step).
