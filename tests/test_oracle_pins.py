@@ -15,6 +15,7 @@ import pytest
 
 from oracle import armt_oracle as O
 from recurrent_memory_transformer_gb300 import inputs as I
+from tests import plain_bf16_cell
 from tests.plain_llama import plain_layer, plain_stack
 
 pytestmark = pytest.mark.oracle
@@ -385,6 +386,31 @@ def test_bf16_precision_model_is_close_to_fp64_and_rounds():
     model_d = O.forward(cfg, W, tok, 3, order="diag", operands="bf16")
     for a, b in zip(model, model_d):
         np.testing.assert_array_equal(a, b)
+
+
+def test_bf16_precision_model_matches_an_independent_emulation():
+    """The precision model rounds to bf16 at exactly its listed operand points.
+
+    tests/plain_bf16_cell.py re-implements two-layer ARMT cells with loops and
+    torch's bfloat16 conversion, rounding at the named points and nowhere
+    else.  The oracle's model must agree with it to fp64 rounding noise, and
+    leaving out any single rounding point of the emulation must move the
+    result by far more than that -- so a missing, misplaced or extra rounding
+    point in the model fails here.  Weights are N(0, 0.1) so that at this tiny
+    size the memory read carries enough weight for its points to show."""
+    cfg = dataclasses.replace(I.TINY, n_layers=2, dtype="bf16")
+    W = I.make_weights(cfg, seed=16, std=0.1, norm_jitter=0.1)
+    tok = I.make_tokens(cfg, 2, seed=16)
+    model = O.forward(cfg, W, tok, 2, operands="bf16")
+    rel = lambda a, b: float(np.abs(a - b).max() / np.abs(b).max())
+    emu = plain_bf16_cell.forward(cfg, W, tok, 2)
+    for a, b in zip(emu, model):
+        assert rel(a, b) <= 1e-12
+    for point in plain_bf16_cell.ALL_POINTS:
+        part = plain_bf16_cell.forward(cfg, W, tok, 2, points=set(plain_bf16_cell.ALL_POINTS) - {point})
+        assert max(rel(a, b) for a, b in zip(part, model)) >= 1e-4, point
+    exact = O.forward(cfg, W, tok, 2)
+    assert min(rel(a, b) for a, b in zip(exact, model)) >= 1e-4
 
 
 def test_lm_head_logits_closed_forms():
