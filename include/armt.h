@@ -40,7 +40,18 @@
  *   - Errors are returned as armt_status and never abort the process.
  *     Argument and shape checks happen before any work is enqueued; on an
  *     argument error nothing is written.  A device-side bounded wait that
- *     gives up records ARMT_ERR_TIMEOUT, reported by armt_sync_status().
+ *     gives up records ARMT_ERR_TIMEOUT, reported by armt_sync_status() (or
+ *     armt_block_sync_status / armt_noalloc_sync_status for the building
+ *     blocks); the kernel then lets the copies and tensor-core operations it
+ *     already issued finish, frees its tensor memory and returns.
+ *   - Environment (read at every call; for tests of the failure paths):
+ *     ARMT_ALLOC_CAP_BYTES  cap on the bytes a model allocates (ARMT_ERR_OOM
+ *                           beyond it);
+ *     ARMT_WAIT_LIMIT_MS    limit of every bounded device-side wait
+ *                           (default 2000 ms);
+ *     ARMT_TEST_STALL_AFTER the tensor-core kernels' copy producers stop
+ *                           after that many stage loads, as a stuck producer
+ *                           would, so that the waits run out (unset: off).
  *   - Not thread-safe per model: one host thread at a time per armt_model,
  *     and calls on one model must not overlap on the device (they share the
  *     model's activation workspace).  Different models are independent.
@@ -254,6 +265,15 @@ ARMT_API armt_status armt_segment_attention_bf16(const void* qk, const void* vt,
                                                  int32_t T, int32_t Hq, int32_t Hkv, int32_t hd,
                                                  void* stream);
 
+/* Status of the two building blocks above, which run without a model: waits
+ * for `stream`, then reports ARMT_ERR_TIMEOUT if a bounded device-side wait
+ * of either gave up on the current device since the last call, and clears it.
+ * Their error word is a device global of the library (one per device, looked
+ * up on the first call with the device current); it stays set until read,
+ * and while it is set the blocks' waits give up early, so their outputs are
+ * then undefined.  Allocates nothing. */
+ARMT_API armt_status armt_block_sync_status(void* stream);
+
 /* Fixed device scratch of armt_segment_attention_bf16_noalloc (bytes). */
 #define ARMT_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
@@ -271,14 +291,23 @@ ARMT_API armt_status armt_segment_attention_bf16(const void* qk, const void* vt,
  * ARMT_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
  * the process exits; larger problems are rejected with ARMT_ERR_SHAPE before
  * anything is enqueued.  The first call on a device (with that device
- * current) looks up the array's device address; make that first call before
- * any stream capture.  Every call on a device shares the one array, which
- * keeps the last call's contents, so calls that overlap on the GPU (e.g. on
- * two streams without ordering) race -- order them.  hd in {64, 128},
+ * current, and again after its context changed, e.g. after cudaDeviceReset)
+ * looks up the array's device address and clears the error word; make that
+ * first call before any stream capture.  Every call on a device shares the
+ * one array, which keeps the last call's contents, so calls that overlap on
+ * the GPU (e.g. on two streams without ordering) race -- order them.  A
+ * bounded device-side wait that gives up records a code in the error word;
+ * it stays set, and later calls' waits give up early, until
+ * armt_noalloc_sync_status reads and clears it.  hd in {64, 128}, any T >= 1,
  * 16-byte aligned pointers. */
 ARMT_API armt_status armt_segment_attention_bf16_noalloc(const void* qkv, void* out, int32_t G,
                                                          int32_t T, int32_t Hq, int32_t Hkv,
                                                          int32_t hd, void* stream);
+
+/* Waits for `stream`, then reports ARMT_ERR_TIMEOUT if the no-allocation
+ * attention recorded a timeout on the current device since the last call,
+ * and clears it.  Allocates nothing. */
+ARMT_API armt_status armt_noalloc_sync_status(void* stream);
 
 /* LM head over hidden states (the logits behind the error-accumulation
  * study of section 四 of the summary page: diagonal batching vs the

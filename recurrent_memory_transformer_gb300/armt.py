@@ -31,7 +31,7 @@ EXPORTED = ("armt_create", "armt_destroy", "armt_forward", "armt_forward_sequent
             "armt_segment_attention_bf16_noalloc", "armt_forward_full_attention", "armt_state_sizes",
             "armt_memory_bytes", "armt_lm_head", "armt_launch_count",
             "armt_set_profiling", "armt_set_profiling_mask", "armt_kernel_times", "armt_sync_status", "armt_status_string",
-            "armt_last_error")
+            "armt_last_error", "armt_block_sync_status", "armt_noalloc_sync_status")
 
 
 class ArmtError(RuntimeError):
@@ -91,6 +91,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.armt_set_profiling_mask.argtypes = [P, ctypes.c_uint32]
     lib.armt_kernel_times.argtypes = [P, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double), I32]
     lib.armt_sync_status.argtypes = [P, P]
+    lib.armt_block_sync_status.argtypes = [P]
+    lib.armt_noalloc_sync_status.argtypes = [P]
     for name in EXPORTED:
         getattr(lib, name).restype = S
     lib.armt_status_string.restype = ctypes.c_char_p
@@ -314,3 +316,15 @@ def armt_segment_attention_bf16_noalloc(qkv, out, Hq, Hkv, hd, stream=None):
     _check(lib.armt_segment_attention_bf16_noalloc(_ptr(qkv), _ptr(out), G, T, Hq, Hkv, hd,
                                                    _stream_ptr(stream)),
            "armt_segment_attention_bf16_noalloc")
+
+
+def armt_block_sync_status(stream=None):
+    """Raises ArmtError(ARMT_ERR_TIMEOUT) if a building block's bounded wait gave up on this device."""
+    lib = load_library()
+    _check(lib.armt_block_sync_status(_stream_ptr(stream)), "armt_block_sync_status")
+
+
+def armt_noalloc_sync_status(stream=None):
+    """Raises ArmtError(ARMT_ERR_TIMEOUT) if the no-allocation attention's bounded wait gave up."""
+    lib = load_library()
+    _check(lib.armt_noalloc_sync_status(_stream_ptr(stream)), "armt_noalloc_sync_status")

@@ -154,6 +154,7 @@ struct ModelBase {
   DevAllocs mem;
   long long weight_bytes = 0;  // part of mem.total holding the weights
   int* d_err = nullptr;
+  WaitPolicy wp;  // refreshed from the environment at every public call
   // profiling: launches of the classes in prof_mask get an event pair
   bool profiling = false;
   uint32_t prof_mask = 0;
@@ -566,11 +567,12 @@ struct Model : ModelBase {
       bool done = false;
       if constexpr (BN == 256) {
         if (tb2 != nullptr && pair_tiles_pay_off(rows)) {
-          CK((launch_gemm_tc2<Epi, EPI_WG>(ta, *tb2, rows, N, K, lo, g, d_err, epi, num_sms, st, map)));
+          CK((launch_gemm_tc2<Epi, EPI_WG>(ta, *tb2, rows, N, K, lo, g, d_err, epi, num_sms, st, map, wp)));
           done = true;
         }
       }
-      if (!done) CK((launch_gemm_tc<Epi, BN, EPI_WG>(ta, tb, rows, N, K, lo, g, d_err, epi, num_sms, st, map)));
+      if (!done)
+        CK((launch_gemm_tc<Epi, BN, EPI_WG>(ta, tb, rows, N, K, lo, g, d_err, epi, num_sms, st, map, wp)));
     } else {
       const SimtAMap am{map.row0, map.a_slot_off, map.b_div, map.alt_lo, map.alt_hi, map.alt_row0};
       const float* b0 = reinterpret_cast<const float*>(b) + (long long)map.b_slot_off * N * K;
@@ -651,6 +653,7 @@ struct Model : ModelBase {
       aa.n_qtiles = (T + 127) / 128;
       aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
       aa.err = d_err;
+      aa.wp = wp;
       if (hd == 64)
         CK(launch_attn_tc<64>(w.tmQK, w.tmVt, aa, g * nb, num_sms, st));
       else
@@ -800,9 +803,11 @@ struct Model : ModelBase {
           return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         SEpiStore epi{logits + r0 * V, (long long)V, 0};
         if (pair_tiles_pay_off(rows_c))
-          CK((launch_gemm_tc2<SEpiStore, 1>(ta, tb, rows_c, V, d, 0, 1, d_err, epi, num_sms, st)));
+          CK((launch_gemm_tc2<SEpiStore, 1>(ta, tb, rows_c, V, d, 0, 1, d_err, epi, num_sms, st,
+                                            GemmGroupMap(), wp)));
         else
-          CK((launch_gemm_tc<SEpiStore, 256>(ta, tb1, rows_c, V, d, 0, 1, d_err, epi, num_sms, st)));
+          CK((launch_gemm_tc<SEpiStore, 256>(ta, tb1, rows_c, V, d, 0, 1, d_err, epi, num_sms, st,
+                                             GemmGroupMap(), wp)));
       }
     } else {
       for (int64_t r0 = 0; r0 < n_rows; r0 += kLmChunk) {
@@ -824,8 +829,8 @@ struct Model : ModelBase {
                                  int rows, int N, int K, int g_first, int g_count, int* err,
                                  const Epi& epi, int nsm, cudaStream_t st, const GemmGroupMap& map) {
     if (pair_tiles_pay_off(rows))
-      return launch_gemm_tc2<Epi, EPI_WG>(ta, tb2, rows, N, K, g_first, g_count, err, epi, nsm, st, map);
-    return launch_gemm_tc<Epi, 256, EPI_WG>(ta, tb, rows, N, K, g_first, g_count, err, epi, nsm, st, map);
+      return launch_gemm_tc2<Epi, EPI_WG>(ta, tb2, rows, N, K, g_first, g_count, err, epi, nsm, st, map, wp);
+    return launch_gemm_tc<Epi, 256, EPI_WG>(ta, tb, rows, N, K, g_first, g_count, err, epi, nsm, st, map, wp);
   }
 
   static GemmGroupMap layer_map(int l) {
@@ -876,6 +881,7 @@ struct Model : ModelBase {
           aa.n_qtiles = (T + 127) / 128;
           aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
           aa.err = d_err;
+          aa.wp = wp;
           if (hd == 64)
             CK(launch_attn_tc<64>(tmQKf, tmVtf, aa, 1, num_sms, st));
           else
@@ -983,10 +989,66 @@ static armt_status validate(const armt_config* c) {
   return ARMT_OK;
 }
 
-static int g_num_sms(int dev) {
-  int n = 0;
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 148;
+static armt_status sm_count(int dev, int* n) {
+  *n = 0;
+  CK(cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev));
+  if (*n <= 0) return fail(ARMT_ERR_CUDA, "multiprocessor count query returned " + std::to_string(*n));
+  return ARMT_OK;
+}
+
+// ------------------------------------------ building blocks' error word --
+//
+// armt_grouped_gemm_bf16 and armt_segment_attention_bf16 run without a model,
+// so their bounded waits report into a device global: every device that
+// loads the library has its own copy, and no call allocates for it.  Host
+// code needs its device address, looked up once per device (with it current)
+// and again if the device's context changed (e.g. after cudaDeviceReset).
+static __device__ int g_block_err;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+namespace armt {
+void* current_context() {
+  static std::atomic<CtxGetCurrentFn> fn{nullptr};
+  CtxGetCurrentFn f = fn.load();
+  if (f == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    f = reinterpret_cast<CtxGetCurrentFn>(p);
+    fn.store(f);
+  }
+  CUcontext c = nullptr;
+  return f(&c) == CUDA_SUCCESS ? static_cast<void*>(c) : nullptr;
+}
+}  // namespace armt
+
+namespace {
+constexpr int kMaxDevices = 64;
+struct DeviceWord {
+  std::atomic<void*> ctx{nullptr};
+  std::atomic<int*> ptr{nullptr};
+};
+DeviceWord g_block_err_addr[kMaxDevices];
+}  // namespace
+
+static armt_status block_err_word(int dev, int** out) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(ARMT_ERR_NO_DEVICE, "device ordinal out of range");
+  void* ctx = current_context();
+  DeviceWord& w = g_block_err_addr[dev];
+  int* p = w.ptr.load();
+  if (p == nullptr || w.ctx.load() != ctx) {
+    void* a = nullptr;
+    CK(cudaGetSymbolAddress(&a, g_block_err));
+    CK(cudaMemset(a, 0, sizeof(int)));
+    w.ptr.store(static_cast<int*>(a));
+    w.ctx.store(ctx);
+    p = static_cast<int*>(a);
+  }
+  *out = p;
+  return ARMT_OK;
 }
 
 // ------------------------------------------------------------- C ABI --
@@ -1041,8 +1103,9 @@ armt_status armt_create(const armt_config* cfg, const armt_weights* w, void* str
                                          : static_cast<ModelBase*>(new Model<float>());
   m->cfg = *cfg;
   m->device = dev;
-  m->num_sms = g_num_sms(dev);
-  armt_status s = m->create(w, reinterpret_cast<cudaStream_t>(stream));
+  m->wp = wait_policy_from_env();
+  armt_status s = sm_count(dev, &m->num_sms);
+  if (s == ARMT_OK) s = m->create(w, reinterpret_cast<cudaStream_t>(stream));
   if (s != ARMT_OK) {
     cudaDeviceSynchronize();
     delete m;
@@ -1068,6 +1131,7 @@ static armt_status forward_common(armt_model* m, const int32_t* tokens, int64_t 
   if (n <= 0) return fail(ARMT_ERR_ARG, "n_segments must be positive");
   if (mem_in_valid != 0 && mem_in_valid != 1) return fail(ARMT_ERR_ARG, "mem_in_valid must be 0 or 1");
   if (n > ((int64_t)1 << 24)) return fail(ARMT_ERR_SHAPE, "n_segments too large");
+  m->impl->wp = wait_policy_from_env();
   return m->impl->forward(tokens, n * m->impl->cfg.seg_len, 1, hidden, A, z, mem_in_valid, schedule,
                           reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1085,6 +1149,7 @@ armt_status armt_forward_batch(armt_model* m, const int32_t* tokens, int32_t bat
   if (n_tokens > ((int64_t)1 << 24) * c.seg_len) return fail(ARMT_ERR_SHAPE, "n_tokens too large");
   if (batch > ARMT_MAX_BATCH || (int64_t)batch * c.n_layers > 65535)
     return fail(ARMT_ERR_SHAPE, "batch > ARMT_MAX_BATCH or batch * n_layers > 65535");
+  m->impl->wp = wait_policy_from_env();
   return m->impl->forward(tokens, n_tokens, batch, hidden_out, mem_A, mem_z, mem_in_valid, schedule,
                           reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1186,6 +1251,7 @@ armt_status armt_forward_full_attention(armt_model* m, const int32_t* tokens, in
   if (m == nullptr || tokens == nullptr || hidden_out == nullptr)
     return fail(ARMT_ERR_ARG, "NULL argument");
   if (n_tokens <= 0) return fail(ARMT_ERR_ARG, "n_tokens must be positive");
+  m->impl->wp = wait_policy_from_env();
   return m->impl->forward_full(tokens, n_tokens, hidden_out, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -1196,6 +1262,7 @@ armt_status armt_lm_head(armt_model* m, const float* hidden, int64_t n_rows, con
   if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(logits) |
        reinterpret_cast<uintptr_t>(w_head)) & 15)
     return fail(ARMT_ERR_ARG, "pointers must be 16-byte aligned");
+  m->impl->wp = wait_policy_from_env();
   return m->impl->lm_head(hidden, n_rows, w_head, logits, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -1209,23 +1276,22 @@ armt_status armt_grouped_gemm_bf16(const void* A, const void* B, float* C, int32
     return fail(ARMT_ERR_ARG, "pointers must be 16-byte aligned");
   if ((long long)M > (1ll << 30) || (long long)G * N > (1ll << 30))
     return fail(ARMT_ERR_SHAPE, "sizes too large");
-  int dev = 0;
+  int dev = 0, nsm = 0;
+  int* err = nullptr;
   CKS(check_device(&dev));
-  static int* err = nullptr;
-  if (err == nullptr) {
-    CK(cudaMalloc(&err, sizeof(int)));
-    CK(cudaMemset(err, 0, sizeof(int)));
-  }
+  CKS(sm_count(dev, &nsm));
+  CKS(block_err_word(dev, &err));
   CUtensorMap ta, tb;
   const bool pairs = pair_tiles_pay_off(M);
   if (!encode_tmap_bf16_3d(&ta, A, K, M, G, TC_BM) || !encode_tmap_bf16_3d(&tb, B, K, N, G, pairs ? 128 : 256))
     return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   SEpiStore epi{C, (long long)N, (long long)M * N};
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const WaitPolicy wp = wait_policy_from_env();
   if (pairs)
-    CK((launch_gemm_tc2<SEpiStore, 1>(ta, tb, M, N, K, 0, G, err, epi, g_num_sms(dev), st)));
+    CK((launch_gemm_tc2<SEpiStore, 1>(ta, tb, M, N, K, 0, G, err, epi, nsm, st, GemmGroupMap(), wp)));
   else
-    CK((launch_gemm_tc<SEpiStore, 256>(ta, tb, M, N, K, 0, G, err, epi, g_num_sms(dev), st)));
+    CK((launch_gemm_tc<SEpiStore, 256>(ta, tb, M, N, K, 0, G, err, epi, nsm, st, GemmGroupMap(), wp)));
   return ARMT_OK;
 }
 
@@ -1240,13 +1306,11 @@ armt_status armt_segment_attention_bf16(const void* qk, const void* vt, void* ou
   if ((reinterpret_cast<uintptr_t>(qk) | reinterpret_cast<uintptr_t>(vt) |
        reinterpret_cast<uintptr_t>(out)) & 15)
     return fail(ARMT_ERR_ARG, "pointers must be 16-byte aligned");
-  int dev = 0;
+  int dev = 0, nsm = 0;
+  int* err = nullptr;
   CKS(check_device(&dev));
-  static int* err = nullptr;
-  if (err == nullptr) {
-    CK(cudaMalloc(&err, sizeof(int)));
-    CK(cudaMemset(err, 0, sizeof(int)));
-  }
+  CKS(sm_count(dev, &nsm));
+  CKS(block_err_word(dev, &err));
   CUtensorMap tq, tv;
   if (!encode_tmap_bf16_3d(&tq, qk, (Hq + Hkv) * hd, T, G, 128) ||
       !encode_tmap_bf16_3d(&tv, vt, T, hd, G * Hkv, hd))
@@ -1260,11 +1324,27 @@ armt_status armt_segment_attention_bf16(const void* qk, const void* vt, void* ou
   aa.n_qtiles = (T + 127) / 128;
   aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
   aa.err = err;
+  aa.wp = wait_policy_from_env();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (hd == 64)
-    CK(launch_attn_tc<64>(tq, tv, aa, G, g_num_sms(dev), st));
+    CK(launch_attn_tc<64>(tq, tv, aa, G, nsm, st));
   else
-    CK(launch_attn_tc<128>(tq, tv, aa, G, g_num_sms(dev), st));
+    CK(launch_attn_tc<128>(tq, tv, aa, G, nsm, st));
+  return ARMT_OK;
+}
+
+armt_status armt_block_sync_status(void* stream) {
+  int dev = 0;
+  int* err = nullptr;
+  CKS(check_device(&dev));
+  CKS(block_err_word(dev, &err));
+  CK(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+  int h = 0;
+  CK(cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (h != 0) {
+    CK(cudaMemset(err, 0, sizeof(int)));
+    return fail(ARMT_ERR_TIMEOUT, "device wait timed out (code " + std::to_string(h) + ")");
+  }
   return ARMT_OK;
 }
 

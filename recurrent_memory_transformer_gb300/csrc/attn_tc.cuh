@@ -52,6 +52,7 @@ struct AttnArgs {
   int n_qtiles;
   float scale_log2;  // log2(e) / sqrt(HD)
   int* err;
+  WaitPolicy wp;     // wait limit and the test stall hook (counted in K/V tile loads)
 };
 
 // Work item i (heaviest query tiles first): m = n_qtiles - 1 - i / (Hq * G),
@@ -72,7 +73,7 @@ __device__ __forceinline__ AttnItem attn_item(const AttnArgs& a, int i) {
 // S_FULL/O_FULL/BUF_FREE come in pairs, one per TMEM buffer.
 enum AttnBar {
   B_Q = 0, B_KF, B_KE, B_VF, B_VE, B_PF,
-  B_SF0, B_SF1, B_OF0, B_OF1, B_FREE0, B_FREE1, B_COUNT
+  B_SF0, B_SF1, B_OF0, B_OF1, B_FREE0, B_FREE1, B_DRAIN, B_COUNT
 };
 
 template <int HD>
@@ -105,6 +106,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
       mbar_init(&bar[B_OF0 + bb], 1);
       mbar_init(&bar[B_FREE0 + bb], 4);
     }
+    mbar_init(&bar[B_DRAIN], 1);
     fence_barrier_init();
     fence_proxy_async_smem();
     tma_prefetch_desc(&tmQK);
@@ -120,31 +122,44 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
     if (lane == 0) {
       int c = 0;  // running tile count
       bool ok = true;
+      // phases armed on the Q, K and V barriers; each is re-armed only after
+      // its previous phase was consumed, so at most the last one is in flight
+      int nq = 0, nk = 0, nv = 0;
+      const uint64_t lim = a.wp.limit_ns;
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
         const AttnItem it = attn_item(a, i);
         const int g = it.h / (a.Hq / a.Hkv);
         // Q is reused once every S of the previous item has run
-        if (c > 0 && !mbar_wait_bounded(&bar[B_KE], (c - 1) & 1, a.err, DEV_TIMEOUT_EMPTY)) break;
+        if (c > 0 && !mbar_wait_bounded(&bar[B_KE], (c - 1) & 1, a.err, DEV_TIMEOUT_EMPTY, lim)) break;
         mbar_arrive_expect_tx(&bar[B_Q], C::Q_BYTES);
         for (int at = 0; at < C::HD_ATOMS; ++at)
           tma_load_3d(sQ + at * 16384, &tmQK, it.h * HD + 64 * at, it.m * 128, it.l, &bar[B_Q]);
+        ++nq;
         for (int j = 0; j <= it.m; ++j, ++c) {
-          if (j > 0 && !mbar_wait_bounded(&bar[B_KE], (c - 1) & 1, a.err, DEV_TIMEOUT_EMPTY)) {
+          if (nk == a.wp.stall_after ||
+              (j > 0 && !mbar_wait_bounded(&bar[B_KE], (c - 1) & 1, a.err, DEV_TIMEOUT_EMPTY, lim))) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&bar[B_KF], C::K_BYTES);
           for (int at = 0; at < C::HD_ATOMS; ++at)
             tma_load_3d(sK + at * 16384, &tmQK, (a.Hq + g) * HD + 64 * at, j * 128, it.l, &bar[B_KF]);
-          if (c > 0 && !mbar_wait_bounded(&bar[B_VE], (c - 1) & 1, a.err, DEV_TIMEOUT_EMPTY)) {
+          ++nk;
+          if (c > 0 && !mbar_wait_bounded(&bar[B_VE], (c - 1) & 1, a.err, DEV_TIMEOUT_EMPTY, lim)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&bar[B_VF], C::V_BYTES);
           for (int at = 0; at < 2; ++at)
             tma_load_3d(sV + at * (HD * 128), &tmV, j * 128 + 64 * at, 0, it.l * a.Hkv + g, &bar[B_VF]);
+          ++nv;
         }
       }
+      // Drain: the last Q, K and V loads land before the CTA lets go of its
+      // shared memory, also when a consumer stopped waiting for them.
+      if (nq > 0) mbar_wait_drain(&bar[B_Q], (uint32_t)((nq - 1) & 1));
+      if (nk > 0) mbar_wait_drain(&bar[B_KF], (uint32_t)((nk - 1) & 1));
+      if (nv > 0) mbar_wait_drain(&bar[B_VF], (uint32_t)((nv - 1) & 1));
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -154,9 +169,9 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
       // previous tile (cc - 2) has been folded by the softmax and K arrived
       auto issue_S = [&](int cc) -> bool {
         if (cc >= 2 && !mbar_wait_bounded(&bar[B_FREE0 + (cc & 1)], ((cc - 2) >> 1) & 1, a.err,
-                                          DEV_TIMEOUT_ACC_EMPTY))
+                                          DEV_TIMEOUT_ACC_EMPTY, a.wp.limit_ns))
           return false;
-        if (!mbar_wait_bounded(&bar[B_KF], cc & 1, a.err, DEV_TIMEOUT_FULL)) return false;
+        if (!mbar_wait_bounded(&bar[B_KF], cc & 1, a.err, DEV_TIMEOUT_FULL, a.wp.limit_ns)) return false;
         tc_fence_after();
         const uint32_t d = tmem + 128u * (uint32_t)(cc & 1);
 #pragma unroll
@@ -174,13 +189,13 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
         const AttnItem it = attn_item(a, i);
         const int nj = it.m + 1;
-        ok = mbar_wait_bounded(&bar[B_Q], k & 1, a.err, DEV_TIMEOUT_FULL) && issue_S(c) &&
+        ok = mbar_wait_bounded(&bar[B_Q], k & 1, a.err, DEV_TIMEOUT_FULL, a.wp.limit_ns) && issue_S(c) &&
              (nj < 2 || issue_S(c + 1));
         for (int j = 0; ok && j < nj; ++j) {
           const int cj = c + j;
           // P written (the softmax has read S) and V arrived
-          ok = mbar_wait_bounded(&bar[B_PF], cj & 1, a.err, DEV_TIMEOUT_ACC_FULL) &&
-               mbar_wait_bounded(&bar[B_VF], cj & 1, a.err, DEV_TIMEOUT_FULL);
+          ok = mbar_wait_bounded(&bar[B_PF], cj & 1, a.err, DEV_TIMEOUT_ACC_FULL, a.wp.limit_ns) &&
+               mbar_wait_bounded(&bar[B_VF], cj & 1, a.err, DEV_TIMEOUT_FULL, a.wp.limit_ns);
           if (!ok) break;
           tc_fence_after();
           const uint32_t d = tmem + 128u * (uint32_t)(cj & 1);
@@ -197,6 +212,9 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
         }
         c += nj;
       }
+      // Drain: every MMA issued above has finished before TMEM is freed.
+      tc_commit(&bar[B_DRAIN]);
+      mbar_wait_drain(&bar[B_DRAIN], 0);
     }
   } else {
     const int quarter = warp & 3;
@@ -211,7 +229,8 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
     bool idle = false;
     // o = o * corr + O_t (O_t = P_t V_t, in buffer t % 2), then free the buffer
     auto fold = [&](int t, float corr) -> bool {
-      const bool got = mbar_wait_bounded(&bar[B_OF0 + (t & 1)], (t >> 1) & 1, a.err, DEV_TIMEOUT_ACC_FULL);
+      const bool got = mbar_wait_bounded(&bar[B_OF0 + (t & 1)], (t >> 1) & 1, a.err, DEV_TIMEOUT_ACC_FULL,
+                                         a.wp.limit_ns);
       if (!__all_sync(0xffffffffu, got)) return false;
       tc_fence_after();
       if (!idle) {
@@ -252,7 +271,8 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
       float m_run = -INFINITY, l_run = 0.f, corr_prev = 1.f;
       for (int j = 0; j < nj; ++j) {
         const int cj = c + j;
-        const bool got = mbar_wait_bounded(&bar[B_SF0 + (cj & 1)], (cj >> 1) & 1, a.err, DEV_TIMEOUT_ACC_FULL);
+        const bool got = mbar_wait_bounded(&bar[B_SF0 + (cj & 1)], (cj >> 1) & 1, a.err, DEV_TIMEOUT_ACC_FULL,
+                                           a.wp.limit_ns);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;

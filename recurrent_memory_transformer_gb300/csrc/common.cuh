@@ -11,6 +11,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <cstdlib>
 
 namespace armt {
 
@@ -24,6 +25,37 @@ enum DevError : int {
   DEV_TIMEOUT_ACC_FULL = 3,  // epilogue waited too long for an accumulator
   DEV_TIMEOUT_ACC_EMPTY = 4  // MMA issuer waited too long for a drained accumulator
 };
+
+// How long a bounded wait may take, and a failure-injection hook for tests.
+//   limit_ns     wall-clock limit of every pipeline wait (default 2 s);
+//   stall_after  >= 0: the TMA producer stops after that many stage loads,
+//                as a producer that got stuck would, so the consumers' waits
+//                run out (-1: off).  Nothing else sets the barriers it would
+//                have armed; the kernel then records DEV_TIMEOUT_*, drains and
+//                returns.
+// Read from the environment (ARMT_WAIT_LIMIT_MS, ARMT_TEST_STALL_AFTER) once
+// per public call.
+struct WaitPolicy {
+  unsigned long long limit_ns = 2000000000ull;
+  int stall_after = -1;
+};
+
+inline WaitPolicy wait_policy_from_env() {
+  WaitPolicy p;
+  if (const char* s = getenv("ARMT_WAIT_LIMIT_MS")) {
+    const long long ms = atoll(s);
+    if (ms > 0) p.limit_ns = (unsigned long long)ms * 1000000ull;
+  }
+  if (const char* s = getenv("ARMT_TEST_STALL_AFTER")) {
+    const long long n = atoll(s);
+    if (n >= 0 && n < (1ll << 30)) p.stall_after = (int)n;
+  }
+  return p;
+}
+
+// Limit of the waits a kernel makes while draining after an abort (copies
+// and MMAs already issued always complete; this only bounds a broken device).
+constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 
 // ---------------------------------------------------------------- misc --
 
@@ -144,6 +176,28 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Wait for a phase during teardown: bounded by time only (it does not give
+// up early when the error word is set -- by then it is, and the point is to
+// let copies and MMAs already in flight finish).  Returns false on expiry.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
+                                                uint64_t limit_ns = kDrainLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Count `bytes` of the current phase's expected transaction bytes as
+// arrived without a copy (used when draining a stage whose peer copy was
+// never issued).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
 // ----------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -258,6 +312,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
+}
+
+// A 32-bit word of another CTA's shared memory (shared::cluster address).
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
 }
 
 // Every thread of both CTAs arrives and waits (release / acquire at cluster scope).

@@ -53,6 +53,7 @@ struct GemmTcShape {
   int g_first, g_count;
   int m_tiles, n_tiles, k_blocks;
   int* err;       // device error word
+  WaitPolicy wp;  // wait limit and the test stall hook
 };
 
 // EPI_WG epilogue warpgroups (1 or 2); with 2, each takes half of the tile's
@@ -86,7 +87,8 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
   uint64_t* empty = full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* drain = acc_empty + 2;  // completion of every MMA this CTA issued
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0 && lane == 0) {
@@ -98,6 +100,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], C::EPI_WARPS);  // one arrival per epilogue warp
     }
+    mbar_init(drain, 1);
     fence_barrier_init();
     fence_proxy_async_smem();
     tma_prefetch_desc(&tmA);
@@ -117,6 +120,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      int issued = 0;  // stage loads issued (full[] phases armed)
       for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
         const int g = t / tiles_per_g, r = t - g * tiles_per_g;
         const int nt = r / sh.m_tiles, mt = r - nt * sh.m_tiles;
@@ -124,7 +128,8 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
         const int a_row = sh.map.a_row0(layer) + mt * TC_BM;
         const int b_slot = layer / sh.map.b_div + sh.map.b_slot_off;
         for (int kb = 0; kb < sh.k_blocks; ++kb) {
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, sh.err, DEV_TIMEOUT_EMPTY)) {
+          if (issued == sh.wp.stall_after ||
+              !mbar_wait_bounded(&empty[stage], phase ^ 1u, sh.err, DEV_TIMEOUT_EMPTY, sh.wp.limit_ns)) {
             ok = false;
             break;
           }
@@ -132,12 +137,18 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
           tma_load_3d(sA + stage * C::A_BYTES, &tmA, kb * TC_BK, a_row, layer + sh.map.a_slot_off,
                       &full[stage]);
           tma_load_3d(sB + stage * C::B_BYTES, &tmB, kb * TC_BK, nt * BN, b_slot, &full[stage]);
+          ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
+      // Drain: the loads of the last STAGES stages land before the CTA lets
+      // go of its shared memory (the MMA thread may have stopped consuming
+      // them).  Earlier stages were consumed, so they have landed already.
+      for (int j = issued > C::STAGES ? issued - C::STAGES : 0; j < issued; ++j)
+        mbar_wait_drain(&full[j % C::STAGES], (uint32_t)((j / C::STAGES) & 1));
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -153,11 +164,12 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
       for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
         const int mt = (t % tiles_per_g) % sh.m_tiles;
         const uint32_t id = sh.rows - mt * TC_BM <= 16 ? idesc64 : idesc;
-        if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, sh.err, DEV_TIMEOUT_ACC_EMPTY)) break;
+        if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, sh.err, DEV_TIMEOUT_ACC_EMPTY, sh.wp.limit_ns))
+          break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < sh.k_blocks; ++kb) {
-          if (!mbar_wait_bounded(&full[stage], phase, sh.err, DEV_TIMEOUT_FULL)) {
+          if (!mbar_wait_bounded(&full[stage], phase, sh.err, DEV_TIMEOUT_FULL, sh.wp.limit_ns)) {
             ok = false;
             break;
           }
@@ -183,6 +195,10 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
           acc_phase ^= 1u;
         }
       }
+      // Drain: every MMA issued above has finished (and made its arrivals)
+      // before TMEM is freed, also when the loop stopped early.
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0);
     }
   } else {
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
@@ -195,7 +211,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       const int g = t / tiles_per_g, r = t - g * tiles_per_g;
       const int nt = r / sh.m_tiles, mt = r - nt * sh.m_tiles;
-      const bool got = mbar_wait_bounded(&acc_full[acc], acc_phase, sh.err, DEV_TIMEOUT_ACC_FULL);
+      const bool got = mbar_wait_bounded(&acc_full[acc], acc_phase, sh.err, DEV_TIMEOUT_ACC_FULL, sh.wp.limit_ns);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       staged_epilogue<BN, EPI_WG>(epi, sh.g_first + g, mt * TC_BM + quarter * 32, sh.rows, nt * BN,
@@ -229,7 +245,8 @@ bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int K, int rows, in
 template <class Epi, int BN, int EPI_WG = 1>
 static cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, int rows, int N, int K,
                            int g_first, int g_count, int* err, const Epi& epi, int num_sms,
-                           cudaStream_t stream, const GemmGroupMap& map = GemmGroupMap()) {
+                           cudaStream_t stream, const GemmGroupMap& map = GemmGroupMap(),
+                           const WaitPolicy& wp = WaitPolicy()) {
   using C = TcCfg<BN, EPI_WG>;
   static std::atomic<bool> configured{false};  // once per translation unit (set-up is idempotent)
   if (!configured) {
@@ -249,6 +266,7 @@ static cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB
   sh.n_tiles = N / BN;
   sh.k_blocks = K / TC_BK;
   sh.err = err;
+  sh.wp = wp;
   const int tiles = g_count * sh.m_tiles * sh.n_tiles;
   const int grid = tiles < num_sms ? tiles : num_sms;
   if (grid <= 0) return cudaSuccess;

@@ -25,8 +25,13 @@
 //   warps 2..   epilogue in both CTAs, as in gemm_tc.cuh, on the CTA's 128
 //               rows x 256 columns; each warp then arrives on the leader's
 //               accumulator-empty barrier (remote arrive).
-// Every wait is bounded; an error word stops both CTAs, which then meet at
-// the final cluster barrier.  Same fixed K order per element as gemm_tc.cuh.
+// Every wait is bounded; an error word stops both CTAs, which then drain:
+// the leader's MMA thread waits for its last pair commit, and once both
+// producers have stopped (cluster barrier) the leader waits until every
+// stage load either CTA issued has landed -- a stage whose phase one CTA
+// armed or loaded and the other did not is balanced first (see the end of the
+// kernel) -- before both CTAs meet at a second cluster barrier and free TMEM.
+// Same fixed K order per element as gemm_tc.cuh.
 #pragma once
 
 #include "common.cuh"
@@ -66,7 +71,9 @@ __global__ void __launch_bounds__(Tc2Cfg<EPI_WG>::THREADS, 1)
   uint64_t* empty = full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* drain = acc_empty + 2;  // completion of every pair MMA (multicast to both CTAs)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint32_t* issued_slot = tmem_slot + 1;  // this CTA's stage-load count, read by the leader
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -80,6 +87,8 @@ __global__ void __launch_bounds__(Tc2Cfg<EPI_WG>::THREADS, 1)
       mbar_init(&acc_full[a], 1);                  // the pair commit
       mbar_init(&acc_empty[a], 2 * C::EPI_WARPS);  // every epilogue warp of both CTAs
     }
+    mbar_init(drain, 1);
+    *issued_slot = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
     tma_prefetch_desc(&tmA);
@@ -101,6 +110,7 @@ __global__ void __launch_bounds__(Tc2Cfg<EPI_WG>::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      int issued = 0;  // stage loads issued (and, in the leader, full[] phases armed)
       for (int t = cid; ok && t < num_tiles; t += ncl) {
         const int g = t / tiles_per_g, r = t - g * tiles_per_g;
         const int nt = r / m_pairs, mp = r - nt * m_pairs;
@@ -109,7 +119,8 @@ __global__ void __launch_bounds__(Tc2Cfg<EPI_WG>::THREADS, 1)
         const int b_row = nt * C::BN + (int)rank * (C::BN / 2);
         const int b_slot = layer / sh.map.b_div + sh.map.b_slot_off;
         for (int kb = 0; kb < sh.k_blocks; ++kb) {
-          if (!mbar_wait_bounded_cluster(&empty[stage], phase ^ 1u, sh.err, DEV_TIMEOUT_EMPTY)) {
+          if (issued == sh.wp.stall_after ||
+              !mbar_wait_bounded_cluster(&empty[stage], phase ^ 1u, sh.err, DEV_TIMEOUT_EMPTY, sh.wp.limit_ns)) {
             ok = false;
             break;
           }
@@ -117,12 +128,14 @@ __global__ void __launch_bounds__(Tc2Cfg<EPI_WG>::THREADS, 1)
           const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
           tma_load_3d_pair(sA + stage * C::A_BYTES, &tmA, kb * TC_BK, a_row, layer + sh.map.a_slot_off, fb);
           tma_load_3d_pair(sB + stage * C::B_BYTES, &tmB, kb * TC_BK, b_row, b_slot, fb);
+          ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
+      *issued_slot = (uint32_t)issued;
     }
   } else if (warp == 1) {
     if (leader && lane == 0) {
@@ -131,12 +144,13 @@ __global__ void __launch_bounds__(Tc2Cfg<EPI_WG>::THREADS, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int t = cid; ok && t < num_tiles; t += ncl) {
-        if (!mbar_wait_bounded_cluster(&acc_empty[acc], acc_phase ^ 1u, sh.err, DEV_TIMEOUT_ACC_EMPTY))
+        if (!mbar_wait_bounded_cluster(&acc_empty[acc], acc_phase ^ 1u, sh.err, DEV_TIMEOUT_ACC_EMPTY,
+                                       sh.wp.limit_ns))
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::BN);
         for (int kb = 0; kb < sh.k_blocks; ++kb) {
-          if (!mbar_wait_bounded_cluster(&full[stage], phase, sh.err, DEV_TIMEOUT_FULL)) {
+          if (!mbar_wait_bounded_cluster(&full[stage], phase, sh.err, DEV_TIMEOUT_FULL, sh.wp.limit_ns)) {
             ok = false;
             break;
           }
@@ -160,6 +174,10 @@ __global__ void __launch_bounds__(Tc2Cfg<EPI_WG>::THREADS, 1)
           acc_phase ^= 1u;
         }
       }
+      // Drain: every pair MMA issued above has finished (its arrivals made in
+      // both CTAs) before either CTA frees TMEM, also after an early stop.
+      tc_commit_pair(drain);
+      mbar_wait_drain(drain, 0);
     }
   } else {
     const int quarter = warp & 3;
@@ -173,7 +191,7 @@ __global__ void __launch_bounds__(Tc2Cfg<EPI_WG>::THREADS, 1)
       const int g = t / tiles_per_g, r = t - g * tiles_per_g;
       const int nt = r / m_pairs, mp = r - nt * m_pairs;
       const bool got =
-          mbar_wait_bounded_cluster(&acc_full[acc], acc_phase, sh.err, DEV_TIMEOUT_ACC_FULL);
+          mbar_wait_bounded_cluster(&acc_full[acc], acc_phase, sh.err, DEV_TIMEOUT_ACC_FULL, sh.wp.limit_ns);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const int row0 = mp * 2 * TC_BM + (int)rank * TC_BM + quarter * 32;
@@ -191,7 +209,36 @@ __global__ void __launch_bounds__(Tc2Cfg<EPI_WG>::THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // no remote arrival or pair MMA is still aimed at this CTA
+  cluster_sync_all();  // both producers have stopped issuing; the pair MMAs have finished
+  // Every stage load of both CTAs completes on the leader's full[] barriers,
+  // so the leader drains them for the pair.  With a and b the two CTAs' load
+  // counts, iterations below min(a, b) were armed and loaded by both and
+  // complete; at most one iteration per stage lies in [min, max) (a CTA runs
+  // at most STAGES loads ahead of the MMA's consumption, which needs both
+  // halves), and its phase lacks one share: the peer's bytes (balanced with
+  // complete_tx) or the leader's arming (balanced with arrive.expect_tx for
+  // the peer's bytes already in flight).  Its earlier phase is waited for
+  // first, so the balancing lands in the right phase.
+  if (leader && warp == 0 && lane == 0) {
+    const int a = (int)*issued_slot;
+    const int b = (int)ld_shared_cluster_u32(mapa_shared(smem_u32(issued_slot), 1));
+    const int lo = a < b ? a : b, hi = a < b ? b : a;
+    for (int s = 0; s < C::STAGES && s < hi; ++s) {
+      const int j = s + ((hi - 1 - s) / C::STAGES) * C::STAGES;  // last iteration of stage s
+      if (j >= lo) {
+        if (j >= C::STAGES) mbar_wait_drain(&full[s], (uint32_t)(((j - C::STAGES) / C::STAGES) & 1));
+        if (j < a)
+          mbar_complete_tx(&full[s], C::STAGE_BYTES);
+        else
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+      }
+      mbar_wait_drain(&full[s], (uint32_t)((j / C::STAGES) & 1));
+    }
+  }
+  // the leader's final pair commit also arrives here
+  if (!leader && warp == 1 && lane == 0) mbar_wait_drain(drain, 0);
+  __syncthreads();
+  cluster_sync_all();  // no copy, remote arrival or pair MMA is still aimed at either CTA
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
@@ -203,7 +250,8 @@ __global__ void __launch_bounds__(Tc2Cfg<EPI_WG>::THREADS, 1)
 template <class Epi, int EPI_WG = 1>
 static cudaError_t launch_gemm_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, int rows, int N, int K,
                             int g_first, int g_count, int* err, const Epi& epi, int num_sms,
-                            cudaStream_t stream, const GemmGroupMap& map = GemmGroupMap()) {
+                            cudaStream_t stream, const GemmGroupMap& map = GemmGroupMap(),
+                            const WaitPolicy& wp = WaitPolicy()) {
   using C = Tc2Cfg<EPI_WG>;
   static std::atomic<int> max_clusters{0};  // once per translation unit (the query is idempotent)
   cudaLaunchConfig_t cfg = {};
@@ -239,6 +287,7 @@ static cudaError_t launch_gemm_tc2(const CUtensorMap& tmA, const CUtensorMap& tm
   sh.n_tiles = N / C::BN;
   sh.k_blocks = K / TC_BK;
   sh.err = err;
+  sh.wp = wp;
   const int tiles = g_count * ((rows + 2 * TC_BM - 1) / (2 * TC_BM)) * sh.n_tiles;
   const int mc = max_clusters.load();
   const int clusters = tiles < mc ? tiles : mc;

@@ -7,7 +7,10 @@
 // hit cudaMalloc's implicit device-wide synchronisation.  This entry point
 // takes q|k|v in the plain fused row layout and keeps all of its scratch --
 // the transposed values and the error word -- in one file-scope device array
-// of fixed size, so it calls no allocator at all.
+// of fixed size, so it calls no allocator at all.  A bounded wait inside the
+// attention kernel that gives up records a code in that error word, which
+// stays set (later calls see it too) until armt_noalloc_sync_status reads
+// and clears it.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -23,6 +26,7 @@ namespace armt {
 bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int K, int rows, int layers,
                          int box_rows);
 void set_last_error(const std::string& msg);  // text returned by armt_last_error()
+void* current_context();                      // the calling thread's driver context
 }
 
 // Scratch shared by every call in the process on a given device: 256 bytes
@@ -34,11 +38,47 @@ namespace {
 
 constexpr size_t kErrBytes = 256;
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};  // device address of g_noalloc_scratch, per device
+// Device address of g_noalloc_scratch per device, and the context it was
+// looked up in: a new context (e.g. after cudaDeviceReset) reloads the
+// module, so the address is looked up again.
+struct ScratchAddr {
+  std::atomic<void*> ctx{nullptr};
+  std::atomic<unsigned char*> base{nullptr};
+};
+ScratchAddr g_scratch_addr[kMaxDevices];
 
 armt_status nfail(armt_status s, const std::string& msg) {
   set_last_error(msg);
   return s;
+}
+
+// Device address of the scratch array on the current device.  Set-up, the
+// first time on a device (or context): cudaGetSymbolAddress with the device
+// current, and the error word cleared.  Allocates nothing.
+armt_status scratch_base(unsigned char** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nfail(ARMT_ERR_NO_DEVICE, "no current CUDA device");
+  }
+  void* ctx = current_context();
+  ScratchAddr& a = g_scratch_addr[dev];
+  unsigned char* base = a.base.load();
+  if (base == nullptr || a.ctx.load() != ctx) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return nfail(ARMT_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+    }
+    e = cudaMemset(p, 0, sizeof(int));  // the error word starts clear
+    if (e != cudaSuccess) return nfail(ARMT_ERR_CUDA, std::string("cudaMemset: ") + cudaGetErrorString(e));
+    base = static_cast<unsigned char*>(p);
+    a.base.store(base);
+    a.ctx.store(ctx);
+  }
+  *out = base;
+  return ARMT_OK;
 }
 
 // vt[g][kvh][c][t] = qkv[g][t][(Hq + Hkv + kvh) * hd + c] for t < T, 0 for
@@ -82,29 +122,25 @@ extern "C" ARMT_API armt_status armt_segment_attention_bf16_noalloc(const void* 
                                      " bytes exceeds the fixed scratch of " +
                                      std::to_string((long long)ARMT_NOALLOC_SCRATCH_BYTES - (long long)kErrBytes) +
                                      " bytes");
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return nfail(ARMT_ERR_NO_DEVICE, "no current CUDA device");
   }
-  // First call on this device (with it current): look up the array's device
-  // address.  The name is only a host-side stand-in; kernels need this address.
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return nfail(ARMT_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
-    }
-    g_scratch_addr[dev] = p;
+  if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0) {
+    cudaGetLastError();
+    return nfail(ARMT_ERR_CUDA, "multiprocessor count query failed");
   }
-  unsigned char* base = static_cast<unsigned char*>(g_scratch_addr[dev]);
+  // The array's name is only a host-side stand-in; kernels get this address.
+  unsigned char* base = nullptr;
+  {
+    const armt_status sb = scratch_base(&base);
+    if (sb != ARMT_OK) return sb;
+  }
   int* err = reinterpret_cast<int*>(base);
   bf16* vt = reinterpret_cast<bf16*>(base + kErrBytes);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // the error word must start at zero for this call
-  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), st);
-  if (e != cudaSuccess) return nfail(ARMT_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
+  cudaError_t e;
   transpose_v_kernel<<<dim3((unsigned)((t_pad + 31) / 32), (unsigned)Hkv, (unsigned)G), 256, 0, st>>>(
       reinterpret_cast<const bf16*>(qkv), vt, T, (int)t_pad, Hq, Hkv, hd);
   e = cudaGetLastError();
@@ -122,12 +158,30 @@ extern "C" ARMT_API armt_status armt_segment_attention_bf16_noalloc(const void* 
   aa.n_qtiles = (T + 127) / 128;
   aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
   aa.err = err;
-  int nsm = 0;
-  if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0) {
-    cudaGetLastError();
-    nsm = 148;
-  }
+  aa.wp = wait_policy_from_env();
   e = hd == 64 ? launch_attn_tc<64>(tq, tv, aa, G, nsm, st) : launch_attn_tc<128>(tq, tv, aa, G, nsm, st);
   if (e != cudaSuccess) return nfail(ARMT_ERR_CUDA, std::string("attention: ") + cudaGetErrorString(e));
+  return ARMT_OK;
+}
+
+// Waits for `stream`, then reports (ARMT_ERR_TIMEOUT) and clears a timeout
+// that the no-allocation attention recorded on the current device since the
+// last call.  Allocates nothing.
+extern "C" ARMT_API armt_status armt_noalloc_sync_status(void* stream) {
+  unsigned char* base = nullptr;
+  {
+    const armt_status sb = scratch_base(&base);
+    if (sb != ARMT_OK) return sb;
+  }
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return nfail(ARMT_ERR_CUDA, std::string("cudaStreamSynchronize: ") + cudaGetErrorString(e));
+  int h = 0;
+  e = cudaMemcpy(&h, base, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return nfail(ARMT_ERR_CUDA, std::string("cudaMemcpy: ") + cudaGetErrorString(e));
+  if (h != 0) {
+    e = cudaMemset(base, 0, sizeof(int));
+    if (e != cudaSuccess) return nfail(ARMT_ERR_CUDA, std::string("cudaMemset: ") + cudaGetErrorString(e));
+    return nfail(ARMT_ERR_TIMEOUT, "device wait timed out (code " + std::to_string(h) + ")");
+  }
   return ARMT_OK;
 }
