@@ -279,11 +279,12 @@ def main():
     gu_launches, gu_ms = kt_timed["gemm_gateup"]
     gu_tflops = fl["gemm_gateup"] * cells / (gu_ms / 1000.0) / 1e12 if gu_ms > 0 else None
     peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-    # DRAM bytes of the gate-up GEMM per cell from one ncu capture of an 8-cell
-    # launch of the current kernel (profiles/gemm_gateup_armt1b_8k.md):
-    # traffic scales with cells (each cell's layer weights + activations), so
-    # per launch it is this times the launch's cells.  None until a capture
-    # of the current kernel exists.
+    # DRAM bytes of the gate-up GEMM per cell: dram__bytes_read.sum +
+    # dram__bytes_write.sum of one ncu capture of an 8-cell launch of the
+    # current kernel (ARMT-1B, 8 segments), divided by 8.  Traffic scales with
+    # cells (each cell's layer weights + activations), so per launch it is
+    # this times the launch's cells.  None until a capture of the current
+    # kernel exists.
     GATEUP_DRAM_BYTES_PER_CELL_1B = 86.4e6
     gu_traffic = (GATEUP_DRAM_BYTES_PER_CELL_1B * cells / gu_launches
                   if (GATEUP_DRAM_BYTES_PER_CELL_1B and gu_launches and args.workload.startswith("armt-1b"))
@@ -413,8 +414,10 @@ def main():
         h_A = torch.empty(model.a_elems, dtype=torch.float32).pin_memory()
         h_z = torch.empty(model.z_elems, dtype=torch.float32).pin_memory()
         model.armt_forward_host(h_tok, n_seg, h_hidden, h_A, h_z, 0, B.SCHEDULE_DIAGONAL, stream)
+        # the same K steps as the headline; host wall clock, because every
+        # call synchronises (its copies back to the host are part of the step)
         t0 = time.perf_counter()
-        ke = max(1, min(args.steps, 3))
+        ke = args.steps
         for _ in range(ke):
             model.armt_forward_host(h_tok, n_seg, h_hidden, h_A, h_z, 0, B.SCHEDULE_DIAGONAL, stream)
         dt = (time.perf_counter() - t0) / ke

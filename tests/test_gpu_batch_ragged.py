@@ -2,8 +2,8 @@
 
   - short last segment: n_tokens not a multiple of S; the last segment holds
     the remaining tokens followed by the memory tokens.  Against the fp64
-    oracle (fp32 model: max-abs <= 1e-4; bf16: the derived bounds of
-    test_gpu_parity), diagonal == sequential bitwise, and everything before
+    oracle (fp32 model: the bounds of test_gpu_parity.assert_fp32_close; bf16:
+    the derived bounds of test_gpu_parity), diagonal == sequential bitwise, and everything before
     the last segment bitwise equal to the run without it;
   - batch: each sequence of a batched call is bitwise equal to the same
     sequence run alone (batch 1), in both schedules; resuming a batch from
@@ -26,7 +26,7 @@ if not torch.cuda.is_available():
 from recurrent_memory_transformer_gb300 import armt as B  # noqa: E402
 from recurrent_memory_transformer_gb300 import build as build_mod  # noqa: E402
 
-from tests.test_gpu_parity import _derived_bounds_hold, record, stats  # noqa: E402
+from tests.test_gpu_parity import _derived_bounds_hold, assert_fp32_close, record, stats  # noqa: E402
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -63,7 +63,7 @@ def test_tiny_fp32_short_last_segment_matches_oracle(n_tok):
     sz = stats(zd[:, 0].cpu().numpy(), zo)
     record(f"tiny_short_{n_tok}", hidden=sh, A=sa, z=sz)
     assert hd.shape == (1, n_tok, cfg.d_model)
-    assert sh["max_abs"] <= 1e-4 and sa["max_abs"] <= 1e-4 and sz["max_abs"] <= 1e-4, (sh, sa, sz)
+    assert_fp32_close(sh, sa, sz)
     # the full segments before the short one do not depend on it
     full = (n_seg - 1) * cfg.seg_len
     if full > 0:
@@ -106,9 +106,8 @@ def test_tiny_fp32_batch_equals_each_sequence_alone(batch, n_tok):
         torch.cuda.synchronize()
         assert _equal(h1[0], hd[b]) and _equal(A1[:, 0], Ad[:, b]) and _equal(z1[:, 0], zd[:, b]), b
         ho, Ao, zo = O.forward(cfg, W, tok[b], n_seg)
-        assert np.abs(hd[b].cpu().numpy() - ho).max() <= 1e-4
-        assert np.abs(Ad[:, b].cpu().numpy() - Ao).max() <= 1e-4
-        assert np.abs(zd[:, b].cpu().numpy() - zo).max() <= 1e-4
+        assert_fp32_close(stats(hd[b].cpu().numpy(), ho), stats(Ad[:, b].cpu().numpy(), Ao),
+                          stats(zd[:, b].cpu().numpy(), zo))
     m.armt_sync_status()
     m.close()
 

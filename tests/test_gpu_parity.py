@@ -1,7 +1,11 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 oracle.
 
 Tolerances:
-  fp32 model (tiny):   max |gpu - oracle| <= 1e-4 on hidden states, A and z.
+  fp32 model (tiny):   max |gpu - oracle| <= 1e-4 on hidden states, A and z,
+                       and, since the state is tiny in these models (|A| ~
+                       1e-6, |z| ~ 3e-4, where an absolute 1e-4 would accept
+                       an all-zero state), also max-abs <= 1e-4 x max |oracle|
+                       and cosine >= 1 - 1e-9 on each of them.
   bf16 models, against the fp64 oracle:
     hidden states      cosine >= 0.999, and
                        max-abs <= 2 x the max-abs error of the oracle's own
@@ -37,12 +41,15 @@ if not torch.cuda.is_available():
 from recurrent_memory_transformer_gb300 import armt as B  # noqa: E402
 from recurrent_memory_transformer_gb300 import build as build_mod  # noqa: E402
 
-STATS_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
-                          "gpurun_out", "parity_stats.json")
+# Measured errors are written as JSON to the file named by ARMT_TEST_STATS
+# (nothing is written when it is unset).
+STATS_PATH = os.environ.get("ARMT_TEST_STATS")
 
 
 def record(name, **kv):
-    os.makedirs(os.path.dirname(STATS_PATH), exist_ok=True)
+    if not STATS_PATH:
+        return
+    os.makedirs(os.path.dirname(os.path.abspath(STATS_PATH)), exist_ok=True)
     data = {}
     if os.path.exists(STATS_PATH):
         try:
@@ -69,6 +76,23 @@ def stats(gpu, ref):
     err = np.abs(gpu - ref)
     return dict(max_abs=float(err.max()), mean_abs=float(err.mean()), ref_absmax=float(np.abs(ref).max()),
                 cos=cosine(gpu, ref), finite=bool(np.isfinite(gpu).all()))
+
+
+FP32_ABS, FP32_REL, FP32_COS = 1e-4, 1e-4, 1e-9
+
+
+def fp32_close(s):
+    """The fp32 model's bound on one output (a stats() dict)."""
+    return (s["finite"] and s["max_abs"] <= FP32_ABS and s["max_abs"] <= FP32_REL * s["ref_absmax"]
+            or s["max_abs"] == 0.0) and s["cos"] >= 1.0 - FP32_COS
+
+
+def assert_fp32_close(hidden, A, z):
+    """hidden: max-abs <= 1e-4 (and cosine); A, z: max-abs <= 1e-4 absolute and
+    relative to max |oracle|, cosine >= 1 - 1e-9."""
+    assert hidden["finite"] and hidden["max_abs"] <= FP32_ABS and hidden["cos"] >= 1.0 - FP32_COS, hidden
+    assert fp32_close(A), A
+    assert fp32_close(z), z
 
 
 def run_gpu(cfg, W, tok, n_seg, schedule):
@@ -191,9 +215,7 @@ def test_tiny_fp32_matches_oracle(name, over, n_seg, jit):
     sh, sa, sz = stats(hd, ho), stats(Ad, Ao), stats(zd, zo)
     record(name, hidden=sh, A=sa, z=sz)
     assert np.array_equal(hd, hs) and np.array_equal(Ad, As) and np.array_equal(zd, zs)
-    assert sh["max_abs"] <= 1e-4, sh
-    assert sa["max_abs"] <= 1e-4, sa
-    assert sz["max_abs"] <= 1e-4, sz
+    assert_fp32_close(sh, sa, sz)
 
 
 def test_tiny_resume_and_determinism():
