@@ -88,6 +88,28 @@ typedef enum armt_dtype {
   ARMT_BF16 = 1   /* weights bf16, matrix products on tcgen05 tensor cores, fp32 accumulation */
 } armt_dtype;
 
+/* Operand precision of the bf16 model's weight products (ignored by
+ * ARMT_F32 models).  The weights are bf16 either way.
+ *   ARMT_PRECISION_BF16    activations rounded to bf16 before every weight
+ *                          product (fastest);
+ *   ARMT_PRECISION_BF16X2  split operands: each activation operand of a
+ *                          weight product is carried as a bf16 high part plus
+ *                          a bf16 low part (its rounding residual), so the
+ *                          tensor cores see it with about 16 significant
+ *                          bits; the weight products run their K loop twice
+ *                          (about twice the tensor-core time).  The
+ *                          associative read splits both of its operands (the
+ *                          features and the state copy: four K passes).  The
+ *                          model holds a low copy of every split tensor.
+ * In both, the attention's own operands (q, k, v, probabilities) are fp16,
+ * and accumulation, the residual stream, norms, softmax statistics and the
+ * memory state are fp32.  The full-attention baseline and the LM head use
+ * plain bf16 operands. */
+typedef enum armt_precision {
+  ARMT_PRECISION_BF16 = 0,
+  ARMT_PRECISION_BF16X2 = 1
+} armt_precision;
+
 typedef enum armt_schedule {
   ARMT_SCHEDULE_DIAGONAL = 0,   /* one grouped launch per anti-diagonal l + s = i */
   ARMT_SCHEDULE_SEQUENTIAL = 1  /* segment by segment, layer by layer, one cell per launch */
@@ -110,6 +132,7 @@ typedef struct armt_config {
   float assoc_eps;     /* epsilon in the associative denominators */
   double rope_base;    /* RoPE base (theta) */
   int32_t dtype;       /* armt_dtype */
+  int32_t precision;   /* armt_precision (ARMT_BF16 models) */
 } armt_config;
 
 /* Weights, stacked over layers (section 三: one grouped layer holds every

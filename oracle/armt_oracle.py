@@ -58,13 +58,21 @@ used as a library primitive; nothing is blocked, fused or reordered beyond
 the definitions above.
 
 Optional precision model (``operands="bf16"``): the same arithmetic in fp64,
-except that every tensor-core operand of a bf16 kernel path is rounded to the
-nearest bf16 value first -- the layer input for the associative query, the
-features and the state copy of the associative read, both RMSNorm outputs,
-q/k after RoPE and v, the attention probabilities (before normalisation by
-the row sum) and the attention output, the SwiGLU output, and the memory
-rows fed to the write projections.  This is a model of a design choice, not
-of the method; the default (``operands=None``) is the method itself.
+except that every tensor-core operand of the bf16 kernel path is rounded to
+its 16-bit type first.  Operands of the weight products are rounded to bf16
+(the weights' type): the layer input for the associative query, the features
+and the state copy of the associative read, both RMSNorm outputs, the
+attention output, the SwiGLU output, and the memory rows fed to the write
+projections.  The attention's own operands -- q and k after RoPE, v, and the
+probabilities (before normalisation by the row sum) -- are activations only,
+and the kernel path gives them fp16 (same width, three more mantissa bits),
+so the model rounds them to fp16.  ``operands="bf16x2"`` models the split
+precision mode of the same path: the operands of the weight products and of
+the associative read (features and state copy) are carried as a bf16 high
+part plus the bf16 rounding of the residual (about 16 significant bits);
+the attention operands stay fp16.  These are models of
+design choices, not of the method; the default (``operands=None``) is the
+method itself.
 """
 from __future__ import annotations
 
@@ -95,7 +103,31 @@ def round_bf16(a):
     return r.view(np.float32).astype(F64)
 
 
-ROUNDING = {None: _identity, "bf16": round_bf16}
+def round_f16(a):
+    """Nearest IEEE half-precision value (ties to even), via float32, as float64."""
+    return np.asarray(a, dtype=np.float32).astype(np.float16).astype(F64)
+
+
+class OperandRounding:
+    """Where the precision model rounds: ``mm`` for operands of the weight
+    products, ``att`` for the attention's q, k, v and probabilities, ``read``
+    for the associative read's features and state copy (default: ``mm``)."""
+
+    def __init__(self, mm, att, read=None):
+        self.mm, self.att = mm, att
+        self.read = mm if read is None else read
+
+
+def round_split(a):
+    """bf16 high part plus the bf16 rounding of what it drops (via float32)."""
+    a32 = np.asarray(a, dtype=np.float32).astype(F64)
+    hi = round_bf16(a32)
+    return hi + round_bf16(a32 - hi)
+
+
+EXACT = OperandRounding(_identity, _identity)
+ROUNDING = {None: EXACT, "bf16": OperandRounding(round_bf16, round_f16),
+            "bf16x2": OperandRounding(round_split, round_f16)}
 
 
 # --------------------------------------------------------------------------
@@ -169,16 +201,16 @@ def causal_gqa_attention(q, k, v, rnd=_identity):
 # Associative memory (delta rule)
 # --------------------------------------------------------------------------
 
-def assoc_lookup(A, z, phi, eps, rnd=_identity):
+def assoc_lookup(A, z, phi, eps, rnd=EXACT):
     """A phi / (z^T phi + eps) for each row of phi [R, P]; A [d, P], z [P]."""
-    num = rnd(phi) @ rnd(A).T
+    num = rnd.read(phi) @ rnd.read(A).T
     den = phi @ z + eps
     return num / den[:, None]
 
 
-def assoc_read(x, wq_a, A, z, nu, eps, rnd=_identity):
+def assoc_read(x, wq_a, A, z, nu, eps, rnd=EXACT):
     """Memory read added to the residual stream: x + lookup(phi(W_Q x))."""
-    phi = dpfp(rnd(x) @ wq_a.T, nu)
+    phi = dpfp(rnd.mm(x) @ wq_a.T, nu)
     return x + assoc_lookup(A, z, phi, eps, rnd)
 
 
@@ -196,13 +228,13 @@ def delta_rule_update(A, z, keys, values, beta, nu, eps) -> Tuple[np.ndarray, np
     return A + dA, z + dz
 
 
-def assoc_write(h_mem, wk_a, wv_a, wb_a, A, z, nu, eps, rnd=_identity):
+def assoc_write(h_mem, wk_a, wv_a, wb_a, A, z, nu, eps, rnd=EXACT):
     """Write from the memory-token rows h_mem [M, d] of one layer's output.
 
     The rows are written one after another in row order; write i sees the
     state that write i-1 produced.
     """
-    h_mem = rnd(h_mem)
+    h_mem = rnd.mm(h_mem)
     keys = h_mem @ wk_a.T
     values = h_mem @ wv_a.T
     beta = sigmoid(h_mem @ wb_a)
@@ -215,23 +247,23 @@ def assoc_write(h_mem, wk_a, wv_a, wb_a, A, z, nu, eps, rnd=_identity):
 # One cell and the whole grid
 # --------------------------------------------------------------------------
 
-def llama_block(x, cfg, W, l, rnd=_identity):
+def llama_block(x, cfg, W, l, rnd=EXACT):
     """Pre-norm LLaMA decoder layer on the rows of one cell (x [T_c, d])."""
     T = x.shape[0]
     Hq, Hkv, hd = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
-    n = rnd(rmsnorm(x, W["norm1"][l], cfg.norm_eps))
+    n = rnd.mm(rmsnorm(x, W["norm1"][l], cfg.norm_eps))
     q = (n @ W["wq"][l].T).reshape(T, Hq, hd)
     k = (n @ W["wk"][l].T).reshape(T, Hkv, hd)
-    v = rnd((n @ W["wv"][l].T).reshape(T, Hkv, hd))
-    q = rnd(rope_rotate_half(q, cfg.rope_base))
-    k = rnd(rope_rotate_half(k, cfg.rope_base))
-    y = x + rnd(causal_gqa_attention(q, k, v, rnd)) @ W["wo"][l].T
-    n2 = rnd(rmsnorm(y, W["norm2"][l], cfg.norm_eps))
-    u = rnd(silu(n2 @ W["w_gate"][l].T) * (n2 @ W["w_up"][l].T))
+    v = rnd.att((n @ W["wv"][l].T).reshape(T, Hkv, hd))
+    q = rnd.att(rope_rotate_half(q, cfg.rope_base))
+    k = rnd.att(rope_rotate_half(k, cfg.rope_base))
+    y = x + rnd.mm(causal_gqa_attention(q, k, v, rnd.att)) @ W["wo"][l].T
+    n2 = rnd.mm(rmsnorm(y, W["norm2"][l], cfg.norm_eps))
+    u = rnd.mm(silu(n2 @ W["w_gate"][l].T) * (n2 @ W["w_up"][l].T))
     return y + u @ W["w_down"][l].T
 
 
-def cell_forward(x, cfg, W, l, A, z, rnd=_identity):
+def cell_forward(x, cfg, W, l, A, z, rnd=EXACT):
     """Cell (l, s): read, LLaMA block, write.  Returns (h, A', z')."""
     nu, eps = cfg.dpfp_nu, cfg.assoc_eps
     x = assoc_read(x, W["a_wq"][l], A, z, nu, eps, rnd)

@@ -22,6 +22,7 @@ ARMT_OK = 0
 STATUS_NAMES = {0: "ARMT_OK", 1: "ARMT_ERR_ARG", 2: "ARMT_ERR_SHAPE", 3: "ARMT_ERR_UNSUPPORTED",
                 4: "ARMT_ERR_OOM", 5: "ARMT_ERR_CUDA", 6: "ARMT_ERR_TIMEOUT", 7: "ARMT_ERR_NO_DEVICE"}
 ARMT_F32, ARMT_BF16 = 0, 1
+PRECISION_BF16, PRECISION_BF16X2 = 0, 1
 SCHEDULE_DIAGONAL, SCHEDULE_SEQUENTIAL = 0, 1
 KERNEL_CLASSES = ("gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down", "attention", "assoc_read",
                   "assoc_write", "norm", "other")
@@ -48,7 +49,7 @@ class armt_config(ctypes.Structure):
                 ("n_mem", ctypes.c_int32), ("key_dim", ctypes.c_int32),
                 ("dpfp_nu", ctypes.c_int32), ("norm_eps", ctypes.c_float),
                 ("assoc_eps", ctypes.c_float), ("rope_base", ctypes.c_double),
-                ("dtype", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("precision", ctypes.c_int32)]
 
 
 _WKEYS = ("embed", "mem", "wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "a_wq", "a_wk",
@@ -113,7 +114,8 @@ def make_config(cfg: "_inputs.ArmtConfig") -> armt_config:
     return armt_config(cfg.n_layers, cfg.d_model, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim,
                        cfg.ffn_dim, cfg.vocab, cfg.seg_len, cfg.n_mem, cfg.key_dim, cfg.dpfp_nu,
                        cfg.norm_eps, cfg.assoc_eps, cfg.rope_base,
-                       ARMT_BF16 if cfg.dtype == "bf16" else ARMT_F32)
+                       ARMT_BF16 if cfg.dtype == "bf16" else ARMT_F32,
+                       PRECISION_BF16X2 if cfg.precision == "bf16x2" else PRECISION_BF16)
 
 
 def _stream_ptr(stream) -> Optional[int]:

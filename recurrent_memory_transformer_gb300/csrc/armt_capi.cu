@@ -299,11 +299,15 @@ template <typename WT>
 struct Model : ModelBase {
   static constexpr bool kTC = sizeof(WT) == 2;  // bf16: tensor-core GEMMs
   typedef WT AT;                               // activation dtype of GEMM operands
+  // attention operands (q, k, v): fp16 on the tensor-core path -- they are
+  // activations, not weights, so they may take the 16-bit type with the
+  // longer mantissa at the same tensor-core rate; fp32 on the fp32 path
+  typedef std::conditional_t<kTC, f16, float> QT;
   // epilogue functors: staged (lanes across columns) on the tensor-core
   // path, thread-per-row on the fp32 path
   using FStore = std::conditional_t<kTC, SEpiStore, EpiStore>;
   using FRead = std::conditional_t<kTC, SEpiAssocRead<AT>, EpiAssocRead<AT>>;
-  using FQkv = std::conditional_t<kTC, SEpiQkvRope<AT>, EpiQkvRope<AT>>;
+  using FQkv = std::conditional_t<kTC, SEpiQkvRope<QT>, EpiQkvRope<QT>>;
   using FRes = std::conditional_t<kTC, SEpiResidual<AT>, EpiResidual<AT>>;
   using FSwi = std::conditional_t<kTC, SEpiSwiGLU<AT>, EpiSwiGLU<AT>>;
 
@@ -314,6 +318,10 @@ struct Model : ModelBase {
   int npart = 0;  // partial sums of squares per row (one per epilogue column tile)
   int nw = 0;  // rows of Ww per layer (d + k + 1 rounded up to the tile width)
   int qkv_ld = 0, t_pad = 0;  // row stride of QKV; padded row count of Vt
+  // split precision (ARMT_PRECISION_BF16X2): Nrm, Att, U and Xa hold a bf16
+  // low part behind the high one (twice the slots), and the weight GEMMs read
+  // both (GemmGroupMap::a_lo_slot)
+  bool split = false;
   int nmax = 0;  // widest GEMM output (fp32 scratch row stride)
   // weight tensor maps (bf16 path); the *2 maps have 128-row boxes for CTA-pair tiles
   CUtensorMap tmAWq, tmWqkv, tmWo, tmWgu, tmWd, tmWw, tmWqkv2, tmWo2, tmWgu2, tmWd2;
@@ -329,8 +337,8 @@ struct Model : ModelBase {
     float *X = nullptr, *Res = nullptr, *Qa = nullptr, *Den = nullptr, *VKB = nullptr,
           *PhiM = nullptr, *Coef = nullptr, *Cscr = nullptr, *Ssq = nullptr, *cosT = nullptr,
           *sinT = nullptr;
-    AT *Xa = nullptr, *Nrm = nullptr, *QKV = nullptr, *Att = nullptr, *U = nullptr,
-       *Phi = nullptr, *Aa = nullptr, *Vt = nullptr;
+    AT *Xa = nullptr, *Nrm = nullptr, *Att = nullptr, *U = nullptr, *Phi = nullptr, *Aa = nullptr;
+    QT *QKV = nullptr, *Vt = nullptr;
     // row views {width, R, layers}; group views {width, T, layers * nb}
     CUtensorMap tmXa, tmNrm, tmAtt, tmU, tmXaW, tmPhi, tmAa, tmQK, tmVt;
   };
@@ -347,7 +355,8 @@ struct Model : ModelBase {
   AT* lm_rows = nullptr;
   static constexpr int64_t kLmChunk = 8192;
   float *Xf = nullptr, *Resf = nullptr, *Ssqf = nullptr, *cosF = nullptr, *sinF = nullptr;
-  AT *Nrmf = nullptr, *QKVf = nullptr, *Vtf = nullptr, *Attf = nullptr, *Uf = nullptr;
+  AT *Nrmf = nullptr, *Attf = nullptr, *Uf = nullptr;
+  QT *QKVf = nullptr, *Vtf = nullptr;
   CUtensorMap tmNrmf, tmQKf, tmVtf, tmAttf, tmUf;
   ~Model() override {
     full_mem.free_all();
@@ -443,6 +452,7 @@ struct Model : ModelBase {
       ok &= encode_tmap_bf16_3d(&tmWw, Ww, (int)d, nw, (int)L, 256);
       if (!ok) return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     }
+    split = kTC && c.precision == ARMT_PRECISION_BF16X2;
     CKS(alloc_work(w1, 1, mem, st));
     CKS(mem.alloc_n(&d_err, 1));
     CK(cudaMemsetAsync(d_err, 0, sizeof(int), st));
@@ -494,38 +504,39 @@ struct Model : ModelBase {
       CK(cudaMemcpy(w.cosT, hc.data(), hc.size() * 4, cudaMemcpyHostToDevice));
       CK(cudaMemcpy(w.sinT, hs.data(), hs.size() * 4, cudaMemcpyHostToDevice));
     }
+    const size_t halves = split ? 2 : 1;  // split precision: high and low parts
     CKS(pool.alloc_n(&w.X, (L + 1) * R * d));
     if (kTC) {
-      CKS(pool.alloc_n(&w.Xa, (L + 1) * R * d));
+      CKS(pool.alloc_n(&w.Xa, halves * (L + 1) * R * d));
     } else {
       w.Xa = reinterpret_cast<AT*>(w.X);
     }
     CKS(pool.alloc_n(&w.Res, L * R * d));
-    CKS(pool.alloc_n(&w.Nrm, L * R * d));
+    CKS(pool.alloc_n(&w.Nrm, halves * L * R * d));
     // bf16: q|k rows in QKV, v transposed into Vt; fp32: q|k|v rows in QKV
     CKS(pool.alloc_n(&w.QKV, L * R * (size_t)qkv_ld));
     if (kTC) CKS(pool.alloc_n(&w.Vt, L * nb * Hkv * hd * (size_t)t_pad));
-    CKS(pool.alloc_n(&w.Att, L * R * Hq * hd));
-    CKS(pool.alloc_n(&w.U, L * R * F));
+    CKS(pool.alloc_n(&w.Att, halves * L * R * Hq * hd));
+    CKS(pool.alloc_n(&w.U, halves * L * R * F));
     CKS(pool.alloc_n(&w.Qa, L * R * k));
-    CKS(pool.alloc_n(&w.Phi, L * R * P));
+    CKS(pool.alloc_n(&w.Phi, halves * L * R * P));
     CKS(pool.alloc_n(&w.Den, L * R));
     CKS(pool.alloc_n(&w.Ssq, L * R * (size_t)npart));
     CKS(pool.alloc_n(&w.VKB, L * nb * M * (size_t)nw));
     CKS(pool.alloc_n(&w.PhiM, L * nb * M * P));
     CKS(pool.alloc_n(&w.Coef, L * nb * M * 2));
-    if (kTC) CKS(pool.alloc_n(&w.Aa, L * nb * d * P));
+    if (kTC) CKS(pool.alloc_n(&w.Aa, halves * L * nb * d * P));
     if (!kTC) CKS(pool.alloc_n(&w.Cscr, L * R * (size_t)nmax));
     if (kTC) {
-      const int iR = (int)R, iT = (int)T, iL = (int)L, G = (int)L * nb;
+      const int iR = (int)R, iT = (int)T, iL = (int)L, G = (int)L * nb, h = (int)halves;
       bool ok = true;
-      ok &= encode_tmap_bf16_3d(&w.tmXa, w.Xa, (int)d, iR, iL + 1, TC_BM);
-      ok &= encode_tmap_bf16_3d(&w.tmNrm, w.Nrm, (int)d, iR, iL, TC_BM);
-      ok &= encode_tmap_bf16_3d(&w.tmAtt, w.Att, (int)(Hq * hd), iR, iL, TC_BM);
-      ok &= encode_tmap_bf16_3d(&w.tmU, w.U, (int)F, iR, iL, TC_BM);
-      ok &= encode_tmap_bf16_3d(&w.tmXaW, w.Xa, (int)d, iT, (iL + 1) * nb, TC_BM);
-      ok &= encode_tmap_bf16_3d(&w.tmPhi, w.Phi, (int)P, iT, G, TC_BM);
-      ok &= encode_tmap_bf16_3d(&w.tmAa, w.Aa, (int)P, (int)d, G, 256);
+      ok &= encode_tmap_bf16_3d(&w.tmXa, w.Xa, (int)d, iR, h * (iL + 1), TC_BM);
+      ok &= encode_tmap_bf16_3d(&w.tmNrm, w.Nrm, (int)d, iR, h * iL, TC_BM);
+      ok &= encode_tmap_bf16_3d(&w.tmAtt, w.Att, (int)(Hq * hd), iR, h * iL, TC_BM);
+      ok &= encode_tmap_bf16_3d(&w.tmU, w.U, (int)F, iR, h * iL, TC_BM);
+      ok &= encode_tmap_bf16_3d(&w.tmXaW, w.Xa, (int)d, iT, h * (iL + 1) * nb, TC_BM);
+      ok &= encode_tmap_bf16_3d(&w.tmPhi, w.Phi, (int)P, iT, h * G, TC_BM);
+      ok &= encode_tmap_bf16_3d(&w.tmAa, w.Aa, (int)P, (int)d, h * G, 256);
       ok &= encode_tmap_bf16_3d(&w.tmQK, w.QKV, qkv_ld, iT, G, 128);
       ok &= encode_tmap_bf16_3d(&w.tmVt, w.Vt, t_pad, (int)hd, G * (int)Hkv, (int)hd);
       if (!ok) return fail(ARMT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
@@ -602,21 +613,36 @@ struct Model : ModelBase {
     const long long Rd = (long long)R * d;
     // the last segment holds last_len <= S tokens; its memory rows follow them
     const int last_len = last_segment_len(n_tok, S);
+    // split precision: where the low parts live (elements, and A slots of the
+    // GEMM operand maps); all zero when the model is not split
+    const long long xa_lo = split ? (long long)(L + 1) * Rd : 0, nrm_lo = split ? (long long)L * Rd : 0;
+    const long long att_lo = split ? (long long)L * R * Hq * hd : 0, u_lo = split ? (long long)L * R * F : 0;
+    GemmGroupMap layer_lo;  // A slot l + L holds the low part of slot l
+    layer_lo.a_lo_slot = split ? L : 0;
+    GemmGroupMap xa_map;    // Xa slots: L + 1 of them
+    xa_map.a_lo_slot = split ? L + 1 : 0;
+    GemmGroupMap read_map;  // features x state copy, both split: L * nb groups each
+    read_map.a_lo_slot = split ? L * nb : 0;
+    read_map.b_lo_slot = split ? L * nb : 0;
+    const long long phi_lo = split ? (long long)L * R * P : 0;
+    const long long aa_lo = split ? (long long)L * nb * d * P : 0;
     const int64_t l_last = last_segment_layer(lo, s_lo, n_seg);  // layer of the last segment's cell
     const bool short_here = last_len < S && l_last >= lo && l_last <= hi;
     if (lo == 0) {
       const int n_rows = s_lo == n_seg - 1 ? last_len : S;
       CKS(prof_begin(ARMT_KC_OTHER, st));
       embed_gather_kernel<WT><<<dim3(T, nb), 256, 0, st>>>(tokens + s_lo * S, n_tok, embed, memtok,
-                                                           w.X, w.Xa, T, n_rows, M, d, c.vocab);
+                                                           w.X, w.Xa, T, n_rows, M, d, c.vocab, xa_lo);
       CK(cudaGetLastError());
       CKS(prof_end(st));
     }
     // associative read: q = Wq_a x, phi, den, then x' = x + A phi / den.  On the
     // tensor-core path phi and den come out of the query GEMM's epilogue.
     if constexpr (kTC) {
-      CKS((gemm<64, SEpiPhi<AT>>(ARMT_KC_ASSOC_READ, w, w.tmXa, tmAWq, w.Xa, Rd, aWq, k, d,
-                                 SEpiPhi<AT>{w.Phi, w.Den, z, R, T, nb, c.assoc_eps}, lo, g, st, R)));
+      SEpiPhi<AT> ph{w.Phi, w.Den, z, R, T, nb, c.assoc_eps};
+      ph.lo_off = phi_lo;
+      CKS((gemm<64, SEpiPhi<AT>>(ARMT_KC_ASSOC_READ, w, w.tmXa, tmAWq, w.Xa, Rd, aWq, k, d, ph, lo, g, st, R,
+                                 xa_map)));
     } else {
       CKS((gemm<64>(ARMT_KC_ASSOC_READ, w, w.tmXa, tmAWq, w.Xa, Rd, aWq, k, d,
                     FStore{w.Qa, (long long)k, (long long)R * k}, lo, g, st, R)));
@@ -633,15 +659,16 @@ struct Model : ModelBase {
     {
       RowNormOut<AT> n1{g1, w.Nrm, w.Ssq};
       n1.gdiv = nb;
+      n1.lo_off = nrm_lo;
       CKS((gemm<256, FRead, 2>(ARMT_KC_ASSOC_READ, w, w.tmPhi, w.tmAa, w.Phi, (long long)T * P,
                                reinterpret_cast<const WT*>(Asrc), d, P,
-                               FRead{w.X, w.Den, w.Res, T, d, n1}, lo * nb, g * nb, st, T)));
+                               FRead{w.X, w.Den, w.Res, T, d, n1}, lo * nb, g * nb, st, T, read_map)));
     }
     // attention sub-layer (RMSNorm 1 completes in the QKV epilogue)
     CKS((gemm<256, FQkv, 1>(ARMT_KC_GEMM_QKV, w, w.tmNrm, tmWqkv, w.Nrm, Rd, Wqkv, Nq, d,
                             FQkv{w.QKV, w.cosT, w.sinT, R, hd, (Hq + Hkv) * hd, qkv_ld, w.Vt, Hkv,
                                  t_pad, norm_in, T, nb},
-                            lo, g, st, R, GemmGroupMap(), &tmWqkv2)));
+                            lo, g, st, R, layer_lo, &tmWqkv2)));
     CKS(prof_begin(ARMT_KC_ATTENTION, st));
     if constexpr (kTC) {
       AttnArgs aa;
@@ -654,10 +681,11 @@ struct Model : ModelBase {
       aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
       aa.err = d_err;
       aa.wp = wp;
+      aa.out_lo_off = att_lo;
       if (hd == 64)
-        CK(launch_attn_tc<64>(w.tmQK, w.tmVt, aa, g * nb, num_sms, st));
+        CK((launch_attn_tc<64, QT>(w.tmQK, w.tmVt, aa, g * nb, num_sms, st)));
       else
-        CK(launch_attn_tc<128>(w.tmQK, w.tmVt, aa, g * nb, num_sms, st));
+        CK((launch_attn_tc<128, QT>(w.tmQK, w.tmVt, aa, g * nb, num_sms, st)));
     } else {
       dim3 grid((T + 63) / 64, Hq, g * nb);
       const float scale = 1.0f / sqrtf((float)hd);
@@ -670,16 +698,26 @@ struct Model : ModelBase {
       CK(cudaGetLastError());
     }
     CKS(prof_end(st));
-    CKS((gemm<256, FRes, 2>(ARMT_KC_GEMM_O, w, w.tmAtt, tmWo, w.Att, (long long)R * Hq * hd, Wo, d,
-                            Hq * hd, FRes{w.Res, w.Res, nullptr, R, d, 0, RowNormOut<AT>{g2, w.Nrm, w.Ssq}},
-                            lo, g, st, R, GemmGroupMap(), &tmWo2)));
+    {
+      RowNormOut<AT> n2{g2, w.Nrm, w.Ssq};
+      n2.lo_off = nrm_lo;
+      CKS((gemm<256, FRes, 2>(ARMT_KC_GEMM_O, w, w.tmAtt, tmWo, w.Att, (long long)R * Hq * hd, Wo, d,
+                              Hq * hd, FRes{w.Res, w.Res, nullptr, R, d, 0, n2}, lo, g, st, R, layer_lo,
+                              &tmWo2)));
+    }
     // MLP sub-layer (RMSNorm 2 completes in the gate-up epilogue)
-    CKS((gemm<256, FSwi, 1>(ARMT_KC_GEMM_GATEUP, w, w.tmNrm, tmWgu, w.Nrm, Rd, Wgu, 2 * F, d,
-                            FSwi{w.U, R, F, norm_in}, lo, g, st, R, GemmGroupMap(), &tmWgu2)));
-    CKS((gemm<256, FRes, 1>(ARMT_KC_GEMM_DOWN, w, w.tmU, tmWd, w.U, (long long)R * F, Wd, d, F,
-                            FRes{w.Res, w.X, kTC ? w.Xa : nullptr, R, d, 1,
-                                 RowNormOut<AT>{nullptr, nullptr, nullptr}},
-                            lo, g, st, R, GemmGroupMap(), &tmWd2)));
+    {
+      FSwi swi{w.U, R, F, norm_in};
+      FRes down{w.Res, w.X, kTC ? w.Xa : nullptr, R, d, 1, RowNormOut<AT>{nullptr, nullptr, nullptr}};
+      if constexpr (kTC) {
+        swi.lo_off = u_lo;
+        down.copy_lo_off = xa_lo;
+      }
+      CKS((gemm<256, FSwi, 1>(ARMT_KC_GEMM_GATEUP, w, w.tmNrm, tmWgu, w.Nrm, Rd, Wgu, 2 * F, d, swi, lo, g, st,
+                              R, layer_lo, &tmWgu2)));
+      CKS((gemm<256, FRes, 1>(ARMT_KC_GEMM_DOWN, w, w.tmU, tmWd, w.U, (long long)R * F, Wd, d, F, down, lo,
+                              g, st, R, layer_lo, &tmWd2)));
+    }
     // delta-rule write from the memory-token rows of this layer's output:
     // [v | k | beta] = h_mem [Wv_a; Wk_a; wbeta_a]^T on the tensor cores, per
     // (layer, sequence) group: A = the M memory rows of the cell in layer
@@ -691,6 +729,7 @@ struct Model : ModelBase {
       wm.row0 = S;
       wm.a_slot_off = nb;
       wm.b_div = nb;
+      wm.a_lo_slot = split ? (L + 1) * nb : 0;
       if (short_here) {
         wm.alt_lo = (int)l_last * nb;
         wm.alt_hi = (int)(l_last + 1) * nb;
@@ -711,13 +750,13 @@ struct Model : ModelBase {
       const int gf0 = lo * nb;
       if (P == 96)
         assoc_write_update_kernel<AT, 3><<<grid, 128, upd_smem, st>>>(w.VKB, nw, w.PhiM, w.Coef, A, Adst,
-                                                                      M, d, upd_rows_per_block, gf0);
+                                                                      M, d, upd_rows_per_block, gf0, aa_lo);
       else if (P == 192)
         assoc_write_update_kernel<AT, 6><<<grid, 128, upd_smem, st>>>(w.VKB, nw, w.PhiM, w.Coef, A, Adst,
-                                                                      M, d, upd_rows_per_block, gf0);
+                                                                      M, d, upd_rows_per_block, gf0, aa_lo);
       else
         assoc_write_update_kernel<AT, 12><<<grid, 128, upd_smem, st>>>(w.VKB, nw, w.PhiM, w.Coef, A, Adst,
-                                                                       M, d, upd_rows_per_block, gf0);
+                                                                       M, d, upd_rows_per_block, gf0, aa_lo);
       CK(cudaGetLastError());
     }
     CKS(prof_end(st));
@@ -883,9 +922,9 @@ struct Model : ModelBase {
           aa.err = d_err;
           aa.wp = wp;
           if (hd == 64)
-            CK(launch_attn_tc<64>(tmQKf, tmVtf, aa, 1, num_sms, st));
+            CK((launch_attn_tc<64, QT>(tmQKf, tmVtf, aa, 1, num_sms, st)));
           else
-            CK(launch_attn_tc<128>(tmQKf, tmVtf, aa, 1, num_sms, st));
+            CK((launch_attn_tc<128, QT>(tmQKf, tmVtf, aa, 1, num_sms, st)));
         }
         CKS(prof_end(st));
         CKS(prof_begin(ARMT_KC_GEMM_O, st));
@@ -924,10 +963,10 @@ struct Model : ModelBase {
     if (!mem_in_valid) {
       CK(cudaMemsetAsync(A, 0, a_n * sizeof(float), st));
       CK(cudaMemsetAsync(z, 0, z_n * sizeof(float), st));
-      if (kTC) CK(cudaMemsetAsync(w.Aa, 0, a_n * sizeof(AT), st));
+      if (kTC) CK(cudaMemsetAsync(w.Aa, 0, (split ? 2 : 1) * a_n * sizeof(AT), st));
     } else if (kTC) {
       CKS(prof_begin(ARMT_KC_OTHER, st));
-      convert_state_kernel<AT><<<4 * num_sms, 256, 0, st>>>(A, w.Aa, (long long)a_n);
+      convert_state_kernel<AT><<<4 * num_sms, 256, 0, st>>>(A, w.Aa, (long long)a_n, split ? (long long)a_n : 0);
       CK(cudaGetLastError());
       CKS(prof_end(st));
     }
@@ -959,6 +998,10 @@ static armt_status validate(const armt_config* c) {
   if (!(c->norm_eps > 0.f) || !(c->assoc_eps > 0.f) || !(c->rope_base > 1.0))
     return fail(ARMT_ERR_ARG, "norm_eps, assoc_eps must be > 0 and rope_base > 1");
   if (c->dtype != ARMT_F32 && c->dtype != ARMT_BF16) return fail(ARMT_ERR_ARG, "unknown dtype");
+  if (c->precision != ARMT_PRECISION_BF16 && c->precision != ARMT_PRECISION_BF16X2)
+    return fail(ARMT_ERR_ARG, "unknown precision");
+  if (c->precision == ARMT_PRECISION_BF16X2 && c->dtype != ARMT_BF16)
+    return fail(ARMT_ERR_UNSUPPORTED, "split precision needs a bf16 model");
   if (c->n_q_heads % c->n_kv_heads != 0)
     return fail(ARMT_ERR_SHAPE, "n_q_heads must be a multiple of n_kv_heads");
   if (c->n_mem > 32) return fail(ARMT_ERR_UNSUPPORTED, "n_mem > 32");

@@ -25,7 +25,12 @@
 // gives every barrier's phase: per-tile barriers complete once per tile,
 // buffer c % 2 holds tile c, and its barriers complete once every 2 tiles.
 // V comes pre-transposed (Vt[l][g][hd][T], written by the QKV epilogue) so
-// that every MMA operand is K-major.  fp32 accumulation and softmax.
+// that every MMA operand is K-major.  fp32 accumulation and softmax.  The
+// operands (q, k, v and the probabilities P) are 16-bit of type OpT: bf16
+// for the stand-alone entry points, fp16 inside the bf16 model, whose
+// attention operands are activations (10 mantissa bits instead of 7 at the
+// same tensor-core rate; q and k come from RMS-normalised rows, P lies in
+// [0, 1]).  The output is bf16, the operand type of the output projection.
 #pragma once
 
 #include "common.cuh"
@@ -53,6 +58,7 @@ struct AttnArgs {
   float scale_log2;  // log2(e) / sqrt(HD)
   int* err;
   WaitPolicy wp;     // wait limit and the test stall hook (counted in K/V tile loads)
+  long long out_lo_off = 0;  // split precision: bf16 low part of the output at out + out_lo_off
 };
 
 // Work item i (heaviest query tiles first): m = n_qtiles - 1 - i / (Hq * G),
@@ -76,7 +82,7 @@ enum AttnBar {
   B_SF0, B_SF1, B_OF0, B_OF1, B_FREE0, B_FREE1, B_DRAIN, B_COUNT
 };
 
-template <int HD>
+template <int HD, typename OpT>
 __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant__ CUtensorMap tmV,
                    const AttnArgs a) {
@@ -163,8 +169,8 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128);
-      constexpr uint32_t idO = idesc_bf16_f32(128, HD);
+      constexpr uint32_t idS = idesc_16bit_f32<OpT>(128, 128);
+      constexpr uint32_t idO = idesc_16bit_f32<OpT>(128, HD);
       // S for running tile cc = Q K^T into buffer cc % 2, once the buffer's
       // previous tile (cc - 2) has been folded by the softmax and K arrived
       auto issue_S = [&](int cc) -> bool {
@@ -313,7 +319,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
           break;
         }
         // pass 2: p = 2^(s * scale - m) (masked keys: 2^-inf = 0), row sum
-        // in four independent pairs, bf16 P into shared memory
+        // in four independent pairs, 16-bit P into shared memory
         float2 rs4[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) rs4[i] = make_float2(0.f, 0.f);
@@ -338,10 +344,10 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
           for (int v = 0; v < 4; ++v) {
             const int chunk = 4 * (cc & 1) + v;  // 16-byte chunk within the 128-byte row
             uint4 pk;
-            pk.x = pack_bf16x2(sv[8 * v + 0], sv[8 * v + 1]);
-            pk.y = pack_bf16x2(sv[8 * v + 2], sv[8 * v + 3]);
-            pk.z = pack_bf16x2(sv[8 * v + 4], sv[8 * v + 5]);
-            pk.w = pack_bf16x2(sv[8 * v + 6], sv[8 * v + 7]);
+            pk.x = pack2<OpT>(sv[8 * v + 0], sv[8 * v + 1]);
+            pk.y = pack2<OpT>(sv[8 * v + 2], sv[8 * v + 3]);
+            pk.z = pack2<OpT>(sv[8 * v + 4], sv[8 * v + 5]);
+            pk.w = pack2<OpT>(sv[8 * v + 6], sv[8 * v + 7]);
             *reinterpret_cast<uint4*>(atom + ((chunk ^ (r & 7)) << 4)) = pk;
           }
         }
@@ -368,6 +374,17 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
           pk.w = pack_bf16x2(o[cc + 6] * inv, o[cc + 7] * inv);
           *reinterpret_cast<uint4*>(dst + cc) = pk;
         }
+        if (a.out_lo_off != 0) {
+#pragma unroll
+          for (int cc = 0; cc < HD; cc += 8) {
+            uint4 pk;
+            pk.x = pack_bf16x2(bf16_residual(o[cc + 0] * inv), bf16_residual(o[cc + 1] * inv));
+            pk.y = pack_bf16x2(bf16_residual(o[cc + 2] * inv), bf16_residual(o[cc + 3] * inv));
+            pk.z = pack_bf16x2(bf16_residual(o[cc + 4] * inv), bf16_residual(o[cc + 5] * inv));
+            pk.w = pack_bf16x2(bf16_residual(o[cc + 6] * inv), bf16_residual(o[cc + 7] * inv));
+            *reinterpret_cast<uint4*>(dst + a.out_lo_off + cc) = pk;
+          }
+        }
       }
       c += nj;
     }
@@ -382,13 +399,13 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::MIN_BLOCKS)
 
 // Internal linkage: every translation unit that launches the kernel configures
 // (shared-memory opt-in) and launches its own copy of it.
-template <int HD>
+template <int HD, typename OpT = bf16>
 static cudaError_t launch_attn_tc(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnArgs& a,
                            int g_count, int num_sms, cudaStream_t stream) {
   using C = AttnCfg<HD>;
   static std::atomic<bool> configured{false};  // once per translation unit (set-up is idempotent)
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, OpT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
@@ -397,7 +414,7 @@ static cudaError_t launch_attn_tc(const CUtensorMap& tmQK, const CUtensorMap& tm
   aa.g_count = g_count;
   const int n_items = a.Hq * g_count * a.n_qtiles;
   const int grid = n_items < C::MIN_BLOCKS * num_sms ? n_items : C::MIN_BLOCKS * num_sms;
-  attn_tc_kernel<HD><<<grid, 192, C::SMEM, stream>>>(tmQK, tmV, aa);
+  attn_tc_kernel<HD, OpT><<<grid, 192, C::SMEM, stream>>>(tmQK, tmV, aa);
   return cudaGetLastError();
 }
 

@@ -7,6 +7,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -16,6 +17,7 @@
 namespace armt {
 
 typedef __nv_bfloat16 bf16;
+typedef __half f16;  // attention operands (q, k, v, probabilities) of the bf16 model
 
 // Device-side error codes written into the model's error word.
 enum DevError : int {
@@ -77,13 +79,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 p = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// v - bf16(v): what bf16 drops of v.  Rounded to bf16 itself it becomes the
+// low part of a split operand (v ~ hi + lo with about 16 significant bits).
+__device__ __forceinline__ float bf16_residual(float v) { return v - bf2f(f2bf(v)); }
+
+// Two values rounded to the 16-bit type T and packed (lo in the low half).
+template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t pack2<bf16>(float lo, float hi) { return pack_bf16x2(lo, hi); }
+template <> __device__ __forceinline__ uint32_t pack2<f16>(float lo, float hi) { return pack_f16x2(lo, hi); }
+
 // Load/store helpers that work for float and bf16 element types.
 template <typename T> __device__ __forceinline__ float ld_as_f32(const T* p);
 template <> __device__ __forceinline__ float ld_as_f32<float>(const float* p) { return *p; }
 template <> __device__ __forceinline__ float ld_as_f32<bf16>(const bf16* p) { return bf2f(*p); }
+template <> __device__ __forceinline__ float ld_as_f32<f16>(const f16* p) { return __half2float(*p); }
 template <typename T> __device__ __forceinline__ void st_from_f32(T* p, float v);
 template <> __device__ __forceinline__ void st_from_f32<float>(float* p, float v) { *p = v; }
 template <> __device__ __forceinline__ void st_from_f32<bf16>(bf16* p, float v) { *p = f2bf(v); }
+template <> __device__ __forceinline__ void st_from_f32<f16>(f16* p, float v) { *p = __float2half_rn(v); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -428,5 +446,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
 }
+
+// The same with fp16 A and B (A and B formats 0); same tensor-core rate.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Descriptor for operands of the 16-bit type T (both operands T).
+template <typename T> __host__ __device__ constexpr uint32_t idesc_16bit_f32(int M, int N);
+template <> __host__ __device__ constexpr uint32_t idesc_16bit_f32<bf16>(int M, int N) { return idesc_bf16_f32(M, N); }
+template <> __host__ __device__ constexpr uint32_t idesc_16bit_f32<f16>(int M, int N) { return idesc_f16_f32(M, N); }
 
 }  // namespace armt

@@ -51,6 +51,22 @@ __device__ __forceinline__ void store_row(bf16* dst, const float* v, int n) {
   }
 }
 
+__device__ __forceinline__ void store_row(f16* dst, const float* v, int n) {
+  if (n == 32 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+      uint4 p;
+      p.x = pack_f16x2(v[i], v[i + 1]);
+      p.y = pack_f16x2(v[i + 2], v[i + 3]);
+      p.z = pack_f16x2(v[i + 4], v[i + 5]);
+      p.w = pack_f16x2(v[i + 6], v[i + 7]);
+      *reinterpret_cast<uint4*>(dst + i) = p;
+    }
+  } else {
+    for (int i = 0; i < n; ++i) dst[i] = __float2half_rn(v[i]);
+  }
+}
+
 __device__ __forceinline__ void load_row(const float* src, float* v, int n) {
   if (n == 32 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
 #pragma unroll
@@ -98,6 +114,7 @@ struct RowNormOut {
   AT* out;            // [groups][rows][d] gain-weighted row
   float* ssq;         // [groups][rows][npart]
   int gdiv = 1;       // group g uses the gains of layer g / gdiv
+  long long lo_off = 0;  // split precision: bf16 low part at out + lo_off (staged path only)
   // v: 32 fp32 values of row `row` at columns col..col+31 (col0 = start of
   // this call's columns; the call's partial index is col0 / ncols).
   __device__ __forceinline__ void put(int l, int rows, int d, int row, int col, const float* v,

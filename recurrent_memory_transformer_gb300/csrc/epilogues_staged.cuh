@@ -47,7 +47,17 @@ __device__ __forceinline__ void st4(bf16* p, float4 v) {
   u.y = pack_bf16x2(v.z, v.w);
   *reinterpret_cast<uint2*>(p) = u;
 }
+__device__ __forceinline__ void st4(f16* p, float4 v) {
+  uint2 u;
+  u.x = pack_f16x2(v.x, v.y);
+  u.y = pack_f16x2(v.z, v.w);
+  *reinterpret_cast<uint2*>(p) = u;
+}
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+// bf16 rounding residuals of four values (the low part of a split operand)
+__device__ __forceinline__ float4 residual4(float4 v) {
+  return make_float4(bf16_residual(v.x), bf16_residual(v.y), bf16_residual(v.z), bf16_residual(v.w));
+}
 
 // Sum over the 16 lanes of each half-warp (lanes sharing a row).
 __device__ __forceinline__ float half_warp_sum(float v) {
@@ -140,7 +150,10 @@ struct SEpiStore {
 template <typename AT>
 __device__ __forceinline__ float norm_put4(const RowNormOut<AT>& n, int l, int rows, int d, int row,
                                            int col, float4 v, float4 g) {
-  st4(n.out + ((long long)l * rows + row) * d + col, make_float4(v.x * g.x, v.y * g.y, v.z * g.z, v.w * g.w));
+  const long long i = ((long long)l * rows + row) * d + col;
+  const float4 w = make_float4(v.x * g.x, v.y * g.y, v.z * g.z, v.w * g.w);
+  st4(n.out + i, w);
+  if (n.lo_off != 0) st4(n.out + i + n.lo_off, residual4(w));
   return v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
 }
 
@@ -192,6 +205,7 @@ struct SEpiResidual {
   CopyT* copy;
   int rows, n, out_slot_offset;
   RowNormOut<CopyT> norm;
+  long long copy_lo_off = 0;  // split precision: low part of the copy at copy + copy_lo_off
   __device__ static void unit(int u, int& a, int& b) { a = 64 * u; b = 64 * u + 32; }
   __device__ bool direct_tile(int) const { return false; }
   template <class Src> __device__ void direct(int, int, bool, int, int, Src&) const {}
@@ -207,7 +221,10 @@ struct SEpiResidual {
                                   ((long long)(l + out_slot_offset) * rows + row) * n + col;
                               const float4 y = make_float4(r.x + v.x, r.y + v.y, r.z + v.z, r.w + v.w);
                               st4(out + oi, y);
-                              if (copy != nullptr) st4(copy + oi, y);
+                              if (copy != nullptr) {
+                                st4(copy + oi, y);
+                                if (copy_lo_off != 0) st4(copy + oi + copy_lo_off, residual4(y));
+                              }
                               if (norm.gain == nullptr) return 0.f;
                               return norm_put4(norm, l, rows, n, row, col, y, g);
                             },
@@ -274,6 +291,7 @@ struct SEpiSwiGLU {
   OutT* out;
   int rows, F;
   RowNormIn norm;
+  long long lo_off = 0;  // split precision: low part at out + lo_off
   // unit u: gate columns 32u..32u+31 and their up columns 128 later
   __device__ static void unit(int u, int& a, int& b) { a = 32 * u; b = 32 * u + GU_BLK; }
   __device__ bool direct_tile(int) const { return false; }
@@ -285,9 +303,11 @@ struct SEpiSwiGLU {
                                           const float* stage, float ctx, float*) const {
     const int f0 = (colA / (2 * GU_BLK)) * GU_BLK + (colA % (2 * GU_BLK));
     staged_rows_paired(stage, row0, rows_, ctx, [&](int row, int i, float4 g, float4 u, float rs) {
-      st4(out + ((long long)l * rows + row) * F + f0 + i,
-          make_float4(silu_f(g.x * rs) * (u.x * rs), silu_f(g.y * rs) * (u.y * rs),
-                      silu_f(g.z * rs) * (u.z * rs), silu_f(g.w * rs) * (u.w * rs)));
+      const long long o = ((long long)l * rows + row) * F + f0 + i;
+      const float4 y = make_float4(silu_f(g.x * rs) * (u.x * rs), silu_f(g.y * rs) * (u.y * rs),
+                                   silu_f(g.z * rs) * (u.z * rs), silu_f(g.w * rs) * (u.w * rs));
+      st4(out + o, y);
+      if (lo_off != 0) st4(out + o + lo_off, residual4(y));
     });
   }
   __device__ void finish(int, int, int, int, float) const {}
@@ -311,6 +331,7 @@ struct SEpiPhi {
   const float* z;  // [L * nb][384]
   int rows, cell_rows, nb;
   float eps;
+  long long lo_off = 0;  // split precision: bf16 low part of phi at phi + lo_off
   __device__ static void unit(int u, int& a, int& b) { a = 64 * u; b = 64 * u + 32; }
   __device__ bool direct_tile(int) const { return false; }
   template <class Src> __device__ void direct(int, int, bool, int, int, Src&) const {}
@@ -346,6 +367,7 @@ struct SEpiPhi {
         const float f0 = r_at(stage, r, c) * r_at(stage, r, (c - j) & 127);
         const float f1 = r_at(stage, r, c + 1) * r_at(stage, r, (c + 1 - j) & 127);
         out[32 * t] = pack_bf16x2(f0, f1);
+        if (lo_off != 0) out[lo_off / 2 + 32 * t] = pack_bf16x2(bf16_residual(f0), bf16_residual(f1));
         acc = fmaf(zz[t].x, f0, acc);
         acc = fmaf(zz[t].y, f1, acc);
       }

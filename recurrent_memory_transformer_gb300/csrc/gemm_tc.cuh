@@ -40,9 +40,18 @@ constexpr int TC_BK = 64;  // one 128-byte swizzle row of bf16
 //           memory rows sit elsewhere, e.g. after a short last segment);
 //   B       slot gi / b_div + b_slot_off (b_div = sequences per layer when
 //           the groups are (layer, sequence) pairs sharing a layer's weights).
+//   a_lo_slot > 0: A is split into a bf16 high part and a bf16 low part
+//           (the rounding residual), the low part a_lo_slot slots after the
+//           high one; b_lo_slot > 0: the same for B.  The K loop then runs
+//           once per pair of parts (A high / low x B high / low, A fastest),
+//           so the product sees split operands with about 16 significant
+//           bits (split precision).
 struct GemmGroupMap {
   int row0 = 0, a_slot_off = 0, b_slot_off = 0, b_div = 1;
   int alt_lo = 0, alt_hi = 0, alt_row0 = 0;
+  int a_lo_slot = 0, b_lo_slot = 0;
+  __host__ __device__ int a_parts() const { return a_lo_slot > 0 ? 2 : 1; }
+  __host__ __device__ int passes() const { return a_parts() * (b_lo_slot > 0 ? 2 : 1); }
   __host__ __device__ int a_row0(int gi) const { return gi >= alt_lo && gi < alt_hi ? alt_row0 : row0; }
 };
 
@@ -52,6 +61,7 @@ struct GemmTcShape {
   int N, K;
   int g_first, g_count;
   int m_tiles, n_tiles, k_blocks;
+  int kb_split;   // k blocks of one pass when an operand is split (map.passes() > 1), else 0
   int* err;       // device error word
   WaitPolicy wp;  // wait limit and the test stall hook
 };
@@ -133,10 +143,15 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
             ok = false;
             break;
           }
+          // split operands: pass p = kb / kb_split reads A part p % a_parts
+          // and B part p / a_parts (0 = high, 1 = low)
+          const int pass = sh.kb_split > 0 ? kb / sh.kb_split : 0;
+          const int kc = (kb - pass * sh.kb_split) * TC_BK;
+          const int ap = pass % sh.map.a_parts(), bp = pass / sh.map.a_parts();
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_3d(sA + stage * C::A_BYTES, &tmA, kb * TC_BK, a_row, layer + sh.map.a_slot_off,
-                      &full[stage]);
-          tma_load_3d(sB + stage * C::B_BYTES, &tmB, kb * TC_BK, nt * BN, b_slot, &full[stage]);
+          tma_load_3d(sA + stage * C::A_BYTES, &tmA, kc, a_row,
+                      layer + sh.map.a_slot_off + ap * sh.map.a_lo_slot, &full[stage]);
+          tma_load_3d(sB + stage * C::B_BYTES, &tmB, kc, nt * BN, b_slot + bp * sh.map.b_lo_slot, &full[stage]);
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -238,6 +253,8 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI_WG>::THREADS, 1)
 
 // Encodes a 3-D bf16 tensor map over [layers][rows][K] (K contiguous) with a
 // box of {64, box_rows, 1} and 128-byte swizzling.  Returns false on error.
+// Also used for fp16 data: a tile copy moves the 16-bit elements unchanged
+// and its zero fill (all bits clear) is +0 in either type.
 bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int K, int rows, int layers,
                          int box_rows);
 
@@ -264,7 +281,8 @@ static cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB
   sh.g_count = g_count;
   sh.m_tiles = (rows + TC_BM - 1) / TC_BM;
   sh.n_tiles = N / BN;
-  sh.k_blocks = K / TC_BK;
+  sh.kb_split = map.passes() > 1 ? K / TC_BK : 0;
+  sh.k_blocks = (K / TC_BK) * map.passes();
   sh.err = err;
   sh.wp = wp;
   const int tiles = g_count * sh.m_tiles * sh.n_tiles;

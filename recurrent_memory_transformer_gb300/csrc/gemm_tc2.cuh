@@ -126,8 +126,13 @@ __global__ void __launch_bounds__(Tc2Cfg<EPI_WG>::THREADS, 1)
           }
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
           const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-          tma_load_3d_pair(sA + stage * C::A_BYTES, &tmA, kb * TC_BK, a_row, layer + sh.map.a_slot_off, fb);
-          tma_load_3d_pair(sB + stage * C::B_BYTES, &tmB, kb * TC_BK, b_row, b_slot, fb);
+          // split operands: pass p reads A part p % a_parts, B part p / a_parts
+          const int pass = sh.kb_split > 0 ? kb / sh.kb_split : 0;
+          const int kc = (kb - pass * sh.kb_split) * TC_BK;
+          const int ap = pass % sh.map.a_parts(), bp = pass / sh.map.a_parts();
+          tma_load_3d_pair(sA + stage * C::A_BYTES, &tmA, kc, a_row,
+                           layer + sh.map.a_slot_off + ap * sh.map.a_lo_slot, fb);
+          tma_load_3d_pair(sB + stage * C::B_BYTES, &tmB, kc, b_row, b_slot + bp * sh.map.b_lo_slot, fb);
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -285,7 +290,8 @@ static cudaError_t launch_gemm_tc2(const CUtensorMap& tmA, const CUtensorMap& tm
   sh.g_count = g_count;
   sh.m_tiles = (rows + TC_BM - 1) / TC_BM;
   sh.n_tiles = N / C::BN;
-  sh.k_blocks = K / TC_BK;
+  sh.kb_split = map.passes() > 1 ? K / TC_BK : 0;
+  sh.k_blocks = (K / TC_BK) * map.passes();
   sh.err = err;
   sh.wp = wp;
   const int tiles = g_count * ((rows + 2 * TC_BM - 1) / (2 * TC_BM)) * sh.n_tiles;

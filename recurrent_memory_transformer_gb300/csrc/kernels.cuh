@@ -25,12 +25,13 @@ namespace armt {
 // tokens from tokens + b * tok_stride and fills rows [b * T, (b + 1) * T):
 // n_seg token rows, then the M memory rows, then zero rows up to T (a short
 // last segment; the zero rows come after every real row, so under the causal
-// mask no real row ever sees them).
+// mask no real row ever sees them).  xa_lo_off != 0 (split precision): the
+// bf16 low part of Xa at Xa + xa_lo_off.
 template <typename WT>
 __global__ void embed_gather_kernel(const int32_t* __restrict__ tokens, long long tok_stride,
                                     const WT* __restrict__ embed, const WT* __restrict__ mem,
                                     float* __restrict__ X, WT* __restrict__ Xa, int T, int n_seg,
-                                    int M, int d, int vocab) {
+                                    int M, int d, int vocab, long long xa_lo_off = 0) {
   const int t = blockIdx.x, b = blockIdx.y;
   const WT* src = nullptr;
   if (t < n_seg) {
@@ -47,7 +48,10 @@ __global__ void embed_gather_kernel(const int32_t* __restrict__ tokens, long lon
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
     const float v = src != nullptr ? ld_as_f32(src + i) : 0.f;
     xo[i] = v;
-    if (copy) st_from_f32(xa + i, v);
+    if (copy) {
+      st_from_f32(xa + i, v);
+      if (xa_lo_off != 0) st_from_f32(xa + xa_lo_off + i, bf16_residual(v));
+    }
   }
 }
 
@@ -212,12 +216,13 @@ __global__ void __launch_bounds__(256) assoc_write_feat_kernel(
 // reading and writing each row of A once.  v_i[j] comes from the memory-row
 // projection GEMM (vkb), phi_i and the coefficients from the feature kernel.
 // Also refreshes the activation-dtype copy Aa of the state (the next read's
-// GEMM operand) when Aa != A.  M <= 32.
+// GEMM operand) when Aa != A, and with aa_lo_off != 0 (split precision) its
+// bf16 low part at Aa + aa_lo_off.  M <= 32.
 template <typename AT, int NT>
 __global__ void __launch_bounds__(128) assoc_write_update_kernel(
     const float* __restrict__ vkb, int nw, const float* __restrict__ phiM,
     const float* __restrict__ coef, float* __restrict__ A, AT* __restrict__ Aa, int M, int d,
-    int rows_per_block, int g_first) {
+    int rows_per_block, int g_first, long long aa_lo_off = 0) {
   constexpr int P = 32 * NT;
   extern __shared__ float sm[];
   float* ps = sm;                 // [M][P]
@@ -277,19 +282,26 @@ __global__ void __launch_bounds__(128) assoc_write_update_kernel(
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           Al[(long long)j * P + lane + 32 * t] = a[r][t];
-          if ((void*)Aal != (void*)Al) st_from_f32(Aal + (long long)j * P + lane + 32 * t, a[r][t]);
+          if ((void*)Aal != (void*)Al) {
+            st_from_f32(Aal + (long long)j * P + lane + 32 * t, a[r][t]);
+            if (aa_lo_off != 0) st_from_f32(Aal + aa_lo_off + (long long)j * P + lane + 32 * t, bf16_residual(a[r][t]));
+          }
         }
       }
     }
   }
 }
 
-// State copy in the activation dtype: Aa = A (all layers).
+// State copy in the activation dtype: Aa = A (all layers); with lo_off != 0
+// (split precision) also the bf16 low part at Aa + lo_off.
 template <typename AT>
-__global__ void convert_state_kernel(const float* __restrict__ A, AT* __restrict__ Aa, long long n) {
+__global__ void convert_state_kernel(const float* __restrict__ A, AT* __restrict__ Aa, long long n,
+                                     long long lo_off = 0) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x)
+       i += (long long)gridDim.x * blockDim.x) {
     st_from_f32(Aa + i, A[i]);
+    if (lo_off != 0) st_from_f32(Aa + lo_off + i, bf16_residual(A[i]));
+  }
 }
 
 // ------------------------------------------------------ SIMT attention --

@@ -57,6 +57,7 @@ class ArmtConfig:
     rope_base: float = 10000.0
     assoc_eps: float = 1e-6
     dtype: str = "f32"    # "f32" or "bf16"
+    precision: str = "bf16"  # bf16 models: "bf16" or "bf16x2" (split activations)
 
     @property
     def rows(self) -> int:

@@ -1,4 +1,4 @@
-"""An independently written bf16-operand emulation of ARMT cells, for pinning
+"""An independently written 16-bit-operand emulation of ARMT cells, for pinning
 the oracle's precision model (``armt_oracle.forward(operands="bf16")``).
 
 Used only by tests.  It shares nothing with oracle/armt_oracle.py: every
@@ -6,19 +6,22 @@ step is written out per row and per head with Python loops, DPFP by index
 arithmetic, rotary embedding as multiplication by unit complex numbers,
 softmax with an explicit maximum, and the rounding to bf16 goes through
 torch's own float32 -> bfloat16 conversion (round to nearest even) instead
-of the oracle's bit manipulation.  Slow by design; tiny inputs only.
+of the oracle's bit manipulation (torch's float16 conversion for the
+attention operands).  Slow by design; tiny inputs only.
 
-The precision model rounds a value to bf16 at the points where a bf16 kernel
-path feeds a tensor-core operand, and nowhere else:
+The precision model rounds a value to its operand type at the points where
+the bf16 kernel path feeds a tensor-core operand, and nowhere else -- bf16
+for the operands of weight products, fp16 for the attention's own operands
+(marked *):
   "xq"    the layer input, before the associative query projection;
   "phi"   the read features in the numerator A phi (the denominator
           z^T phi + eps keeps the unrounded features);
   "A"     the state copy in that numerator;
   "n1"    the first RMSNorm output (input of the q, k, v projections);
-  "qk"    q and k after the rotary embedding;
-  "v"     v;
+  "qk"    q and k after the rotary embedding (*);
+  "v"     v (*);
   "P"     the attention probabilities exp(s - max) before they multiply v
-          (the row sum stays unrounded);
+          (the row sum stays unrounded) (*);
   "att"   the attention output (input of the output projection);
   "n2"    the second RMSNorm output (input of the gate / up projections);
   "u"     the SwiGLU output (input of the down projection);
@@ -26,26 +29,45 @@ path feeds a tensor-core operand, and nowhere else:
           key / value / strength projections.
 Everything else -- the residual stream, norm statistics, softmax maxima and
 sums, the memory state and the write arithmetic -- is exact (fp64).
+
+With ``split=True`` it emulates the split precision mode instead: the
+operands of the weight products and of the read ("xq", "phi", "A", "n1",
+"att", "n2", "u", "hmem") are carried as a bf16 high part plus the bf16
+rounding of the residual; the attention operands stay fp16.
 """
 import math
 
 import numpy as np
 
 ALL_POINTS = ("xq", "phi", "A", "n1", "qk", "v", "P", "att", "n2", "u", "hmem")
+HALF_POINTS = ("qk", "v", "P")   # rounded to fp16; the rest to bf16
 
 
-def _to_bf16(a):
+def _to_16bit(a, half):
     import torch
     t = torch.from_numpy(np.asarray(a, np.float64).astype(np.float32))
-    return t.to(torch.bfloat16).to(torch.float64).numpy()
+    return t.to(torch.float16 if half else torch.bfloat16).to(torch.float64).numpy()
+
+
+def _to_split(a):
+    import torch
+    t = torch.from_numpy(np.asarray(a, np.float64).astype(np.float32))
+    hi = t.to(torch.bfloat16).to(torch.float32)
+    lo = (t - hi).to(torch.bfloat16).to(torch.float32)
+    return hi.to(torch.float64).numpy() + lo.to(torch.float64).numpy()
 
 
 class _Round:
-    def __init__(self, points):
+    def __init__(self, points, split=False):
         self.points = set(points)
+        self.split = split
 
     def __call__(self, name, a):
-        return _to_bf16(a) if name in self.points else np.asarray(a, np.float64)
+        if name not in self.points:
+            return np.asarray(a, np.float64)
+        if self.split and name not in HALF_POINTS:
+            return _to_split(a)
+        return _to_16bit(a, name in HALF_POINTS)
 
 
 def _dpfp(x, nu):
@@ -130,9 +152,9 @@ def cell(X, W, l, A, z, cfg, rnd):
     return H, A, z
 
 
-def forward(cfg, W, tokens, n_segments, points=ALL_POINTS):
+def forward(cfg, W, tokens, n_segments, points=ALL_POINTS, split=False):
     """Segment by segment, layer by layer; returns (hidden, A [L,d,P], z [L,P])."""
-    rnd = _Round(points)
+    rnd = _Round(points, split)
     L, d, P, S = cfg.n_layers, cfg.d_model, cfg.phi_dim, cfg.seg_len
     emb, mem, gf = (np.asarray(W[k], np.float64) for k in ("embed", "mem", "norm_f"))
     A = [np.zeros((d, P)) for _ in range(L)]

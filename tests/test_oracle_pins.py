@@ -372,6 +372,13 @@ def test_round_bf16_matches_torch_and_ties_to_even():
     # exact ties: 1 + 2^-8 is halfway between 1 and 1 + 2^-7 -> even (1.0)
     assert O.round_bf16(np.array([1.0 + 2.0 ** -8]))[0] == 1.0
     assert O.round_bf16(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 1.0 + 2.0 ** -6
+    # fp16 (the attention operands' type): against torch, ties to even, range
+    y = x[np.abs(x) < 6e4]
+    want16 = torch.from_numpy(y.astype(np.float32)).to(torch.float16).double().numpy()
+    np.testing.assert_array_equal(O.round_f16(y), want16)
+    assert O.round_f16(np.array([1.0 + 2.0 ** -11]))[0] == 1.0
+    assert O.round_f16(np.array([1.0 + 3 * 2.0 ** -11]))[0] == 1.0 + 2.0 ** -9
+    assert O.round_f16(np.array([65504.0]))[0] == 65504.0
 
 
 def test_bf16_precision_model_is_close_to_fp64_and_rounds():
@@ -411,6 +418,19 @@ def test_bf16_precision_model_matches_an_independent_emulation():
         assert max(rel(a, b) for a, b in zip(part, model)) >= 1e-4, point
     exact = O.forward(cfg, W, tok, 2)
     assert min(rel(a, b) for a, b in zip(exact, model)) >= 1e-4
+    # the split precision mode's model: same agreement; every point still
+    # matters (its ~2^-17 rounding moves the result far beyond fp64 noise),
+    # and the split model sits far closer to fp64 than the bf16 one
+    split = O.forward(cfg, W, tok, 2, operands="bf16x2")
+    emu_split = plain_bf16_cell.forward(cfg, W, tok, 2, split=True)
+    for a, b in zip(emu_split, split):
+        assert rel(a, b) <= 1e-12
+    for point in plain_bf16_cell.ALL_POINTS:
+        part = plain_bf16_cell.forward(cfg, W, tok, 2, points=set(plain_bf16_cell.ALL_POINTS) - {point},
+                                       split=True)
+        assert max(rel(a, b) for a, b in zip(part, split)) >= 1e-8, point
+    for a, b, c in zip(split, model, exact):
+        assert rel(a, c) <= 0.3 * rel(b, c)
 
 
 def test_lm_head_logits_closed_forms():
