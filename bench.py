@@ -7,13 +7,14 @@ inputs already resident in HBM.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ours|reference] [--no-seq] [--no-cpu] [--no-e2e]
-                  [--no-full] [--no-microbatch]
+                  [--no-full] [--no-microbatch] [--no-split]
 
 Inside the timed region only the roofline kernel (the gate-up GEMM) carries
 per-launch CUDA events; the per-kernel-class table comes from one more forward
 after it.  Besides the timed forward the line reports the sequential schedule,
 the uniform-load bound, the LM head, the full-attention LLaMA on the same
-weights, diagonal batching vs micro-batching, the end-to-end host-buffer path,
+weights, diagonal batching vs micro-batching, the split-precision mode
+(activations as bf16 high + low parts), the end-to-end host-buffer path,
 device memory, and the oracle on the host cores.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
@@ -56,6 +57,8 @@ def parse():
                    help="skip the full-causal-attention LLaMA baseline on the same weights")
     p.add_argument("--no-microbatch", action="store_true",
                    help="skip the diagonal-batching vs micro-batching comparison")
+    p.add_argument("--no-split", action="store_true",
+                   help="skip the split-precision (bf16 high + low activations) forward")
     return p.parse_args()
 
 
@@ -406,6 +409,30 @@ def main():
                       "batch_workspace_bytes": model.armt_memory_bytes()[1] - ws_create}
         torch.cuda.empty_cache()
 
+    # ---- split precision: activations as bf16 high + low parts -----------
+    # The same workload and weights with ARMT_PRECISION_BF16X2: every weight
+    # product's K loop runs twice (high, then low part of the activations).
+    split = None
+    if not args.no_split and cfg.dtype == "bf16" and W is not None:
+        cfg_x2 = dataclasses.replace(cfg, precision="bf16x2")
+        model_x2 = B.Model(cfg_x2, B.device_weight_tensors(cfg_x2, W))
+        torch.cuda.empty_cache()
+        model_x2.armt_forward(tokens, n_seg, hidden, A, z, 0, stream, B.SCHEDULE_DIAGONAL)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        model_x2.armt_forward(tokens, n_seg, hidden, A, z, 0, stream, B.SCHEDULE_DIAGONAL)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        model_x2.armt_sync_status()
+        x2_ms = e0.elapsed_time(e1)
+        split = {"ms_per_step": x2_ms, "tokens_per_s": n_tok / (x2_ms / 1000.0),
+                 "slowdown_vs_bf16": x2_ms / ms_step,
+                 "workspace_bytes": model_x2.armt_memory_bytes()[1]}
+        model_x2.close()
+        del model_x2
+        torch.cuda.empty_cache()
+
     # ---- end to end through the host-buffer entry point ------------------
     e2e = None
     if not args.no_e2e:
@@ -454,6 +481,7 @@ def main():
             "config": {"workload": args.workload, "tokens": n_tok, "segments": n_seg,
                        "segment_len": cfg.seg_len, "memory_tokens": cfg.n_mem, "layers": cfg.n_layers,
                        "batch": 1, "schedule": "diagonal", "parallelism": "replicas" if world > 1 else "single",
+                       "precision": "bf16 weight-product operands, fp16 attention operands, fp32 accumulation",
                        "l2": "no flush: every diagonal re-reads all layers' weights (~2 GB) and "
                              "~1 GB of activations, far above the 129 MB L2"},
             "roofline": {"bound": "tensor", "kernel": "grouped GEMM gate-up + SwiGLU (tcgen05)",
@@ -471,6 +499,7 @@ def main():
             "lm_head": lm,
             "full_attention": full,
             "microbatch": microbatch,
+            "split_precision": split,
             "memory": memory,
             "e2e": e2e,
             "cpu_baseline": cpu,

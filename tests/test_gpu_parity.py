@@ -6,20 +6,23 @@ Tolerances:
                        1e-6, |z| ~ 3e-4, where an absolute 1e-4 would accept
                        an all-zero state), also max-abs <= 1e-4 x max |oracle|
                        and cosine >= 1 - 1e-9 on each of them.
-  bf16 models, against the fp64 oracle:
+  bf16 models (bf16 precision), against the fp64 oracle:
     hidden states      cosine >= 0.999, and
-                       max-abs <= 2 x the max-abs error of the oracle's own
-                       bf16 operand-rounding precision model;
+                       max-abs <= 1.5 x the max-abs error of the oracle's own
+                       operand-rounding precision model;
     memory state A, z  1 - cosine <= 1.5 x (1 - cosine of that model), and
-                       max-abs <= 2 x that model's max-abs error.
-    (The bulk measure, cosine, gets the tighter factor; a single maximum over
-    millions of entries is a noisy tail statistic: on the 8-segment 1B run the
-    largest A deviation was 1.67 x the model's while 1 - cosine was 1.45 x.)
+                       max-abs <= 1.5 x that model's max-abs error;
+    relative logits    per segment <= 1.5 x the model's.
+    The factor covers the spread between two draws of rounding noise (the
+    GPU's and the model's rounding orders differ): over six seeds the GPU /
+    model ratios were 0.49-1.24 (max-abs) and 0.65-1.37 (1 - cosine).
     A fixed max-abs of 2e-2 cannot be met by any implementation whose matrix
     products take bf16 operands: the precision model alone (exact fp64 apart
     from rounding the operands) is at ~0.1 after 16 layers of one segment.
-    The bounds above ask the kernels to be as accurate as ideal bf16
-    arithmetic, within sampling noise.
+  bf16 models in split precision (activations as bf16 high + low parts):
+    the absolute bounds -- max-abs <= 2e-2 on hidden states, cosine >= 0.999
+    on hidden states, A and z, and max-abs <= 2e-2 x max |oracle| on A and z
+    (whose entries reach ~2e4).
   diagonal vs sequential schedule on the GPU: bitwise equal, always.
 """
 import dataclasses
@@ -79,6 +82,11 @@ def stats(gpu, ref):
 
 
 FP32_ABS, FP32_REL, FP32_COS = 1e-4, 1e-4, 1e-9
+# bf16 models: GPU error <= factor x the bf16 precision model's error
+# (ratios measured over six seeds of the 2-layer ARMT-1B shape in
+# test_bf16_error_ratio_over_seeds: max-abs 0.49-1.24, 1 - cosine 0.65-1.37;
+# relative logits error per segment on ARMT-1B, 8 segments: 0.45-0.82)
+MAXABS_FACTOR, COS_FACTOR, RLE_FACTOR = 1.5, 1.5, 1.5
 
 
 def fp32_close(s):
@@ -292,7 +300,14 @@ def armt1b():
     return cfg, n, W, tok
 
 
-def test_armt1b_8k_matches_oracle_and_schedules_agree(armt1b):
+@pytest.fixture(scope="module")
+def armt1b_exact(armt1b):
+    """The fp64 oracle on the ARMT-1B 8-segment workload (computed once)."""
+    cfg, n, W, tok = armt1b
+    return O.forward(cfg, W, tok, n)
+
+
+def test_armt1b_8k_matches_oracle_and_schedules_agree(armt1b, armt1b_exact):
     cfg, n, W, tok = armt1b
     S = cfg.seg_len
     m = B.Model(cfg, B.device_weight_tensors(cfg, W))
@@ -314,7 +329,7 @@ def test_armt1b_8k_matches_oracle_and_schedules_agree(armt1b):
     lg_d = lg_d.cpu().numpy()
     m.close()
     res = {"bitwise_diag_seq": bitwise, "logits_bitwise_diag_seq": logits_bitwise}
-    ho, Ao, zo = O.forward(cfg, W, tok, n)
+    ho, Ao, zo = armt1b_exact
     hm, Am, zm = O.forward(cfg, W, tok, n, operands="bf16")
     # relative logits error per segment (the error-accumulation measure of
     # section 四), GPU and the bf16 precision model against fp64
@@ -338,13 +353,79 @@ def test_armt1b_8k_matches_oracle_and_schedules_agree(armt1b):
     assert bitwise and logits_bitwise
     rle = res["relative_logits_error"]
     for s in range(n):
-        assert rle["gpu"][s] <= 2.0 * rle["bf16_model"][s], (s, rle)
+        assert rle["gpu"][s] <= RLE_FACTOR * rle["bf16_model"][s], (s, rle)
     g, m = res["gpu_vs_fp64"], res["model_vs_fp64"]
     assert g["hidden"]["finite"] and g["hidden"]["cos"] >= 0.999, g["hidden"]
     for key in ("hidden", "A", "z"):
-        assert g[key]["max_abs"] <= 2.0 * m[key]["max_abs"], (key, g[key], m[key])
+        assert g[key]["max_abs"] <= MAXABS_FACTOR * m[key]["max_abs"], (key, g[key], m[key])
     for key in ("A", "z"):
-        assert 1.0 - g[key]["cos"] <= 1.5 * (1.0 - m[key]["cos"]), (key, g[key], m[key])
+        assert 1.0 - g[key]["cos"] <= COS_FACTOR * (1.0 - m[key]["cos"]), (key, g[key], m[key])
+
+
+@pytest.mark.parametrize("seed", [81, 82, 83, 84, 85, 86])
+def test_bf16_error_ratio_over_seeds(seed):
+    """How close the GPU comes to ideal bf16-operand arithmetic, over seeds.
+
+    ARMT-1B cell shape (full width) at 2 layers, 2 segments, norm gains
+    jittered: the GPU's max-abs error against fp64, divided by the precision
+    model's, and the same for 1 - cosine, on hidden states, A and z.  The
+    ratios are recorded per seed (the spread behind the max-abs factor of the
+    bf16 bounds) and each is held to the bounds' factors."""
+    cfg = dataclasses.replace(I.ARMT_1B, n_layers=2, vocab=4096)
+    W = I.make_weights(cfg, seed, norm_jitter=0.1)
+    tok = I.make_tokens(cfg, 2, seed)
+    m = B.Model(cfg, B.device_weight_tensors(cfg, W))
+    hd, Ad, zd = m.forward(torch.from_numpy(tok).cuda(), 2)
+    torch.cuda.synchronize()
+    m.armt_sync_status()
+    gpu = (hd.cpu().numpy(), Ad.cpu().numpy(), zd.cpu().numpy())
+    m.close()
+    exact = O.forward(cfg, W, tok, 2)
+    model = O.forward(cfg, W, tok, 2, operands="bf16")
+    ratios = {}
+    for key, g, e, md in zip(("hidden", "A", "z"), gpu, exact, model):
+        sg, sm = stats(g, e), stats(md, e)
+        ratios[key] = {"max_abs": sg["max_abs"] / sm["max_abs"],
+                       "one_minus_cos": (1.0 - sg["cos"]) / (1.0 - sm["cos"]),
+                       "gpu_cos": sg["cos"], "model_cos": sm["cos"]}
+    record(f"seed_ratio_{seed}", **ratios)
+    for key in ("hidden", "A", "z"):
+        assert ratios[key]["max_abs"] <= MAXABS_FACTOR, (key, ratios[key])
+        assert ratios[key]["one_minus_cos"] <= COS_FACTOR, (key, ratios[key])
+        assert ratios[key]["gpu_cos"] >= 0.999, (key, ratios[key])
+
+
+def test_armt1b_8k_split_precision_meets_the_absolute_bounds(armt1b, armt1b_exact):
+    """Split precision (activations as bf16 high + low parts, fp16 attention
+    operands) on the ARMT-1B 8-segment workload, against the exact fp64
+    oracle, with the absolute tolerance of the bf16 configs: max-abs <= 2e-2
+    and cosine >= 0.999 on the final hidden states and on the memory state.
+    The memory entries reach ~2e4, so for A and z max-abs is read relative to
+    their scale (<= 2e-2 x max |oracle|).  The diagonal and sequential
+    schedules stay bitwise equal, and the GPU stays within the factors of
+    the mode's own precision model."""
+    cfg, n, W, tok = armt1b
+    cfg = dataclasses.replace(cfg, precision="bf16x2")
+    m = B.Model(cfg, B.device_weight_tensors(cfg, W))
+    t = torch.from_numpy(tok).cuda()
+    hd, Ad, zd = m.forward(t, n, schedule=B.SCHEDULE_DIAGONAL)
+    hs, As, zs = m.forward(t, n, schedule=B.SCHEDULE_SEQUENTIAL)
+    torch.cuda.synchronize()
+    m.armt_sync_status()
+    bitwise = bool(torch.equal(hd, hs) and torch.equal(Ad, As) and torch.equal(zd, zs))
+    gpu = (hd.cpu().numpy(), Ad.cpu().numpy(), zd.cpu().numpy())
+    m.close()
+    model = O.forward(cfg, W, tok, n, operands="bf16x2")
+    g = {k: stats(a, b) for k, a, b in zip(("hidden", "A", "z"), gpu, armt1b_exact)}
+    md = {k: stats(a, b) for k, a, b in zip(("hidden", "A", "z"), model, armt1b_exact)}
+    record("armt1b_8k_split", bitwise_diag_seq=bitwise, gpu_vs_fp64=g, model_vs_fp64=md)
+    assert bitwise
+    assert g["hidden"]["finite"] and g["hidden"]["max_abs"] <= 2e-2, g["hidden"]
+    for key in ("hidden", "A", "z"):
+        assert g[key]["cos"] >= 0.999, (key, g[key])
+        assert 1.0 - g[key]["cos"] <= COS_FACTOR * (1.0 - md[key]["cos"]), (key, g[key], md[key])
+    for key in ("A", "z"):
+        assert g[key]["max_abs"] <= 2e-2 * g[key]["ref_absmax"], (key, g[key])
 
 
 def _derived_bounds_hold(gpu, exact, model, S, n):
@@ -352,9 +433,9 @@ def _derived_bounds_hold(gpu, exact, model, S, n):
     m = dict(hidden=stats(model[0], exact[0]), A=stats(model[1], exact[1]), z=stats(model[2], exact[2]))
     ok = g["hidden"]["cos"] >= 0.999
     for key in ("hidden", "A", "z"):
-        ok &= g[key]["max_abs"] <= 2.0 * m[key]["max_abs"]
+        ok &= g[key]["max_abs"] <= MAXABS_FACTOR * m[key]["max_abs"]
     for key in ("A", "z"):
-        ok &= 1.0 - g[key]["cos"] <= 1.5 * (1.0 - m[key]["cos"])
+        ok &= 1.0 - g[key]["cos"] <= COS_FACTOR * (1.0 - m[key]["cos"])
     return bool(ok), g, m
 
 
@@ -443,7 +524,7 @@ def test_full_attention_baseline_matches_oracle(T):
     g, mm = stats(got, exact), stats(model, exact)
     record(f"full_attention_T{T}", gpu_vs_fp64=g, model_vs_fp64=mm)
     assert g["finite"] and g["cos"] >= 0.999, g
-    assert g["max_abs"] <= 2.0 * mm["max_abs"], (g, mm)
+    assert g["max_abs"] <= MAXABS_FACTOR * mm["max_abs"], (g, mm)
 
 
 def test_full_attention_baseline_equals_armt_first_segment_up_to_rounding():
