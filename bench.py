@@ -7,15 +7,16 @@ inputs already resident in HBM.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ours|reference] [--no-seq] [--no-cpu] [--no-e2e]
-                  [--no-full] [--no-microbatch] [--no-split]
+                  [--no-full] [--no-microbatch] [--no-split] [--no-wavefront]
 
 Inside the timed region only the roofline kernel (the gate-up GEMM) carries
 per-launch CUDA events; the per-kernel-class table comes from one more forward
 after it.  Besides the timed forward the line reports the sequential schedule,
 the uniform-load bound, the LM head, the full-attention LLaMA on the same
 weights, diagonal batching vs micro-batching, the split-precision mode
-(activations as bf16 high + low parts), the end-to-end host-buffer path,
-device memory, and the oracle on the host cores.
+(activations as bf16 high + low parts), the persistent wavefront schedule
+against per-diagonal launches on an fp32 model, the end-to-end host-buffer
+path, device memory, and the oracle on the host cores.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
 sample of the same workload (one segment through every layer per step).
@@ -59,6 +60,8 @@ def parse():
                    help="skip the diagonal-batching vs micro-batching comparison")
     p.add_argument("--no-split", action="store_true",
                    help="skip the split-precision (bf16 high + low activations) forward")
+    p.add_argument("--no-wavefront", action="store_true",
+                   help="skip the persistent-wavefront comparison (fp32 model)")
     return p.parse_args()
 
 
@@ -288,7 +291,7 @@ def main():
     # cells (each cell's layer weights + activations), so per launch it is
     # this times the launch's cells.  None until a capture of the current
     # kernel exists.
-    GATEUP_DRAM_BYTES_PER_CELL_1B = 86.4e6
+    GATEUP_DRAM_BYTES_PER_CELL_1B = 86.5e6
     gu_traffic = (GATEUP_DRAM_BYTES_PER_CELL_1B * cells / gu_launches
                   if (GATEUP_DRAM_BYTES_PER_CELL_1B and gu_launches and args.workload.startswith("armt-1b"))
                   else None)
@@ -433,6 +436,42 @@ def main():
         del model_x2
         torch.cuda.empty_cache()
 
+    # ---- persistent wavefront vs per-diagonal launches (fp32 model) ------
+    # The wavefront schedule runs fp32 models: one cooperative launch for the
+    # whole forward, each stage of each cell starting when the stages it
+    # reads from are done (device-side counters).  A 4-layer d=256 fp32
+    # model at 8 and 64 segments of 64 tokens, same weights and tokens.
+    wavefront = None
+    if not args.no_wavefront:
+        cfg_w = dataclasses.replace(I.ARMT_1B, n_layers=4, d_model=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                                    ffn_dim=512, vocab=1000, seg_len=64, dtype="f32")
+        model_w = B.Model(cfg_w, I.make_weights(cfg_w, 7))
+        wavefront = {"workload": "fp32 ARMT, 4 layers, d 256, 4/2 heads of 64, F 512, 64 + 16 rows per cell",
+                     "runs": []}
+        for n_w in (8, 64):
+            tw = torch.from_numpy(I.make_tokens(cfg_w, n_w, 7)).cuda().view(1, -1)
+            hw = torch.empty((1, n_w * cfg_w.seg_len, cfg_w.d_model), dtype=torch.float32, device="cuda")
+            Aw = torch.empty((cfg_w.n_layers, 1, model_w.a_elems // cfg_w.n_layers), dtype=torch.float32, device="cuda")
+            zw = torch.empty((cfg_w.n_layers, 1, model_w.z_elems // cfg_w.n_layers), dtype=torch.float32, device="cuda")
+            row = {"segments": n_w}
+            for name, sch in (("diagonal", B.SCHEDULE_DIAGONAL), ("wavefront", B.SCHEDULE_WAVEFRONT)):
+                model_w.armt_forward_batch(tw, hw, Aw, zw, 0, sch, stream)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(3):
+                    model_w.armt_forward_batch(tw, hw, Aw, zw, 0, sch, stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                model_w.armt_sync_status()
+                row[name + "_ms"] = e0.elapsed_time(e1) / 3
+                row[name + "_launches"] = model_w.armt_launch_count(n_w, sch)
+            row["speedup_wavefront_over_diagonal"] = row["diagonal_ms"] / row["wavefront_ms"]
+            wavefront["runs"].append(row)
+        model_w.close()
+        del model_w
+        torch.cuda.empty_cache()
+
     # ---- end to end through the host-buffer entry point ------------------
     e2e = None
     if not args.no_e2e:
@@ -500,6 +539,7 @@ def main():
             "full_attention": full,
             "microbatch": microbatch,
             "split_precision": split,
+            "wavefront": wavefront,
             "memory": memory,
             "e2e": e2e,
             "cpu_baseline": cpu,

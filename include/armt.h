@@ -51,7 +51,9 @@
  *                           (default 2000 ms);
  *     ARMT_TEST_STALL_AFTER the tensor-core kernels' copy producers stop
  *                           after that many stage loads, as a stuck producer
- *                           would, so that the waits run out (unset: off).
+ *                           would, so that the waits run out; the wavefront
+ *                           schedule stops counting completed tasks from
+ *                           that task index on (unset: off).
  *   - Not thread-safe per model: one host thread at a time per armt_model,
  *     and calls on one model must not overlap on the device (they share the
  *     model's activation workspace).  Different models are independent.
@@ -112,7 +114,12 @@ typedef enum armt_precision {
 
 typedef enum armt_schedule {
   ARMT_SCHEDULE_DIAGONAL = 0,   /* one grouped launch per anti-diagonal l + s = i */
-  ARMT_SCHEDULE_SEQUENTIAL = 1  /* segment by segment, layer by layer, one cell per launch */
+  ARMT_SCHEDULE_SEQUENTIAL = 1, /* segment by segment, layer by layer, one cell per launch */
+  ARMT_SCHEDULE_WAVEFRONT = 2   /* one persistent launch for the whole forward: each stage of
+                                   each cell starts as soon as the stages it reads from are done,
+                                   tracked by device-side (layer, segment, stage) counters;
+                                   ARMT_F32 models, one sequence (armt_forward_batch with batch 1,
+                                   armt_forward_host); ARMT_ERR_UNSUPPORTED otherwise */
 } armt_schedule;
 
 /* Model shape.  LLaMA decoder layer + per-layer associative memory. */
@@ -196,7 +203,9 @@ ARMT_API armt_status armt_forward(armt_model* m, const int32_t* tokens, int64_t 
 
 /* Same arguments and results; cells run one per step, segment by segment and
  * layer by layer (the schedule the diagonal one reorders), through the same
- * kernels.  For checking and as the speed-up denominator. */
+ * kernels.  For checking and as the speed-up denominator.  The third
+ * schedule, ARMT_SCHEDULE_WAVEFRONT, is reached through armt_forward_batch
+ * (batch 1) and armt_forward_host; all three give bit-identical results. */
 ARMT_API armt_status armt_forward_sequential(armt_model* m, const int32_t* tokens, int64_t n_segments,
                                     float* hidden_out, float* mem_A, float* mem_z,
                                     int32_t mem_in_valid, void* stream);
@@ -348,6 +357,54 @@ ARMT_API armt_status armt_noalloc_sync_status(void* stream);
  * model. */
 ARMT_API armt_status armt_lm_head(armt_model* m, const float* hidden, int64_t n_rows,
                                   const void* w_head, float* logits, void* stream);
+
+/* Gradient buffers of armt_backward: device fp32, each in the layout of the
+ * armt_weights field of the same name, overwritten (not accumulated).  All
+ * required except mem_A / mem_z, the gradients with respect to the initial
+ * memory state ([L, d, P] and [L, P]; NULL skips them). */
+typedef struct armt_grads {
+  float *embed, *mem, *wq, *wk, *wv, *wo, *w_gate, *w_up, *w_down;
+  float *a_wq, *a_wk, *a_wv, *a_wbeta, *norm1, *norm2, *norm_f;
+  float *mem_A, *mem_z;
+} armt_grads;
+
+/* Backward pass (training support; section 四 of the summary page: diagonal
+ * batching carries over to the backward pass, so training and inference
+ * share one schedule).  Runs the forward over n_tokens tokens of one
+ * sequence with the diagonal schedule, keeping each cell's input rows and
+ * the memory state it starts from, then the adjoint cell by cell over the
+ * anti-diagonals in reverse order: every cell (l, s) of a reverse diagonal
+ * recomputes its forward, then hands the adjoint of its input rows to cell
+ * (l-1, s) and that of its entry state to cell (l, s-1), and adds its share
+ * of layer l's weight gradients; the cells of one diagonal run side by side.
+ * The gradient is that of the scalar
+ *   loss = <hidden, cot_hidden> + <A_final, cot_A> + <z_final, cot_z>,
+ * i.e. the vector-Jacobian product of the forward with those cotangents.
+ *   tokens       device int32 [n_tokens] (ids clamped to [0, V) as in the
+ *                forward; a short last segment is allowed)
+ *   mem_A0/z0    device fp32 [L, d, P] / [L, P] initial state, or both NULL
+ *                (zero state)
+ *   cot_hidden   device fp32 [n_tokens, d], cot_A [L, d, P], cot_z [L, P];
+ *                each may be NULL (zero)
+ *   hidden_out, mem_A_out, mem_z_out: the forward's results (as from
+ *                armt_forward_batch with batch 1), each may be NULL
+ *   grads        see armt_grads
+ * fp32 models only (ARMT_ERR_UNSUPPORTED for bf16).  Arithmetic is fp32 with
+ * every reduction in a fixed order: repeated calls give bitwise equal
+ * gradients.  The first call (and one with more segments or tokens than
+ * before) allocates the backward's workspace, which grows with the number
+ * of segments (saved cell inputs and states); the allocation synchronises
+ * `stream`; ARMT_ERR_OOM if it does not fit.  Asynchronous on `stream`
+ * otherwise.  Buffers must not alias. */
+ARMT_API armt_status armt_backward(armt_model* m, const int32_t* tokens, int64_t n_tokens,
+                                   const float* mem_A0, const float* mem_z0, const float* cot_hidden,
+                                   const float* cot_A, const float* cot_z, float* hidden_out,
+                                   float* mem_A_out, float* mem_z_out, const armt_grads* grads,
+                                   void* stream);
+
+/* Kernel launches of the last armt_backward (its forward not included) and
+ * the bytes of its workspace. */
+ARMT_API armt_status armt_backward_stats(const armt_model* m, int64_t* launches, int64_t* workspace_bytes);
 
 /* Sizes of the memory state buffers of one sequence (elements); a batch of
  * B sequences needs B times these. */

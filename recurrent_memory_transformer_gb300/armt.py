@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "ARMT_OK", 1: "ARMT_ERR_ARG", 2: "ARMT_ERR_SHAPE", 3: "ARMT_E
                 4: "ARMT_ERR_OOM", 5: "ARMT_ERR_CUDA", 6: "ARMT_ERR_TIMEOUT", 7: "ARMT_ERR_NO_DEVICE"}
 ARMT_F32, ARMT_BF16 = 0, 1
 PRECISION_BF16, PRECISION_BF16X2 = 0, 1
-SCHEDULE_DIAGONAL, SCHEDULE_SEQUENTIAL = 0, 1
+SCHEDULE_DIAGONAL, SCHEDULE_SEQUENTIAL, SCHEDULE_WAVEFRONT = 0, 1, 2
 KERNEL_CLASSES = ("gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down", "attention", "assoc_read",
                   "assoc_write", "norm", "other")
 
@@ -32,7 +32,8 @@ EXPORTED = ("armt_create", "armt_destroy", "armt_forward", "armt_forward_sequent
             "armt_segment_attention_bf16_noalloc", "armt_forward_full_attention", "armt_state_sizes",
             "armt_memory_bytes", "armt_lm_head", "armt_launch_count",
             "armt_set_profiling", "armt_set_profiling_mask", "armt_kernel_times", "armt_sync_status", "armt_status_string",
-            "armt_last_error", "armt_block_sync_status", "armt_noalloc_sync_status")
+            "armt_last_error", "armt_block_sync_status", "armt_noalloc_sync_status", "armt_backward",
+            "armt_backward_stats")
 
 
 class ArmtError(RuntimeError):
@@ -58,6 +59,13 @@ _WKEYS = ("embed", "mem", "wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "a
 
 class armt_weights(ctypes.Structure):
     _fields_ = [(k, ctypes.c_void_p) for k in _WKEYS] + [("on_device", ctypes.c_int32)]
+
+
+GRAD_KEYS = _WKEYS + ("mem_A", "mem_z")
+
+
+class armt_grads(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_void_p) for k in GRAD_KEYS]
 
 
 _lib = None
@@ -94,6 +102,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.armt_sync_status.argtypes = [P, P]
     lib.armt_block_sync_status.argtypes = [P]
     lib.armt_noalloc_sync_status.argtypes = [P]
+    lib.armt_backward.argtypes = [P, P, I64, P, P, P, P, P, P, P, P, ctypes.POINTER(armt_grads), P]
+    lib.armt_backward_stats.argtypes = [P, ctypes.POINTER(I64), ctypes.POINTER(I64)]
     for name in EXPORTED:
         getattr(lib, name).restype = S
     lib.armt_status_string.restype = ctypes.c_char_p
@@ -246,6 +256,44 @@ class Model:
         self.armt_forward(tokens, n_segments, hidden, A, z, 1 if valid else 0, stream, schedule)
         L, d, P = self.cfg.n_layers, self.cfg.d_model, self.cfg.phi_dim
         return hidden, A.view(L, d, P), z.view(L, P)
+
+    def armt_backward(self, tokens, grads, mem_A0=None, mem_z0=None, cot_hidden=None, cot_A=None,
+                      cot_z=None, hidden_out=None, mem_A_out=None, mem_z_out=None, stream=None):
+        """Device tensors (None where the header allows NULL); grads: dict of
+        fp32 device tensors keyed like the weights (+ optional mem_A, mem_z)."""
+        g = armt_grads()
+        for k in GRAD_KEYS:
+            t = grads.get(k)
+            setattr(g, k, None if t is None else _ptr(t))
+
+        def opt(t):
+            return None if t is None else _ptr(t)
+        _check(_lib.armt_backward(self._h, _ptr(tokens), int(tokens.numel()), opt(mem_A0), opt(mem_z0),
+                                  opt(cot_hidden), opt(cot_A), opt(cot_z), opt(hidden_out), opt(mem_A_out),
+                                  opt(mem_z_out), ctypes.byref(g), _stream_ptr(stream)), "armt_backward")
+
+    def armt_backward_stats(self):
+        """(kernel launches of the last backward, backward workspace bytes)."""
+        a, b = ctypes.c_int64(), ctypes.c_int64()
+        _check(_lib.armt_backward_stats(self._h, ctypes.byref(a), ctypes.byref(b)), "armt_backward_stats")
+        return a.value, b.value
+
+    def backward(self, tokens, cot_hidden=None, cot_A=None, cot_z=None, mem_A0=None, mem_z0=None,
+                 state_grads=False, stream=None):
+        """Allocates the gradients with torch; returns (grads dict, (hidden, A, z))."""
+        import torch
+        c, dev = self.cfg, tokens.device
+        L, d, P = c.n_layers, c.d_model, c.phi_dim
+        shapes = _inputs.weight_shapes(c)
+        grads = {k: torch.empty(shapes[k], dtype=torch.float32, device=dev) for k in _WKEYS}
+        if state_grads:
+            grads["mem_A"] = torch.empty((L, d, P), dtype=torch.float32, device=dev)
+            grads["mem_z"] = torch.empty((L, P), dtype=torch.float32, device=dev)
+        hidden = torch.empty((tokens.numel(), d), dtype=torch.float32, device=dev)
+        A = torch.empty((L, d, P), dtype=torch.float32, device=dev)
+        z = torch.empty((L, P), dtype=torch.float32, device=dev)
+        self.armt_backward(tokens, grads, mem_A0, mem_z0, cot_hidden, cot_A, cot_z, hidden, A, z, stream)
+        return grads, (hidden, A, z)
 
     def armt_forward_full_attention(self, tokens, hidden_out, stream=None):
         """Plain causal LLaMA over all tokens (no memory), same weights."""

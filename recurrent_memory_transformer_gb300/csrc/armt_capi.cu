@@ -36,6 +36,7 @@
 #include "gemm_tc2.cuh"
 #include "kernels.cuh"
 #include "schedule.h"
+#include "wavefront.cuh"
 
 using namespace armt;
 
@@ -66,6 +67,9 @@ void set_last_error(const std::string& msg) { g_last_error = msg; }
     armt_status s_ = (expr);        \
     if (s_ != ARMT_OK) return s_;   \
   } while (0)
+
+// the backward's host plan reports through fail / CK / CKS
+#include "backward_plan.cuh"
 
 // --------------------------------------------------------- TMA maps --
 
@@ -205,6 +209,13 @@ struct ModelBase {
   virtual long long full_workspace_bytes() const = 0;
   virtual armt_status lm_head(const float* hidden, int64_t n_rows, const void* w_head, float* logits,
                               cudaStream_t st) = 0;
+  // Gradients of <hidden, cot_h> + <A, cot_A> + <z, cot_z> for one sequence
+  // of n_tok tokens (armt_backward).
+  virtual armt_status backward(const int32_t* tokens, int64_t n_tok, const float* A0, const float* z0,
+                               const float* cot_h, const float* cot_A, const float* cot_z, float* hidden,
+                               float* A, float* z, const armt_grads& g, cudaStream_t st) = 0;
+  virtual long long backward_workspace_bytes() const = 0;
+  long long bw_launches = 0;  // kernel launches of the last backward
 
   int rows() const { return cfg.seg_len + cfg.n_mem; }
 
@@ -254,6 +265,7 @@ struct ModelBase {
   int64_t launches(int64_t n_seg, int schedule, int mem_in_valid) const {
     const int L = cfg.n_layers;
     int64_t total = (mem_in_valid && cfg.dtype == ARMT_BF16) ? 1 : 0;  // state copy
+    if (schedule == ARMT_SCHEDULE_WAVEFRONT) return total + 1;     // one persistent launch
     if (schedule == ARMT_SCHEDULE_DIAGONAL) {
       for (int64_t i = 0; i < diagonal_steps(L, n_seg); ++i) {
         const CellRange c = diagonal_step(i, L, n_seg);
@@ -358,14 +370,33 @@ struct Model : ModelBase {
   AT *Nrmf = nullptr, *Attf = nullptr, *Uf = nullptr;
   QT *QKVf = nullptr, *Vtf = nullptr;
   CUtensorMap tmNrmf, tmQKf, tmVtf, tmAttf, tmUf;
+  // backward (fp32 models): saved cell inputs and entry states, workspace
+  struct BwSave {
+    float *Xs, *As, *zs;
+    int64_t n;
+  };
+  const BwSave* bw_save = nullptr;  // set while the backward's forward runs
+  DevAllocs bw_mem;
+  BwView bwv{};
+  int64_t bw_n_cap = 0, bw_tok_cap = 0;
+  float *bw_hidden = nullptr, *bw_A = nullptr, *bw_z = nullptr;  // forward results nobody asked for
   ~Model() override {
+    bw_mem.free_all();
+    wf_mem.free_all();
     full_mem.free_all();
     lm_mem.free_all();
     wb_mem.free_all();
   }
   long long full_workspace_bytes() const override { return full_mem.total; }
+  long long backward_workspace_bytes() const override { return bw_mem.total; }
   long long batch_workspace_bytes() const override { return wb_mem.total; }
   int upd_rows_per_block = 32;
+  // persistent wavefront (fp32 models): task list and (cell, stage) counters
+  DevAllocs wf_mem;
+  WfTask* wf_tasks_d = nullptr;
+  int* wf_ctr = nullptr;
+  size_t wf_tasks_cap = 0, wf_ctr_cap = 0;
+  std::vector<WfTask> wf_tasks_h;  // kept until the next call (the upload reads it)
 
   armt_status copy_in(void* dst, const void* src, size_t bytes, cudaStream_t st) {
     CK(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, st));
@@ -647,7 +678,9 @@ struct Model : ModelBase {
       CKS((gemm<64>(ARMT_KC_ASSOC_READ, w, w.tmXa, tmAWq, w.Xa, Rd, aWq, k, d,
                     FStore{w.Qa, (long long)k, (long long)R * k}, lo, g, st, R)));
       CKS(prof_begin(ARMT_KC_ASSOC_READ, st));
-      assoc_phi_kernel<AT><<<dim3(R, g), 128, 2 * k * sizeof(float), st>>>(
+      // 256 threads, as in the persistent wavefront: the denominator's
+      // reduction order depends on the block size
+      assoc_phi_kernel<AT><<<dim3(R, g), 256, 2 * k * sizeof(float), st>>>(
           w.Qa, z, w.Phi, w.Den, R, k, c.dpfp_nu, c.assoc_eps, lo, T, nb);
       CK(cudaGetLastError());
       CKS(prof_end(st));
@@ -953,10 +986,364 @@ struct Model : ModelBase {
     }
   }
 
+  // The whole forward of one sequence as one persistent launch (fp32 models;
+  // wavefront.cuh): the same block code and data as step(), with device-side
+  // (cell, stage) counters in place of the launch boundaries.
+  armt_status forward_wavefront(const int32_t* tokens, int64_t n_tok, int64_t n, float* hidden, float* A,
+                                float* z, int mem_in_valid, cudaStream_t st) {
+    if constexpr (kTC) {
+      return fail(ARMT_ERR_UNSUPPORTED, "the wavefront schedule runs fp32 models");
+    } else {
+      const armt_config& c = cfg;
+      const int L = c.n_layers, d = c.d_model, hd = c.head_dim, F = c.ffn_dim, T = rows();
+      const int Hq = c.n_q_heads, Hkv = c.n_kv_heads, k = c.key_dim, P = phi_dim(), M = c.n_mem;
+      const int S = c.seg_len, Nq = n_qkv();
+      Work& w = w1;
+      const long long Rd = (long long)T * d;
+      if (!mem_in_valid) {
+        CK(cudaMemsetAsync(A, 0, (size_t)L * d * P * sizeof(float), st));
+        CK(cudaMemsetAsync(z, 0, (size_t)L * P * sizeof(float), st));
+      }
+      WfArgs a{};
+      a.embed = embed;
+      a.memtok = memtok;
+      a.gf = gf;
+      a.T = T; a.S = S; a.M = M; a.d = d; a.k = k; a.nu = c.dpfp_nu; a.vocab = c.vocab;
+      a.Hq = Hq; a.Hkv = Hkv; a.hd = hd; a.P = P; a.nw = nw; a.nmax = nmax; a.L = L;
+      a.assoc_eps = c.assoc_eps; a.norm_eps = c.norm_eps; a.attn_scale = 1.0f / sqrtf((float)hd);
+      a.upd_rows = upd_rows_per_block;
+      a.X = w.X; a.Cscr = w.Cscr; a.Qa = w.Qa; a.Phi = w.Phi; a.Den = w.Den; a.QKV = w.QKV;
+      a.Att = w.Att; a.VKB = w.VKB; a.PhiM = w.PhiM; a.Coef = w.Coef;
+      a.tokens = tokens; a.n_tok = n_tok; a.n_seg = n; a.last_len = last_segment_len(n_tok, S);
+      a.hidden = hidden; a.A = A; a.z = z;
+      auto g = [&](const float* Aop, long long a_gs, int K, const float* B, int N, int rows_, SimtAMap am) {
+        WfGemm r;
+        r.A = Aop; r.a_gs = a_gs; r.lda = K; r.B = B; r.b_gs = (long long)N * K;
+        r.N = N; r.K = K; r.rows = rows_; r.nbx = (N + 63) / 64; r.am = am;
+        return r;
+      };
+      const SimtAMap plain{0, 0, 1, 0, 0, 0};
+      a.gq = g(w.X, Rd, d, reinterpret_cast<const float*>(aWq), k, T, plain);
+      a.gr = g(w.Phi, (long long)T * P, P, A, d, T, plain);
+      a.gqkv = g(w.Nrm, Rd, d, reinterpret_cast<const float*>(Wqkv), Nq, T, plain);
+      a.go = g(w.Att, (long long)T * Hq * hd, Hq * hd, reinterpret_cast<const float*>(Wo), d, T, plain);
+      a.ggu = g(w.Nrm, Rd, d, reinterpret_cast<const float*>(Wgu), 2 * F, T, plain);
+      a.gd = g(w.U, (long long)T * F, F, reinterpret_cast<const float*>(Wd), d, T, plain);
+      a.gw = g(w.X, Rd, d, reinterpret_cast<const float*>(Ww), nw, M, SimtAMap{S, 1, 1, 0, 0, 0});
+      const RowNormIn norm_in{w.Ssq, npart, 1.0f / (float)d, c.norm_eps};
+      a.eq = EpiStore{w.Qa, (long long)k, (long long)T * k};
+      {
+        RowNormOut<float> n1{g1, w.Nrm, w.Ssq};
+        a.er = EpiAssocRead<float>{w.X, w.Den, w.Res, T, d, n1};
+      }
+      a.eqkv = EpiQkvRope<float>{w.QKV, w.cosT, w.sinT, T, hd, (Hq + Hkv) * hd, qkv_ld, nullptr, Hkv, t_pad,
+                                 norm_in, T, 1};
+      a.eo = EpiResidual<float>{w.Res, w.Res, nullptr, T, d, 0, RowNormOut<float>{g2, w.Nrm, w.Ssq}};
+      a.egu = EpiSwiGLU<float>{w.U, T, F, norm_in};
+      a.ed = EpiResidual<float>{w.Res, w.X, nullptr, T, d, 1, RowNormOut<float>{nullptr, nullptr, nullptr}};
+      a.ew = EpiStore{w.VKB, (long long)nw, (long long)M * nw};
+      a.err = d_err;
+      a.wp = wp;
+      wf_tasks_h = wf_tasks(a, n);
+      const size_t nt = wf_tasks_h.size(), nc = (size_t)L * n * WF_NSTAGE + 1;
+      if (nt > (size_t)INT32_MAX || nc > (size_t)INT32_MAX) return fail(ARMT_ERR_SHAPE, "too many wavefront tasks");
+      if (nt > wf_tasks_cap || nc > wf_ctr_cap) {
+        CK(cudaStreamSynchronize(st));
+        wf_mem.free_all();
+        wf_tasks_d = nullptr;
+        wf_ctr = nullptr;
+        wf_tasks_cap = wf_ctr_cap = 0;
+        CKS(wf_mem.alloc_n(&wf_tasks_d, nt));
+        CKS(wf_mem.alloc_n(&wf_ctr, nc));
+        wf_tasks_cap = nt;
+        wf_ctr_cap = nc;
+      }
+      CK(cudaMemcpyAsync(wf_tasks_d, wf_tasks_h.data(), nt * sizeof(WfTask), cudaMemcpyHostToDevice, st));
+      CK(cudaMemsetAsync(wf_ctr, 0, nc * sizeof(int), st));
+      int* next = wf_ctr + (nc - 1);  // the task counter
+      const size_t smem = std::max(std::max(attn_smem, feat_smem), std::max(upd_smem, (size_t)2 * k * sizeof(float)));
+      CKS(prof_begin(ARMT_KC_OTHER, st));
+      armt_status r = ARMT_OK;
+      if (hd == 32) r = launch_wavefront<32>(nt, next, smem, a, st);
+      else if (hd == 64) r = launch_wavefront<64>(nt, next, smem, a, st);
+      else r = launch_wavefront<128>(nt, next, smem, a, st);
+      CKS(r);
+      CKS(prof_end(st));
+      return ARMT_OK;
+    }
+  }
+
+  template <int HD>
+  armt_status launch_wavefront(size_t nt, int* next, size_t smem, const WfArgs& a, cudaStream_t st) {
+    auto kern = wavefront_kernel<HD>;
+    CK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    int per_sm = 0;
+    CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem));
+    if (per_sm <= 0) return fail(ARMT_ERR_UNSUPPORTED, "the wavefront kernel does not fit an SM");
+    // every block resident at once (cooperative launch), none idle beyond the task count
+    const long long grid = std::min<long long>((long long)per_sm * num_sms, (long long)nt);
+    const WfTask* tasks = wf_tasks_d;
+    int n_tasks = (int)nt;
+    int* ctr = wf_ctr;
+    void* args[] = {(void*)&tasks, (void*)&n_tasks, (void*)&next, (void*)&ctr, (void*)&a};
+    CK(cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(256), args, smem, st));
+    return ARMT_OK;
+  }
+
+  // The backward's forward keeps, for every cell, its input rows and the
+  // state it starts from: before a step, the input slots l >= 1 (written by
+  // the cell below in the previous step) and the states; after it, layer 0's
+  // gathered input.  Batch 1.
+  armt_status save_cells(Work& w, const CellRange& c, const float* A, const float* z, bool before,
+                         cudaStream_t st) {
+    const int d = cfg.d_model, P = phi_dim(), T = rows();
+    const int64_t n = bw_save->n;
+    const size_t Td = (size_t)T * d;
+    for (int l = c.lo; l <= c.hi; ++l) {
+      const int64_t s = c.s_lo - (l - c.lo);
+      const size_t cell = (size_t)l * n + s;
+      if (before) {
+        CK(cudaMemcpyAsync(bw_save->As + cell * d * P, A + (size_t)l * d * P, (size_t)d * P * sizeof(float),
+                           cudaMemcpyDeviceToDevice, st));
+        CK(cudaMemcpyAsync(bw_save->zs + cell * P, z + (size_t)l * P, (size_t)P * sizeof(float),
+                           cudaMemcpyDeviceToDevice, st));
+      }
+      if ((l >= 1) == before)
+        CK(cudaMemcpyAsync(bw_save->Xs + cell * Td, w.X + (size_t)l * Td, Td * sizeof(float),
+                           cudaMemcpyDeviceToDevice, st));
+    }
+    return ARMT_OK;
+  }
+
+  // Backward workspace for n segments of n_tok tokens (grown on demand).
+  armt_status bw_alloc(int64_t n, int64_t n_tok, cudaStream_t st) {
+    if (n <= bw_n_cap && n_tok <= bw_tok_cap) return ARMT_OK;
+    CK(cudaStreamSynchronize(st));
+    bw_mem.free_all();
+    bw_n_cap = bw_tok_cap = 0;
+    const armt_config& c = cfg;
+    const size_t L = c.n_layers, d = c.d_model, k = c.key_dim, P = phi_dim(), T = rows(), M = c.n_mem;
+    const size_t F = c.ffn_dim, Nq = n_qkv(), HA = (size_t)c.n_q_heads * c.head_dim, Td = T * d;
+    BwView& v = bwv;
+    v = BwView{};
+    auto A = [&](float** p, size_t nel) { return bw_mem.alloc_n(p, nel); };
+    CKS(A(&v.Xs, L * n * Td));
+    CKS(A(&v.As, L * n * d * P));
+    CKS(A(&v.zs, L * n * P));
+    CKS(A(&v.Qa, L * T * k));
+    CKS(A(&v.Phi, L * T * P));
+    CKS(A(&v.Den, L * T));
+    float** td_bufs[] = {&v.Rr, &v.X1, &v.N1, &v.Y, &v.N2, &v.H, &v.N2bar, &v.Ybar, &v.N1bar, &v.X1bar, &v.XS};
+    for (float** b : td_bufs) CKS(A(b, L * Td));
+    CKS(A(&v.QKV, L * T * Nq));
+    CKS(A(&v.dQKV, L * T * Nq));
+    CKS(A(&v.LSE, L * T * c.n_q_heads));
+    CKS(A(&v.Dsum, L * T * c.n_q_heads));
+    CKS(A(&v.Att, L * T * HA));
+    CKS(A(&v.dAtt, L * T * HA));
+    CKS(A(&v.GU, L * T * 2 * F));
+    CKS(A(&v.GUbar, L * T * 2 * F));
+    CKS(A(&v.U, L * T * F));
+    CKS(A(&v.Ubar, L * T * F));
+    CKS(A(&v.VKB, L * M * nw));
+    CKS(A(&v.VKBbar, L * M * nw));
+    CKS(A(&v.PhiM, L * M * P));
+    CKS(A(&v.PhiBarM, L * M * P));
+    CKS(A(&v.Sc, L * M * WS_NSC));
+    CKS(A(&v.Gm, L * M * M));
+    CKS(A(&v.Coef, L * M * M));
+    float** md_bufs[] = {&v.Cw, &v.Vb, &v.CB, &v.Wv};
+    for (float** b : md_bufs) CKS(A(b, L * M * d));
+    CKS(A(&v.Srow, L * T));
+    CKS(A(&v.Dbar, L * T));
+    CKS(A(&v.PhiBar, L * T * P));
+    CKS(A(&v.QaBar, L * T * k));
+    for (int q = 0; q < 2; ++q) {
+      CKS(A(&v.Hbar[q], L * Td));
+      CKS(A(&v.SA[q], L * d * P));
+      CKS(A(&v.Sz[q], L * P));
+    }
+    CKS(A(&v.XB0, n * Td));
+    CKS(A(&v.dWqkv, L * Nq * d));
+    CKS(A(&v.dWgu, L * 2 * F * d));
+    CKS(A(&v.dWw, L * nw * d));
+    CKS(A(&bw_hidden, (size_t)n_tok * d));
+    CKS(A(&bw_A, L * d * P));
+    CKS(A(&bw_z, L * P));
+    // kernels with more than 48 KB of dynamic shared memory
+    const int hd = c.head_dim;
+    const int fwd_smem = (int)bw_attn_fwd_smem(hd), dq_smem = (int)bw_attn_dq_smem(hd),
+              dkv_smem = (int)bw_attn_dkv_smem(hd);
+    if (hd == 32) {
+      CK(cudaFuncSetAttribute(bw_attn_fwd_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd_smem));
+      CK(cudaFuncSetAttribute(bw_attn_dq_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem));
+      CK(cudaFuncSetAttribute(bw_attn_dkv_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv_smem));
+    } else if (hd == 64) {
+      CK(cudaFuncSetAttribute(bw_attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd_smem));
+      CK(cudaFuncSetAttribute(bw_attn_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem));
+      CK(cudaFuncSetAttribute(bw_attn_dkv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv_smem));
+    } else {
+      CK(cudaFuncSetAttribute(bw_attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd_smem));
+      CK(cudaFuncSetAttribute(bw_attn_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem));
+      CK(cudaFuncSetAttribute(bw_attn_dkv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv_smem));
+    }
+    const int rows_smem = (int)((M * P + M * WS_NSC) * sizeof(float));
+    if (P == 96)
+      CK(cudaFuncSetAttribute(bw_write_rows_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, rows_smem));
+    else if (P == 192)
+      CK(cudaFuncSetAttribute(bw_write_rows_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, rows_smem));
+    else
+      CK(cudaFuncSetAttribute(bw_write_rows_kernel<12>, cudaFuncAttributeMaxDynamicSharedMemorySize, rows_smem));
+    CK(cudaFuncSetAttribute(bw_write_feat_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                            (int)((M * 2 * k + M * (P + 1)) * sizeof(float))));
+    bw_n_cap = n;
+    bw_tok_cap = n_tok;
+    return ARMT_OK;
+  }
+
+  armt_status backward(const int32_t* tokens, int64_t n_tok, const float* A0, const float* z0,
+                       const float* cot_h, const float* cot_A, const float* cot_z, float* hidden, float* A,
+                       float* z, const armt_grads& gr, cudaStream_t st) override {
+    if constexpr (kTC) {
+      return fail(ARMT_ERR_UNSUPPORTED, "the backward pass runs fp32 models");
+    } else {
+      const armt_config& c = cfg;
+      const int L = c.n_layers, d = c.d_model, P = phi_dim(), S = c.seg_len, M = c.n_mem, k = c.key_dim;
+      const int F = c.ffn_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads, hd = c.head_dim;
+      const int64_t n = n_segments_for(n_tok, S);
+      CKS(bw_alloc(n, n_tok, st));
+      BwView& v = bwv;
+      if (hidden == nullptr) hidden = bw_hidden;
+      if (A == nullptr) A = bw_A;
+      if (z == nullptr) z = bw_z;
+      const size_t a_n = (size_t)L * d * P, z_n = (size_t)L * P;
+      // the forward, keeping every cell's input rows and entry state
+      const bool resume = A0 != nullptr;
+      if (resume) {
+        CK(cudaMemcpyAsync(A, A0, a_n * sizeof(float), cudaMemcpyDeviceToDevice, st));
+        CK(cudaMemcpyAsync(z, z0, z_n * sizeof(float), cudaMemcpyDeviceToDevice, st));
+      }
+      const BwSave sv{v.Xs, v.As, v.zs, n};
+      bw_save = &sv;
+      const armt_status fs = forward(tokens, n_tok, 1, hidden, A, z, resume ? 1 : 0, ARMT_SCHEDULE_DIAGONAL, st);
+      bw_save = nullptr;
+      CKS(fs);
+      // sizes and weights
+      v.L = L;
+      v.d = d;
+      v.k = k;
+      v.nu = c.dpfp_nu;
+      v.P = P;
+      v.Hq = Hq;
+      v.Hkv = Hkv;
+      v.hd = hd;
+      v.F = F;
+      v.Nq = (int)n_qkv();
+      v.nw = nw;
+      v.T = rows();
+      v.S = S;
+      v.M = M;
+      v.vocab = c.vocab;
+      v.norm_eps = c.norm_eps;
+      v.assoc_eps = c.assoc_eps;
+      v.n_seg = n;
+      v.n_tok = n_tok;
+      v.last_len = last_segment_len(n_tok, S);
+      v.aWq = aWq;
+      v.Wqkv = Wqkv;
+      v.Wo = Wo;
+      v.Wgu = Wgu;
+      v.Wd = Wd;
+      v.Ww = Ww;
+      v.g1 = g1;
+      v.g2 = g2;
+      v.gf = gf;
+      v.cosT = w1.cosT;
+      v.sinT = w1.sinT;
+      v.cot_h = cot_h;
+      // gradients accumulate from zero: the unfused ones in the caller's buffers
+      v.dWo = gr.wo;
+      v.dWd = gr.w_down;
+      v.daWq = gr.a_wq;
+      v.dg1 = gr.norm1;
+      v.dg2 = gr.norm2;
+      v.dgf = gr.norm_f;
+      const size_t HA = (size_t)Hq * hd;
+      CK(cudaMemsetAsync(gr.wo, 0, (size_t)L * d * HA * 4, st));
+      CK(cudaMemsetAsync(gr.w_down, 0, (size_t)L * d * F * 4, st));
+      CK(cudaMemsetAsync(gr.a_wq, 0, (size_t)L * k * d * 4, st));
+      CK(cudaMemsetAsync(gr.norm1, 0, (size_t)L * d * 4, st));
+      CK(cudaMemsetAsync(gr.norm2, 0, (size_t)L * d * 4, st));
+      CK(cudaMemsetAsync(gr.norm_f, 0, (size_t)d * 4, st));
+      CK(cudaMemsetAsync(gr.embed, 0, (size_t)c.vocab * d * 4, st));
+      CK(cudaMemsetAsync(gr.mem, 0, (size_t)M * d * 4, st));
+      CK(cudaMemsetAsync(v.dWqkv, 0, (size_t)L * v.Nq * d * 4, st));
+      CK(cudaMemsetAsync(v.dWgu, 0, (size_t)L * 2 * F * d * 4, st));
+      CK(cudaMemsetAsync(v.dWw, 0, (size_t)L * nw * d * 4, st));
+      // the final state's adjoints enter layer l's first cell in reverse order,
+      // (l, n - 1) on diagonal l + n - 1, which reads buffer (l + n - 1) & 1
+      for (int l = 0; l < L; ++l) {
+        const int q = (int)((l + n - 1) & 1);
+        float* sa = v.SA[q] + (size_t)l * d * P;
+        float* sz = v.Sz[q] + (size_t)l * P;
+        if (cot_A != nullptr)
+          CK(cudaMemcpyAsync(sa, cot_A + (size_t)l * d * P, (size_t)d * P * 4, cudaMemcpyDeviceToDevice, st));
+        else
+          CK(cudaMemsetAsync(sa, 0, (size_t)d * P * 4, st));
+        if (cot_z != nullptr)
+          CK(cudaMemcpyAsync(sz, cot_z + (size_t)l * P, (size_t)P * 4, cudaMemcpyDeviceToDevice, st));
+        else
+          CK(cudaMemsetAsync(sz, 0, (size_t)P * 4, st));
+      }
+      BwRun run{v, st};
+      for (int64_t i = diagonal_steps(L, n) - 1; i >= 0; --i) CKS(run.diagonal(i));
+      bw_embed_grad_kernel<<<(d + 127) / 128, 128, 0, st>>>(v.XB0, tokens, n_tok, S, rows(), M, d, c.vocab, n,
+                                                            gr.embed, gr.mem);
+      CKS(run.check());
+      // the initial state's adjoints: layer l's cell (l, 0) ran on diagonal l
+      for (int l = 0; l < L; ++l) {
+        const int q = (l + 1) & 1;
+        if (gr.mem_A != nullptr)
+          CK(cudaMemcpyAsync(gr.mem_A + (size_t)l * d * P, v.SA[q] + (size_t)l * d * P, (size_t)d * P * 4,
+                             cudaMemcpyDeviceToDevice, st));
+        if (gr.mem_z != nullptr)
+          CK(cudaMemcpyAsync(gr.mem_z + (size_t)l * P, v.Sz[q] + (size_t)l * P, (size_t)P * 4,
+                             cudaMemcpyDeviceToDevice, st));
+      }
+      // fused accumulators to the caller's layout (the reverse of create()'s copies)
+      const size_t Nq = v.Nq, es = sizeof(float);
+      CK(cudaMemcpy2DAsync(gr.wq, HA * d * es, v.dWqkv, Nq * d * es, HA * d * es, L, cudaMemcpyDeviceToDevice, st));
+      CK(cudaMemcpy2DAsync(gr.wk, (size_t)Hkv * hd * d * es, v.dWqkv + HA * d, Nq * d * es, (size_t)Hkv * hd * d * es,
+                           L, cudaMemcpyDeviceToDevice, st));
+      CK(cudaMemcpy2DAsync(gr.wv, (size_t)Hkv * hd * d * es, v.dWqkv + (HA + (size_t)Hkv * hd) * d, Nq * d * es,
+                           (size_t)Hkv * hd * d * es, L, cudaMemcpyDeviceToDevice, st));
+      const size_t blk = (size_t)GU_BLK * d * es, nblk = (size_t)L * F / GU_BLK;
+      CK(cudaMemcpy2DAsync(gr.w_gate, blk, v.dWgu, 2 * blk, blk, nblk, cudaMemcpyDeviceToDevice, st));
+      CK(cudaMemcpy2DAsync(gr.w_up, blk, reinterpret_cast<char*>(v.dWgu) + blk, 2 * blk, blk, nblk,
+                           cudaMemcpyDeviceToDevice, st));
+      CK(cudaMemcpy2DAsync(gr.a_wv, (size_t)d * d * es, v.dWw, (size_t)nw * d * es, (size_t)d * d * es, L,
+                           cudaMemcpyDeviceToDevice, st));
+      CK(cudaMemcpy2DAsync(gr.a_wk, (size_t)k * d * es, v.dWw + (size_t)d * d, (size_t)nw * d * es,
+                           (size_t)k * d * es, L, cudaMemcpyDeviceToDevice, st));
+      CK(cudaMemcpy2DAsync(gr.a_wbeta, (size_t)d * es, v.dWw + (size_t)(d + k) * d, (size_t)nw * d * es,
+                           (size_t)d * es, L, cudaMemcpyDeviceToDevice, st));
+      bw_launches = run.launches;
+      return ARMT_OK;
+    }
+  }
+
   armt_status forward(const int32_t* tokens, int64_t n_tok, int nb, float* hidden, float* A,
                       float* z, int mem_in_valid, int schedule, cudaStream_t st) override {
     const int L = cfg.n_layers, d = cfg.d_model, P = phi_dim(), S = cfg.seg_len;
     const int64_t n = n_segments_for(n_tok, S);
+    if (schedule == ARMT_SCHEDULE_WAVEFRONT) {
+      if constexpr (kTC) {
+        return fail(ARMT_ERR_UNSUPPORTED, "the wavefront schedule runs fp32 models");
+      } else {
+        if (nb != 1) return fail(ARMT_ERR_UNSUPPORTED, "the wavefront schedule runs one sequence");
+        return forward_wavefront(tokens, n_tok, n, hidden, A, z, mem_in_valid, st);
+      }
+    }
     if (nb > 1) CKS(ensure_batch(nb, st));
     Work& w = nb == 1 ? w1 : wb;
     const size_t a_n = (size_t)L * nb * d * P, z_n = (size_t)L * nb * P;
@@ -974,7 +1361,9 @@ struct Model : ModelBase {
     if (schedule == ARMT_SCHEDULE_DIAGONAL) {
       for (int64_t i = 0; i < diagonal_steps(L, n); ++i) {
         const CellRange c = diagonal_step(i, L, n);
+        if (bw_save != nullptr) CKS(save_cells(w, c, A, z, true, st));
         CKS(step(w, c.lo, c.hi, c.s_lo, tokens, n_tok, n, hidden, A, z, st));
+        if (bw_save != nullptr) CKS(save_cells(w, c, A, z, false, st));
         if (report)
           CKS(sink_progress(diagonal_rows_final(i, L, S, n_tok), diagonal_layers_final(i, n), st));
       }
@@ -1186,7 +1575,8 @@ armt_status armt_forward_batch(armt_model* m, const int32_t* tokens, int32_t bat
     return fail(ARMT_ERR_ARG, "NULL argument");
   if (batch <= 0 || n_tokens <= 0) return fail(ARMT_ERR_ARG, "batch and n_tokens must be positive");
   if (mem_in_valid != 0 && mem_in_valid != 1) return fail(ARMT_ERR_ARG, "mem_in_valid must be 0 or 1");
-  if (schedule != ARMT_SCHEDULE_DIAGONAL && schedule != ARMT_SCHEDULE_SEQUENTIAL)
+  if (schedule != ARMT_SCHEDULE_DIAGONAL && schedule != ARMT_SCHEDULE_SEQUENTIAL &&
+      schedule != ARMT_SCHEDULE_WAVEFRONT)
     return fail(ARMT_ERR_ARG, "unknown schedule");
   const armt_config& c = m->impl->cfg;
   if (n_tokens > ((int64_t)1 << 24) * c.seg_len) return fail(ARMT_ERR_SHAPE, "n_tokens too large");
@@ -1210,6 +1600,33 @@ armt_status armt_forward_sequential(armt_model* m, const int32_t* tokens, int64_
                         ARMT_SCHEDULE_SEQUENTIAL, stream);
 }
 
+armt_status armt_backward(armt_model* m, const int32_t* tokens, int64_t n_tokens, const float* mem_A0,
+                          const float* mem_z0, const float* cot_hidden, const float* cot_A, const float* cot_z,
+                          float* hidden_out, float* mem_A_out, float* mem_z_out, const armt_grads* grads,
+                          void* stream) {
+  if (m == nullptr || tokens == nullptr || grads == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
+  const float* gp[] = {grads->embed, grads->mem, grads->wq, grads->wk, grads->wv, grads->wo, grads->w_gate,
+                       grads->w_up, grads->w_down, grads->a_wq, grads->a_wk, grads->a_wv, grads->a_wbeta,
+                       grads->norm1, grads->norm2, grads->norm_f};
+  for (const float* p : gp)
+    if (p == nullptr) return fail(ARMT_ERR_ARG, "NULL gradient pointer");
+  if ((mem_A0 == nullptr) != (mem_z0 == nullptr))
+    return fail(ARMT_ERR_ARG, "mem_A0 and mem_z0 must both be given or both be NULL");
+  if (n_tokens <= 0) return fail(ARMT_ERR_ARG, "n_tokens must be positive");
+  const armt_config& c = m->impl->cfg;
+  if (n_tokens > ((int64_t)1 << 24) * c.seg_len) return fail(ARMT_ERR_SHAPE, "n_tokens too large");
+  m->impl->wp = wait_policy_from_env();
+  return m->impl->backward(tokens, n_tokens, mem_A0, mem_z0, cot_hidden, cot_A, cot_z, hidden_out, mem_A_out,
+                           mem_z_out, *grads, reinterpret_cast<cudaStream_t>(stream));
+}
+
+armt_status armt_backward_stats(const armt_model* m, int64_t* launches, int64_t* workspace_bytes) {
+  if (m == nullptr || launches == nullptr || workspace_bytes == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
+  *launches = m->impl->bw_launches;
+  *workspace_bytes = m->impl->backward_workspace_bytes();
+  return ARMT_OK;
+}
+
 static bool is_pinned(const void* p) {
   cudaPointerAttributes a;
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
@@ -1225,7 +1642,8 @@ armt_status armt_forward_host(armt_model* m, const int32_t* h_tokens, int64_t n,
   if (m == nullptr || h_tokens == nullptr || h_hidden == nullptr || h_A == nullptr || h_z == nullptr)
     return fail(ARMT_ERR_ARG, "NULL argument");
   if (n <= 0) return fail(ARMT_ERR_ARG, "n_segments must be positive");
-  if (schedule != ARMT_SCHEDULE_DIAGONAL && schedule != ARMT_SCHEDULE_SEQUENTIAL)
+  if (schedule != ARMT_SCHEDULE_DIAGONAL && schedule != ARMT_SCHEDULE_SEQUENTIAL &&
+      schedule != ARMT_SCHEDULE_WAVEFRONT)
     return fail(ARMT_ERR_ARG, "unknown schedule");
   ModelBase* b = m->impl;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -1412,7 +1830,8 @@ armt_status armt_memory_bytes(const armt_model* m, int64_t* weights, int64_t* wo
 armt_status armt_launch_count(const armt_model* m, int64_t n, int32_t schedule, int64_t* launches) {
   if (m == nullptr || launches == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
   if (n <= 0) return fail(ARMT_ERR_ARG, "n_segments must be positive");
-  if (schedule != ARMT_SCHEDULE_DIAGONAL && schedule != ARMT_SCHEDULE_SEQUENTIAL)
+  if (schedule != ARMT_SCHEDULE_DIAGONAL && schedule != ARMT_SCHEDULE_SEQUENTIAL &&
+      schedule != ARMT_SCHEDULE_WAVEFRONT)
     return fail(ARMT_ERR_ARG, "unknown schedule");
   *launches = m->impl->launches(n, schedule, 0);
   return ARMT_OK;

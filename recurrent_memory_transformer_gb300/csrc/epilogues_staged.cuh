@@ -71,10 +71,11 @@ __device__ __forceinline__ float half_warp_sum(float v) {
 // run of a row.  Two callbacks per 4-column piece:
 //   pre(row, col) -> float4   global input the piece needs (e.g. the residual),
 //   op(row, col, v, pre, ctx) -> float   the work; returns its row-sum part.
-// The inputs of 8 rows are loaded before any of their outputs are stored, so
-// a warp keeps 8 loads in flight even though the compiler must assume inputs
-// and outputs alias.  Shuffles run on all lanes; the work is predicated on
-// the row being valid.
+// The inputs of all 16 rows a lane handles are loaded before any of their
+// outputs are stored, so a warp keeps 16 loads in flight even though the
+// compiler must assume inputs and outputs alias (the epilogue waits on
+// these loads: more in flight hides more of their latency).  Shuffles run on
+// all lanes; the work is predicated on the row being valid.
 template <class Pre, class Op>
 __device__ __forceinline__ void staged_rows_elementwise(const float* stage, int row0, int rows,
                                                         int colA, int colB, float ctx, Pre&& pre,
@@ -82,16 +83,17 @@ __device__ __forceinline__ void staged_rows_elementwise(const float* stage, int 
   const int lane = threadIdx.x & 31;
   const int q = lane & 15, half = lane >> 4;
   const int col = (q < 8 ? colA + 4 * q : colB + 4 * (q - 8));
+  constexpr int PREF = 8;  // rows whose inputs are in flight together
 #pragma unroll 1
-  for (int it0 = 0; it0 < 16; it0 += 8) {
-    float4 in[8];
+  for (int it0 = 0; it0 < 16; it0 += PREF) {
+    float4 in[PREF];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < PREF; ++k) {
       const int row = row0 + 2 * (it0 + k) + half;
       in[k] = row < rows ? pre(row, col) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < PREF; ++k) {
       const int r = 2 * (it0 + k) + half;
       const float4 v = stage_ld4(stage, r, q);
       const float c = __shfl_sync(0xffffffffu, ctx, r);
@@ -319,9 +321,13 @@ struct SEpiSwiGLU {
 //   r = [relu(q), relu(-q)],  phi_{128 (j-1) + c} = r_c r_{(c-j) mod 128}, j = 1..3,
 //   den = z^T phi + eps with z of the row's (layer, sequence) group,
 // phi stored in the activation dtype, den in fp32 (from the unrounded phi).
-// Per row, lane L computes the pairs p, p + 1 with p = 64 t + 2 L, t < 6
-// (c = 2 L + 64 (t mod 2), j = t / 2 + 1) and stores them as one bf16 pair; z
-// is reloaded only when the rows pass into another sequence's cell.
+// Per row, lane L holds q_{2L}, q_{2L+1} and computes the pairs p, p + 1 with
+// p = 64 t + 2 L, t < 6 (c = 2 L + 64 (t mod 2), j = t / 2 + 1), storing each
+// as one bf16 pair.  The rolled factors r_{c-j}, r_{c+1-j} are q values of
+// lanes L-1 and L-2 (three shuffles per row); where c - j falls below the
+// start of its half (L = 0, or L <= 1 for j = 3) it wraps into the other half
+// of r, i.e. the sign of the relu flips.  z is reloaded only when the rows
+// pass into another sequence's cell.
 template <typename AT>
 struct SEpiPhi {
   static_assert(sizeof(AT) == 2, "bf16 features");
@@ -336,36 +342,52 @@ struct SEpiPhi {
   __device__ bool direct_tile(int) const { return false; }
   template <class Src> __device__ void direct(int, int, bool, int, int, Src&) const {}
   __device__ float row_ctx(int, int, bool) const { return 0.f; }
-  // r_c of stage row `r` (stage columns 0..63 = q_0..q_63, 16-byte chunks swizzled by row & 7)
-  __device__ __forceinline__ static float r_at(const float* stage, int r, int c) {
-    const int e = c & 63;
-    const float q = stage[r * 64 + (((e >> 2) ^ (r & 7)) << 2) + (e & 3)];
-    return c < 64 ? fmaxf(q, 0.f) : fmaxf(-q, 0.f);
-  }
+  // relu(x) in the first half of r, relu(-x) in the second
+  __device__ __forceinline__ static float rv(float x, bool neg) { return neg ? fmaxf(-x, 0.f) : fmaxf(x, 0.f); }
   __device__ __forceinline__ void process(int l, int row0, int rows_, int, int, const float* stage,
                                           float, float*) const {
     const int lane = threadIdx.x & 31;
-    int cell = -1;
+    const bool w1 = lane == 0, w3 = lane <= 1;  // the lanes whose rolled factors wrap
+    int cell = -1, next_cell_row = 0;
     float2 zz[6];
 #pragma unroll 1
     for (int r = 0; r < 32; ++r) {
       const int row = row0 + r;
       if (row >= rows_) break;  // warp-uniform
-      const int cb = row / cell_rows;
-      if (cb != cell) {
-        cell = cb;
-        const float* zr = z + ((long long)l * nb + cb) * 384 + 2 * lane;
+      if (row >= next_cell_row) {
+        const int cb = row / cell_rows;
+        next_cell_row = (cb + 1) * cell_rows;
+        if (cb != cell) {
+          cell = cb;
+          const float* zr = z + ((long long)l * nb + cb) * 384 + 2 * lane;
 #pragma unroll
-        for (int t = 0; t < 6; ++t) zz[t] = *reinterpret_cast<const float2*>(zr + 64 * t);
+          for (int t = 0; t < 6; ++t) zz[t] = *reinterpret_cast<const float2*>(zr + 64 * t);
+        }
       }
+      // q_{2L}, q_{2L+1} of stage row r (16-byte chunks swizzled by r & 7)
+      const float2 q = *reinterpret_cast<const float2*>(stage + r * 64 + ((((2 * lane) >> 2) ^ (r & 7)) << 2) +
+                                                        ((2 * lane) & 3));
+      const float a0 = __shfl_sync(0xffffffffu, q.x, (lane - 1) & 31);  // q_{2L-2}
+      const float a1 = __shfl_sync(0xffffffffu, q.y, (lane - 1) & 31);  // q_{2L-1}
+      const float b1 = __shfl_sync(0xffffffffu, q.y, (lane - 2) & 31);  // q_{2L-3}
       uint32_t* out = reinterpret_cast<uint32_t*>(phi + ((long long)l * rows + row) * 384) + lane;
       float acc = 0.f;
 #pragma unroll
       for (int t = 0; t < 6; ++t) {
         const int j = t / 2 + 1;
-        const int c = 2 * lane + 64 * (t % 2);
-        const float f0 = r_at(stage, r, c) * r_at(stage, r, (c - j) & 127);
-        const float f1 = r_at(stage, r, c + 1) * r_at(stage, r, (c + 1 - j) & 127);
+        const bool h = (t & 1) != 0;  // c in the second half of r
+        const float rc0 = rv(q.x, h), rc1 = rv(q.y, h);
+        float f0, f1;
+        if (j == 1) {
+          f0 = rc0 * rv(a1, h != w1);
+          f1 = rc1 * rc0;
+        } else if (j == 2) {
+          f0 = rc0 * rv(a0, h != w1);
+          f1 = rc1 * rv(a1, h != w1);
+        } else {
+          f0 = rc0 * rv(b1, h != w3);
+          f1 = rc1 * rv(a0, h != w1);
+        }
         out[32 * t] = pack_bf16x2(f0, f1);
         if (lo_off != 0) out[lo_off / 2 + 32 * t] = pack_bf16x2(bf16_residual(f0), bf16_residual(f1));
         acc = fmaf(zz[t].x, f0, acc);

@@ -28,11 +28,11 @@ namespace armt {
 // mask no real row ever sees them).  xa_lo_off != 0 (split precision): the
 // bf16 low part of Xa at Xa + xa_lo_off.
 template <typename WT>
-__global__ void embed_gather_kernel(const int32_t* __restrict__ tokens, long long tok_stride,
-                                    const WT* __restrict__ embed, const WT* __restrict__ mem,
-                                    float* __restrict__ X, WT* __restrict__ Xa, int T, int n_seg,
-                                    int M, int d, int vocab, long long xa_lo_off = 0) {
-  const int t = blockIdx.x, b = blockIdx.y;
+__device__ __forceinline__ void embed_gather_kernel_block(const uint3 bid, const int32_t* tokens, long long tok_stride,
+                                    const WT* embed, const WT* mem,
+                                    float* X, WT* Xa, int T, int n_seg,
+                                    int M, int d, int vocab, long long xa_lo_off) {
+  const int t = bid.x, b = bid.y;
   const WT* src = nullptr;
   if (t < n_seg) {
     int id = tokens[b * tok_stride + t];
@@ -55,24 +55,39 @@ __global__ void embed_gather_kernel(const int32_t* __restrict__ tokens, long lon
   }
 }
 
+template <typename WT>
+__global__ void embed_gather_kernel(const int32_t* __restrict__ tokens, long long tok_stride,
+                                    const WT* __restrict__ embed, const WT* __restrict__ mem,
+                                    float* __restrict__ X, WT* __restrict__ Xa, int T, int n_seg,
+                                    int M, int d, int vocab, long long xa_lo_off = 0) {
+  embed_gather_kernel_block<WT>(blockIdx, tokens, tok_stride, embed, mem, X, Xa, T, n_seg, M, d, vocab, xa_lo_off);
+}
+
 // ------------------------------------------------------------- RMSNorm --
 
 // out[l][row] = x[l][row] / sqrt(mean(x^2) + eps) * gain[l]  for the rows
 // [0, rows) of layers g_first + blockIdx.y.  One block per row.
 template <typename OutT>
-__global__ void rmsnorm_kernel(const float* __restrict__ x, long long x_gs, const float* __restrict__ gain,
-                               long long gain_gs, OutT* __restrict__ out, long long out_gs, int d,
+__device__ __forceinline__ void rmsnorm_kernel_block(const uint3 bid, const float* x, long long x_gs, const float* gain,
+                               long long gain_gs, OutT* out, long long out_gs, int d,
                                float eps, int g_first) {
   __shared__ float red[32];
-  const int l = g_first + blockIdx.y;
-  const float* xr = x + l * x_gs + (long long)blockIdx.x * d;
+  const int l = g_first + bid.y;
+  const float* xr = x + l * x_gs + (long long)bid.x * d;
   float ss = 0.f;
   for (int i = threadIdx.x; i < d; i += blockDim.x) ss += xr[i] * xr[i];
   ss = block_sum(ss, red);
   const float inv = 1.0f / sqrtf(ss / (float)d + eps);
   const float* g = gain + l * gain_gs;
-  OutT* o = out + l * out_gs + (long long)blockIdx.x * d;
+  OutT* o = out + l * out_gs + (long long)bid.x * d;
   for (int i = threadIdx.x; i < d; i += blockDim.x) st_from_f32(o + i, xr[i] * inv * g[i]);
+}
+
+template <typename OutT>
+__global__ void rmsnorm_kernel(const float* __restrict__ x, long long x_gs, const float* __restrict__ gain,
+                               long long gain_gs, OutT* __restrict__ out, long long out_gs, int d,
+                               float eps, int g_first) {
+  rmsnorm_kernel_block<OutT>(blockIdx, x, x_gs, gain, gain_gs, out, out_gs, d, eps, g_first);
 }
 
 // ----------------------------------------------- associative read side --
@@ -82,12 +97,12 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, long long x_gs, cons
 // rows are nb cells of cell_rows rows; cell b of layer l reads the
 // normaliser z[l * nb + b].
 template <typename PhiT>
-__global__ void assoc_phi_kernel(const float* __restrict__ q, const float* __restrict__ z,
-                                 PhiT* __restrict__ phi, float* __restrict__ den, int rows, int k,
+__device__ __forceinline__ void assoc_phi_kernel_block(const uint3 bid, const float* q, const float* z,
+                                 PhiT* phi, float* den, int rows, int k,
                                  int nu, float eps, int g_first, int cell_rows, int nb) {
   extern __shared__ float r[];  // 2k
   __shared__ float red[32];
-  const int l = g_first + blockIdx.y, row = blockIdx.x;
+  const int l = g_first + bid.y, row = bid.x;
   const int k2 = 2 * k, P = k2 * nu;
   const float* qr = q + ((long long)l * rows + row) * k;
   for (int i = threadIdx.x; i < k; i += blockDim.x) {
@@ -111,6 +126,13 @@ __global__ void assoc_phi_kernel(const float* __restrict__ q, const float* __res
   if (threadIdx.x == 0) den[(long long)l * rows + row] = acc + eps;
 }
 
+template <typename PhiT>
+__global__ void assoc_phi_kernel(const float* __restrict__ q, const float* __restrict__ z,
+                                 PhiT* __restrict__ phi, float* __restrict__ den, int rows, int k,
+                                 int nu, float eps, int g_first, int cell_rows, int nb) {
+  assoc_phi_kernel_block<PhiT>(blockIdx, q, z, phi, den, rows, k, nu, eps, g_first, cell_rows, nb);
+}
+
 // ---------------------------------------------- associative write side --
 
 // Per layer (one block), memory tokens i = 0..M-1 in order:
@@ -125,13 +147,13 @@ __global__ void assoc_phi_kernel(const float* __restrict__ q, const float* __res
 // vkb[l][i] = [v_i (d) | k_i (k) | beta logit | pad] (row stride nw), the
 // output of the memory-row projection GEMM.  Index arithmetic uses no
 // division: a warp takes one token, its lanes the feature columns.  M <= 32.
-__global__ void __launch_bounds__(256) assoc_write_feat_kernel(
-    const float* __restrict__ vkb, float* __restrict__ z, float* __restrict__ phiM,
-    float* __restrict__ coef, int M, int k, int nu, float eps, int d, int nw, int g_first) {
+__device__ __forceinline__ void assoc_write_feat_kernel_block(const uint3 bid,
+    const float* vkb, float* z, float* phiM,
+    float* coef, int M, int k, int nu, float eps, int d, int nw, int g_first) {
   extern __shared__ float sm[];  // r: M * 2k, phi: M * (P + 1), z0: P
   __shared__ float G[32][33];
   __shared__ float z0phi[32], gam[32], logit[32];
-  const int l = g_first + blockIdx.x;
+  const int l = g_first + bid.x;
   const int k2 = 2 * k, P = k2 * nu, Pp = P + 1;
   float* r = sm;
   float* ph = sm + M * k2;
@@ -207,6 +229,12 @@ __global__ void __launch_bounds__(256) assoc_write_feat_kernel(
   }
 }
 
+__global__ void __launch_bounds__(256) assoc_write_feat_kernel(
+    const float* __restrict__ vkb, float* __restrict__ z, float* __restrict__ phiM,
+    float* __restrict__ coef, int M, int k, int nu, float eps, int d, int nw, int g_first) {
+  assoc_write_feat_kernel_block(blockIdx, vkb, z, phiM, coef, M, k, nu, eps, d, nw, g_first);
+}
+
 // Delta-rule update of the rows of A_l, memory tokens applied in order.
 // Row j of A only ever needs row j of the values, so each warp keeps rows of
 // A in registers (lane owns entries lane + 32 t, t < NT = P / 32) and runs,
@@ -219,20 +247,20 @@ __global__ void __launch_bounds__(256) assoc_write_feat_kernel(
 // GEMM operand) when Aa != A, and with aa_lo_off != 0 (split precision) its
 // bf16 low part at Aa + aa_lo_off.  M <= 32.
 template <typename AT, int NT>
-__global__ void __launch_bounds__(128) assoc_write_update_kernel(
-    const float* __restrict__ vkb, int nw, const float* __restrict__ phiM,
-    const float* __restrict__ coef, float* __restrict__ A, AT* __restrict__ Aa, int M, int d,
-    int rows_per_block, int g_first, long long aa_lo_off = 0) {
+__device__ __forceinline__ void assoc_write_update_kernel_block(const uint3 bid,
+    const float* vkb, int nw, const float* phiM,
+    const float* coef, float* A, AT* Aa, int M, int d,
+    int rows_per_block, int g_first, long long aa_lo_off) {
   constexpr int P = 32 * NT;
   extern __shared__ float sm[];
   float* ps = sm;                 // [M][P]
   float* cs = ps + M * P;         // [M][2]
-  const int l = g_first + blockIdx.y;
+  const int l = g_first + bid.y;
   for (int t = threadIdx.x; t < M * P; t += blockDim.x) ps[t] = phiM[(long long)l * M * P + t];
   for (int t = threadIdx.x; t < 2 * M; t += blockDim.x) cs[t] = coef[(long long)l * M * 2 + t];
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw_ = blockDim.x >> 5;
-  const int j0 = blockIdx.x * rows_per_block;
+  const int j0 = bid.x * rows_per_block;
   float* Al = A + (long long)l * d * P;
   AT* Aal = Aa + (long long)l * d * P;
   const float* vl = vkb + (long long)l * M * nw;
@@ -292,6 +320,14 @@ __global__ void __launch_bounds__(128) assoc_write_update_kernel(
   }
 }
 
+template <typename AT, int NT>
+__global__ void __launch_bounds__(128) assoc_write_update_kernel(
+    const float* __restrict__ vkb, int nw, const float* __restrict__ phiM,
+    const float* __restrict__ coef, float* __restrict__ A, AT* __restrict__ Aa, int M, int d,
+    int rows_per_block, int g_first, long long aa_lo_off = 0) {
+  assoc_write_update_kernel_block<AT, NT>(blockIdx, vkb, nw, phiM, coef, A, Aa, M, d, rows_per_block, g_first, aa_lo_off);
+}
+
 // State copy in the activation dtype: Aa = A (all layers); with lo_off != 0
 // (split precision) also the bf16 low part at Aa + lo_off.
 template <typename AT>
@@ -312,15 +348,15 @@ __global__ void convert_state_kernel(const float* __restrict__ A, AT* __restrict
 // owning hd/4 dimensions; keys processed in tiles of 64 with an online
 // softmax.  Grid (ceil(rows/64), Hq, layers).
 template <typename T, int HD>
-__global__ void __launch_bounds__(256) attn_simt_kernel(const T* __restrict__ qkv, T* __restrict__ out,
+__device__ __forceinline__ void attn_simt_kernel_block(const uint3 bid, const T* qkv, T* out,
                                                         int rows, int Hq, int Hkv, float scale,
                                                         int g_first) {
   constexpr int DPT = HD / 4;  // dims per thread
   extern __shared__ float kv[];  // K tile [64][HD], V tile [64][HD]
   float* Ks = kv;
   float* Vs = kv + 64 * HD;
-  const int l = g_first + blockIdx.z, h = blockIdx.y, kvh = (h * Hkv) / Hq;
-  const int qi = blockIdx.x * 64 + (threadIdx.x >> 2), part = threadIdx.x & 3;
+  const int l = g_first + bid.z, h = bid.y, kvh = (h * Hkv) / Hq;
+  const int qi = bid.x * 64 + (threadIdx.x >> 2), part = threadIdx.x & 3;
   const int ncols = (Hq + 2 * Hkv) * HD;
   const T* base = qkv + (long long)l * rows * ncols;
   float q[DPT], o[DPT];
@@ -331,7 +367,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const T* __restrict__ qk
     o[e] = 0.f;
   }
   float m = -INFINITY, lsum = 0.f;
-  const int q_last = min(blockIdx.x * 64 + 63, rows - 1);
+  const int q_last = min(bid.x * 64 + 63, rows - 1);
   for (int k0 = 0; k0 <= q_last; k0 += 64) {
     __syncthreads();
     for (int t = threadIdx.x; t < 64 * HD; t += blockDim.x) {
@@ -381,6 +417,13 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const T* __restrict__ qk
   }
 }
 
+template <typename T, int HD>
+__global__ void __launch_bounds__(256) attn_simt_kernel(const T* __restrict__ qkv, T* __restrict__ out,
+                                                        int rows, int Hq, int Hkv, float scale,
+                                                        int g_first) {
+  attn_simt_kernel_block<T, HD>(blockIdx, qkv, out, rows, Hq, Hkv, scale, g_first);
+}
+
 // --------------------------------------------------- fp32 SIMT GEMM ----
 
 // C[l] = A[l] * B[l / b_div]^T, fp32, for l = g_first + blockIdx.z.  A
@@ -390,19 +433,19 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const T* __restrict__ qk
 struct SimtAMap {
   int row0, a_slot_off, b_div, alt_lo, alt_hi, alt_row0;
 };
-__global__ void __launch_bounds__(256) gemm_simt_f32_kernel(const float* __restrict__ A, long long a_gs,
-                                                            int lda, const float* __restrict__ B,
-                                                            long long b_gs, float* __restrict__ C,
+__device__ __forceinline__ void gemm_simt_f32_kernel_block(const uint3 bid, const float* A, long long a_gs,
+                                                            int lda, const float* B,
+                                                            long long b_gs, float* C,
                                                             long long c_gs, int ldc, int rows, int N,
                                                             int K, int g_first, SimtAMap am) {
   __shared__ float As[16][64 + 4];
   __shared__ float Bs[16][64 + 4];
-  const int l = g_first + blockIdx.z;
+  const int l = g_first + bid.z;
   const int r0 = (l >= am.alt_lo && l < am.alt_hi) ? am.alt_row0 : am.row0;
   const float* Al = A + (l + am.a_slot_off) * a_gs + (long long)r0 * lda;
   const float* Bl = B + (l / am.b_div) * b_gs;
   float* Cl = C + l * c_gs;
-  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const int m0 = bid.y * 64, n0 = bid.x * 64;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   float acc[4][4] = {};
   for (int k0 = 0; k0 < K; k0 += 16) {
@@ -437,18 +480,32 @@ __global__ void __launch_bounds__(256) gemm_simt_f32_kernel(const float* __restr
     }
 }
 
+__global__ void __launch_bounds__(256) gemm_simt_f32_kernel(const float* __restrict__ A, long long a_gs,
+                                                            int lda, const float* __restrict__ B,
+                                                            long long b_gs, float* __restrict__ C,
+                                                            long long c_gs, int ldc, int rows, int N,
+                                                            int K, int g_first, SimtAMap am) {
+  gemm_simt_f32_kernel_block(blockIdx, A, a_gs, lda, B, b_gs, C, c_gs, ldc, rows, N, K, g_first, am);
+}
+
 // Applies an epilogue functor to raw fp32 GEMM output rows (the fp32 path's
 // counterpart of the tensor-core epilogue warps).  Grid (rows, layers).
 template <class Epi>
-__global__ void epi_rows_kernel(const float* __restrict__ C, long long c_gs, int ldc, int N,
+__device__ __forceinline__ void epi_rows_kernel_block(const uint3 bid, const float* C, long long c_gs, int ldc, int N,
                                 int g_first, Epi epi) {
-  const int l = g_first + blockIdx.y, row = blockIdx.x;
+  const int l = g_first + bid.y, row = bid.x;
   const float* cr = C + l * c_gs + (long long)row * ldc;
   // N must be a multiple of Epi::GROUP (checked when the model is created)
   for (int grp = threadIdx.x; grp < N / Epi::GROUP; grp += blockDim.x) {
     PtrSrc src{cr + grp * Epi::GROUP};
     epi(l, row, true, grp * Epi::GROUP, Epi::GROUP, src);
   }
+}
+
+template <class Epi>
+__global__ void epi_rows_kernel(const float* __restrict__ C, long long c_gs, int ldc, int N,
+                                int g_first, Epi epi) {
+  epi_rows_kernel_block<Epi>(blockIdx, C, c_gs, ldc, N, g_first, epi);
 }
 
 }  // namespace armt

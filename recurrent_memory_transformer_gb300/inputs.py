@@ -166,6 +166,17 @@ def make_weights(cfg: ArmtConfig, seed: int, std: float = 0.02,
     return w
 
 
+def weight_shapes(cfg: ArmtConfig) -> Dict[str, tuple]:
+    """Shape of every weight array, in draw order (linear maps stored (out, in))."""
+    L, d, hd, F = cfg.n_layers, cfg.d_model, cfg.head_dim, cfg.ffn_dim
+    return {"embed": (cfg.vocab, d), "mem": (cfg.n_mem, d),
+            "wq": (L, cfg.n_q_heads * hd, d), "wk": (L, cfg.n_kv_heads * hd, d),
+            "wv": (L, cfg.n_kv_heads * hd, d), "wo": (L, d, cfg.n_q_heads * hd),
+            "w_gate": (L, F, d), "w_up": (L, F, d), "w_down": (L, d, F),
+            "a_wq": (L, cfg.key_dim, d), "a_wk": (L, cfg.key_dim, d), "a_wv": (L, d, d),
+            "a_wbeta": (L, d), "norm1": (L, d), "norm2": (L, d), "norm_f": (d,)}
+
+
 def make_weights_device(cfg: ArmtConfig, seed: int, std: float = 0.02, device="cuda"):
     """Random-init weights drawn on the GPU, for shapes too large to draw on the host.
 
@@ -185,13 +196,8 @@ def make_weights_device(cfg: ArmtConfig, seed: int, std: float = 0.02, device="c
         a.mul_(std)
         return a.to(dt)
 
-    shapes = (("embed", (cfg.vocab, d)), ("mem", (cfg.n_mem, d)),
-              ("wq", (L, cfg.n_q_heads * hd, d)), ("wk", (L, cfg.n_kv_heads * hd, d)),
-              ("wv", (L, cfg.n_kv_heads * hd, d)), ("wo", (L, d, cfg.n_q_heads * hd)),
-              ("w_gate", (L, F, d)), ("w_up", (L, F, d)), ("w_down", (L, d, F)),
-              ("a_wq", (L, cfg.key_dim, d)), ("a_wk", (L, cfg.key_dim, d)), ("a_wv", (L, d, d)),
-              ("a_wbeta", (L, d)))
-    w = {k: normal(*shape) for k, shape in shapes}
+    shapes = weight_shapes(cfg)
+    w = {k: normal(*shapes[k]) for k in shapes if not k.startswith("norm")}
     w["norm1"] = torch.ones((L, d), device=device, dtype=dt)
     w["norm2"] = torch.ones((L, d), device=device, dtype=dt)
     w["norm_f"] = torch.ones((d,), device=device, dtype=dt)
