@@ -8,6 +8,7 @@ inputs already resident in HBM.  Prints one JSON line (rank 0).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ours|reference] [--no-seq] [--no-cpu] [--no-e2e]
                   [--no-full] [--no-microbatch] [--no-split] [--no-wavefront]
+                  [--no-backward]
 
 Inside the timed region only the roofline kernel (the gate-up GEMM) carries
 per-launch CUDA events; the per-kernel-class table comes from one more forward
@@ -15,8 +16,9 @@ after it.  Besides the timed forward the line reports the sequential schedule,
 the uniform-load bound, the LM head, the full-attention LLaMA on the same
 weights, diagonal batching vs micro-batching, the split-precision mode
 (activations as bf16 high + low parts), the persistent wavefront schedule
-against per-diagonal launches on an fp32 model, the end-to-end host-buffer
-path, device memory, and the oracle on the host cores.
+against per-diagonal launches on an fp32 model, the backward pass on the same
+fp32 model, the end-to-end host-buffer path, device memory, and the oracle on
+the host cores.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
 sample of the same workload (one segment through every layer per step).
@@ -60,6 +62,8 @@ def parse():
                    help="skip the diagonal-batching vs micro-batching comparison")
     p.add_argument("--no-split", action="store_true",
                    help="skip the split-precision (bf16 high + low activations) forward")
+    p.add_argument("--no-backward", action="store_true",
+                   help="skip the backward-pass timing (fp32 model)")
     p.add_argument("--no-wavefront", action="store_true",
                    help="skip the persistent-wavefront comparison (fp32 model)")
     return p.parse_args()
@@ -472,6 +476,67 @@ def main():
         del model_w
         torch.cuda.empty_cache()
 
+    # ---- backward pass over reverse diagonals (fp32 model) ----------------
+    # armt_backward runs a forward that keeps each cell's inputs and entry
+    # state, then the adjoint over the anti-diagonals in reverse (recompute,
+    # write, block and read adjoints; all cells of a diagonal per launch).
+    # fp32 products on the CUDA cores: the roofline is the fp32 FMA rate,
+    # 152 SMs x 128 lanes x 2 FLOP x the sampled SM clock.
+    backward = None
+    if not args.no_backward:
+        small = dataclasses.replace(I.ARMT_1B, n_layers=4, d_model=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                                    ffn_dim=512, vocab=1000, seg_len=64, dtype="f32")
+        mid = dataclasses.replace(I.ARMT_1B, n_layers=4, d_model=1024, n_q_heads=16, n_kv_heads=4, head_dim=64,
+                                  ffn_dim=4096, vocab=4096, seg_len=512, dtype="f32")
+        backward = {"workloads": {
+            "small": "fp32 ARMT, 4 layers, d 256, 4/2 heads of 64, F 512, 64 + 16 rows per cell",
+            "mid": "fp32 ARMT, 4 layers, d 1024, 16/4 heads of 64, F 4096, 512 + 16 rows per cell"},
+            "runs": []}
+        for wl, cfg_b, n_b in (("small", small, 8), ("small", small, 64), ("mid", mid, 8)):
+            model_b = B.Model(cfg_b, I.make_weights(cfg_b, 8))
+            tb = torch.from_numpy(I.make_tokens(cfg_b, n_b, 8)).cuda()
+            rng_b = torch.Generator(device="cuda")
+            rng_b.manual_seed(8)
+            cot_h = torch.randn((tb.numel(), cfg_b.d_model), generator=rng_b, device="cuda")
+            model_b.backward(tb, cot_hidden=cot_h)           # sizes the workspace
+            hb = torch.empty((1, tb.numel(), cfg_b.d_model), dtype=torch.float32, device="cuda")
+            Ab = torch.empty((cfg_b.n_layers, 1, model_b.a_elems // cfg_b.n_layers), dtype=torch.float32,
+                             device="cuda")
+            zb = torch.empty((cfg_b.n_layers, 1, model_b.z_elems // cfg_b.n_layers), dtype=torch.float32,
+                             device="cuda")
+            shapes_b = I.weight_shapes(cfg_b)
+            grads_b = {k: torch.empty(shapes_b[k], dtype=torch.float32, device="cuda") for k in shapes_b}
+            row = {"workload": wl, "segments": n_b, "tokens": tb.numel()}
+            for name in ("forward", "backward"):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record(stream)
+                for _ in range(3):
+                    if name == "forward":
+                        model_b.armt_forward_batch(tb.view(1, -1), hb, Ab, zb, 0, B.SCHEDULE_DIAGONAL, stream)
+                    else:
+                        model_b.armt_backward(tb, grads_b, cot_hidden=cot_h, stream=stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                model_b.armt_sync_status()
+                row[name + "_ms"] = e0.elapsed_time(e1) / 3
+            launches_b, flops_b, ws_b = model_b.armt_backward_stats()
+            adj_ms = row["backward_ms"] - row["forward_ms"]
+            row.update({"backward_includes_forward": True, "adjoint_ms": adj_ms,
+                        "adjoint_launches": launches_b, "adjoint_gflop": flops_b / 1e9,
+                        "adjoint_tflops": flops_b / (adj_ms * 1e-3) / 1e12,
+                        "tokens_per_s": tb.numel() / (row["backward_ms"] * 1e-3),
+                        "workspace_bytes": ws_b})
+            backward["runs"].append(row)
+            model_b.close()
+            del model_b, grads_b
+            torch.cuda.empty_cache()
+        # fp32 FMA peak from the unit counts and the SM clock sampled in the timed region
+        mhz = (clocks or {}).get("sm_mhz") or 2070.0
+        backward["fp32_fma_peak_tflops"] = 152 * 128 * 2 * mhz * 1e6 / 1e12
+        for row in backward["runs"]:
+            row["adjoint_frac_of_fp32_peak"] = row["adjoint_tflops"] / backward["fp32_fma_peak_tflops"]
+
     # ---- end to end through the host-buffer entry point ------------------
     e2e = None
     if not args.no_e2e:
@@ -540,6 +605,7 @@ def main():
             "microbatch": microbatch,
             "split_precision": split,
             "wavefront": wavefront,
+            "backward": backward,
             "memory": memory,
             "e2e": e2e,
             "cpu_baseline": cpu,

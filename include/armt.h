@@ -402,9 +402,13 @@ ARMT_API armt_status armt_backward(armt_model* m, const int32_t* tokens, int64_t
                                    float* mem_A_out, float* mem_z_out, const armt_grads* grads,
                                    void* stream);
 
-/* Kernel launches of the last armt_backward (its forward not included) and
- * the bytes of its workspace. */
-ARMT_API armt_status armt_backward_stats(const armt_model* m, int64_t* launches, int64_t* workspace_bytes);
+/* Of the last armt_backward (its forward not included): kernel launches and
+ * the algorithmic FLOPs of its products and attention (recompute included:
+ * 2 M N K per product, 2 T (T + 1) hd per head for the causal attention
+ * recompute and 7 T (T + 1) hd for its adjoint); and the bytes of the
+ * backward's workspace.  Any output pointer may be NULL. */
+ARMT_API armt_status armt_backward_stats(const armt_model* m, int64_t* launches, int64_t* workspace_bytes,
+                                         double* flops);
 
 /* Sizes of the memory state buffers of one sequence (elements); a batch of
  * B sequences needs B times these. */

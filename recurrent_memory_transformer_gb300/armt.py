@@ -103,7 +103,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.armt_block_sync_status.argtypes = [P]
     lib.armt_noalloc_sync_status.argtypes = [P]
     lib.armt_backward.argtypes = [P, P, I64, P, P, P, P, P, P, P, P, ctypes.POINTER(armt_grads), P]
-    lib.armt_backward_stats.argtypes = [P, ctypes.POINTER(I64), ctypes.POINTER(I64)]
+    lib.armt_backward_stats.argtypes = [P, ctypes.POINTER(I64), ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double)]
     for name in EXPORTED:
         getattr(lib, name).restype = S
     lib.armt_status_string.restype = ctypes.c_char_p
@@ -273,10 +273,11 @@ class Model:
                                   opt(mem_z_out), ctypes.byref(g), _stream_ptr(stream)), "armt_backward")
 
     def armt_backward_stats(self):
-        """(kernel launches of the last backward, backward workspace bytes)."""
-        a, b = ctypes.c_int64(), ctypes.c_int64()
-        _check(_lib.armt_backward_stats(self._h, ctypes.byref(a), ctypes.byref(b)), "armt_backward_stats")
-        return a.value, b.value
+        """(kernel launches, algorithmic FLOPs) of the last backward, and its workspace bytes."""
+        a, b, f = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_double()
+        _check(_lib.armt_backward_stats(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(f)),
+               "armt_backward_stats")
+        return a.value, f.value, b.value
 
     def backward(self, tokens, cot_hidden=None, cot_A=None, cot_z=None, mem_A0=None, mem_z0=None,
                  state_grads=False, stream=None):

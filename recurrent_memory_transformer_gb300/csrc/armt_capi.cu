@@ -216,6 +216,7 @@ struct ModelBase {
                                float* A, float* z, const armt_grads& g, cudaStream_t st) = 0;
   virtual long long backward_workspace_bytes() const = 0;
   long long bw_launches = 0;  // kernel launches of the last backward
+  double bw_flops = 0;        // and its algorithmic FLOPs (products and attention)
 
   int rows() const { return cfg.seg_len + cfg.n_mem; }
 
@@ -1164,6 +1165,8 @@ struct Model : ModelBase {
       CKS(A(&v.Sz[q], L * P));
     }
     CKS(A(&v.XB0, n * Td));
+    v.part_cap = (long long)1 << 22;  // 16 MB of split-K partial products
+    CKS(A(&v.Part, (size_t)v.part_cap));
     CKS(A(&v.dWqkv, L * Nq * d));
     CKS(A(&v.dWgu, L * 2 * F * d));
     CKS(A(&v.dWw, L * nw * d));
@@ -1261,6 +1264,7 @@ struct Model : ModelBase {
       v.cosT = w1.cosT;
       v.sinT = w1.sinT;
       v.cot_h = cot_h;
+      v.num_sms = num_sms;
       // gradients accumulate from zero: the unfused ones in the caller's buffers
       v.dWo = gr.wo;
       v.dWd = gr.w_down;
@@ -1328,6 +1332,7 @@ struct Model : ModelBase {
       CK(cudaMemcpy2DAsync(gr.a_wbeta, (size_t)d * es, v.dWw + (size_t)(d + k) * d, (size_t)nw * d * es,
                            (size_t)d * es, L, cudaMemcpyDeviceToDevice, st));
       bw_launches = run.launches;
+      bw_flops = run.flops;
       return ARMT_OK;
     }
   }
@@ -1620,10 +1625,11 @@ armt_status armt_backward(armt_model* m, const int32_t* tokens, int64_t n_tokens
                            mem_z_out, *grads, reinterpret_cast<cudaStream_t>(stream));
 }
 
-armt_status armt_backward_stats(const armt_model* m, int64_t* launches, int64_t* workspace_bytes) {
-  if (m == nullptr || launches == nullptr || workspace_bytes == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
-  *launches = m->impl->bw_launches;
-  *workspace_bytes = m->impl->backward_workspace_bytes();
+armt_status armt_backward_stats(const armt_model* m, int64_t* launches, int64_t* workspace_bytes, double* flops) {
+  if (m == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
+  if (launches != nullptr) *launches = m->impl->bw_launches;
+  if (workspace_bytes != nullptr) *workspace_bytes = m->impl->backward_workspace_bytes();
+  if (flops != nullptr) *flops = m->impl->bw_flops;
   return ARMT_OK;
 }
 

@@ -58,7 +58,10 @@ struct BwMat {
 
 // C = E + alpha * rs[r] * sum_k A(r, k) B(k, c) for every cell of a
 // diagonal; E may be C itself (accumulate) or absent (E.m.p == nullptr);
-// rs absent: 1; rs_div: the row factor divides instead.
+// rs absent: 1; rs_div: the row factor divides instead.  ksplit > 1: the K
+// range is cut into ksplit chunks of kchunk (a multiple of 16); each chunk's
+// raw product goes to part[(kz * groups + cell)][M][N] and bw_gemm_reduce
+// sums the chunks in order and applies the epilogue (deterministic).
 struct BwGemm {
   BwMat A, B, C, E;
   CellPtr rs;
@@ -67,73 +70,111 @@ struct BwGemm {
   int M = 0, N = 0, K = 0;
   int l0 = 0;
   long long s0 = 0;
+  int groups = 1, ksplit = 1, kchunk = 0;
+  float* part = nullptr;
 };
 
+// One thread's share of a 64 x 16 A tile and a 16 x 64 B tile: element q of
+// the thread is e = tid + 256 q, laid out along the operand's contiguous
+// dimension.
+__device__ __forceinline__ void bw_tile_index(int e, int trans_a, int trans_b, int& ia, int& ka, int& jb, int& kb) {
+  if (trans_a) {
+    ia = e & 63;
+    ka = e >> 6;
+  } else {
+    ka = e & 15;
+    ia = e >> 4;
+  }
+  if (trans_b) {
+    kb = e & 15;
+    jb = e >> 4;
+  } else {
+    jb = e & 63;
+    kb = e >> 6;
+  }
+}
+
 // 64 x 64 output tile per 256-thread block, 4 x 4 per thread, K in steps of
-// 16 through shared memory.  Each operand tile is loaded along its
-// contiguous dimension (the trans flag is uniform over the launch).
+// 16 through two shared-memory buffers: the next step's operands are loaded
+// into registers while the current step computes.
 __global__ void __launch_bounds__(256) bw_gemm_kernel(const BwGemm g) {
-  __shared__ float As[16][64 + 4];
-  __shared__ float Bs[16][64 + 4];
-  const int z = blockIdx.z, l = g.l0 + z;
-  const long long s = g.s0 - z;
+  __shared__ float As[2][16][64 + 4];
+  __shared__ float Bs[2][16][64 + 4];
+  const int cell = blockIdx.z % g.groups, kz = blockIdx.z / g.groups;
+  const int l = g.l0 + cell;
+  const long long s = g.s0 - cell;
   const float* A = g.A.m.at(l, s);
   const float* B = g.B.m.at(l, s);
   const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int kbeg = g.ksplit > 1 ? kz * g.kchunk : 0;
+  const int kend = g.ksplit > 1 ? min(g.K, kbeg + g.kchunk) : g.K;
   float acc[4][4];
 #pragma unroll
   for (int u = 0; u < 4; ++u)
 #pragma unroll
     for (int v = 0; v < 4; ++v) acc[u][v] = 0.f;
-  for (int k0 = 0; k0 < g.K; k0 += 16) {
+  float ra[4], rb[4];
+  auto load = [&](int k0) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const int e = threadIdx.x + 256 * q;
-      int ii, kk;
-      if (g.A.trans) {
-        ii = e & 63;
-        kk = e >> 6;
-      } else {
-        kk = e & 15;
-        ii = e >> 4;
-      }
-      {
-        const int r = i0 + ii, c = k0 + kk;
-        float v = 0.f;
-        if (r < g.M && c < g.K) v = g.A.trans ? A[(long long)c * g.A.ld + r] : A[(long long)r * g.A.ld + c];
-        As[kk][ii] = v;
-      }
-      int jj;
-      if (g.B.trans) {
-        kk = e & 15;
-        jj = e >> 4;
-      } else {
-        jj = e & 63;
-        kk = e >> 6;
-      }
-      {
-        const int c = j0 + jj, r = k0 + kk;
-        float v = 0.f;
-        if (c < g.N && r < g.K) v = g.B.trans ? B[(long long)c * g.B.ld + r] : B[(long long)r * g.B.ld + c];
-        Bs[kk][jj] = v;
-      }
+      int ia, ka, jb, kb;
+      bw_tile_index(threadIdx.x + 256 * q, g.A.trans, g.B.trans, ia, ka, jb, kb);
+      const int r = i0 + ia, c = k0 + ka;
+      ra[q] = (r < g.M && c < kend) ? (g.A.trans ? A[(long long)c * g.A.ld + r] : A[(long long)r * g.A.ld + c]) : 0.f;
+      const int cb = j0 + jb, rk = k0 + kb;
+      rb[q] = (cb < g.N && rk < kend) ? (g.B.trans ? B[(long long)cb * g.B.ld + rk] : B[(long long)rk * g.B.ld + cb])
+                                      : 0.f;
     }
-    __syncthreads();
+  };
+  auto stash = [&](int buf) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      int ia, ka, jb, kb;
+      bw_tile_index(threadIdx.x + 256 * q, g.A.trans, g.B.trans, ia, ka, jb, kb);
+      As[buf][ka][ia] = ra[q];
+      Bs[buf][kb][jb] = rb[q];
+    }
+  };
+  int buf = 0;
+  if (kbeg < kend) {
+    load(kbeg);
+    stash(0);
+  }
+  __syncthreads();
+  for (int k0 = kbeg; k0 < kend; k0 += 16) {
+    const bool more = k0 + 16 < kend;
+    if (more) load(k0 + 16);
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
       float a[4], b[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        a[u] = As[kk][ty * 4 + u];
-        b[u] = Bs[kk][tx * 4 + u];
+        a[u] = As[buf][kk][ty * 4 + u];
+        b[u] = Bs[buf][kk][tx * 4 + u];
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u)
 #pragma unroll
         for (int v = 0; v < 4; ++v) acc[u][v] += a[u] * b[v];
     }
+    if (more) stash(buf ^ 1);
     __syncthreads();
+    buf ^= 1;
+  }
+  if (g.ksplit > 1) {
+    float* pt = g.part + ((long long)kz * g.groups + cell) * g.M * g.N;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = i0 + ty * 4 + u;
+      if (r >= g.M) continue;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int c = j0 + tx * 4 + v;
+        if (c < g.N) pt[(long long)r * g.N + c] = acc[u][v];
+      }
+    }
+    return;
   }
   float* C = g.C.m.at(l, s);
   const float* E = g.E.m.p != nullptr ? g.E.m.at(l, s) : nullptr;
@@ -153,6 +194,26 @@ __global__ void __launch_bounds__(256) bw_gemm_kernel(const BwGemm g) {
       C[(long long)r * g.C.ld + c] = val;
     }
   }
+}
+
+// The split-K epilogue: C = E + alpha rs[r] sum_kz part[kz], chunks in order.
+__global__ void bw_gemm_reduce_kernel(const BwGemm g) {
+  const int cell = blockIdx.y, l = g.l0 + cell;
+  const long long s = g.s0 - cell;
+  const long long mn = (long long)g.M * g.N;
+  const long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (idx >= mn) return;
+  const int r = (int)(idx / g.N), c = (int)(idx - (long long)r * g.N);
+  float acc = 0.f;
+  for (int kz = 0; kz < g.ksplit; ++kz) acc += g.part[((long long)kz * g.groups + cell) * mn + idx];
+  float f = g.alpha;
+  if (g.rs.p != nullptr) {
+    const float rv = g.rs.at(l, s)[r];
+    f = g.rs_div ? f / rv : f * rv;
+  }
+  float val = f * acc;
+  if (g.E.m.p != nullptr) val += g.E.m.at(l, s)[(long long)r * g.E.ld + c];
+  g.C.m.at(l, s)[(long long)r * g.C.ld + c] = val;
 }
 
 // ------------------------------------------------------ row kernels --
@@ -317,21 +378,31 @@ __global__ void bw_rmsnorm_bwd_rows_kernel(CellPtr X, CellPtr G, CellPtr Ybar, l
   if (threadIdx.x == 0) Srow.at(l, s)[row] = sc;
 }
 
-// dg[c] += sum_{r < valid} Ybar[r][c] X[r][c] s[r]: the gain's gradient, in
-// row order (one thread per column).
-__global__ void bw_gain_grad_kernel(CellPtr X, CellPtr Ybar, long long ldy, CellPtr Srow, CellPtr dG, int d,
-                                    int valid, int alt_l, int alt_valid, int l0, long long s0) {
+// dg[c] += sum_{r < valid} Ybar[r][c] X[r][c] s[r]: the gain's gradient.  A
+// block takes 32 columns (one per lane); warp w sums rows w, w + 8, ... and
+// the 8 partial sums are added in warp order (deterministic).  256 threads.
+__global__ void __launch_bounds__(256) bw_gain_grad_kernel(CellPtr X, CellPtr Ybar, long long ldy, CellPtr Srow,
+                                                           CellPtr dG, int d, int valid, int alt_l, int alt_valid,
+                                                           int l0, long long s0) {
+  __shared__ float part[8][32];
   const int l = l0 + blockIdx.y;
   const long long s = s0 - blockIdx.y;
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= d) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + lane;
   const int v = l == alt_l ? alt_valid : valid;
   const float* x = X.at(l, s);
   const float* yb = Ybar.at(l, s);
   const float* sr = Srow.at(l, s);
   float acc = 0.f;
-  for (int r = 0; r < v; ++r) acc += yb[(long long)r * ldy + c] * x[(long long)r * d + c] * sr[r];
-  dG.at(l, s)[c] += acc;
+  if (c < d)
+    for (int r = warp; r < v; r += 8) acc += yb[(long long)r * ldy + c] * x[(long long)r * d + c] * sr[r];
+  part[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0 && c < d) {
+    float t = 0.f;
+    for (int w = 0; w < 8; ++w) t += part[w][lane];
+    dG.at(l, s)[c] += t;
+  }
 }
 
 // RoPE (rotate-half, positions 0 .. T-1 of the cell) on the first n_rope
@@ -747,16 +818,16 @@ __global__ void __launch_bounds__(256) bw_write_feat_kernel(CellPtr VKB, CellPtr
   for (int t = threadIdx.x; t < M * M; t += blockDim.x) gm[t] = G[t / M][t % M];
 }
 
-// Per row j of the state (a warp per row, lanes over the P features):
-// forward over the writes from A_in[j] (c_i[j], vbar_i[j]), then backward
-// from A_bar[j] (c_bar_i[j], w_i[j]), and A_bar_in[j] = A_bar[j] + sum_i w_i[j] phi_i.
-// Stores C, Vb, CB, W as [M][d].
+// Per row j of the state (lanes over the P features; each warp runs RW rows
+// side by side, independent chains): forward over the writes from A_in[j]
+// (c_i[j], vbar_i[j]), then backward from A_bar[j] (c_bar_i[j], w_i[j]), and
+// A_bar_in[j] = A_bar[j] + sum_i w_i[j] phi_i.  Stores C, Vb, CB, W as [M][d].
 template <int NT>
 __global__ void __launch_bounds__(128) bw_write_rows_kernel(CellPtr Ain, CellPtr Abar, CellPtr AbarIn, CellPtr PhiM,
                                                             CellPtr Sc, CellPtr VKB, CellPtr Cw, CellPtr Vb,
                                                             CellPtr CB, CellPtr Wv, int M, int d, int nw,
                                                             int rows_per_block, int l0, long long s0) {
-  constexpr int P = 32 * NT;
+  constexpr int P = 32 * NT, RW = 4;
   extern __shared__ float sm[];
   float* ps = sm;           // [M][P]
   float* cs = ps + M * P;   // [M][WS_NSC]
@@ -774,50 +845,93 @@ __global__ void __launch_bounds__(128) bw_write_rows_kernel(CellPtr Ain, CellPtr
   const float* vkb = VKB.at(l, s);
   float *cw = Cw.at(l, s), *vb = Vb.at(l, s), *cb = CB.at(l, s), *wv = Wv.at(l, s);
   const int j_end = min(d, (int)(blockIdx.x + 1) * rows_per_block);
-  for (int j = blockIdx.x * rows_per_block + warp; j < j_end; j += nwarps) {
-    float a[NT];
+  for (int jb = blockIdx.x * rows_per_block + warp * RW; jb < j_end; jb += nwarps * RW) {
+    float a[RW][NT], vj[RW], my_c[RW], my_vb[RW], my_cb[RW], my_w[RW];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) a[t] = ain[(long long)j * P + lane + 32 * t];
-    const float vj = lane < M ? vkb[(long long)lane * nw + j] : 0.f;  // lane i holds v_i[j]
-    float my_c = 0.f, my_vb = 0.f, my_cb = 0.f, my_w = 0.f;
+    for (int r = 0; r < RW; ++r) {
+      const int j = jb + r;
+      const bool ok = j < j_end;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) a[r][t] = ok ? ain[(long long)j * P + lane + 32 * t] : 0.f;
+      vj[r] = (ok && lane < M) ? vkb[(long long)lane * nw + j] : 0.f;  // lane i holds v_i[j]
+      my_c[r] = my_vb[r] = my_cb[r] = my_w[r] = 0.f;
+    }
     for (int i = 0; i < M; ++i) {
       const float* pi = ps + i * P + lane;
-      float dot = 0.f;
+      float ph[NT];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) dot += a[t] * pi[32 * t];
-      dot = warp_sum(dot);
-      const float vbar = dot / cs[i * WS_NSC + WS_D];
-      const float c = cs[i * WS_NSC + WS_BETA] * (__shfl_sync(0xffffffffu, vj, i) - vbar);
+      for (int t = 0; t < NT; ++t) ph[t] = pi[32 * t];
+      float dot[RW];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) a[t] += c * pi[32 * t];
-      if (lane == i) {
-        my_c = c;
-        my_vb = vbar;
+      for (int r = 0; r < RW; ++r) {
+        dot[r] = 0.f;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) dot[r] += a[r][t] * ph[t];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int r = 0; r < RW; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
+      const float beta = cs[i * WS_NSC + WS_BETA], D = cs[i * WS_NSC + WS_D];
+#pragma unroll
+      for (int r = 0; r < RW; ++r) {
+        const float vbar = dot[r] / D;
+        const float c = beta * (__shfl_sync(0xffffffffu, vj[r], i) - vbar);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) a[r][t] += c * ph[t];
+        if (lane == i) {
+          my_c[r] = c;
+          my_vb[r] = vbar;
+        }
       }
     }
 #pragma unroll
-    for (int t = 0; t < NT; ++t) a[t] = abar[(long long)j * P + lane + 32 * t];
+    for (int r = 0; r < RW; ++r) {
+      const int j = jb + r;
+      const bool ok = j < j_end;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) a[r][t] = ok ? abar[(long long)j * P + lane + 32 * t] : 0.f;
+    }
     for (int i = M - 1; i >= 0; --i) {
       const float* pi = ps + i * P + lane;
-      float dot = 0.f;
+      float ph[NT];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) dot += a[t] * pi[32 * t];
-      dot = warp_sum(dot);
-      const float w = -cs[i * WS_NSC + WS_BETA] * dot / cs[i * WS_NSC + WS_D];
+      for (int t = 0; t < NT; ++t) ph[t] = pi[32 * t];
+      float dot[RW];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) a[t] += w * pi[32 * t];
-      if (lane == i) {
-        my_cb = dot;
-        my_w = w;
+      for (int r = 0; r < RW; ++r) {
+        dot[r] = 0.f;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) dot[r] += a[r][t] * ph[t];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int r = 0; r < RW; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
+      const float beta = cs[i * WS_NSC + WS_BETA], D = cs[i * WS_NSC + WS_D];
+#pragma unroll
+      for (int r = 0; r < RW; ++r) {
+        const float w = -beta * dot[r] / D;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) a[r][t] += w * ph[t];
+        if (lane == i) {
+          my_cb[r] = dot[r];
+          my_w[r] = w;
+        }
       }
     }
 #pragma unroll
-    for (int t = 0; t < NT; ++t) abin[(long long)j * P + lane + 32 * t] = a[t];
-    if (lane < M) {
-      cw[(long long)lane * d + j] = my_c;
-      vb[(long long)lane * d + j] = my_vb;
-      cb[(long long)lane * d + j] = my_cb;
-      wv[(long long)lane * d + j] = my_w;
+    for (int r = 0; r < RW; ++r) {
+      const int j = jb + r;
+      if (j >= j_end) continue;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) abin[(long long)j * P + lane + 32 * t] = a[r][t];
+      if (lane < M) {
+        cw[(long long)lane * d + j] = my_c[r];
+        vb[(long long)lane * d + j] = my_vb[r];
+        cb[(long long)lane * d + j] = my_cb[r];
+        wv[(long long)lane * d + j] = my_w[r];
+      }
     }
   }
 }
@@ -845,30 +959,58 @@ __global__ void __launch_bounds__(256) bw_write_scalars_kernel(CellPtr Cw, CellP
   float* sc = Sc.at(l, s);
   const float* gm = Gm.at(l, s);
   for (int t = threadIdx.x; t < M * M; t += blockDim.x) G[t / M][t % M] = gm[t];
-  for (int t = warp; t < M * M + 3 * M; t += nwarp) {
-    float acc = 0.f;
-    if (t < M * M) {
-      const int j = t / M, i = t - j * M;
-      for (int r = lane; r < d; r += 32) acc += wv[(long long)j * d + r] * cw[(long long)i * d + r];
-      acc = warp_sum(acc);
-      if (lane == 0) X[j][i] = acc;
-    } else if (t < M * M + M) {
-      const int i = t - M * M;
-      for (int r = lane; r < d; r += 32)
-        acc += cb[(long long)i * d + r] * (vkb[(long long)i * nw + r] - vb[(long long)i * d + r]);
-      acc = warp_sum(acc);
-      if (lane == 0) bbar[i] = acc;
-    } else if (t < M * M + 2 * M) {
-      const int i = t - M * M - M;
-      for (int r = lane; r < d; r += 32) acc += wv[(long long)i * d + r] * vb[(long long)i * d + r];
-      acc = warp_sum(acc);
-      if (lane == 0) e[i] = acc;
-    } else {
-      const int i = t - M * M - 2 * M;
-      for (int p = lane; p < P; p += 32) acc += zbar[p] * phiM[(long long)i * P + p];
-      acc = warp_sum(acc);
-      if (lane == 0) zfp[i] = acc;
+  // the dot products over the d rows of the state, 32 rows at a time through
+  // shared memory: thread t owns pairs (j, i) = t, t + 256, ... of X and, for
+  // t < M, b_bar_t and e_t; every sum runs in row order
+  {
+    __shared__ float sW[32][33], sC[32][33], sB[32][33], sE[32][33], sV[32][33];
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, ab = 0.f, ae = 0.f;
+    for (int r0 = 0; r0 < d; r0 += 32) {
+      __syncthreads();
+      for (int e2 = threadIdx.x; e2 < M * 32; e2 += blockDim.x) {
+        const int i = e2 >> 5, c = e2 & 31, r = r0 + c;
+        const bool ok = r < d;
+        const long long o = (long long)i * d + r;
+        sW[i][c] = ok ? wv[o] : 0.f;
+        sC[i][c] = ok ? cw[o] : 0.f;
+        sB[i][c] = ok ? cb[o] : 0.f;
+        sV[i][c] = ok ? vb[o] : 0.f;
+        sE[i][c] = ok ? vkb[(long long)i * nw + r] - vb[o] : 0.f;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int t = threadIdx.x + 256 * q;
+        if (t < M * M) {
+          const int j = t / M, i = t - j * M;
+          float a = acc[q];
+          for (int c = 0; c < 32; ++c) a += sW[j][c] * sC[i][c];
+          acc[q] = a;
+        }
+      }
+      if (threadIdx.x < M) {
+        const int i = threadIdx.x;
+        for (int c = 0; c < 32; ++c) {
+          ab += sB[i][c] * sE[i][c];
+          ae += sW[i][c] * sV[i][c];
+        }
+      }
     }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int t = threadIdx.x + 256 * q;
+      if (t < M * M) X[t / M][t % M] = acc[q];
+    }
+    if (threadIdx.x < M) {
+      bbar[threadIdx.x] = ab;
+      e[threadIdx.x] = ae;
+    }
+  }
+  for (int i = warp; i < M; i += nwarp) {
+    float acc = 0.f;
+    for (int p = lane; p < P; p += 32) acc += zbar[p] * phiM[(long long)i * P + p];
+    acc = warp_sum(acc);
+    if (lane == 0) zfp[i] = acc;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -947,10 +1089,20 @@ __global__ void bw_embed_grad_kernel(const float* XB0, const int32_t* tokens, lo
     const long long t0 = s * S;
     const int n_rows = (int)min((long long)S, n_tok - t0);
     const float* xb = XB0 + s * T * (long long)d;
-    for (int t = 0; t < n_rows; ++t) {
-      int id = tokens[t0 + t];
-      id = id < 0 ? 0 : (id >= vocab ? vocab - 1 : id);
-      dE[(long long)id * d + c] += xb[(long long)t * d + c];
+    // eight rows' loads in flight; the adds stay in row order
+    for (int t = 0; t < n_rows; t += 8) {
+      int id[8];
+      float x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const bool ok = t + u < n_rows;
+        const int v = ok ? tokens[t0 + t + u] : 0;
+        id[u] = v < 0 ? 0 : (v >= vocab ? vocab - 1 : v);
+        x[u] = ok ? xb[(long long)(t + u) * d + c] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (t + u < n_rows) dE[(long long)id[u] * d + c] += x[u];
     }
     for (int i = 0; i < M; ++i) dMem[(long long)i * d + c] += xb[(long long)(n_rows + i) * d + c];
   }

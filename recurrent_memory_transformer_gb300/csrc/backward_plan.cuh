@@ -39,12 +39,17 @@ struct BwView {
   float *Hbar[2], *SA[2], *Sz[2], *XB0;
   // gradient accumulators (fused layouts as the weights)
   float *dWqkv, *dWo, *dWgu, *dWd, *daWq, *dWw, *dg1, *dg2, *dgf;
+  // split-K partial products
+  float* Part;
+  long long part_cap;
+  int num_sms;
 };
 
 struct BwRun {
   const BwView& v;
   cudaStream_t st;
   long long launches = 0;
+  double flops = 0;  // algorithmic FLOPs of the products and of attention
   // the current diagonal
   int l0 = 0, g = 0, alt_l = -1;
   long long s0 = 0;
@@ -80,14 +85,38 @@ struct BwRun {
     p.s0 = s0 - (p.l0 - l0);
     const int groups = gg < 0 ? g : gg;
     if (M == 0 || N == 0 || groups == 0) return ARMT_OK;
-    bw_gemm_kernel<<<dim3((N + 63) / 64, (M + 63) / 64, groups), 256, 0, st>>>(p);
-    return check();
+    flops += 2.0 * M * N * K * groups;
+    p.groups = groups;
+    // too few tiles to fill the SMs and a long K: split K (about two blocks
+    // per SM), partial products to scratch, summed in order by a second kernel
+    const long long tiles = (long long)((N + 63) / 64) * ((M + 63) / 64) * groups;
+    int ks = 1;
+    if (tiles < v.num_sms && K >= 128) {
+      ks = (int)std::min<long long>((2LL * v.num_sms + tiles - 1) / tiles, K / 64);
+      while (ks > 1 && (long long)ks * groups * M * N > v.part_cap) --ks;
+    }
+    if (ks > 1) {
+      p.kchunk = ((K + ks - 1) / ks + 15) / 16 * 16;
+      p.ksplit = (K + p.kchunk - 1) / p.kchunk;
+      p.part = v.Part;
+    }
+    bw_gemm_kernel<<<dim3((N + 63) / 64, (M + 63) / 64, groups * p.ksplit), 256, 0, st>>>(p);
+    CKS(check());
+    if (p.ksplit > 1) {
+      const long long mn = (long long)M * N;
+      bw_gemm_reduce_kernel<<<dim3((unsigned)((mn + 255) / 256), groups), 256, 0, st>>>(p);
+      CKS(check());
+    }
+    return ARMT_OK;
   }
   dim3 rows_grid(int rows) const { return dim3((unsigned)rows, (unsigned)g); }
 
   template <int HD>
   armt_status attention(const BwAttn& a, bool forward) {
     const dim3 grid((v.T + 31) / 32, v.Hq, g);
+    // causal products of T (T + 1) / 2 row pairs over hd: two in the forward
+    // (q k, p v), three for q_bar (q k, o_bar v, s_bar k), four for k_bar and v_bar
+    flops += (forward ? 2.0 : 7.0) * v.T * (v.T + 1.0) * v.hd * v.Hq * g;
     if (forward) {
       bw_attn_fwd_kernel<HD><<<grid, 256, bw_attn_fwd_smem(HD), st>>>(a);
       return check();
@@ -107,7 +136,7 @@ struct BwRun {
 
   template <int NT>
   armt_status write_rows(CellPtr Ain, CellPtr Abar, CellPtr AbarIn) {
-    const int rpb = 32;
+    const int rpb = 16;  // 4 warps x 4 rows
     const size_t smem = ((size_t)v.M * v.P + (size_t)v.M * WS_NSC) * sizeof(float);
     bw_write_rows_kernel<NT><<<dim3((v.d + rpb - 1) / rpb, g), 128, smem, st>>>(
         Ain, Abar, AbarIn, slot(v.PhiM, (long long)v.M * v.P), slot(v.Sc, (long long)v.M * WS_NSC),
@@ -206,7 +235,7 @@ struct BwRun {
         bw_rmsnorm_bwd_rows_kernel<<<dim3(T, 1), 128, 0, st>>>(H, gf, cot, d, none, HB, Srow, d, v.norm_eps, S,
                                                                alt_l, v.last_len, ll, sl);
         CKS(check());
-        bw_gain_grad_kernel<<<dim3((d + 127) / 128, 1), 128, 0, st>>>(H, cot, d, Srow, dgf, d, S, alt_l,
+        bw_gain_grad_kernel<<<dim3((d + 31) / 32, 1), 256, 0, st>>>(H, cot, d, Srow, dgf, d, S, alt_l,
                                                                       v.last_len, ll, sl);
         CKS(check());
       } else {
@@ -283,7 +312,7 @@ struct BwRun {
     bw_rmsnorm_bwd_rows_kernel<<<rows_grid(T), 128, 0, st>>>(Y, g2, N2bar, d, HB, Ybar, Srow, d, v.norm_eps, T,
                                                              -1, 0, l0, s0);
     CKS(check());
-    bw_gain_grad_kernel<<<dim3((d + 127) / 128, g), 128, 0, st>>>(Y, N2bar, d, Srow, slot(v.dg2, d), d, T, -1, 0,
+    bw_gain_grad_kernel<<<dim3((d + 31) / 32, g), 256, 0, st>>>(Y, N2bar, d, Srow, slot(v.dg2, d), d, T, -1, 0,
                                                                   l0, s0);
     CKS(check());
     // y = x1 + att Wo^T
@@ -305,7 +334,7 @@ struct BwRun {
     bw_rmsnorm_bwd_rows_kernel<<<rows_grid(T), 128, 0, st>>>(X1, g1, N1bar, d, Ybar, X1bar, Srow, d, v.norm_eps, T,
                                                              -1, 0, l0, s0);
     CKS(check());
-    bw_gain_grad_kernel<<<dim3((d + 127) / 128, g), 128, 0, st>>>(X1, N1bar, d, Srow, slot(v.dg1, d), d, T, -1, 0,
+    bw_gain_grad_kernel<<<dim3((d + 31) / 32, g), 256, 0, st>>>(X1, N1bar, d, Srow, slot(v.dg1, d), d, T, -1, 0,
                                                                   l0, s0);
     CKS(check());
 

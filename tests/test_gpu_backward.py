@@ -126,8 +126,8 @@ def test_backward_matches_fp64_gradients(name, over, n_seg, short, with_state, p
     torch.cuda.synchronize()
     for k in grads:
         assert torch.equal(grads[k], grads2[k]), k
-    launches, ws = m.armt_backward_stats()
-    assert launches > 0 and ws > 0
+    launches, flops, ws = m.armt_backward_stats()
+    assert launches > 0 and flops > 0 and ws > 0
     m.close()
 
 
