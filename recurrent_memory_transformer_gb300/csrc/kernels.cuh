@@ -246,21 +246,15 @@ __global__ void __launch_bounds__(256) assoc_write_feat_kernel(
 // Also refreshes the activation-dtype copy Aa of the state (the next read's
 // GEMM operand) when Aa != A, and with aa_lo_off != 0 (split precision) its
 // bf16 low part at Aa + aa_lo_off.  M <= 32.
+// The rows [j0, j0 + rows_per_block) of A_l (one block's share), features ps
+// [M][P] and coefficients cs [M][2] = {beta_i, 1 / (zphi_i + eps)} in shared
+// memory.
 template <typename AT, int NT>
-__device__ __forceinline__ void assoc_write_update_kernel_block(const uint3 bid,
-    const float* vkb, int nw, const float* phiM,
-    const float* coef, float* A, AT* Aa, int M, int d,
-    int rows_per_block, int g_first, long long aa_lo_off) {
+__device__ __forceinline__ void assoc_write_rows(const float* ps, const float* cs, const float* vkb, int nw,
+                                                 float* A, AT* Aa, int M, int d, int j0, int rows_per_block, int l,
+                                                 long long aa_lo_off) {
   constexpr int P = 32 * NT;
-  extern __shared__ float sm[];
-  float* ps = sm;                 // [M][P]
-  float* cs = ps + M * P;         // [M][2]
-  const int l = g_first + bid.y;
-  for (int t = threadIdx.x; t < M * P; t += blockDim.x) ps[t] = phiM[(long long)l * M * P + t];
-  for (int t = threadIdx.x; t < 2 * M; t += blockDim.x) cs[t] = coef[(long long)l * M * 2 + t];
-  __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw_ = blockDim.x >> 5;
-  const int j0 = bid.x * rows_per_block;
   float* Al = A + (long long)l * d * P;
   AT* Aal = Aa + (long long)l * d * P;
   const float* vl = vkb + (long long)l * M * nw;
@@ -318,6 +312,31 @@ __device__ __forceinline__ void assoc_write_update_kernel_block(const uint3 bid,
       }
     }
   }
+}
+
+
+template <typename AT, int NT>
+__device__ __forceinline__ void assoc_write_update_kernel_block(const uint3 bid,
+    const float* vkb, int nw, const float* phiM,
+    const float* coef, float* A, AT* Aa, int M, int d,
+    int rows_per_block, int g_first, long long aa_lo_off) {
+  constexpr int P = 32 * NT;
+  extern __shared__ float sm[];
+  float* ps = sm;                 // [M][P]
+  float* cs = ps + M * P;         // [M][2]
+  const int l = g_first + bid.y;
+  // stage the features 16 bytes at a time, four loads in flight per thread
+  // (M * P is a multiple of 96 floats; the rows of phiM start 16-byte aligned)
+  {
+    const float4* src = reinterpret_cast<const float4*>(phiM + (long long)l * M * P);
+    float4* dst = reinterpret_cast<float4*>(ps);
+    const int n4 = M * P / 4;
+#pragma unroll 4
+    for (int t = threadIdx.x; t < n4; t += blockDim.x) dst[t] = src[t];
+  }
+  for (int t = threadIdx.x; t < 2 * M; t += blockDim.x) cs[t] = coef[(long long)l * M * 2 + t];
+  __syncthreads();
+  assoc_write_rows<AT, NT>(ps, cs, vkb, nw, A, Aa, M, d, bid.x * rows_per_block, rows_per_block, l, aa_lo_off);
 }
 
 template <typename AT, int NT>
