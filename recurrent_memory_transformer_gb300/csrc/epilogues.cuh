@@ -202,7 +202,10 @@ struct EpiAssocRead {
 // keeps its values at vt[l * nb + b].
 template <typename OutT>
 struct EpiQkvRope {
-  static constexpr int GROUP = 64;  // callers pass whole heads (ncols a multiple of hd)
+  // 64-column groups: whole heads for hd <= 64; for hd = 128 a group holds
+  // half a head, and the group holding the first half rotates both halves
+  // (the pairs are (i, i + hd/2)) while the other one does nothing
+  static constexpr int GROUP = 64;
   OutT* out;
   const float* cosT;
   const float* sinT;
@@ -257,6 +260,7 @@ struct EpiQkvRope {
     const long long rbase = ((long long)l * rows + row) * ld;
     const int half = hd >> 1;
     const float rs = valid ? norm.scale(l, rows, row) : 1.f;
+    if (hd > ncols && col0 % hd != 0) return;  // second half of a head: its first half's group writes it
     for (int h0 = 0; h0 < ncols; h0 += hd) {
       const int hcol = col0 + h0;
       if (half >= 32) {

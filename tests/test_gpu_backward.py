@@ -80,6 +80,8 @@ CASES = [
     ("tiny_hidden_only", {}, 3, 0, False, ("hidden",)),
     ("tiny_state_only", {"n_layers": 3}, 4, 3, True, ("A", "z")),
     ("tiny_mem8_P192", {"n_mem": 8, "key_dim": 32}, 3, 0, True, ("hidden", "A", "z")),
+    ("tiny_hd128", {"n_q_heads": 2, "n_kv_heads": 1, "head_dim": 128, "d_model": 256, "ffn_dim": 256}, 2, 3,
+     False, ("hidden", "A", "z")),
     # several 64-wide tiles with ragged edges in every GEMM dimension, 3 attention tiles
     ("mid_tiles", {"n_layers": 3, "d_model": 128, "n_q_heads": 4, "n_kv_heads": 2, "head_dim": 32,
                    "ffn_dim": 256, "seg_len": 64, "n_mem": 16, "key_dim": 32}, 4, 7, True, ("hidden", "A", "z")),
@@ -148,3 +150,25 @@ def test_backward_rejects_bf16_models_and_half_given_state():
         m.backward(t, mem_A0=A0)
     assert e.value.status == ERR_ARG
     m.close()
+
+
+def test_backward_allocation_cap_then_recovers(monkeypatch):
+    """The backward's workspace is allocated on the first call: under a cap
+    that leaves no room for it the call fails with ARMT_ERR_OOM and writes
+    nothing; with the cap lifted the next call is correct."""
+    cfg = I.TINY
+    W = I.make_weights(cfg, seed=121, norm_jitter=0.1)
+    tok = I.make_tokens(cfg, 3, seed=121)
+    cot, _ = _cot(cfg, tok.shape[0], 122)
+    m = B.Model(cfg, W)
+    t = torch.from_numpy(tok).cuda()
+    monkeypatch.setenv("ARMT_ALLOC_CAP_BYTES", "1")
+    with pytest.raises(B.ArmtError) as e:
+        m.backward(t, cot_hidden=_dev(cot["hidden"]))
+    assert e.value.status == 4  # ARMT_ERR_OOM
+    monkeypatch.delenv("ARMT_ALLOC_CAP_BYTES")
+    grads, _ = m.backward(t, cot_hidden=_dev(cot["hidden"]), cot_A=_dev(cot["A"]), cot_z=_dev(cot["z"]))
+    torch.cuda.synchronize()
+    m.armt_sync_status()
+    m.close()
+    _compare("after_oom", grads, G.backward_explicit(cfg, W, tok, 3, cot))

@@ -209,6 +209,8 @@ TINY_CASES = [
     ("tiny_L3_n5", {"n_layers": 3}, 5, 0.1),
     ("tiny_one_segment", {}, 1, 0.1),
     ("tiny_hd64", {"n_q_heads": 2, "n_kv_heads": 1, "head_dim": 64, "d_model": 128}, 3, 0.1),
+    # a head wider than the fp32 epilogue's 64-column groups
+    ("tiny_hd128", {"n_q_heads": 2, "n_kv_heads": 1, "head_dim": 128, "d_model": 256, "ffn_dim": 256}, 3, 0.1),
 ]
 
 

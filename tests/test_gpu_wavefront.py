@@ -55,6 +55,7 @@ CASES = [
     ("tiny_hd64", {"n_q_heads": 2, "n_kv_heads": 1, "head_dim": 64, "d_model": 128}, 48),
     ("tiny_short_last", {"n_layers": 3}, 64 - 5),
     ("tiny_L4_n12", {"n_layers": 4}, 16 * 12),
+    ("tiny_hd128", {"n_q_heads": 2, "n_kv_heads": 1, "head_dim": 128, "d_model": 256, "ffn_dim": 256}, 40),
 ]
 
 
