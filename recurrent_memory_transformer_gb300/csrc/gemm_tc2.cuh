@@ -118,21 +118,28 @@ __global__ void __launch_bounds__(Tc2Cfg<EPI_WG>::THREADS, 1)
         const int a_row = sh.map.a_row0(layer) + mp * 2 * TC_BM + (int)rank * TC_BM;
         const int b_row = nt * C::BN + (int)rank * (C::BN / 2);
         const int b_slot = layer / sh.map.b_div + sh.map.b_slot_off;
+        // split operands: pass p (K blocks kpp p .. kpp (p + 1) - 1) reads A part
+        // p % a_parts and B part p / a_parts (0 = high, 1 = low); tracked
+        // incrementally, so the unsplit loop does no division
+        const int kpp = sh.kb_split > 0 ? sh.kb_split : sh.k_blocks, two_a = sh.map.a_parts() == 2;
+        int kk = 0, pass = 0;
         for (int kb = 0; kb < sh.k_blocks; ++kb) {
           if (issued == sh.wp.stall_after ||
               !mbar_wait_bounded_cluster(&empty[stage], phase ^ 1u, sh.err, DEV_TIMEOUT_EMPTY, sh.wp.limit_ns)) {
             ok = false;
             break;
           }
+          const int kc = kk * TC_BK;
+          const int ap = two_a ? (pass & 1) : 0, bp = two_a ? (pass >> 1) : pass;
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
           const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-          // split operands: pass p reads A part p % a_parts, B part p / a_parts
-          const int pass = sh.kb_split > 0 ? kb / sh.kb_split : 0;
-          const int kc = (kb - pass * sh.kb_split) * TC_BK;
-          const int ap = pass % sh.map.a_parts(), bp = pass / sh.map.a_parts();
           tma_load_3d_pair(sA + stage * C::A_BYTES, &tmA, kc, a_row,
                            layer + sh.map.a_slot_off + ap * sh.map.a_lo_slot, fb);
           tma_load_3d_pair(sB + stage * C::B_BYTES, &tmB, kc, b_row, b_slot + bp * sh.map.b_lo_slot, fb);
+          if (++kk == kpp) {
+            kk = 0;
+            ++pass;
+          }
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
