@@ -389,8 +389,12 @@ typedef struct armt_grads {
  *   hidden_out, mem_A_out, mem_z_out: the forward's results (as from
  *                armt_forward_batch with batch 1), each may be NULL
  *   grads        see armt_grads
- * fp32 models only (ARMT_ERR_UNSUPPORTED for bf16).  Arithmetic is fp32 with
- * every reduction in a fixed order: repeated calls give bitwise equal
+ * fp32 models: everything in fp32.  bf16 models: the forward runs as
+ * armt_forward does (the model's precision mode, tensor cores) and keeps its
+ * fp32 cell inputs and states; the adjoint runs in fp32 against fp32 copies
+ * of the bf16 weights, made on the first call (kept by the model) -- the
+ * gradients of the exact model at the bf16 forward's cell inputs.  Every
+ * reduction runs in a fixed order: repeated calls give bitwise equal
  * gradients.  The first call (and one with more segments or tokens than
  * before) allocates the backward's workspace, which grows with the number
  * of segments (saved cell inputs and states); the allocation synchronises

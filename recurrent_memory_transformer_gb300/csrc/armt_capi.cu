@@ -381,7 +381,13 @@ struct Model : ModelBase {
   BwView bwv{};
   int64_t bw_n_cap = 0, bw_tok_cap = 0;
   float *bw_hidden = nullptr, *bw_A = nullptr, *bw_z = nullptr;  // forward results nobody asked for
+  // bf16 models: fp32 copies of the weight products' weights (the backward's
+  // arithmetic is fp32), made on the first backward
+  DevAllocs bw_w32_mem;
+  float *aWq32 = nullptr, *Wqkv32 = nullptr, *Wo32 = nullptr, *Wgu32 = nullptr, *Wd32 = nullptr,
+        *Ww32 = nullptr;
   ~Model() override {
+    bw_w32_mem.free_all();
     bw_mem.free_all();
     wf_mem.free_all();
     full_mem.free_all();
@@ -389,7 +395,7 @@ struct Model : ModelBase {
     wb_mem.free_all();
   }
   long long full_workspace_bytes() const override { return full_mem.total; }
-  long long backward_workspace_bytes() const override { return bw_mem.total; }
+  long long backward_workspace_bytes() const override { return bw_mem.total + bw_w32_mem.total; }
   long long batch_workspace_bytes() const override { return wb_mem.total; }
   int upd_rows_per_block = 32;
   // persistent wavefront (fp32 models): task list and (cell, stage) counters
@@ -1204,12 +1210,36 @@ struct Model : ModelBase {
     return ARMT_OK;
   }
 
+  // fp32 copies of the bf16 weights the backward multiplies with (once)
+  armt_status bw_weights_f32(cudaStream_t st) {
+    if (aWq32 != nullptr) return ARMT_OK;
+    const armt_config& c = cfg;
+    const size_t L = c.n_layers, d = c.d_model, k = c.key_dim, F = c.ffn_dim, Nq = n_qkv();
+    const size_t HA = (size_t)c.n_q_heads * c.head_dim;
+    struct Item {
+      float** dst;
+      const WT* src;
+      size_t n;
+    } items[] = {{&aWq32, aWq, L * k * d}, {&Wqkv32, Wqkv, L * Nq * d}, {&Wo32, Wo, L * d * HA},
+                 {&Wgu32, Wgu, L * 2 * F * d}, {&Wd32, Wd, L * d * F}, {&Ww32, Ww, L * (size_t)nw * d}};
+    for (const Item& it : items) {
+      armt_status s = bw_w32_mem.alloc_n(it.dst, it.n);
+      if (s != ARMT_OK) {
+        bw_w32_mem.free_all();
+        aWq32 = nullptr;
+        return s;
+      }
+      to_f32_kernel<WT><<<4 * num_sms, 256, 0, st>>>(it.src, *it.dst, (long long)it.n);
+      CK(cudaGetLastError());
+    }
+    return ARMT_OK;
+  }
+
   armt_status backward(const int32_t* tokens, int64_t n_tok, const float* A0, const float* z0,
                        const float* cot_h, const float* cot_A, const float* cot_z, float* hidden, float* A,
                        float* z, const armt_grads& gr, cudaStream_t st) override {
-    if constexpr (kTC) {
-      return fail(ARMT_ERR_UNSUPPORTED, "the backward pass runs fp32 models");
-    } else {
+    {
+      if constexpr (kTC) CKS(bw_weights_f32(st));
       const armt_config& c = cfg;
       const int L = c.n_layers, d = c.d_model, P = phi_dim(), S = c.seg_len, M = c.n_mem, k = c.key_dim;
       const int F = c.ffn_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads, hd = c.head_dim;
@@ -1252,12 +1282,21 @@ struct Model : ModelBase {
       v.n_seg = n;
       v.n_tok = n_tok;
       v.last_len = last_segment_len(n_tok, S);
-      v.aWq = aWq;
-      v.Wqkv = Wqkv;
-      v.Wo = Wo;
-      v.Wgu = Wgu;
-      v.Wd = Wd;
-      v.Ww = Ww;
+      if constexpr (kTC) {
+        v.aWq = aWq32;
+        v.Wqkv = Wqkv32;
+        v.Wo = Wo32;
+        v.Wgu = Wgu32;
+        v.Wd = Wd32;
+        v.Ww = Ww32;
+      } else {
+        v.aWq = aWq;
+        v.Wqkv = Wqkv;
+        v.Wo = Wo;
+        v.Wgu = Wgu;
+        v.Wd = Wd;
+        v.Ww = Ww;
+      }
       v.g1 = g1;
       v.g2 = g2;
       v.gf = gf;

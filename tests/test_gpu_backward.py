@@ -28,7 +28,7 @@ from recurrent_memory_transformer_gb300 import build as build_mod  # noqa: E402
 
 from tests.test_gpu_parity import record  # noqa: E402
 
-ERR_ARG, ERR_UNSUPPORTED = 1, 3
+ERR_ARG = 1
 REL, COS = 1e-4, 1e-9
 
 
@@ -133,15 +133,51 @@ def test_backward_matches_fp64_gradients(name, over, n_seg, short, with_state, p
     m.close()
 
 
-def test_backward_rejects_bf16_models_and_half_given_state():
-    cfg = dataclasses.replace(I.ARMT_1B, n_layers=1, vocab=4096)
-    W = I.make_weights(cfg, seed=94)
+BF16_SMALL = dataclasses.replace(I.ARMT_1B, n_layers=2, d_model=512, n_q_heads=4, n_kv_heads=4, head_dim=64,
+                                 ffn_dim=1024, vocab=512, seg_len=128)
+
+
+@pytest.mark.parametrize("precision", ["bf16", "bf16x2"])
+def test_backward_of_bf16_models(precision):
+    """bf16 models: the forward runs in the model's precision on the tensor
+    cores and keeps fp32 cell inputs and states; the adjoint runs in fp32
+    against fp32 copies of the bf16 weights.  The gradients are those of the
+    exact model evaluated at the bf16 forward's cell inputs, so they sit
+    within the forward's rounding of the fp64 gradients: cosine >= 0.999
+    (the bound the forward's outputs are held to) on every gradient tensor
+    in both precision modes, and in split precision also a relative L2
+    error <= 5e-3 (its forward is accurate to ~1e-3).  Measured: bf16
+    1 - cos <= 2.8e-4, relative L2 <= 2.4 %; split 1 - cos < 5e-7, relative
+    L2 <= 6e-4."""
+    cfg = dataclasses.replace(BF16_SMALL, precision=precision)
+    W = I.make_weights(cfg, seed=131, norm_jitter=0.1)
+    n_seg = 3
+    tok = I.make_tokens(cfg, n_seg, seed=131)[:-9]
+    cot, _ = _cot(cfg, tok.shape[0], 132)
+    ref = G.backward_explicit(cfg, W, tok, n_seg, cot)
     m = B.Model(cfg, B.device_weight_tensors(cfg, W))
-    t = torch.from_numpy(I.make_tokens(cfg, 1, seed=94)).cuda()
-    with pytest.raises(B.ArmtError) as e:
-        m.backward(t)
-    assert e.value.status == ERR_UNSUPPORTED
+    t = torch.from_numpy(tok).cuda()
+    grads, (h, A, z) = m.backward(t, cot_hidden=_dev(cot["hidden"]), cot_A=_dev(cot["A"]), cot_z=_dev(cot["z"]))
+    torch.cuda.synchronize()
+    m.armt_sync_status()
+    hf, Af, zf = m.forward_batch(t.view(1, -1))
+    torch.cuda.synchronize()
+    assert torch.equal(h, hf[0]) and torch.equal(A, Af[:, 0]) and torch.equal(z, zf[:, 0])
     m.close()
+    out = {}
+    for k, r in ref.items():
+        g = grads[k].cpu().numpy().astype(np.float64).reshape(r.shape)
+        nr, ng = np.linalg.norm(r), np.linalg.norm(g)
+        out[k] = {"cos": float(np.sum(g * r) / (nr * ng)) if nr > 0 and ng > 0 else 1.0,
+                  "rel_l2": float(np.linalg.norm(g - r) / nr) if nr > 0 else 0.0}
+    record(f"backward_bf16_model_{precision}", **out)
+    for k, st in out.items():
+        assert np.isfinite(st["rel_l2"]) and st["cos"] >= 0.999, (k, st)
+        if precision == "bf16x2":
+            assert st["rel_l2"] <= 5e-3, (k, st)
+
+
+def test_backward_rejects_half_given_state():
     cfg = I.TINY
     m = B.Model(cfg, I.make_weights(cfg, seed=94))
     t = torch.from_numpy(I.make_tokens(cfg, 2, seed=94)).cuda()
