@@ -490,11 +490,18 @@ def main():
                                   ffn_dim=4096, vocab=4096, seg_len=512, dtype="f32")
         backward = {"workloads": {
             "small": "fp32 ARMT, 4 layers, d 256, 4/2 heads of 64, F 512, 64 + 16 rows per cell",
-            "mid": "fp32 ARMT, 4 layers, d 1024, 16/4 heads of 64, F 4096, 512 + 16 rows per cell"},
+            "mid": "fp32 ARMT, 4 layers, d 1024, 16/4 heads of 64, F 4096, 512 + 16 rows per cell",
+            "main": "the timed model (bf16 forward; fp32 adjoint against fp32 copies of its weights), "
+                    "first 8 segments"},
             "runs": []}
-        for wl, cfg_b, n_b in (("small", small, 8), ("small", small, 64), ("mid", mid, 8)):
-            model_b = B.Model(cfg_b, I.make_weights(cfg_b, 8))
-            tb = torch.from_numpy(I.make_tokens(cfg_b, n_b, 8)).cuda()
+        legs = [("small", small, 8), ("small", small, 64), ("mid", mid, 8)]
+        if cfg.n_layers * cfg.d_model <= 16 * 2048:  # the main model when it is ARMT-1B-sized or smaller
+            legs.append(("main", cfg, min(8, n_seg)))
+        for wl, cfg_b, n_b in legs:
+            own = wl != "main"
+            model_b = B.Model(cfg_b, I.make_weights(cfg_b, 8)) if own else model
+            tb = (torch.from_numpy(I.make_tokens(cfg_b, n_b, 8)) if own
+                  else torch.from_numpy(tok_np[:n_b * cfg.seg_len].copy())).cuda()
             rng_b = torch.Generator(device="cuda")
             rng_b.manual_seed(8)
             cot_h = torch.randn((tb.numel(), cfg_b.d_model), generator=rng_b, device="cuda")
@@ -507,6 +514,7 @@ def main():
             shapes_b = I.weight_shapes(cfg_b)
             grads_b = {k: torch.empty(shapes_b[k], dtype=torch.float32, device="cuda") for k in shapes_b}
             row = {"workload": wl, "segments": n_b, "tokens": tb.numel()}
+            torch.cuda.nvtx.range_push(f"backward:{wl}:{n_b}")  # lets a profiler pick one leg
             for name in ("forward", "backward"):
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 torch.cuda.synchronize()
@@ -520,6 +528,7 @@ def main():
                 torch.cuda.synchronize()
                 model_b.armt_sync_status()
                 row[name + "_ms"] = e0.elapsed_time(e1) / 3
+            torch.cuda.nvtx.range_pop()
             launches_b, flops_b, ws_b = model_b.armt_backward_stats()
             adj_ms = row["backward_ms"] - row["forward_ms"]
             row.update({"backward_includes_forward": True, "adjoint_ms": adj_ms,
@@ -528,7 +537,8 @@ def main():
                         "tokens_per_s": tb.numel() / (row["backward_ms"] * 1e-3),
                         "workspace_bytes": ws_b})
             backward["runs"].append(row)
-            model_b.close()
+            if own:
+                model_b.close()
             del model_b, grads_b
             torch.cuda.empty_cache()
         # fp32 FMA peak from the unit counts and the SM clock sampled in the timed region
