@@ -74,13 +74,14 @@ struct BwGemm {
   float* part = nullptr;
 };
 
-// One thread's share of a 64 x 16 A tile and a 16 x 64 B tile: element q of
+// One thread's share of a BM x 16 A tile and a 16 x BN B tile: element q of
 // the thread is e = tid + 256 q, laid out along the operand's contiguous
 // dimension.
+template <int BM, int BN>
 __device__ __forceinline__ void bw_tile_index(int e, int trans_a, int trans_b, int& ia, int& ka, int& jb, int& kb) {
   if (trans_a) {
-    ia = e & 63;
-    ka = e >> 6;
+    ia = e % BM;
+    ka = e / BM;
   } else {
     ka = e & 15;
     ia = e >> 4;
@@ -89,39 +90,50 @@ __device__ __forceinline__ void bw_tile_index(int e, int trans_a, int trans_b, i
     kb = e & 15;
     jb = e >> 4;
   } else {
-    jb = e & 63;
-    kb = e >> 6;
+    jb = e % BN;
+    kb = e / BN;
   }
 }
 
-// 64 x 64 output tile per 256-thread block, 4 x 4 per thread, K in steps of
-// 16 through two shared-memory buffers: the next step's operands are loaded
-// into registers while the current step computes.
+// A BM x BN output tile per 256-thread block (16 x 16 threads), TM x TN per
+// thread (BM = 16 TM, BN = 16 TN), K in steps of 16 through two shared-memory
+// buffers: the next step's operands are loaded into registers while the
+// current step computes.  Every output element is summed over K in order by
+// one thread (the same order for every tile shape).  64 x 64 tiles for small
+// products, 128 x 128 (8 x 8 per thread, operands read as float4) where there
+// are enough tiles: four shared-memory loads per 64 FMAs instead of eight per 16.
+template <int BM, int BN>
 __global__ void __launch_bounds__(256) bw_gemm_kernel(const BwGemm g) {
-  __shared__ float As[2][16][64 + 4];
-  __shared__ float Bs[2][16][64 + 4];
+  constexpr int TM = BM / 16, TN = BN / 16, QA = BM / 16, QB = BN / 16;
+  __shared__ __align__(16) float As[2][16][BM + 4];
+  __shared__ __align__(16) float Bs[2][16][BN + 4];
   const int cell = blockIdx.z % g.groups, kz = blockIdx.z / g.groups;
   const int l = g.l0 + cell;
   const long long s = g.s0 - cell;
   const float* A = g.A.m.at(l, s);
   const float* B = g.B.m.at(l, s);
-  const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
+  const int i0 = blockIdx.y * BM, j0 = blockIdx.x * BN;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int kbeg = g.ksplit > 1 ? kz * g.kchunk : 0;
   const int kend = g.ksplit > 1 ? min(g.K, kbeg + g.kchunk) : g.K;
-  float acc[4][4];
+  float acc[TM][TN];
 #pragma unroll
-  for (int u = 0; u < 4; ++u)
+  for (int u = 0; u < TM; ++u)
 #pragma unroll
-    for (int v = 0; v < 4; ++v) acc[u][v] = 0.f;
-  float ra[4], rb[4];
+    for (int v = 0; v < TN; ++v) acc[u][v] = 0.f;
+  float ra[QA], rb[QB];
   auto load = [&](int k0) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < QA; ++q) {
       int ia, ka, jb, kb;
-      bw_tile_index(threadIdx.x + 256 * q, g.A.trans, g.B.trans, ia, ka, jb, kb);
+      bw_tile_index<BM, BN>(threadIdx.x + 256 * q, g.A.trans, g.B.trans, ia, ka, jb, kb);
       const int r = i0 + ia, c = k0 + ka;
       ra[q] = (r < g.M && c < kend) ? (g.A.trans ? A[(long long)c * g.A.ld + r] : A[(long long)r * g.A.ld + c]) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < QB; ++q) {
+      int ia, ka, jb, kb;
+      bw_tile_index<BM, BN>(threadIdx.x + 256 * q, g.A.trans, g.B.trans, ia, ka, jb, kb);
       const int cb = j0 + jb, rk = k0 + kb;
       rb[q] = (cb < g.N && rk < kend) ? (g.B.trans ? B[(long long)cb * g.B.ld + rk] : B[(long long)rk * g.B.ld + cb])
                                       : 0.f;
@@ -129,10 +141,15 @@ __global__ void __launch_bounds__(256) bw_gemm_kernel(const BwGemm g) {
   };
   auto stash = [&](int buf) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < QA; ++q) {
       int ia, ka, jb, kb;
-      bw_tile_index(threadIdx.x + 256 * q, g.A.trans, g.B.trans, ia, ka, jb, kb);
+      bw_tile_index<BM, BN>(threadIdx.x + 256 * q, g.A.trans, g.B.trans, ia, ka, jb, kb);
       As[buf][ka][ia] = ra[q];
+    }
+#pragma unroll
+    for (int q = 0; q < QB; ++q) {
+      int ia, ka, jb, kb;
+      bw_tile_index<BM, BN>(threadIdx.x + 256 * q, g.A.trans, g.B.trans, ia, ka, jb, kb);
       Bs[buf][kb][jb] = rb[q];
     }
   };
@@ -147,16 +164,27 @@ __global__ void __launch_bounds__(256) bw_gemm_kernel(const BwGemm g) {
     if (more) load(k0 + 16);
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
-      float a[4], b[4];
+      float a[TM], b[TN];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        a[u] = As[buf][kk][ty * 4 + u];
-        b[u] = Bs[buf][kk][tx * 4 + u];
+      for (int u = 0; u < TM; u += 4) {
+        const float4 t = *reinterpret_cast<const float4*>(&As[buf][kk][ty * TM + u]);
+        a[u] = t.x;
+        a[u + 1] = t.y;
+        a[u + 2] = t.z;
+        a[u + 3] = t.w;
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int v = 0; v < TN; v += 4) {
+        const float4 t = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * TN + v]);
+        b[v] = t.x;
+        b[v + 1] = t.y;
+        b[v + 2] = t.z;
+        b[v + 3] = t.w;
+      }
 #pragma unroll
-        for (int v = 0; v < 4; ++v) acc[u][v] += a[u] * b[v];
+      for (int u = 0; u < TM; ++u)
+#pragma unroll
+        for (int v = 0; v < TN; ++v) acc[u][v] += a[u] * b[v];
     }
     if (more) stash(buf ^ 1);
     __syncthreads();
@@ -165,12 +193,12 @@ __global__ void __launch_bounds__(256) bw_gemm_kernel(const BwGemm g) {
   if (g.ksplit > 1) {
     float* pt = g.part + ((long long)kz * g.groups + cell) * g.M * g.N;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int r = i0 + ty * 4 + u;
+    for (int u = 0; u < TM; ++u) {
+      const int r = i0 + ty * TM + u;
       if (r >= g.M) continue;
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const int c = j0 + tx * 4 + v;
+      for (int v = 0; v < TN; ++v) {
+        const int c = j0 + tx * TN + v;
         if (c < g.N) pt[(long long)r * g.N + c] = acc[u][v];
       }
     }
@@ -180,14 +208,14 @@ __global__ void __launch_bounds__(256) bw_gemm_kernel(const BwGemm g) {
   const float* E = g.E.m.p != nullptr ? g.E.m.at(l, s) : nullptr;
   const float* rs = g.rs.p != nullptr ? g.rs.at(l, s) : nullptr;
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int r = i0 + ty * 4 + u;
+  for (int u = 0; u < TM; ++u) {
+    const int r = i0 + ty * TM + u;
     if (r >= g.M) continue;
     float f = g.alpha;
     if (rs != nullptr) f = g.rs_div ? f / rs[r] : f * rs[r];
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const int c = j0 + tx * 4 + v;
+    for (int v = 0; v < TN; ++v) {
+      const int c = j0 + tx * TN + v;
       if (c >= g.N) continue;
       float val = f * acc[u][v];
       if (E != nullptr) val += E[(long long)r * g.E.ld + c];

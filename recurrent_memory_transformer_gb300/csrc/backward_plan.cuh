@@ -87,9 +87,13 @@ struct BwRun {
     if (M == 0 || N == 0 || groups == 0) return ARMT_OK;
     flops += 2.0 * M * N * K * groups;
     p.groups = groups;
+    // 128 x 128 tiles where they still give every SM a block, else 64 x 64
+    const long long tiles128 = (long long)((N + 127) / 128) * ((M + 127) / 128) * groups;
+    const bool big = M >= 128 && N >= 128 && tiles128 >= v.num_sms;
+    const int bm = big ? 128 : 64;
     // too few tiles to fill the SMs and a long K: split K (about two blocks
     // per SM), partial products to scratch, summed in order by a second kernel
-    const long long tiles = (long long)((N + 63) / 64) * ((M + 63) / 64) * groups;
+    const long long tiles = (long long)((N + bm - 1) / bm) * ((M + bm - 1) / bm) * groups;
     int ks = 1;
     if (tiles < v.num_sms && K >= 128) {
       ks = (int)std::min<long long>((2LL * v.num_sms + tiles - 1) / tiles, K / 64);
@@ -100,7 +104,11 @@ struct BwRun {
       p.ksplit = (K + p.kchunk - 1) / p.kchunk;
       p.part = v.Part;
     }
-    bw_gemm_kernel<<<dim3((N + 63) / 64, (M + 63) / 64, groups * p.ksplit), 256, 0, st>>>(p);
+    const dim3 grid((N + bm - 1) / bm, (M + bm - 1) / bm, groups * p.ksplit);
+    if (big)
+      bw_gemm_kernel<128, 128><<<grid, 256, 0, st>>>(p);
+    else
+      bw_gemm_kernel<64, 64><<<grid, 256, 0, st>>>(p);
     CKS(check());
     if (p.ksplit > 1) {
       const long long mn = (long long)M * N;
