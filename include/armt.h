@@ -457,6 +457,17 @@ ARMT_API armt_status armt_set_profiling(armt_model* m, int32_t enable);
 ARMT_API armt_status armt_set_profiling_mask(armt_model* m, uint32_t class_mask);
 ARMT_API armt_status armt_kernel_times(armt_model* m, int64_t* launches, double* ms, int32_t n_classes);
 
+/* Tracing (off by default): with enable != 0 every step is wrapped in an
+ * NVTX range -- "armt diagonal i (layers lo-hi)" for the diagonal schedule,
+ * "armt segment s (layers l-l)" per cell of the sequential one, "armt
+ * wavefront n (layers 0-L-1)" for a persistent launch, "armt backward
+ * diagonal i (layers lo-hi)" for the reverse diagonals of armt_backward --
+ * so that a profiler (nsys, ncu --nvtx) can attribute or select the kernels
+ * of one step.  The ranges are host-side markers on the calling thread; with
+ * no profiler attached they cost a function call each, with tracing off a
+ * branch. */
+ARMT_API armt_status armt_set_tracing(armt_model* m, int32_t enable);
+
 /* Waits for `stream` and reports a device-side error recorded since the last
  * call (ARMT_ERR_TIMEOUT when a bounded wait gave up), then clears it. */
 ARMT_API armt_status armt_sync_status(armt_model* m, void* stream);

@@ -33,7 +33,7 @@ EXPORTED = ("armt_create", "armt_destroy", "armt_forward", "armt_forward_sequent
             "armt_memory_bytes", "armt_lm_head", "armt_launch_count",
             "armt_set_profiling", "armt_set_profiling_mask", "armt_kernel_times", "armt_sync_status", "armt_status_string",
             "armt_last_error", "armt_block_sync_status", "armt_noalloc_sync_status", "armt_backward",
-            "armt_backward_stats")
+            "armt_backward_stats", "armt_set_tracing")
 
 
 class ArmtError(RuntimeError):
@@ -97,6 +97,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.armt_memory_bytes.argtypes = [P, ctypes.POINTER(I64), ctypes.POINTER(I64), ctypes.POINTER(I64)]
     lib.armt_launch_count.argtypes = [P, I64, I32, ctypes.POINTER(I64)]
     lib.armt_set_profiling.argtypes = [P, I32]
+    lib.armt_set_tracing.argtypes = [P, I32]
     lib.armt_set_profiling_mask.argtypes = [P, ctypes.c_uint32]
     lib.armt_kernel_times.argtypes = [P, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double), I32]
     lib.armt_sync_status.argtypes = [P, P]
@@ -276,7 +277,7 @@ class Model:
         """(kernel launches, algorithmic FLOPs) of the last backward, and its workspace bytes."""
         a, b, f = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_double()
         _check(_lib.armt_backward_stats(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(f)),
-               "armt_backward_stats")
+               "armt_backward_stats", "armt_set_tracing")
         return a.value, f.value, b.value
 
     def backward(self, tokens, cot_hidden=None, cot_A=None, cot_z=None, mem_A0=None, mem_z0=None,
@@ -295,6 +296,10 @@ class Model:
         z = torch.empty((L, P), dtype=torch.float32, device=dev)
         self.armt_backward(tokens, grads, mem_A0, mem_z0, cot_hidden, cot_A, cot_z, hidden, A, z, stream)
         return grads, (hidden, A, z)
+
+    def armt_set_tracing(self, enable=True):
+        """NVTX ranges around every step (forward diagonals or cells, backward diagonals)."""
+        _check(_lib.armt_set_tracing(self._h, 1 if enable else 0), "armt_set_tracing")
 
     def armt_forward_full_attention(self, tokens, hidden_out, stream=None):
         """Plain causal LLaMA over all tokens (no memory), same weights."""

@@ -28,6 +28,8 @@
 #include <type_traits>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/armt.h"
 #include "common.cuh"
 #include "epilogues.cuh"
@@ -162,6 +164,17 @@ struct ModelBase {
   // profiling: launches of the classes in prof_mask get an event pair
   bool profiling = false;
   uint32_t prof_mask = 0;
+  // tracing: NVTX ranges around every step (armt_set_tracing)
+  bool tracing = false;
+  void trace_push(const char* what, long long i, int lo, int hi) const {
+    if (!tracing) return;
+    char name[96];
+    std::snprintf(name, sizeof(name), "armt %s %lld (layers %d-%d)", what, i, lo, hi);
+    nvtxRangePushA(name);
+  }
+  void trace_pop() const {
+    if (tracing) nvtxRangePop();
+  }
   bool prof_open = false;
   std::vector<cudaEvent_t> ev_start, ev_stop;
   std::vector<int> ev_class;
@@ -1339,7 +1352,13 @@ struct Model : ModelBase {
           CK(cudaMemsetAsync(sz, 0, (size_t)P * 4, st));
       }
       BwRun run{v, st};
-      for (int64_t i = diagonal_steps(L, n) - 1; i >= 0; --i) CKS(run.diagonal(i));
+      for (int64_t i = diagonal_steps(L, n) - 1; i >= 0; --i) {
+        const CellRange cr = diagonal_step(i, L, n);
+        trace_push("backward diagonal", i, cr.lo, cr.hi);
+        const armt_status ds = run.diagonal(i);
+        trace_pop();
+        CKS(ds);
+      }
       bw_embed_grad_kernel<<<(d + 127) / 128, 128, 0, st>>>(v.XB0, tokens, n_tok, S, rows(), M, d, c.vocab, n,
                                                             gr.embed, gr.mem);
       CKS(run.check());
@@ -1385,7 +1404,10 @@ struct Model : ModelBase {
         return fail(ARMT_ERR_UNSUPPORTED, "the wavefront schedule runs fp32 models");
       } else {
         if (nb != 1) return fail(ARMT_ERR_UNSUPPORTED, "the wavefront schedule runs one sequence");
-        return forward_wavefront(tokens, n_tok, n, hidden, A, z, mem_in_valid, st);
+        trace_push("wavefront", n, 0, L - 1);
+        const armt_status ws = forward_wavefront(tokens, n_tok, n, hidden, A, z, mem_in_valid, st);
+        trace_pop();
+        return ws;
       }
     }
     if (nb > 1) CKS(ensure_batch(nb, st));
@@ -1406,14 +1428,22 @@ struct Model : ModelBase {
       for (int64_t i = 0; i < diagonal_steps(L, n); ++i) {
         const CellRange c = diagonal_step(i, L, n);
         if (bw_save != nullptr) CKS(save_cells(w, c, A, z, true, st));
-        CKS(step(w, c.lo, c.hi, c.s_lo, tokens, n_tok, n, hidden, A, z, st));
+        trace_push("diagonal", i, c.lo, c.hi);
+        const armt_status ss = step(w, c.lo, c.hi, c.s_lo, tokens, n_tok, n, hidden, A, z, st);
+        trace_pop();
+        CKS(ss);
         if (bw_save != nullptr) CKS(save_cells(w, c, A, z, false, st));
         if (report)
           CKS(sink_progress(diagonal_rows_final(i, L, S, n_tok), diagonal_layers_final(i, n), st));
       }
     } else {
       for (int64_t s = 0; s < n; ++s) {
-        for (int l = 0; l < L; ++l) CKS(step(w, l, l, s, tokens, n_tok, n, hidden, A, z, st));
+        for (int l = 0; l < L; ++l) {
+          trace_push("segment", s, l, l);
+          const armt_status ss = step(w, l, l, s, tokens, n_tok, n, hidden, A, z, st);
+          trace_pop();
+          CKS(ss);
+        }
         if (report) CKS(sink_progress(sequential_rows_final(s, S, n_tok), sequential_layers_final(s, n, L), st));
       }
     }
@@ -1879,6 +1909,12 @@ armt_status armt_launch_count(const armt_model* m, int64_t n, int32_t schedule, 
       schedule != ARMT_SCHEDULE_WAVEFRONT)
     return fail(ARMT_ERR_ARG, "unknown schedule");
   *launches = m->impl->launches(n, schedule, 0);
+  return ARMT_OK;
+}
+
+armt_status armt_set_tracing(armt_model* m, int32_t enable) {
+  if (m == nullptr) return fail(ARMT_ERR_ARG, "NULL argument");
+  m->impl->tracing = enable != 0;
   return ARMT_OK;
 }
 

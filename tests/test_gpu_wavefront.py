@@ -165,3 +165,26 @@ def test_wavefront_time_against_per_diagonal_launches():
             assert torch.equal(a, b), n_seg
     record("wavefront_timing_fp32_d256_L4", **res)
     m.close()
+
+
+def test_tracing_changes_no_result():
+    """armt_set_tracing only wraps steps in NVTX ranges: every schedule and
+    the backward give bitwise the same results with it on."""
+    cfg = dataclasses.replace(I.TINY, n_layers=3)
+    W = I.make_weights(cfg, seed=96, norm_jitter=0.1)
+    tok = I.make_tokens(cfg, 4, seed=96)
+    t = torch.from_numpy(tok).cuda()
+    m = B.Model(cfg, W)
+    outs = {}
+    for tracing in (False, True):
+        m.armt_set_tracing(tracing)
+        res = [_run(m, tok, sch) for sch in (B.SCHEDULE_DIAGONAL, B.SCHEDULE_SEQUENTIAL, B.SCHEDULE_WAVEFRONT)]
+        g, _ = m.backward(t, cot_hidden=torch.ones((tok.shape[0], cfg.d_model), device="cuda"))
+        torch.cuda.synchronize()
+        outs[tracing] = (res, g)
+    m.close()
+    for a, b in zip(outs[False][0], outs[True][0]):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+    for k in outs[False][1]:
+        assert torch.equal(outs[False][1][k], outs[True][1][k]), k
