@@ -257,18 +257,6 @@ __global__ void bw_add_rows_kernel(CellPtr X, CellPtr Y, CellPtr Z, int n, int l
   for (int c = threadIdx.x; c < n; c += blockDim.x) o[c] = x[c] + y[c];
 }
 
-// Copy rows of width n; rows >= valid (alt_valid for the cell of layer
-// alt_l) are written as zeros.
-__global__ void bw_copy_rows_kernel(CellPtr X, CellPtr Z, int n, int valid, int alt_l, int alt_valid, int l0,
-                                    long long s0) {
-  const int l = l0 + blockIdx.y;
-  const long long s = s0 - blockIdx.y, r = blockIdx.x;
-  const int v = l == alt_l ? alt_valid : valid;
-  float* o = Z.at(l, s) + r * n;
-  const float* x = X.at(l, s) + r * n;
-  for (int c = threadIdx.x; c < n; c += blockDim.x) o[c] = r < v ? x[c] : 0.f;
-}
-
 // phi = DPFP_nu(q) for q rows of width k (row stride ldq), and
 // D = z^T phi + eps.  phi rows of width P = 2 k nu.
 __global__ void bw_dpfp_rows_kernel(CellPtr Q, long long ldq, CellPtr Z, CellPtr Phi, CellPtr Den, int k, int nu,

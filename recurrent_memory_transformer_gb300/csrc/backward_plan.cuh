@@ -1,5 +1,5 @@
 // Backward pass of the ARMT forward (fp32): the host side.  One call of
-// bw_diagonal runs every cell of reverse anti-diagonal i (section 四 of the
+// BwRun::diagonal runs every cell of reverse anti-diagonal i (section 四 of the
 // summary page of "Diagonal Batching Unlocks Parallelism in Recurrent Memory
 // Transformers for Long Contexts": the backward pass keeps the diagonal
 // schedule) in the order recompute -> write adjoint -> block adjoint -> read

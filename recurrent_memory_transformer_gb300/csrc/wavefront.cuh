@@ -69,7 +69,7 @@ struct WfTask {
 // Everything the stages read, for the fp32 model with one sequence.
 struct WfArgs {
   // model
-  const float *embed, *memtok, *gf, *A_state_dummy;
+  const float *embed, *memtok, *gf;
   int T, S, M, d, k, nu, vocab, Hq, Hkv, hd, P, nw, nmax, L;
   float assoc_eps, norm_eps, attn_scale;
   int upd_rows;
