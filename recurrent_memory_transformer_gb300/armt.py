@@ -277,7 +277,7 @@ class Model:
         """(kernel launches, algorithmic FLOPs) of the last backward, and its workspace bytes."""
         a, b, f = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_double()
         _check(_lib.armt_backward_stats(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(f)),
-               "armt_backward_stats", "armt_set_tracing")
+               "armt_backward_stats")
         return a.value, f.value, b.value
 
     def backward(self, tokens, cot_hidden=None, cot_A=None, cot_z=None, mem_A0=None, mem_z0=None,
