@@ -101,7 +101,9 @@ __device__ __forceinline__ void bw_tile_index(int e, int trans_a, int trans_b, i
 // current step computes.  Every output element is summed over K in order by
 // one thread (the same order for every tile shape).  64 x 64 tiles for small
 // products, 128 x 128 (8 x 8 per thread, operands read as float4) where there
-// are enough tiles: four shared-memory loads per 64 FMAs instead of eight per 16.
+// are enough tiles: four shared-memory loads per 64 FMAs instead of eight per
+// 16.  With TN = 8 a thread's columns are tx*4 .. +3 and 64 + tx*4 .. +3, so
+// the eight float4 reads of a quarter-warp fall in distinct banks.
 template <int BM, int BN>
 __global__ void __launch_bounds__(256) bw_gemm_kernel(const BwGemm g) {
   constexpr int TM = BM / 16, TN = BN / 16, QA = BM / 16, QB = BN / 16;
@@ -153,6 +155,8 @@ __global__ void __launch_bounds__(256) bw_gemm_kernel(const BwGemm g) {
       Bs[buf][kb][jb] = rb[q];
     }
   };
+  // column of this thread's v-th output
+  auto col_of = [&](int v) { return TN == 8 ? (v < 4 ? tx * 4 + v : 64 + tx * 4 + v - 4) : tx * TN + v; };
   int buf = 0;
   if (kbeg < kend) {
     load(kbeg);
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(256) bw_gemm_kernel(const BwGemm g) {
       }
 #pragma unroll
       for (int v = 0; v < TN; v += 4) {
-        const float4 t = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * TN + v]);
+        const float4 t = *reinterpret_cast<const float4*>(&Bs[buf][kk][col_of(v)]);
         b[v] = t.x;
         b[v + 1] = t.y;
         b[v + 2] = t.z;
@@ -198,7 +202,7 @@ __global__ void __launch_bounds__(256) bw_gemm_kernel(const BwGemm g) {
       if (r >= g.M) continue;
 #pragma unroll
       for (int v = 0; v < TN; ++v) {
-        const int c = j0 + tx * TN + v;
+        const int c = j0 + col_of(v);
         if (c < g.N) pt[(long long)r * g.N + c] = acc[u][v];
       }
     }
@@ -215,7 +219,7 @@ __global__ void __launch_bounds__(256) bw_gemm_kernel(const BwGemm g) {
     if (rs != nullptr) f = g.rs_div ? f / rs[r] : f * rs[r];
 #pragma unroll
     for (int v = 0; v < TN; ++v) {
-      const int c = j0 + tx * TN + v;
+      const int c = j0 + col_of(v);
       if (c >= g.N) continue;
       float val = f * acc[u][v];
       if (E != nullptr) val += E[(long long)r * g.E.ld + c];
