@@ -9,6 +9,7 @@
 #include <algorithm>
 
 #include "backward.cuh"
+#include "bw_plan.h"
 
 namespace armt {
 
@@ -87,25 +88,16 @@ struct BwRun {
     if (M == 0 || N == 0 || groups == 0) return ARMT_OK;
     flops += 2.0 * M * N * K * groups;
     p.groups = groups;
-    // 128 x 128 tiles where they still give every SM a block, else 64 x 64
-    const long long tiles128 = (long long)((N + 127) / 128) * ((M + 127) / 128) * groups;
-    const bool big = M >= 128 && N >= 128 && tiles128 >= v.num_sms;
-    const int bm = big ? 128 : 64;
-    // too few tiles to fill the SMs and a long K: split K (about two blocks
-    // per SM), partial products to scratch, summed in order by a second kernel
-    const long long tiles = (long long)((N + bm - 1) / bm) * ((M + bm - 1) / bm) * groups;
-    int ks = 1;
-    if (tiles < v.num_sms && K >= 128) {
-      ks = (int)std::min<long long>((2LL * v.num_sms + tiles - 1) / tiles, K / 64);
-      while (ks > 1 && (long long)ks * groups * M * N > v.part_cap) --ks;
-    }
-    if (ks > 1) {
-      p.kchunk = ((K + ks - 1) / ks + 15) / 16 * 16;
-      p.ksplit = (K + p.kchunk - 1) / p.kchunk;
+    // partial products of a split K go to scratch and are summed in order by a second kernel
+    const BwGemmPlan plan = bw_gemm_plan(M, N, K, groups, v.num_sms, v.part_cap);
+    const int bm = plan.bm;
+    if (plan.ksplit > 1) {
+      p.kchunk = plan.kchunk;
+      p.ksplit = plan.ksplit;
       p.part = v.Part;
     }
     const dim3 grid((N + bm - 1) / bm, (M + bm - 1) / bm, groups * p.ksplit);
-    if (big)
+    if (bm == 128)
       bw_gemm_kernel<128, 128><<<grid, 256, 0, st>>>(p);
     else
       bw_gemm_kernel<64, 64><<<grid, 256, 0, st>>>(p);
