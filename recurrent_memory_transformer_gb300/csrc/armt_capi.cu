@@ -1339,7 +1339,7 @@ struct Model : ModelBase {
       // the final state's adjoints enter layer l's first cell in reverse order,
       // (l, n - 1) on diagonal l + n - 1, which reads buffer (l + n - 1) & 1
       for (int l = 0; l < L; ++l) {
-        const int q = (int)((l + n - 1) & 1);
+        const int q = bw_state_seed_buf(l, n);
         float* sa = v.SA[q] + (size_t)l * d * P;
         float* sz = v.Sz[q] + (size_t)l * P;
         if (cot_A != nullptr)
@@ -1364,7 +1364,7 @@ struct Model : ModelBase {
       CKS(run.check());
       // the initial state's adjoints: layer l's cell (l, 0) ran on diagonal l
       for (int l = 0; l < L; ++l) {
-        const int q = (l + 1) & 1;
+        const int q = bw_state_result_buf(l);
         if (gr.mem_A != nullptr)
           CK(cudaMemcpyAsync(gr.mem_A + (size_t)l * d * P, v.SA[q] + (size_t)l * d * P, (size_t)d * P * 4,
                              cudaMemcpyDeviceToDevice, st));

@@ -156,7 +156,7 @@ struct BwRun {
     const long long l_last = i - (n - 1);  // layer of the last segment's cell
     const bool short_last = v.last_len < S && l_last >= lo && l_last <= hi;
     alt_l = short_last ? (int)l_last : -1;
-    const int cur = (int)(i & 1), nxt = cur ^ 1;
+    const int cur = bw_in_buf(i), nxt = bw_out_buf(i);
     const long long Td = (long long)T * d;
     const CellPtr none;
     const BwMat no;

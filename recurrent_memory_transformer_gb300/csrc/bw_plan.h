@@ -34,4 +34,18 @@ inline BwGemmPlan bw_gemm_plan(int M, int N, int K, int groups, int num_sms, lon
   return p;
 }
 
+// Adjoints handed between reverse diagonals live in two buffers used by
+// parity.  Reverse diagonal i (cells (l, i - l)) reads the adjoint of its
+// cells' output rows (written by cell (l + 1, s) on diagonal i + 1) and of the
+// state each cell wrote (handed on by cell (l, s + 1) on diagonal i + 1) from
+// buffer bw_in_buf(i), and writes its cells' input-row adjoints (slot l - 1)
+// and entry-state adjoints (slot l) into bw_out_buf(i), which diagonal i - 1
+// reads.  The final state's adjoints enter layer l's first cell in reverse
+// order, (l, n - 1) on diagonal l + n - 1; the initial state's adjoints leave
+// layer l's cell (l, 0) on diagonal l.
+inline int bw_in_buf(long long i) { return (int)(i & 1); }
+inline int bw_out_buf(long long i) { return (int)((i + 1) & 1); }
+inline int bw_state_seed_buf(int l, long long n) { return bw_in_buf(l + n - 1); }
+inline int bw_state_result_buf(int l) { return bw_out_buf(l); }
+
 }  // namespace armt
